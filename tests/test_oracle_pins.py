@@ -1,0 +1,474 @@
+"""Pins for the oracle: checks against what the pages and the mathematics fix.
+
+None of these compares the oracle with itself. Each test uses a closed form,
+a value printed on the pages, a library routine for a special case, brute
+force on tiny inputs, or an invariant that a plausible mistake breaks.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synthetic_inputs as SI
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _tiny_model(**over):
+    m = SI.presets()["tiny"]["model"]
+    m.update(over)
+    return m
+
+
+def _weights64(model, seed=7):
+    return O.weights_to_f64(SI.make_weights(model, seed))
+
+
+# ----------------------------------------------------------------------------
+# bf16 rounding: against torch's float32 -> bfloat16 converter (RNE)
+
+
+def test_round_bf16_matches_torch_on_float32_values():
+    rng = np.random.default_rng(0)
+    # random magnitudes across the exponent range, both signs
+    mant = rng.uniform(1.0, 2.0, 200000)
+    ex = rng.integers(-140, 127, 200000)
+    x = (mant * np.exp2(ex) * rng.choice([-1.0, 1.0], 200000)).astype(np.float32)
+    # exact ties: a bf16 value plus half of its spacing (representable in fp32)
+    base = torch.randn(20000).to(torch.bfloat16).float().numpy()
+    _, e = np.frexp(base.astype(np.float64))
+    ties = (base.astype(np.float64) + np.sign(base) * np.exp2(e - 9)).astype(np.float32)
+    x = np.concatenate([x, ties, np.float32([0.0, -0.0, 1e-45, 3.0e38, -3.0e38])])
+    ref = torch.from_numpy(x).to(torch.bfloat16).float().numpy().astype(np.float64)
+    got = O.round_bf16(x.astype(np.float64))
+    assert np.array_equal(got, ref)
+
+
+def test_round_bf16_ties_to_even():
+    # 1 + 2^-8 lies halfway between 1 and 1 + 2^-7: ties to the even 1.0
+    assert O.round_bf16(1.0 + 2.0 ** -8) == 1.0
+    # 1 + 3*2^-8 lies halfway between 1+2^-7 and 1+2^-6: ties to 1 + 2^-6
+    assert O.round_bf16(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6
+    assert O.round_bf16(1.0 + 2.0 ** -8 + 2.0 ** -20) == 1.0 + 2.0 ** -7
+
+
+# ----------------------------------------------------------------------------
+# RMSNorm and RoPE closed forms
+
+
+def test_rms_norm_constant_vector_closed_form():
+    for c, eps in [(3.0, 1e-6), (0.5, 0.25), (-2.0, 4.0)]:
+        x = np.full((3, 10), c)
+        g = np.arange(1, 11, dtype=np.float64)
+        got = O.rms_norm(x, g, eps)
+        assert np.allclose(got, c / math.sqrt(c * c + eps) * g, rtol=1e-14, atol=0)
+
+
+def test_rms_norm_uses_mean_not_sum():
+    x = np.array([[3.0, 4.0]])  # mean square 12.5
+    got = O.rms_norm(x, np.ones(2), 0.0)
+    assert np.allclose(got, x / math.sqrt(12.5))
+
+
+def test_rope_position_zero_is_identity():
+    x = np.random.default_rng(1).normal(size=(5, 3, 32))
+    assert np.array_equal(O.rope(x, np.zeros((5, 1)), 1e6), x)
+
+
+def test_rope_rotate_half_closed_form():
+    theta = 100.0
+    p = 7.0
+    e = np.eye(4)
+    out = O.rope(e, np.full(4, p), theta)
+    w1 = theta ** -0.5
+    assert np.allclose(out[0], [math.cos(p), 0, math.sin(p), 0])
+    assert np.allclose(out[1], [0, math.cos(p * w1), 0, math.sin(p * w1)])
+    assert np.allclose(out[2], [-math.sin(p), 0, math.cos(p), 0])
+    assert np.allclose(out[3], [0, -math.sin(p * w1), 0, math.cos(p * w1)])
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    rng = np.random.default_rng(2)
+    q, k = rng.normal(size=64), rng.normal(size=64)
+    s1 = O.rope(q, 100, 1e4) @ O.rope(k, 37, 1e4)
+    s2 = O.rope(q, 1063, 1e4) @ O.rope(k, 1000, 1e4)
+    assert abs(s1 - s2) < 1e-9
+    assert abs(np.linalg.norm(O.rope(q, 12345, 1e6)) - np.linalg.norm(q)) < 1e-12
+
+
+# ----------------------------------------------------------------------------
+# attention
+
+
+def _attention_brute(q, k, v):
+    nq, d = q.shape[1], q.shape[2]
+    grp = nq // k.shape[1]
+    out = np.zeros_like(q)
+    for r in range(q.shape[0]):
+        for h in range(nq):
+            g = h // grp
+            sc = [sum(q[r, h, i] * k[j, g, i] for i in range(d)) / math.sqrt(d) for j in range(k.shape[0])]
+            m = max(sc)
+            wts = [math.exp(s - m) for s in sc]
+            tot = sum(wts)
+            for i in range(d):
+                out[r, h, i] = sum(wts[j] * v[j, g, i] for j in range(k.shape[0])) / tot
+    return out
+
+
+def test_attention_matches_brute_force():
+    rng = np.random.default_rng(3)
+    q = rng.normal(size=(16, 4, 8))
+    k = rng.normal(size=(21, 2, 8))
+    v = rng.normal(size=(21, 2, 8))
+    assert np.allclose(O.block_attention(q, k, v), _attention_brute(q, k, v), rtol=1e-12, atol=1e-12)
+
+
+def test_attention_equal_scores_average_values_per_group():
+    rng = np.random.default_rng(4)
+    q = np.zeros((16, 6, 8))  # all scores zero -> uniform weights
+    k = rng.normal(size=(9, 2, 8))
+    v = rng.normal(size=(9, 2, 8))
+    out = O.block_attention(q, k, v)
+    for h in range(6):
+        assert np.allclose(out[:, h, :], v[:, h // 3, :].mean(axis=0))
+
+
+def test_attention_is_not_causal():
+    # the last key is strongly preferred by every row, the first row included
+    q = np.ones((16, 1, 4)) * 5.0
+    k = np.zeros((20, 1, 4))
+    k[-1] = 10.0
+    v = np.zeros((20, 1, 4))
+    v[-1] = 1.0
+    out = O.block_attention(q, k, v)
+    assert np.all(out[0, 0] > 0.999)
+
+
+def test_visible_positions_enumerated():
+    assert list(O.visible_positions(O.SLIDING, 10, 4)) == [6, 7, 8, 9]
+    assert list(O.visible_positions(O.SLIDING, 3, 4)) == [0, 1, 2]
+    assert list(O.visible_positions(O.FULL, 10, 4)) == list(range(10))
+    assert list(O.visible_positions(O.SLIDING, 0, 4)) == []
+
+
+# ----------------------------------------------------------------------------
+# tap fusion
+
+
+def test_fusion_single_tap_identity_fc_is_rmsnorm():
+    rng = np.random.default_rng(5)
+    plane = O.round_bf16(rng.normal(size=(7, 16)))
+    got = O.fuse_taps([plane], np.eye(16), np.ones(16), 1e-6)
+    want = O.round_bf16(plane / np.sqrt((plane ** 2).mean(axis=1, keepdims=True) + 1e-6))
+    assert np.array_equal(got, want)
+
+
+def test_fusion_concatenates_tap_zero_first():
+    rng = np.random.default_rng(6)
+    a = O.round_bf16(rng.normal(size=(3, 8)))
+    b = O.round_bf16(rng.normal(size=(3, 8)))
+    pick0 = np.concatenate([np.eye(8), np.zeros((8, 8))], axis=1)
+    pick1 = np.concatenate([np.zeros((8, 8)), np.eye(8)], axis=1)
+    g = np.ones(8)
+    assert np.array_equal(O.fuse_taps([a, b], pick0, g, 0.0), O.fuse_taps([a], np.eye(8), g, 0.0))
+    assert np.array_equal(O.fuse_taps([a, b], pick1, g, 0.0), O.fuse_taps([b], np.eye(8), g, 0.0))
+
+
+def test_fused_rows_are_bf16():
+    m = _tiny_model()
+    w = _weights64(m)
+    planes = [O.to_f64(p) for p in SI.make_taps(m, 5, 3)]
+    f = O.fuse_taps(planes, w["fc"], w["hidden_norm"], m["rms_eps"])
+    assert np.array_equal(O.round_bf16(f), f)
+
+
+# ----------------------------------------------------------------------------
+# the block forward: structure pinned by special cases
+
+
+def test_block_with_zero_output_projections_reduces_to_lm_head_of_mask_embedding():
+    """With o_proj = down_proj = 0 both residual adds contribute nothing, so
+    the residual stays the embedding and every mask row's logits are the LM
+    head applied to the normed mask-token embedding."""
+    m = _tiny_model(n_layers=1, layer_kinds=[O.FULL])
+    w = _weights64(m)
+    for lw in w["layers"]:
+        lw["o_proj"][:] = 0.0
+        lw["down_proj"][:] = 0.0
+    C = 5
+    ctx_k = [np.zeros((C, m["n_kv_heads"], m["head_dim"]))]
+    ctx_v = [np.zeros((C, m["n_kv_heads"], m["head_dim"]))]
+    logits, X = O.draft_block(m, w, ctx_k, ctx_v, C, anchor=17)
+    e = w["embed"][m["mask_token"]]
+    z = O.round_bf16(e / np.sqrt((e ** 2).mean() + m["rms_eps"]) * w["norm"])
+    want = O.round_bf16(w["embed"] @ z)
+    assert logits.shape == (15, m["vocab"])
+    for r in range(15):
+        assert np.array_equal(logits[r], want)
+    assert np.array_equal(X[0], w["embed"][17])
+
+
+def test_block_attention_with_zero_queries_averages_the_window():
+    """q_proj = 0 makes every score zero, so the attention output of each
+    head is the mean of the values its kv head sees: the sliding window's
+    context rows (positions >= C - W) plus the sixteen block rows."""
+    m = _tiny_model(n_layers=1, layer_kinds=[O.SLIDING], sliding_window=5)
+    w = _weights64(m)
+    lw = w["layers"][0]
+    lw["q_proj"][:] = 0.0
+    lw["down_proj"][:] = 0.0
+    nkv, d, nq, H = m["n_kv_heads"], m["head_dim"], m["n_q_heads"], m["hidden"]
+    C = 12
+    rng = np.random.default_rng(9)
+    ctx_k = [O.round_bf16(rng.normal(size=(C, nkv, d)))]
+    ctx_v = [O.round_bf16(rng.normal(size=(C, nkv, d)))]
+    anchor = 33
+    _, X = O.draft_block(m, w, ctx_k, ctx_v, C, anchor)
+    tokens = [anchor] + [m["mask_token"]] * 15
+    X0 = w["embed"][tokens]
+    h = O.round_bf16(X0 / np.sqrt((X0 ** 2).mean(axis=1, keepdims=True) + m["rms_eps"]) * lw["input_layernorm"])
+    vb = O.round_bf16(h @ lw["v_proj"].T).reshape(16, nkv, d)
+    grp = nq // nkv
+
+    def expect(first):
+        vis = np.concatenate([ctx_v[0][first:], vb], axis=0)
+        mean = vis.mean(axis=0)  # [nkv, d]
+        att = np.stack([mean[hh // grp] for hh in range(nq)]).reshape(nq * d)
+        return X0 + O.round_bf16(att)[None, :] @ lw["o_proj"].T
+
+    # 5 window rows + 16 block rows; a bf16 flip of the averaged value moves
+    # X by a few 1e-5 at most, a wrong window by far more
+    err = np.abs(X - expect(C - 5)).max()
+    assert err < 1e-4
+    assert np.abs(X - expect(0)).max() > 20 * max(err, 1e-6)
+    assert np.abs(X - expect(C - 4)).max() > 20 * max(err, 1e-6)
+
+
+def test_sliding_window_wider_than_context_equals_full():
+    m_full = _tiny_model(layer_kinds=[O.FULL, O.FULL])
+    m_slide = _tiny_model(layer_kinds=[O.SLIDING, O.SLIDING], sliding_window=64)
+    w = _weights64(m_full)
+    rng = np.random.default_rng(10)
+    C = 40
+    ks = [O.round_bf16(rng.normal(size=(C, 4, 32))) for _ in range(2)]
+    vs = [O.round_bf16(rng.normal(size=(C, 4, 32))) for _ in range(2)]
+    a, _ = O.draft_block(m_full, w, ks, vs, C, 5)
+    b, _ = O.draft_block(m_slide, w, ks, vs, C, 5)
+    assert np.array_equal(a, b)
+    m_narrow = _tiny_model(layer_kinds=[O.SLIDING, O.SLIDING], sliding_window=8)
+    c, _ = O.draft_block(m_narrow, w, ks, vs, C, 5)
+    assert not np.array_equal(a, c)
+
+
+def test_context_order_does_not_matter():
+    """Non-causal attention over the context: permuting the context rows
+    (each keeps its own RoPE'd key) leaves the block's output unchanged."""
+    m = _tiny_model()
+    w = _weights64(m)
+    rng = np.random.default_rng(11)
+    C = 30
+    ks = [O.round_bf16(rng.normal(size=(C, 4, 32))) for _ in range(2)]
+    vs = [O.round_bf16(rng.normal(size=(C, 4, 32))) for _ in range(2)]
+    perm = rng.permutation(C)
+    _, Xa = O.draft_block(m, w, ks, vs, C, 5)
+    _, Xb = O.draft_block(m, w, [k[perm] for k in ks], [v[perm] for v in vs], C, 5)
+    assert np.allclose(Xa, Xb, rtol=1e-10, atol=1e-12)
+
+
+def test_streams_chunked_append_and_truncate_equal_fresh():
+    m = _tiny_model()
+    w = _weights64(m)
+    planes = [O.to_f64(p) for p in SI.make_taps(m, 40, 21)]
+    one = O.OracleStreams(m, w, 1)
+    one.append(0, planes)
+    two = O.OracleStreams(m, w, 1)
+    two.append(0, [p[:25] for p in planes])
+    two.append(0, [p[25:] for p in planes])
+    assert np.array_equal(one.fused[0], two.fused[0])
+    for l in range(m["n_layers"]):
+        assert np.array_equal(one.k[0][l], two.k[0][l])
+        assert np.array_equal(one.v[0][l], two.v[0][l])
+    two.truncate(0, 10)
+    two.append(0, [p[10:] for p in planes])
+    la, _ = one.draft(0, 9)
+    lb, _ = two.draft(0, 9)
+    assert np.array_equal(la, lb)
+
+
+# ----------------------------------------------------------------------------
+# candidates and verification
+
+
+def test_topk_matches_sorted_tuples_with_ties():
+    rng = np.random.default_rng(12)
+    row = rng.integers(-3, 4, size=300).astype(np.float64)
+    ids, vals = O.topk(row, 9)
+    want = sorted(range(300), key=lambda i: (-row[i], i))[:9]
+    assert list(ids) == want
+    assert list(vals) == [row[i] for i in want]
+
+
+def test_greedy_golden_cases():
+    with open(os.path.join(GOLDEN, "greedy_verify_cases.json")) as f:
+        spec = json.load(f)
+    for case in spec["cases"]:
+        V = case["vocab"]
+        tl = np.zeros((16, V))
+        for i, pk in enumerate(case["peaks"]):
+            for j in pk:
+                tl[i, j] = 2.0
+        a, toks = O.greedy_verify(case["draft"], tl)
+        assert a == case["expect_a"], case["name"]
+        assert toks == case["expect_tokens"], case["name"]
+
+
+def test_greedy_invariants_random():
+    rng = np.random.default_rng(13)
+    for _ in range(200):
+        V = 5
+        tl = rng.normal(size=(16, V))
+        d = rng.integers(0, V, 15)
+        a, toks = O.greedy_verify(d, tl)
+        assert 0 <= a <= 15
+        assert toks[a] == int(np.argmax(tl[a]))
+        assert all(toks[i] == d[i] == int(np.argmax(tl[i])) for i in range(a))
+        assert all(t == -1 for t in toks[a + 1:])
+
+
+def test_inverse_cdf_midpoint_grid_reproduces_weights():
+    wts = np.array([0.0, 3.0, 1.0, 0.0, 4.0])
+    n = 8000
+    counts = np.zeros(5)
+    for k in range(n):
+        j, _ = O.inverse_cdf(wts, (k + 0.5) / n)
+        counts[j] += 1
+    assert np.allclose(counts / n, wts / wts.sum(), atol=1.0 / n)
+    assert O.inverse_cdf(wts, 0.0)[0] == 1  # zero-weight entries are never drawn
+
+
+def test_sampling_rule_output_distribution_is_target():
+    """The first committed token's distribution equals p (losslessness).
+
+    Exact decomposition of the rule: the draft x ~ q is accepted with
+    probability min(1, p(x)/q(x)); otherwise the residual draw follows
+    max(p - q, 0) normalised. Acceptance and residual frequencies are
+    measured from the oracle on midpoint grids of the uniforms; combined,
+    they must give p within the grids' resolution."""
+    V = 6
+    T = 1.0
+    rng = np.random.default_rng(14)
+    tl = rng.normal(size=(16, V)) * 1.5
+    dl = rng.normal(size=(15, V)) * 1.5
+    p = np.exp(tl[0] - tl[0].max())
+    p /= p.sum()
+    q = np.exp(dl[0] - dl[0].max())
+    q /= q.sum()
+    n = 2000
+    grid = (np.arange(n) + 0.5) / n
+    acc = np.zeros(V)
+    for x in range(V):
+        d = np.full(15, x)
+        d[1:] = 0
+        hits = 0
+        for u in grid:
+            uni = np.zeros((16, 2))
+            uni[0, 0] = u
+            uni[1:, 0] = 0.999999  # later positions do not matter here
+            a, toks, _ = O.sampling_verify(d, tl, dl, uni, T)
+            hits += a >= 1
+        acc[x] = hits / n
+    assert np.allclose(acc, np.minimum(1.0, p / q), atol=1.5 / n)
+    # residual draw: force a rejection at position 0 with a draft x where q > p
+    x = int(np.argmax(q - p))
+    res = np.zeros(V)
+    for u in grid:
+        uni = np.full((16, 2), 0.5)
+        uni[0, 0] = 1.0 - 1e-12
+        uni[0, 1] = u
+        a, toks, _ = O.sampling_verify(np.full(15, x), tl, dl, uni, T)
+        assert a == 0
+        res[toks[0]] += 1
+    res /= n
+    r = np.maximum(p - q, 0)
+    assert np.allclose(res, r / r.sum(), atol=1.5 / n)
+    out = q * acc + (q * (1 - acc)).sum() * res
+    assert np.allclose(out, p, atol=4.0 / n)
+
+
+def test_sampling_rule_chi_square():
+    """Draw d_1 ~ q and run the rule many times; the first committed token
+    must follow p (chi-square at 1e-3 significance)."""
+    from scipy.stats import chisquare
+
+    V = 5
+    rng = np.random.default_rng(15)
+    tl = rng.normal(size=(16, V))
+    dl = rng.normal(size=(15, V))
+    p = np.exp(tl[0] - tl[0].max())
+    p /= p.sum()
+    n = 20000
+    counts = np.zeros(V)
+    for _ in range(n):
+        ud = rng.random(15)
+        d, _ = O.sample_rows(dl, 1.0, ud)
+        a, toks, _ = O.sampling_verify(d, tl, dl, rng.random((16, 2)), 1.0)
+        counts[toks[0]] += 1
+    stat = chisquare(counts, p * n)
+    assert stat.pvalue > 1e-3
+
+
+def test_sampling_all_accepted_draws_bonus_from_last_row():
+    V = 4
+    tl = np.zeros((16, V))
+    dl = np.zeros((15, V))  # p == q everywhere: every test accepts
+    tl[15] = [0.0, 0.0, 50.0, 0.0]
+    d = np.arange(15) % V
+    a, toks, _ = O.sampling_verify(d, tl, dl, np.full((16, 2), 0.5), 1.0)
+    assert a == 15 and toks[:15] == list(d) and toks[15] == 2
+
+
+def test_temperature_scales_logits():
+    row = np.array([0.0, 1.0, 2.0])
+    assert np.allclose(O.softmax_t(row, 2.0), O.softmax_t(row / 2.0, 1.0))
+    assert O.softmax_t(row, 0.01)[2] > 0.999
+
+
+# ----------------------------------------------------------------------------
+# constants, inventory and refusals printed on the pages
+
+
+def test_page_constants():
+    with open(os.path.join(GOLDEN, "page_constants.json")) as f:
+        c = json.load(f)
+    H = c["hidden_9b"]
+    assert O.fused_row_bytes(H) == c["fused_row_bytes_at_4096"]
+    assert O.raw_plane_bytes(c["taps_v1"], H) == c["raw_tap_bytes_at_4096_eight_taps"]
+    assert O.tap_row_bytes(1, c["taps_v1"], H) == c["tap_row_bytes_v1_eight_taps_factor"] * H * 2
+    assert O.tap_row_bytes(2, c["taps_dflash2"], H) == O.raw_plane_bytes(5, H)
+    assert O.drafter_tensor_count(c["layers_9b_drafter"]) == c["tensor_names_9b_drafter"]
+    assert O.BLOCK == c["block"] and O.BLOCK - 1 == c["mask_rows"]
+    assert O.kind_name(1) == c["kind_v1"] and O.kind_name(2) == c["kind_dflash2"]
+    m = SI.presets()["9b"]["model"]
+    assert len(SI.weight_names(m)) == c["tensor_names_9b_drafter"]
+    assert m["n_taps"] == c["taps_v1"]
+    d2 = SI.presets()["dflash2geom"]["model"]
+    assert d2["tap_layers"] == c["dflash2_tap_layers"]
+    assert d2["sliding_window"] == c["dflash2_sliding_window"]
+
+
+def test_refusals():
+    m = SI.presets()["9b"]["model"]
+    assert O.validate_config(m) is None
+    bad = dict(m, tap_layers=[1, 5, 9, 13, 17, 21, 25, 32])
+    assert O.validate_config(bad) == "taps past the target"
+    bad = dict(m, tap_layers=[1, 5, 9, 13, 17, 21, 25, 25])
+    assert O.validate_config(bad) == "taps repeated"
+    bad = dict(m, causal=1)
+    assert O.validate_config(bad) == "causal"
+    for name in SI.presets():
+        assert O.validate_config(SI.presets()[name]["model"]) is None
