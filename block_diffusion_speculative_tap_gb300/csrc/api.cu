@@ -1,0 +1,846 @@
+// Host side of libdflash: argument validation, state and workspace layout,
+// and the launch sequence of each entry point. See include/dflash.h for the
+// contract of every function.
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+#include <atomic>
+#include <new>
+#include <vector>
+
+#include "internal.h"
+
+namespace dfl {
+
+static std::atomic<long long> g_launches{0};
+void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? DFLASH_OK : DFLASH_E_CUDA; }
+
+// Bump allocator over caller-owned memory; with base == nullptr it only sizes.
+struct Carver {
+  char* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<char*>(b)) {}
+  template <class T>
+  T* take(size_t count) {
+    off = (off + 255) & ~size_t(255);
+    T* r = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return r;
+  }
+};
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace dfl
+
+using namespace dfl;
+
+struct LayerMaps {
+  CUtensorMap q, k, v, o, gate, up, down;
+};
+
+struct dflash_handle {
+  dflash_config cfg;
+  int device = 0;
+  int num_sms = 0;
+  const __nv_bfloat16* fc = nullptr;
+  const __nv_bfloat16* hidden_norm = nullptr;
+  const __nv_bfloat16* norm = nullptr;
+  const __nv_bfloat16* embed = nullptr;
+  std::vector<dflash_layer_weights> layers;
+  CUtensorMap fc_map, embed_map;
+  std::vector<LayerMaps> maps;
+};
+
+struct dflash_state {
+  dflash_handle* h = nullptr;
+  int S = 0;
+  int R = 0;
+  int* lens = nullptr;
+  int* status = nullptr;
+  float2* rope = nullptr;
+  __nv_bfloat16* ring = nullptr;
+  std::vector<__nv_bfloat16*> kc, vc;
+  std::vector<int> cap, window;
+  std::vector<int64_t> host_len;
+};
+
+namespace {
+
+constexpr int kFusePass = 4096;       // rows per fc / inject pass of a fill
+constexpr int kDecodeRegimeN = 1024;  // up to this many tokens a GEMM uses the fixed split-K
+
+int head_threads_ok(int d) { return d == 32 || d == 64 || d == 128; }
+
+int ksplit_for(const dflash_handle* h, int rows_m, int K, int N) {
+  if (N > kDecodeRegimeN) return 1;
+  return gemm_choose_ksplit(rows_m / kTileM, K / kTileK, h->num_sms);
+}
+
+int attn_chunk(int cap) { return cap <= 8192 ? 256 : 512; }
+
+int layer_cap(const dflash_config& c, int l, int R) {
+  return c.layer_kind[l] == DFLASH_LAYER_SLIDING ? std::min(c.sliding_window, R) : R;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dflash_strerror(int code) {
+  switch (code) {
+    case DFLASH_OK: return "ok";
+    case DFLASH_E_INVALID_ARG: return "invalid argument";
+    case DFLASH_E_TAPS_RANGE: return "tap count or tap layer out of range";
+    case DFLASH_E_TAPS_REPEATED: return "a target layer is tapped twice";
+    case DFLASH_E_CAUSAL: return "a causal draft is refused";
+    case DFLASH_E_SHAPE: return "unsupported shape";
+    case DFLASH_E_CAPACITY: return "position past the ring capacity";
+    case DFLASH_E_WORKSPACE: return "workspace or state memory too small or misaligned";
+    case DFLASH_E_CUDA: return "CUDA error";
+    case DFLASH_E_TIMEOUT: return "a device-side wait timed out";
+    case DFLASH_E_DEVICE_FAULT: return "the device flagged bad input";
+    case DFLASH_E_UNSUPPORTED: return "unsupported device or driver";
+    default: return "unknown status";
+  }
+}
+
+int64_t dflash_launch_count(void) { return g_launches.load(); }
+
+int dflash_config_validate(const dflash_config* c) {
+  if (!c) return DFLASH_E_INVALID_ARG;
+  if (c->n_taps < 1 || c->n_taps > DFLASH_MAX_TAPS) return DFLASH_E_TAPS_RANGE;
+  for (int i = 0; i < c->n_taps; ++i) {
+    if (c->tap_layers[i] < 0 || c->tap_layers[i] >= c->target_layers) return DFLASH_E_TAPS_RANGE;
+    for (int j = 0; j < i; ++j)
+      if (c->tap_layers[j] == c->tap_layers[i]) return DFLASH_E_TAPS_REPEATED;
+  }
+  if (c->causal != 0) return DFLASH_E_CAUSAL;
+  if (c->variant != DFLASH_VARIANT_V1 && c->variant != DFLASH_VARIANT_2) return DFLASH_E_SHAPE;
+  if (c->block != DFLASH_BLOCK) return DFLASH_E_SHAPE;
+  if (c->n_layers < 1 || c->n_layers > DFLASH_MAX_LAYERS) return DFLASH_E_SHAPE;
+  if (c->n_q_heads < 1 || c->n_kv_heads < 1 || c->n_q_heads % c->n_kv_heads) return DFLASH_E_SHAPE;
+  if (c->n_q_heads / c->n_kv_heads > 8) return DFLASH_E_SHAPE;
+  if (!head_threads_ok(c->head_dim)) return DFLASH_E_SHAPE;
+  if (c->hidden != c->n_q_heads * c->head_dim) return DFLASH_E_SHAPE;
+  if (c->hidden % 128 || c->ffn < 128 || c->ffn % 128 || (c->n_kv_heads * c->head_dim) % 128) return DFLASH_E_SHAPE;
+  if (c->vocab < 128 || c->vocab % 128) return DFLASH_E_SHAPE;
+  if (c->mask_token < 0 || c->mask_token >= c->vocab) return DFLASH_E_SHAPE;
+  if (!(c->rope_theta > 0.f) || !(c->rms_eps >= 0.f)) return DFLASH_E_SHAPE;
+  for (int l = 0; l < c->n_layers; ++l) {
+    if (c->layer_kind[l] != DFLASH_LAYER_FULL && c->layer_kind[l] != DFLASH_LAYER_SLIDING) return DFLASH_E_SHAPE;
+    if (c->layer_kind[l] == DFLASH_LAYER_SLIDING && c->sliding_window <= 0) return DFLASH_E_SHAPE;
+  }
+  return DFLASH_OK;
+}
+
+const char* dflash_kind(const dflash_config* c) {
+  if (!c) return nullptr;
+  return c->variant == DFLASH_VARIANT_V1 ? "DFlash" : "DFlash2";
+}
+
+int64_t dflash_tap_row_bytes(const dflash_config* c) {
+  if (!c) return -1;
+  const int64_t H = c->hidden, N = c->n_taps;
+  return c->variant == DFLASH_VARIANT_V1 ? (2 * N + 2) * H * 2 : N * H * 2;
+}
+
+int64_t dflash_fused_row_bytes(const dflash_config* c) {
+  if (!c) return -1;
+  return static_cast<int64_t>(c->hidden) * 2;
+}
+
+// ---------------------------------------------------------------- handle
+int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_handle** out) {
+  if (!cfg || !w || !out) return DFLASH_E_INVALID_ARG;
+  *out = nullptr;
+  int rc = dflash_config_validate(cfg);
+  if (rc) return rc;
+  const void* ptrs[] = {w->fc, w->hidden_norm, w->norm, w->embed};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return DFLASH_E_INVALID_ARG;
+  if (!w->layers) return DFLASH_E_INVALID_ARG;
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    const dflash_layer_weights& L = w->layers[l];
+    const void* lp[] = {L.input_norm, L.q_proj, L.k_proj, L.v_proj, L.o_proj, L.q_norm,
+                        L.k_norm,     L.post_norm, L.gate_proj, L.up_proj, L.down_proj};
+    for (const void* p : lp)
+      if (!p || !aligned16(p)) return DFLASH_E_INVALID_ARG;
+  }
+  int dev = 0, major = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DFLASH_E_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return DFLASH_E_CUDA;
+  if (major != 10) return DFLASH_E_UNSUPPORTED;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DFLASH_E_CUDA;
+
+  dflash_handle* h = new (std::nothrow) dflash_handle();
+  if (!h) return DFLASH_E_INVALID_ARG;
+  h->cfg = *cfg;
+  h->device = dev;
+  h->num_sms = sms;
+  h->fc = static_cast<const __nv_bfloat16*>(w->fc);
+  h->hidden_norm = static_cast<const __nv_bfloat16*>(w->hidden_norm);
+  h->norm = static_cast<const __nv_bfloat16*>(w->norm);
+  h->embed = static_cast<const __nv_bfloat16*>(w->embed);
+  h->layers.assign(w->layers, w->layers + cfg->n_layers);
+  const int64_t H = cfg->hidden, N = cfg->n_taps, d = cfg->head_dim, F = cfg->ffn, V = cfg->vocab;
+  const int64_t qd = cfg->n_q_heads * d, kvd = cfg->n_kv_heads * d;
+  rc = encode_kmajor_map(&h->fc_map, w->fc, H, N * H, N * H, kTileM);
+  if (!rc) rc = encode_kmajor_map(&h->embed_map, w->embed, V, H, H, kTileM);
+  h->maps.resize(cfg->n_layers);
+  for (int l = 0; l < cfg->n_layers && !rc; ++l) {
+    const dflash_layer_weights& L = w->layers[l];
+    LayerMaps& m = h->maps[l];
+    rc = encode_kmajor_map(&m.q, L.q_proj, qd, H, H, kTileM);
+    if (!rc) rc = encode_kmajor_map(&m.k, L.k_proj, kvd, H, H, kTileM);
+    if (!rc) rc = encode_kmajor_map(&m.v, L.v_proj, kvd, H, H, kTileM);
+    if (!rc) rc = encode_kmajor_map(&m.o, L.o_proj, H, qd, qd, kTileM);
+    if (!rc) rc = encode_kmajor_map(&m.gate, L.gate_proj, F, H, H, kTileM);
+    if (!rc) rc = encode_kmajor_map(&m.up, L.up_proj, F, H, H, kTileM);
+    if (!rc) rc = encode_kmajor_map(&m.down, L.down_proj, H, F, F, kTileM);
+  }
+  if (rc) {
+    delete h;
+    return rc;
+  }
+  *out = h;
+  return DFLASH_OK;
+}
+
+int dflash_destroy(dflash_handle* h) {
+  delete h;
+  return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------- state
+static size_t state_layout(const dflash_handle* h, int S, int R, void* base, dflash_state* st) {
+  const dflash_config& c = h->cfg;
+  Carver cv(base);
+  int* lens = cv.take<int>(S);
+  int* status = cv.take<int>(4);
+  float2* rope = cv.take<float2>(static_cast<size_t>(R + DFLASH_BLOCK) * (c.head_dim / 2));
+  __nv_bfloat16* ring = cv.take<__nv_bfloat16>(static_cast<size_t>(S) * R * c.hidden);
+  if (st) {
+    st->lens = lens;
+    st->status = status;
+    st->rope = rope;
+    st->ring = ring;
+    st->kc.assign(c.n_layers, nullptr);
+    st->vc.assign(c.n_layers, nullptr);
+    st->cap.assign(c.n_layers, 0);
+    st->window.assign(c.n_layers, 0);
+  }
+  for (int l = 0; l < c.n_layers; ++l) {
+    const int cap = layer_cap(c, l, R);
+    const size_t n = static_cast<size_t>(S) * c.n_kv_heads * cap * c.head_dim;
+    __nv_bfloat16* k = cv.take<__nv_bfloat16>(n);
+    __nv_bfloat16* v = cv.take<__nv_bfloat16>(n);
+    if (st) {
+      st->kc[l] = k;
+      st->vc[l] = v;
+      st->cap[l] = cap;
+      st->window[l] = c.layer_kind[l] == DFLASH_LAYER_SLIDING ? cap : 0;
+    }
+  }
+  return cv.off;
+}
+
+int dflash_state_bytes(const dflash_handle* h, int streams, int ring_capacity, size_t* bytes) {
+  if (!h || !bytes || streams < 1 || ring_capacity < 1) return DFLASH_E_INVALID_ARG;
+  *bytes = state_layout(h, streams, ring_capacity, nullptr, nullptr);
+  return DFLASH_OK;
+}
+
+int dflash_state_init(dflash_handle* h, void* dev_mem, size_t bytes, int streams, int ring_capacity,
+                      dflash_stream_t stream, dflash_state** out) {
+  if (!h || !dev_mem || !out || streams < 1 || ring_capacity < 1) return DFLASH_E_INVALID_ARG;
+  *out = nullptr;
+  if ((reinterpret_cast<uintptr_t>(dev_mem) & 255u) != 0) return DFLASH_E_WORKSPACE;
+  if (state_layout(h, streams, ring_capacity, nullptr, nullptr) > bytes) return DFLASH_E_WORKSPACE;
+  dflash_state* st = new (std::nothrow) dflash_state();
+  if (!st) return DFLASH_E_INVALID_ARG;
+  st->h = h;
+  st->S = streams;
+  st->R = ring_capacity;
+  state_layout(h, streams, ring_capacity, dev_mem, st);
+  st->host_len.assign(streams, 0);
+  // RoPE table: angle pos * theta^(-2i/d), evaluated in double precision
+  const int d = h->cfg.head_dim, half = d / 2;
+  const size_t npos = static_cast<size_t>(ring_capacity) + DFLASH_BLOCK;
+  std::vector<float2> tab(npos * half);
+  std::vector<double> inv(half);
+  for (int i = 0; i < half; ++i) inv[i] = pow(static_cast<double>(h->cfg.rope_theta), -2.0 * i / d);
+  for (size_t p = 0; p < npos; ++p)
+    for (int i = 0; i < half; ++i) {
+      const double a = static_cast<double>(p) * inv[i];
+      tab[p * half + i] = make_float2(static_cast<float>(cos(a)), static_cast<float>(sin(a)));
+    }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(st->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(st->lens, 0, sizeof(int) * streams, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(st->status, 0, sizeof(int) * 4, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);  // the host table goes out of scope
+  if (e != cudaSuccess) {
+    delete st;
+    return DFLASH_E_CUDA;
+  }
+  *out = st;
+  return DFLASH_OK;
+}
+
+int dflash_state_free(dflash_state* st) {
+  delete st;
+  return DFLASH_OK;
+}
+
+int dflash_state_length(const dflash_state* st, int s, int64_t* len) {
+  if (!st || !len || s < 0 || s >= st->S) return DFLASH_E_INVALID_ARG;
+  *len = st->host_len[s];
+  return DFLASH_OK;
+}
+
+int dflash_state_ring(const dflash_state* st, void** ring) {
+  if (!st || !ring) return DFLASH_E_INVALID_ARG;
+  *ring = st->ring;
+  return DFLASH_OK;
+}
+
+int dflash_state_cache(const dflash_state* st, int layer, void** k, void** v, int* cap) {
+  if (!st || !k || !v || !cap || layer < 0 || layer >= static_cast<int>(st->kc.size())) return DFLASH_E_INVALID_ARG;
+  *k = st->kc[layer];
+  *v = st->vc[layer];
+  *cap = st->cap[layer];
+  return DFLASH_OK;
+}
+
+int dflash_device_status(dflash_state* st, dflash_stream_t stream, int32_t* out) {
+  if (!st || !out) return DFLASH_E_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, st->status, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(st->status, 0, sizeof(int), s);
+  if (e != cudaSuccess) return DFLASH_E_CUDA;
+  *out = v;
+  if (v & DFLASH_STATUS_TIMEOUT) return DFLASH_E_TIMEOUT;
+  if (v) return DFLASH_E_DEVICE_FAULT;
+  return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------- fusion
+namespace {
+
+struct FuseWs {
+  int* counters;
+  int* row_stream;
+  int* row_pos;
+  float* y;
+  __nv_bfloat16* fused;
+  float* partial;
+  size_t bytes;
+};
+
+// GEMM plans of one fill pass of `rows` rows (fc, and K/V injection of the
+// layers in [l0, l1)).
+GemmPlan fc_plan(const dflash_handle* h, int rows) {
+  const dflash_config& c = h->cfg;
+  GemmPlan p;
+  p.n_aseg = 1;
+  p.a_maps[0] = &h->fc_map;
+  p.a_rows[0] = c.hidden;
+  p.n_b = c.n_taps;
+  p.Kp = c.hidden;
+  p.M = c.hidden;
+  p.N = rows;
+  p.K = c.n_taps * c.hidden;
+  p.ksplit = ksplit_for(h, p.M, p.K, rows);
+  p.epi = EPI_STORE_F32;
+  p.epi_args.ldo = c.hidden;
+  return p;
+}
+
+GemmPlan kv_plan(const dflash_handle* h, const dflash_state* st, int rows, int l0, int l1, bool sliding_only) {
+  const dflash_config& c = h->cfg;
+  GemmPlan p;
+  const int kvd = c.n_kv_heads * c.head_dim;
+  int n = 0;
+  for (int l = l0; l < l1; ++l) {
+    if (sliding_only && c.layer_kind[l] != DFLASH_LAYER_SLIDING) continue;
+    for (int kv = 0; kv < 2; ++kv) {
+      p.a_maps[n] = kv == 0 ? &h->maps[l].k : &h->maps[l].v;
+      p.a_rows[n] = kvd;
+      HeadSeg& sg = p.epi_args.seg[n];
+      sg.kind = kv == 0 ? HEAD_K : HEAD_V;
+      sg.heads = c.n_kv_heads;
+      sg.cap = st ? st->cap[l] : 0;
+      sg.window = st ? st->window[l] : 0;
+      sg.gain = kv == 0 ? static_cast<const __nv_bfloat16*>(h->layers[l].k_norm) : nullptr;
+      sg.dst = st ? (kv == 0 ? st->kc[l] : st->vc[l]) : nullptr;
+      ++n;
+    }
+  }
+  p.n_aseg = n;
+  p.n_b = 1;
+  p.Kp = c.hidden;
+  p.M = n * kvd;
+  p.N = rows;
+  p.K = c.hidden;
+  p.ksplit = ksplit_for(h, p.M, p.K, rows);
+  p.epi = EPI_HEADS;
+  p.epi_args.head_dim = c.head_dim;
+  p.epi_args.eps = c.rms_eps;
+  p.epi_args.pos_mode = 1;
+  return p;
+}
+
+int layers_per_kv_pass() { return kMaxASeg / 2; }
+
+size_t fuse_ws_layout(const dflash_handle* h, int rows, void* base, FuseWs* ws) {
+  const dflash_config& c = h->cfg;
+  const int pass = std::min(std::max(rows, 1), kFusePass);
+  size_t counters = gemm_counter_count(fc_plan(h, pass));
+  size_t partial = gemm_partial_bytes(fc_plan(h, pass));
+  for (int l0 = 0; l0 < c.n_layers; l0 += layers_per_kv_pass()) {
+    const GemmPlan kp = kv_plan(h, nullptr, pass, l0, std::min(c.n_layers, l0 + layers_per_kv_pass()), false);
+    counters += gemm_counter_count(kp);
+    partial = std::max(partial, gemm_partial_bytes(kp));
+  }
+  Carver cv(base);
+  FuseWs w{};
+  w.counters = cv.take<int>(counters * ((rows + pass - 1) / pass + 1));
+  w.row_stream = cv.take<int>(std::max(rows, 1));
+  w.row_pos = cv.take<int>(std::max(rows, 1));
+  w.y = cv.take<float>(static_cast<size_t>(pass) * c.hidden);
+  w.fused = cv.take<__nv_bfloat16>(static_cast<size_t>(pass) * c.hidden);
+  w.partial = cv.take<float>(partial / sizeof(float) + 1);
+  w.bytes = cv.off;
+  if (ws) *ws = w;
+  return cv.off;
+}
+
+// K/V injection for `rows` fused rows already in `fused` (rows tables in ws).
+int inject_kv(dflash_handle* h, dflash_state* st, const __nv_bfloat16* fused, const int* row_stream,
+              const int* row_pos, int rows, bool sliding_only, int*& counters, float* partial, cudaStream_t s) {
+  const dflash_config& c = h->cfg;
+  for (int l0 = 0; l0 < c.n_layers; l0 += layers_per_kv_pass()) {
+    GemmPlan kp = kv_plan(h, st, rows, l0, std::min(c.n_layers, l0 + layers_per_kv_pass()), sliding_only);
+    if (kp.n_aseg == 0) continue;
+    kp.b_ptr[0] = fused;
+    kp.ldb = c.hidden;
+    kp.epi_args.row_stream = row_stream;
+    kp.epi_args.row_pos = row_pos;
+    kp.epi_args.rope = st->rope;
+    const int rc = gemm_launch(kp, partial, counters, st->status, h->num_sms, s);
+    if (rc) return rc;
+    counters += gemm_counter_count(kp);
+  }
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+int dflash_fuse_workspace_bytes(const dflash_handle* h, int rows, size_t* bytes) {
+  if (!h || !bytes || rows < 0) return DFLASH_E_INVALID_ARG;
+  *bytes = fuse_ws_layout(h, rows, nullptr, nullptr);
+  return DFLASH_OK;
+}
+
+int dflash_fuse_taps(dflash_handle* h, dflash_state* st, const void* const* planes, int64_t plane_row_stride,
+                     int nseg, const int32_t* seg_stream, const int64_t* seg_start, const int32_t* seg_rows,
+                     int flags, void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  if (!h || !st || !planes || !seg_stream || !seg_start || !seg_rows || !ws) return DFLASH_E_INVALID_ARG;
+  if (st->h != h || nseg < 1 || nseg > 256 || (flags & ~DFLASH_FUSE_INJECT_KV)) return DFLASH_E_INVALID_ARG;
+  const dflash_config& c = h->cfg;
+  if (plane_row_stride < c.hidden || (plane_row_stride * 2) % 16) return DFLASH_E_SHAPE;
+  for (int i = 0; i < c.n_taps; ++i)
+    if (!planes[i] || !aligned16(planes[i])) return DFLASH_E_INVALID_ARG;
+  int rows = 0;
+  std::vector<int> seen(st->S, 0);
+  std::vector<int> packed(3 * nseg);
+  for (int i = 0; i < nseg; ++i) {
+    const int s = seg_stream[i];
+    if (s < 0 || s >= st->S || seen[s] || seg_rows[i] < 1) return DFLASH_E_INVALID_ARG;
+    seen[s] = 1;
+    if (seg_start[i] != st->host_len[s]) return DFLASH_E_INVALID_ARG;  // append only
+    if (seg_start[i] + seg_rows[i] > st->R) return DFLASH_E_CAPACITY;
+    packed[3 * i] = s;
+    packed[3 * i + 1] = static_cast<int>(seg_start[i]);
+    packed[3 * i + 2] = seg_rows[i];
+    rows += seg_rows[i];
+  }
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return DFLASH_E_WORKSPACE;
+  FuseWs w{};
+  if (fuse_ws_layout(h, rows, ws, &w) > ws_bytes) return DFLASH_E_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool inject = (flags & DFLASH_FUSE_INJECT_KV) != 0;
+
+  int rc = launch_prep_rows(w.row_stream, w.row_pos, nullptr, nullptr, nseg, rows, packed.data(), s);
+  if (rc) return rc;
+  // zero every split-K counter of this call at once
+  const size_t counters_bytes = reinterpret_cast<char*>(w.row_stream) - reinterpret_cast<char*>(w.counters);
+  if (cudaMemsetAsync(w.counters, 0, counters_bytes, s) != cudaSuccess) return DFLASH_E_CUDA;
+  int* counters = w.counters;
+  for (int r0 = 0; r0 < rows; r0 += kFusePass) {
+    const int n = std::min(kFusePass, rows - r0);
+    GemmPlan fp = fc_plan(h, n);
+    for (int i = 0; i < c.n_taps; ++i)
+      fp.b_ptr[i] = static_cast<const __nv_bfloat16*>(planes[i]) + static_cast<int64_t>(r0) * plane_row_stride;
+    fp.ldb = plane_row_stride;
+    fp.epi_args.out = w.y;
+    rc = gemm_launch(fp, w.partial, counters, st->status, h->num_sms, s);
+    if (rc) return rc;
+    counters += gemm_counter_count(fp);
+    rc = launch_hidden_norm(st->ring, w.fused, w.y, h->hidden_norm, w.row_stream + r0, w.row_pos + r0, n, c.hidden,
+                            st->R, c.rms_eps, s);
+    if (rc) return rc;
+    if (inject) {
+      rc = inject_kv(h, st, w.fused, w.row_stream + r0, w.row_pos + r0, n, false, counters, w.partial, s);
+      if (rc) return rc;
+    }
+  }
+  if (inject) {
+    rc = launch_prep_rows(nullptr, nullptr, st->lens, nullptr, nseg, 0, packed.data(), s);
+    if (rc) return rc;
+    for (int i = 0; i < nseg; ++i) st->host_len[seg_stream[i]] = seg_start[i] + seg_rows[i];
+  }
+  return DFLASH_OK;
+}
+
+int dflash_state_truncate(dflash_handle* h, dflash_state* st, int s_id, int64_t new_len, void* ws, size_t ws_bytes,
+                          dflash_stream_t stream) {
+  if (!h || !st || st->h != h || s_id < 0 || s_id >= st->S) return DFLASH_E_INVALID_ARG;
+  const int64_t old_len = st->host_len[s_id];
+  if (new_len < 0 || new_len > old_len) return DFLASH_E_INVALID_ARG;
+  const dflash_config& c = h->cfg;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // sliding caches: positions [new_len - W, old_len - W) were overwritten by
+  // the dropped rows (same ring slots) and are rebuilt from the fused ring
+  bool any_sliding = false;
+  for (int l = 0; l < c.n_layers; ++l) any_sliding |= c.layer_kind[l] == DFLASH_LAYER_SLIDING;
+  const int64_t W = std::min<int64_t>(c.sliding_window, st->R);
+  const int64_t lo = std::max<int64_t>(0, new_len - W);
+  const int64_t hi = std::min<int64_t>(new_len, old_len - W);
+  int packed[3] = {s_id, static_cast<int>(new_len), 0};
+  if (any_sliding && hi > lo) {
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return DFLASH_E_WORKSPACE;
+    const int n = static_cast<int>(hi - lo);
+    FuseWs w{};
+    if (fuse_ws_layout(h, n, ws, &w) > ws_bytes) return DFLASH_E_WORKSPACE;
+    const size_t counters_bytes = reinterpret_cast<char*>(w.row_stream) - reinterpret_cast<char*>(w.counters);
+    if (cudaMemsetAsync(w.counters, 0, counters_bytes, s) != cudaSuccess) return DFLASH_E_CUDA;
+    int seg[3] = {s_id, static_cast<int>(lo), n};
+    int rc = launch_prep_rows(w.row_stream, w.row_pos, nullptr, nullptr, 1, n, seg, s);
+    if (rc) return rc;
+    int* counters = w.counters;
+    for (int r0 = 0; r0 < n; r0 += kFusePass) {
+      const int m = std::min(kFusePass, n - r0);
+      const __nv_bfloat16* rows = st->ring + (static_cast<int64_t>(s_id) * st->R + lo + r0) * c.hidden;
+      rc = inject_kv(h, st, rows, w.row_stream + r0, w.row_pos + r0, m, true, counters, w.partial, s);
+      if (rc) return rc;
+    }
+  }
+  const int rc = launch_prep_rows(nullptr, nullptr, st->lens, nullptr, 1, 0, packed, s);
+  if (rc) return rc;
+  st->host_len[s_id] = new_len;
+  return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------- drafting
+namespace {
+
+struct DraftWs {
+  int* counters;
+  size_t n_counters;
+  float* X;
+  __nv_bfloat16* hbuf;
+  __nv_bfloat16* Q;
+  __nv_bfloat16* Kb;
+  __nv_bfloat16* Vb;
+  __nv_bfloat16* attn;
+  __nv_bfloat16* mid;
+  float* part_o;
+  float* part_ml;
+  float* partial;
+  __nv_bfloat16* logits;
+};
+
+int max_nchunk(const dflash_state* st) {
+  int m = 1;
+  for (size_t l = 0; l < st->cap.size(); ++l) m = std::max(m, (st->cap[l] + attn_chunk(st->cap[l]) - 1) / attn_chunk(st->cap[l]));
+  return m;
+}
+
+void layer_plans(const dflash_handle* h, int l, int T, GemmPlan& qkv, GemmPlan& o, GemmPlan& gu, GemmPlan& dn) {
+  const dflash_config& c = h->cfg;
+  const int qd = c.n_q_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim;
+  const LayerMaps& m = h->maps[l];
+  qkv = GemmPlan();
+  qkv.n_aseg = 3;
+  qkv.a_maps[0] = &m.q;
+  qkv.a_maps[1] = &m.k;
+  qkv.a_maps[2] = &m.v;
+  qkv.a_rows[0] = qd;
+  qkv.a_rows[1] = kvd;
+  qkv.a_rows[2] = kvd;
+  qkv.n_b = 1;
+  qkv.Kp = c.hidden;
+  qkv.M = qd + 2 * kvd;
+  qkv.N = T;
+  qkv.K = c.hidden;
+  qkv.ksplit = ksplit_for(h, qkv.M, qkv.K, T);
+  qkv.epi = EPI_HEADS;
+  o = GemmPlan();
+  o.n_aseg = 1;
+  o.a_maps[0] = &m.o;
+  o.a_rows[0] = c.hidden;
+  o.n_b = 1;
+  o.Kp = qd;
+  o.M = c.hidden;
+  o.N = T;
+  o.K = qd;
+  o.ksplit = ksplit_for(h, o.M, o.K, T);
+  o.epi = EPI_RESID;
+  gu = GemmPlan();
+  gu.n_aseg = 1;
+  gu.a_maps[0] = &m.gate;
+  gu.a_rows[0] = c.ffn;
+  gu.a2_map = &m.up;
+  gu.n_b = 1;
+  gu.Kp = c.hidden;
+  gu.M = c.ffn;
+  gu.N = T;
+  gu.K = c.hidden;
+  gu.ksplit = ksplit_for(h, gu.M, gu.K, T);
+  gu.epi = EPI_SWIGLU;
+  dn = GemmPlan();
+  dn.n_aseg = 1;
+  dn.a_maps[0] = &m.down;
+  dn.a_rows[0] = c.hidden;
+  dn.n_b = 1;
+  dn.Kp = c.ffn;
+  dn.M = c.hidden;
+  dn.N = T;
+  dn.K = c.ffn;
+  dn.ksplit = ksplit_for(h, dn.M, dn.K, T);
+  dn.epi = EPI_RESID;
+}
+
+GemmPlan lm_plan(const dflash_handle* h, int rows) {
+  const dflash_config& c = h->cfg;
+  GemmPlan p;
+  p.n_aseg = 1;
+  p.a_maps[0] = &h->embed_map;
+  p.a_rows[0] = c.vocab;
+  p.n_b = 1;
+  p.Kp = c.hidden;
+  p.M = c.vocab;
+  p.N = rows;
+  p.K = c.hidden;
+  p.ksplit = ksplit_for(h, p.M, p.K, rows);
+  p.epi = EPI_STORE_BF16;
+  p.epi_args.ldo = c.vocab;
+  return p;
+}
+
+size_t draft_ws_layout(const dflash_handle* h, const dflash_state* st, int S, bool need_logits, void* base,
+                       DraftWs* out) {
+  const dflash_config& c = h->cfg;
+  const int T = S * DFLASH_BLOCK;
+  const int qd = c.n_q_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim;
+  size_t counters = 0, partial = 0;
+  for (int l = 0; l < c.n_layers; ++l) {
+    GemmPlan a, b, g, d;
+    layer_plans(h, l, T, a, b, g, d);
+    for (const GemmPlan* p : {&a, &b, &g, &d}) {
+      counters += gemm_counter_count(*p);
+      partial = std::max(partial, gemm_partial_bytes(*p));
+    }
+  }
+  const GemmPlan lp = lm_plan(h, S * (DFLASH_BLOCK - 1));
+  counters += gemm_counter_count(lp);
+  partial = std::max(partial, gemm_partial_bytes(lp));
+  const int nch = max_nchunk(st);
+  Carver cv(base);
+  DraftWs w{};
+  w.counters = cv.take<int>(counters);
+  w.n_counters = counters;
+  w.X = cv.take<float>(static_cast<size_t>(T) * c.hidden);
+  w.hbuf = cv.take<__nv_bfloat16>(static_cast<size_t>(T) * c.hidden);
+  w.Q = cv.take<__nv_bfloat16>(static_cast<size_t>(T) * qd);
+  w.Kb = cv.take<__nv_bfloat16>(static_cast<size_t>(T) * kvd);
+  w.Vb = cv.take<__nv_bfloat16>(static_cast<size_t>(T) * kvd);
+  w.attn = cv.take<__nv_bfloat16>(static_cast<size_t>(T) * qd);
+  w.mid = cv.take<__nv_bfloat16>(static_cast<size_t>(T) * c.ffn);
+  w.part_o = cv.take<float>(static_cast<size_t>(S) * c.n_q_heads * nch * 16 * c.head_dim);
+  w.part_ml = cv.take<float>(static_cast<size_t>(S) * c.n_q_heads * nch * 16 * 2);
+  w.partial = cv.take<float>(partial / sizeof(float) + 1);
+  w.logits = need_logits ? cv.take<__nv_bfloat16>(static_cast<size_t>(S) * (DFLASH_BLOCK - 1) * c.vocab) : nullptr;
+  if (out) *out = w;
+  return cv.off;
+}
+
+}  // namespace
+
+int dflash_draft_workspace_bytes(const dflash_handle* h, const dflash_state* st, int s_count, int need_logits,
+                                 size_t* bytes) {
+  if (!h || !st || !bytes || s_count < 1) return DFLASH_E_INVALID_ARG;
+  *bytes = draft_ws_layout(h, st, s_count, need_logits != 0, nullptr, nullptr);
+  return DFLASH_OK;
+}
+
+int dflash_draft_block(dflash_handle* h, dflash_state* st, int s_begin, int s_count, const int32_t* anchor_ids,
+                       void* logits_out, int32_t* topk_ids, float* topk_vals, int k, void* ws, size_t ws_bytes,
+                       dflash_stream_t stream) {
+  if (!h || !st || st->h != h || !anchor_ids || !ws) return DFLASH_E_INVALID_ARG;
+  if (s_count < 1 || s_begin < 0 || s_begin + s_count > st->S) return DFLASH_E_INVALID_ARG;
+  const bool do_topk = topk_ids != nullptr || topk_vals != nullptr;
+  if (do_topk && (!topk_ids || !topk_vals || k < 1 || k > DFLASH_MAX_TOPK)) return DFLASH_E_INVALID_ARG;
+  if (logits_out && !aligned16(logits_out)) return DFLASH_E_INVALID_ARG;
+  for (int i = 0; i < s_count; ++i)
+    if (st->host_len[s_begin + i] + DFLASH_BLOCK > st->R + DFLASH_BLOCK) return DFLASH_E_CAPACITY;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return DFLASH_E_WORKSPACE;
+  const dflash_config& c = h->cfg;
+  DraftWs w{};
+  if (draft_ws_layout(h, st, s_count, logits_out == nullptr, ws, &w) > ws_bytes) return DFLASH_E_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int T = s_count * DFLASH_BLOCK;
+  const int qd = c.n_q_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim;
+  __nv_bfloat16* logits = logits_out ? static_cast<__nv_bfloat16*>(logits_out) : w.logits;
+
+  if (cudaMemsetAsync(w.counters, 0, w.n_counters * sizeof(int), s) != cudaSuccess) return DFLASH_E_CUDA;
+  int rc = launch_embed(w.X, h->embed, anchor_ids, s_count, c.hidden, c.vocab, c.mask_token, st->status, s);
+  if (rc) return rc;
+  int* counters = w.counters;
+  const int nch = max_nchunk(st);
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dflash_layer_weights& L = h->layers[l];
+    GemmPlan qkv, o, gu, dn;
+    layer_plans(h, l, T, qkv, o, gu, dn);
+    // input RMSNorm -> QKV with q_norm / k_norm + RoPE at positions C..C+15
+    rc = launch_rmsnorm_rows(w.hbuf, w.X, static_cast<const __nv_bfloat16*>(L.input_norm), T, c.hidden, c.rms_eps, 0, s);
+    if (rc) return rc;
+    qkv.b_ptr[0] = w.hbuf;
+    qkv.ldb = c.hidden;
+    EpiArgs& e = qkv.epi_args;
+    e.head_dim = c.head_dim;
+    e.eps = c.rms_eps;
+    e.pos_mode = 0;
+    e.s_begin = s_begin;
+    e.lens = st->lens;
+    e.rope = st->rope;
+    e.seg[0] = HeadSeg{HEAD_Q, c.n_q_heads, 0, 0, static_cast<const __nv_bfloat16*>(L.q_norm), w.Q};
+    e.seg[1] = HeadSeg{HEAD_K, c.n_kv_heads, 0, 0, static_cast<const __nv_bfloat16*>(L.k_norm), w.Kb};
+    e.seg[2] = HeadSeg{HEAD_V, c.n_kv_heads, 0, 0, nullptr, w.Vb};
+    rc = gemm_launch(qkv, w.partial, counters, st->status, h->num_sms, s);
+    if (rc) return rc;
+    counters += gemm_counter_count(qkv);
+    // attention over the layer's window of context + the block
+    AttnArgs a{};
+    a.Q = w.Q;
+    a.Kb = w.Kb;
+    a.Vb = w.Vb;
+    a.Kc = st->kc[l];
+    a.Vc = st->vc[l];
+    a.lens = st->lens;
+    a.s_begin = s_begin;
+    a.cap = st->cap[l];
+    a.window = st->window[l];
+    a.nq = c.n_q_heads;
+    a.nkv = c.n_kv_heads;
+    a.d = c.head_dim;
+    a.chunk = attn_chunk(st->cap[l]);
+    a.nchunk = nch;
+    a.part_o = w.part_o;
+    a.part_ml = w.part_ml;
+    a.out = w.attn;
+    // units beyond this layer's capacity exit at once; the combine reads only
+    // the chunks that hold context
+    rc = launch_attention(a, s_count, s);
+    if (rc) return rc;
+    // O projection added to the residual
+    o.b_ptr[0] = w.attn;
+    o.ldb = qd;
+    o.epi_args.out = w.X;
+    o.epi_args.ldo = c.hidden;
+    rc = gemm_launch(o, w.partial, counters, st->status, h->num_sms, s);
+    if (rc) return rc;
+    counters += gemm_counter_count(o);
+    // post-attention RMSNorm -> SwiGLU -> down projection added to the residual
+    rc = launch_rmsnorm_rows(w.hbuf, w.X, static_cast<const __nv_bfloat16*>(L.post_norm), T, c.hidden, c.rms_eps, 0, s);
+    if (rc) return rc;
+    gu.b_ptr[0] = w.hbuf;
+    gu.ldb = c.hidden;
+    gu.epi_args.out = w.mid;
+    gu.epi_args.ldo = c.ffn;
+    rc = gemm_launch(gu, w.partial, counters, st->status, h->num_sms, s);
+    if (rc) return rc;
+    counters += gemm_counter_count(gu);
+    dn.b_ptr[0] = w.mid;
+    dn.ldb = c.ffn;
+    dn.epi_args.out = w.X;
+    dn.epi_args.ldo = c.hidden;
+    rc = gemm_launch(dn, w.partial, counters, st->status, h->num_sms, s);
+    if (rc) return rc;
+    counters += gemm_counter_count(dn);
+  }
+  (void)kvd;
+  // final norm on the 15 mask rows of every stream, shared LM head
+  const int rows = s_count * (DFLASH_BLOCK - 1);
+  rc = launch_rmsnorm_rows(w.hbuf, w.X, h->norm, rows, c.hidden, c.rms_eps, 1, s);
+  if (rc) return rc;
+  GemmPlan lp = lm_plan(h, rows);
+  lp.b_ptr[0] = w.hbuf;
+  lp.ldb = c.hidden;
+  lp.epi_args.out = logits;
+  rc = gemm_launch(lp, w.partial, counters, st->status, h->num_sms, s);
+  if (rc) return rc;
+  if (do_topk) rc = launch_topk(logits, rows, c.vocab, k, 1.0f, nullptr, topk_ids, topk_vals, nullptr, s);
+  return rc;
+}
+
+// ---------------------------------------------------------------- top-k / verify
+int dflash_topk(const void* logits, int rows, int vocab, int k, float temperature, const float* uniforms,
+                int32_t* ids, float* vals, int32_t* sampled, dflash_stream_t stream) {
+  if (!logits || rows < 0 || vocab < 8 || vocab % 8 || k < 0 || k > DFLASH_MAX_TOPK) return DFLASH_E_INVALID_ARG;
+  if (k > 0 && (!ids || !vals)) return DFLASH_E_INVALID_ARG;
+  if ((uniforms == nullptr) != (sampled == nullptr)) return DFLASH_E_INVALID_ARG;
+  if (uniforms && !(temperature > 0.f)) return DFLASH_E_INVALID_ARG;
+  if (!aligned16(logits)) return DFLASH_E_INVALID_ARG;
+  if (k == 0 && !uniforms) return DFLASH_OK;
+  return launch_topk(static_cast<const __nv_bfloat16*>(logits), rows, vocab, k, uniforms ? temperature : 1.0f,
+                     uniforms, ids, vals, sampled, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dflash_verify_workspace_bytes(int mode, int streams, int vocab, size_t* bytes) {
+  if (!bytes || streams < 0 || vocab < 8) return DFLASH_E_INVALID_ARG;
+  if (mode == DFLASH_VERIFY_GREEDY) *bytes = 0;
+  else if (mode == DFLASH_VERIFY_SAMPLE) *bytes = static_cast<size_t>(streams) * 31 * 2 * sizeof(float);
+  else return DFLASH_E_INVALID_ARG;
+  return DFLASH_OK;
+}
+
+int dflash_verify(int mode, int streams, int vocab, const int32_t* draft_ids, const void* target_logits,
+                  const void* draft_logits, const float* uniforms, float temperature, int32_t* accept_len,
+                  int32_t* out_tokens, void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  if (streams < 0 || vocab < 8 || vocab % 8 || !draft_ids || !target_logits || !accept_len || !out_tokens)
+    return DFLASH_E_INVALID_ARG;
+  if (!aligned16(target_logits)) return DFLASH_E_INVALID_ARG;
+  if (streams == 0) return DFLASH_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (mode == DFLASH_VERIFY_GREEDY) {
+    return launch_verify_greedy(streams, vocab, draft_ids, static_cast<const __nv_bfloat16*>(target_logits),
+                                accept_len, out_tokens, s);
+  }
+  if (mode != DFLASH_VERIFY_SAMPLE) return DFLASH_E_INVALID_ARG;
+  if (!draft_logits || !uniforms || !(temperature > 0.f) || !aligned16(draft_logits)) return DFLASH_E_INVALID_ARG;
+  size_t need = 0;
+  dflash_verify_workspace_bytes(mode, streams, vocab, &need);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 15u)) return DFLASH_E_WORKSPACE;
+  return launch_verify_sample(streams, vocab, draft_ids, static_cast<const __nv_bfloat16*>(target_logits),
+                              static_cast<const __nv_bfloat16*>(draft_logits), uniforms, temperature, accept_len,
+                              out_tokens, static_cast<float*>(ws), s);
+}
+
+}  // extern "C"

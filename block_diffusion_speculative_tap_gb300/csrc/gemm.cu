@@ -1,0 +1,565 @@
+// Tensor-core GEMM for every dense contraction of the drafting hot path:
+// fc over tap rows, K/V injection, the block's Q/K/V, O, gate/up and down
+// projections, and the shared LM head.
+//
+// D[M, N] = A[M, K] * B[N, K]^T with A = weights (output features along M,
+// one or more stacked projections) and B = activations (tokens along N). The
+// weight is always the 128-row M operand, so a batch-1 block (16 tokens) is a
+// 128 x 16 MMA tile and all the bandwidth goes to streaming weights.
+//
+// One CTA = 6 warps:
+//   warp 0     one thread issues TMA tile loads (128-byte swizzle) into a ring
+//              of shared-memory stages, signalling `full` mbarriers;
+//   warp 1     allocates tensor memory; one thread issues tcgen05.mma
+//              (kind::f16, bf16 x bf16 -> fp32 in TMEM) and commits to the
+//              `empty` barrier of each stage and to `tmem_full` per tile;
+//   warps 2-5  the epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//              lanes 32*(w%4)..+31), then the fused epilogue.
+// The accumulator is double-buffered in TMEM when it fits, so the epilogue of
+// one work unit overlaps the MMAs of the next. CTAs are persistent and walk
+// the work units round-robin.
+//
+// Split-K: each weight matrix's reduction is cut into a fixed number of
+// chunks (chosen from its shape only, never from N). A chunk writes its fp32
+// partial tile; the last chunk to finish a tile (atomic counter) adds all
+// partials in chunk order and runs the epilogue. Results are therefore
+// identical whatever the batch composition.
+#include <stdio.h>
+
+#include <algorithm>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dfl {
+
+template <int BN, bool DUAL, int STAGES, int EPI>
+struct GemmTraits {
+  static constexpr int kABytes = kTileM * kTileK * 2;  // 16 KiB
+  static constexpr int kBBytes = BN * kTileK * 2;
+  static constexpr int kStageBytes = kABytes * (DUAL ? 2 : 1) + kBBytes;
+  static constexpr int kAcc = DUAL ? 2 : 1;
+  static constexpr int kAccCols = BN * kAcc;
+  static constexpr int kAccBufs = (kAccCols * 2 <= 512) ? 2 : 1;
+  static constexpr int kTmemNeed = kAccCols * kAccBufs;
+  static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
+                                                            : kTmemNeed <= 256 ? 256 : 512;
+  static constexpr int kBarBytes = 8 * (2 * STAGES + 2 * kAccBufs + 1) + 16;
+  static constexpr int kXchFloats = EPI == EPI_HEADS ? kTileM * 17 : 0;  // rope partner exchange
+  static constexpr int kRedFloats = EPI == EPI_HEADS ? 4 * 16 : 0;       // per-warp sums of squares
+  static constexpr int kSmemBytes =
+      1024 /*alignment slack*/ + STAGES * kStageBytes + kBarBytes + 4 * (kXchFloats + kRedFloats) + 64;
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, BN);
+};
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+__device__ __forceinline__ void decode_unit(const GemmArgs& a, int u, int& m_tile, int& kc, int& n_tile) {
+  n_tile = u % a.n_tiles;
+  const int r = u / a.n_tiles;
+  kc = r % a.ksplit;
+  m_tile = r / a.ksplit;
+}
+
+__device__ __forceinline__ int seg_of_tile(const GemmArgs& a, int m_tile) {
+  int s = 0;
+  while (s + 1 < a.n_aseg && m_tile >= a.a_seg_tile[s + 1]) ++s;
+  return s;
+}
+
+// ---------------------------------------------------------------- epilogues
+// v0 (and v1 for the dual GEMM) hold the accumulator of output feature
+// m = m_tile*128 + row for tokens t = n0 + j, j = 0..15.
+template <int EPI>
+__device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0, int row, int q, int lane,
+                                          const float (&v0)[16], const float (&v1)[16], float* xch, float* red) {
+  const int m = m_tile * kTileM + row;
+  if constexpr (EPI == EPI_STORE_F32 || EPI == EPI_STORE_BF16 || EPI == EPI_RESID || EPI == EPI_SWIGLU) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int t = n0 + j;
+      if (t >= a.N) break;
+      const int64_t o = static_cast<int64_t>(t) * a.epi.ldo + m;
+      if constexpr (EPI == EPI_STORE_F32) {
+        static_cast<float*>(a.epi.out)[o] = v0[j];
+      } else if constexpr (EPI == EPI_STORE_BF16) {
+        static_cast<__nv_bfloat16*>(a.epi.out)[o] = __float2bfloat16_rn(v0[j]);
+      } else if constexpr (EPI == EPI_RESID) {
+        float* X = static_cast<float*>(a.epi.out);
+        X[o] = X[o] + v0[j];
+      } else {
+        static_cast<__nv_bfloat16*>(a.epi.out)[o] = __float2bfloat16_rn(silu_f(v0[j]) * v1[j]);
+      }
+    }
+  } else {
+    // heads: per-head RMSNorm over d (q_norm / k_norm), rotate-half RoPE, bf16
+    const int sidx = seg_of_tile(a, m_tile);
+    const HeadSeg& sg = a.epi.seg[sidx];
+    const int d = a.epi.head_dim;
+    const int f = (m_tile - a.a_seg_tile[sidx]) * kTileM + row;  // feature inside the projection
+    const int head = f / d;
+    const int dim = f - head * d;
+    const int half = d >> 1;
+    int pos[16];
+    int strm[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int t = n0 + j;
+      pos[j] = 0;
+      strm[j] = 0;
+      if (t < a.N) {
+        if (a.epi.pos_mode == 0) {
+          strm[j] = a.epi.s_begin + t / 16;
+          pos[j] = a.epi.lens[strm[j]] + (t & 15);
+        } else {
+          strm[j] = a.epi.row_stream[t];
+          pos[j] = a.epi.row_pos[t];
+        }
+      }
+    }
+    float y[16];
+    if (sg.kind != HEAD_V) {
+      float ss[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) ss[j] = v0[j] * v0[j];
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) ss[j] += __shfl_xor_sync(0xffffffffu, ss[j], off);
+      }
+      const int wph = d >> 5;  // warps per head (1, 2 or 4)
+      if (wph > 1) {
+        if (lane == 0) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) red[q * 16 + j] = ss[j];
+        }
+        named_bar_sync(1, 128);
+        const int q0 = (q / wph) * wph;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float s = 0.f;
+          for (int qq = 0; qq < wph; ++qq) s += red[(q0 + qq) * 16 + j];
+          ss[j] = s;
+        }
+      }
+      const float g = __bfloat162float(sg.gain[dim]);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) y[j] = v0[j] * rsqrtf(ss[j] / static_cast<float>(d) + a.epi.eps) * g;
+      // partner value (dim +- d/2) via shared memory
+#pragma unroll
+      for (int j = 0; j < 16; ++j) xch[row * 17 + j] = y[j];
+      named_bar_sync(1, 128);
+      const int prow = dim < half ? row + half : row - half;
+      const int fi = dim < half ? dim : dim - half;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float yp = xch[prow * 17 + j];
+        const float2 cs = a.epi.rope[static_cast<int64_t>(pos[j]) * half + fi];
+        y[j] = dim < half ? (y[j] * cs.x - yp * cs.y) : (y[j] * cs.x + yp * cs.y);
+      }
+      named_bar_sync(1, 128);  // xch / red reusable by the next chunk
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) y[j] = v0[j];
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int t = n0 + j;
+      if (t >= a.N) break;
+      int64_t o;
+      if (a.epi.pos_mode == 0) {
+        o = static_cast<int64_t>(t) * (sg.heads * d) + f;
+      } else {
+        const int slot = sg.window > 0 ? (pos[j] % sg.window) : pos[j];
+        o = ((static_cast<int64_t>(strm[j]) * sg.heads + head) * sg.cap + slot) * d + dim;
+      }
+      sg.dst[o] = __float2bfloat16_rn(y[j]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- kernel
+template <int BN, bool DUAL, int STAGES, int EPI, int MINB>
+__global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_constant__ GemmArgs args) {
+  using Tr = GemmTraits<BN, DUAL, STAGES, EPI>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* tiles = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(tiles + STAGES * Tr::kStageBytes);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + Tr::kAccBufs;
+  uint64_t* drain = tempty + Tr::kAccBufs;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_word = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_word = abort_word + 1;
+  float* xch = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + Tr::kBarBytes);
+  float* red = xch + Tr::kXchFloats;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < Tr::kAccBufs; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_word = 0;
+    *last_word = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Tr::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      for (int i = 0; i < args.n_aseg; ++i) tma_prefetch_desc(&args.a_map[i]);
+      const uint64_t pol_w = policy_evict_first();  // weights stream through once
+      const uint64_t pol_x = policy_evict_last();   // activations are re-read by every tile
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < args.units && ok; u += gridDim.x) {
+        int m_tile, kc, n_tile;
+        decode_unit(args, u, m_tile, kc, n_tile);
+        const int kb0 = static_cast<int>(static_cast<long long>(kc) * args.kb_total / args.ksplit);
+        const int kb1 = static_cast<int>(static_cast<long long>(kc + 1) * args.kb_total / args.ksplit);
+        const int sidx = seg_of_tile(args, m_tile);
+        const int arow = (m_tile - args.a_seg_tile[sidx]) * kTileM;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, args.err, DFLASH_STATUS_TIMEOUT, abort_word)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = tiles + stage * Tr::kStageBytes;
+          mbar_arrive_expect_tx(&full[stage], Tr::kStageBytes);
+          tma_load_2d(st, &args.a_map[sidx], &full[stage], kb * kTileK, arow, pol_w);
+          if constexpr (DUAL) tma_load_2d(st + Tr::kABytes, &args.a2_map, &full[stage], kb * kTileK, arow, pol_w);
+          const int pl = kb / args.b_plane_kb;
+          const int kin = kb - pl * args.b_plane_kb;
+          tma_load_2d(st + Tr::kABytes * (DUAL ? 2 : 1), &args.b_map[pl], &full[stage], kin * kTileK, n_tile * BN,
+                      pol_x);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // make sure no copy is still landing in shared memory when the CTA ends
+      for (int s = 0; s < STAGES; ++s) {
+        if (issued > s) {
+          const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
+          mbar_wait(&full[s], par, args.err, DFLASH_STATUS_TIMEOUT, nullptr);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      bool any = false;
+      for (int u = blockIdx.x; u < args.units && ok; u += gridDim.x) {
+        int m_tile, kc, n_tile;
+        decode_unit(args, u, m_tile, kc, n_tile);
+        const int kb0 = static_cast<int>(static_cast<long long>(kc) * args.kb_total / args.ksplit);
+        const int kb1 = static_cast<int>(static_cast<long long>(kc + 1) * args.kb_total / args.ksplit);
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, args.err, DFLASH_STATUS_TIMEOUT, abort_word)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Tr::kAccCols);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&full[stage], phase, args.err, DFLASH_STATUS_TIMEOUT, abort_word)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(tiles + stage * Tr::kStageBytes);
+          const uint32_t b_addr = a_addr + Tr::kABytes * (DUAL ? 2 : 1);
+#pragma unroll
+          for (int kk = 0; kk < kTileK / 16; ++kk) {
+            const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
+            const uint64_t bdesc = sdesc_sw128(b_addr + kk * 32);
+            umma_bf16(d_tmem, sdesc_sw128(a_addr + kk * 32), bdesc, Tr::kIdesc, accum);
+            if constexpr (DUAL)
+              umma_bf16(d_tmem + BN, sdesc_sw128(a_addr + Tr::kABytes + kk * 32), bdesc, Tr::kIdesc, accum);
+          }
+          any = true;
+          umma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        if (++acc == Tr::kAccBufs) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // all MMAs of this CTA complete before tensor memory is released
+      if (any) {
+        umma_commit(drain);
+        mbar_wait(drain, 0, args.err, DFLASH_STATUS_TIMEOUT, nullptr);
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int row = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const bool epi_leader = (warp == 2 && lane == 0);
+    for (int u = blockIdx.x; u < args.units; u += gridDim.x) {
+      int m_tile, kc, n_tile;
+      decode_unit(args, u, m_tile, kc, n_tile);
+      const bool ok = mbar_wait(&tfull[acc], acc_phase, args.err, DFLASH_STATUS_TIMEOUT, abort_word);
+      // the four epilogue warps leave together, so none is left at a named barrier
+      if (named_bar_or(1, 128, ok ? 0 : 1)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * Tr::kAccCols);
+      float v0[16], v1[16];
+      if (args.ksplit == 1) {
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          tmem_ld16(tbase + c0, v0);
+          if constexpr (DUAL) tmem_ld16(tbase + BN + c0, v1);
+          epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red);
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+      } else {
+        float* slot = args.partial + static_cast<size_t>(u) * (Tr::kAcc * BN * kTileM);
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          tmem_ld16(tbase + c0, v0);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) slot[(c0 + j) * kTileM + row] = v0[j];
+          if constexpr (DUAL) {
+            tmem_ld16(tbase + BN + c0, v1);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) slot[(BN + c0 + j) * kTileM + row] = v1[j];
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (epi_leader) {
+          const int old = atomicAdd(&args.counters[m_tile * args.n_tiles + n_tile], 1);
+          *last_word = (old == args.ksplit - 1) ? 1 : 0;
+        }
+        named_bar_sync(1, 128);
+        const bool last = *last_word != 0;
+        if (last) {
+          __threadfence();
+          for (int c0 = 0; c0 < BN; c0 += 16) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              v0[j] = 0.f;
+              v1[j] = 0.f;
+            }
+            for (int k2 = 0; k2 < args.ksplit; ++k2) {
+              const int u2 = (m_tile * args.ksplit + k2) * args.n_tiles + n_tile;
+              const float* s2 = args.partial + static_cast<size_t>(u2) * (Tr::kAcc * BN * kTileM);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                v0[j] += __ldcg(&s2[(c0 + j) * kTileM + row]);
+                if constexpr (DUAL) v1[j] += __ldcg(&s2[(BN + c0 + j) * kTileM + row]);
+              }
+            }
+            epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red);
+          }
+        }
+      }
+      if (++acc == Tr::kAccBufs) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, Tr::kTmemCols);
+}
+
+// ---------------------------------------------------------------- host side
+namespace {
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn get_encode() {
+  static EncodeFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  }
+  return fn;
+}
+
+template <int BN, bool DUAL, int STAGES, int EPI, int MINB>
+int launch_inst(const GemmArgs& a, int num_sms, cudaStream_t st) {
+  using Tr = GemmTraits<BN, DUAL, STAGES, EPI>;
+  auto kern = gemm_kernel<BN, DUAL, STAGES, EPI, MINB>;
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kSmemBytes) != cudaSuccess)
+      return DFLASH_E_CUDA;
+    configured = true;
+  }
+  const int grid = std::max(1, std::min(a.units, num_sms * MINB));
+  kern<<<grid, kGemmThreads, Tr::kSmemBytes, st>>>(a);
+  count_launch();
+  return cuda_status(cudaGetLastError());
+}
+
+template <int BN, bool DUAL, int STAGES, int MINB>
+int launch_epi(const GemmArgs& a, int epi, int num_sms, cudaStream_t st) {
+  switch (epi) {
+    case EPI_STORE_F32:
+      if constexpr (!DUAL) return launch_inst<BN, DUAL, STAGES, EPI_STORE_F32, MINB>(a, num_sms, st);
+      break;
+    case EPI_STORE_BF16:
+      if constexpr (!DUAL) return launch_inst<BN, DUAL, STAGES, EPI_STORE_BF16, MINB>(a, num_sms, st);
+      break;
+    case EPI_RESID:
+      if constexpr (!DUAL) return launch_inst<BN, DUAL, STAGES, EPI_RESID, MINB>(a, num_sms, st);
+      break;
+    case EPI_HEADS:
+      if constexpr (!DUAL) return launch_inst<BN, DUAL, STAGES, EPI_HEADS, MINB>(a, num_sms, st);
+      break;
+    case EPI_SWIGLU:
+      if constexpr (DUAL) return launch_inst<BN, DUAL, STAGES, EPI_SWIGLU, MINB>(a, num_sms, st);
+      break;
+    default:
+      break;
+  }
+  return DFLASH_E_INVALID_ARG;
+}
+
+}  // namespace
+
+int encode_kmajor_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+  EncodeFn enc = get_encode();
+  if (!enc) return DFLASH_E_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0 || (ld * 2) % 16 != 0 || cols % kTileK != 0)
+    return DFLASH_E_SHAPE;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileK), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_E_CUDA;
+}
+
+int gemm_bn_for(int N) {
+  if (N <= 16) return 16;
+  if (N <= 128) return 128;
+  return 256;
+}
+
+int gemm_choose_ksplit(int m_tiles, int kb_total, int num_sms) {
+  // Fill the 2-CTA-per-SM batch-1 configuration as evenly as possible: the
+  // smallest split whose wave efficiency is within 5% of the best one, with
+  // at least 4 reduction blocks per chunk and at most 16 chunks.
+  const int slots = 2 * num_sms;
+  const int kmax = std::max(1, std::min(16, kb_total / 4));
+  double eff[17] = {0.0};
+  double best = 0.0;
+  for (int ks = 1; ks <= kmax; ++ks) {
+    const long long units = static_cast<long long>(m_tiles) * ks;
+    const long long waves = (units + slots - 1) / slots;
+    eff[ks] = static_cast<double>(units) / static_cast<double>(waves * slots);
+    best = std::max(best, eff[ks]);
+  }
+  for (int ks = 1; ks <= kmax; ++ks)
+    if (eff[ks] >= 0.95 * best) return ks;
+  return 1;
+}
+
+static void fill_args(const GemmPlan& p, GemmArgs& a, int BN) {
+  a.n_aseg = p.n_aseg;
+  a.a_seg_tile[0] = 0;
+  for (int i = 0; i < p.n_aseg; ++i) {
+    a.a_map[i] = *p.a_maps[i];
+    a.a_seg_tile[i + 1] = a.a_seg_tile[i] + p.a_rows[i] / kTileM;
+  }
+  if (p.a2_map) a.a2_map = *p.a2_map;
+  a.M = p.M;
+  a.N = p.N;
+  a.K = p.K;
+  a.m_tiles = p.M / kTileM;
+  a.n_tiles = (p.N + BN - 1) / BN;
+  a.kb_total = p.K / kTileK;
+  a.b_plane_kb = p.Kp / kTileK;
+  a.ksplit = p.ksplit;
+  a.units = a.m_tiles * a.n_tiles * a.ksplit;
+  a.epi = p.epi_args;
+}
+
+size_t gemm_partial_bytes(const GemmPlan& p) {
+  if (p.ksplit <= 1) return 0;
+  const int BN = gemm_bn_for(p.N);
+  const size_t units = static_cast<size_t>(p.M / kTileM) * ((p.N + BN - 1) / BN) * p.ksplit;
+  return units * (p.a2_map ? 2 : 1) * BN * kTileM * sizeof(float);
+}
+
+size_t gemm_counter_count(const GemmPlan& p) {
+  const int BN = gemm_bn_for(p.N);
+  return static_cast<size_t>(p.M / kTileM) * ((p.N + BN - 1) / BN);
+}
+
+int gemm_launch(const GemmPlan& p, float* partial, int* counters, int* err, int num_sms, cudaStream_t st) {
+  if (p.M % kTileM || p.K % kTileK || p.Kp % kTileK || p.N <= 0 || p.n_aseg < 1 || p.n_aseg > kMaxASeg ||
+      p.n_b < 1 || p.n_b > kMaxBPlane || p.Kp * p.n_b != p.K)
+    return DFLASH_E_SHAPE;
+  const int BN = gemm_bn_for(p.N);
+  static thread_local GemmArgs a;  // ~4 KiB: kept off the stack
+  memset(&a, 0, sizeof(a));
+  fill_args(p, a, BN);
+  for (int i = 0; i < p.n_b; ++i) {
+    const int rc = encode_kmajor_map(&a.b_map[i], p.b_ptr[i], p.N, p.Kp, p.ldb, BN);
+    if (rc) return rc;
+  }
+  a.partial = partial;
+  a.counters = counters;
+  a.err = err;
+  if (a.ksplit > 1 && (partial == nullptr || counters == nullptr)) return DFLASH_E_WORKSPACE;
+  const bool dual = p.a2_map != nullptr;
+  if (BN == 16) {
+    return dual ? launch_epi<16, true, 3, 2>(a, p.epi, num_sms, st) : launch_epi<16, false, 5, 2>(a, p.epi, num_sms, st);
+  } else if (BN == 128) {
+    return dual ? launch_epi<128, true, 4, 1>(a, p.epi, num_sms, st)
+                : launch_epi<128, false, 6, 1>(a, p.epi, num_sms, st);
+  }
+  return dual ? launch_epi<256, true, 3, 1>(a, p.epi, num_sms, st) : launch_epi<256, false, 4, 1>(a, p.epi, num_sms, st);
+}
+
+}  // namespace dfl

@@ -1,0 +1,139 @@
+// Internal declarations shared by the host and device translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "dflash.h"
+
+namespace dfl {
+
+constexpr int kMaxASeg = 16;   // projections stacked along the output features
+constexpr int kMaxBPlane = 8;  // tap planes stacked along the reduction
+constexpr int kTileM = 128;    // output features per tile (TMEM lanes)
+constexpr int kTileK = 64;     // reduction per pipeline stage (one 128-byte swizzle row)
+constexpr int kGemmThreads = 192;
+
+enum EpiKind { EPI_STORE_F32 = 0, EPI_STORE_BF16 = 1, EPI_RESID = 2, EPI_SWIGLU = 3, EPI_HEADS = 4 };
+enum HeadKind { HEAD_Q = 0, HEAD_K = 1, HEAD_V = 2 };
+
+// One projection (Q, K or V of one layer) inside a heads epilogue.
+struct HeadSeg {
+  int kind;                   // HeadKind
+  int heads;                  // heads in this projection
+  int cap;                    // cache mode: rows per (stream, head); block mode: unused
+  int window;                 // cache mode: > 0 -> slot = pos % window (sliding ring)
+  const __nv_bfloat16* gain;  // [d] RMSNorm gain (Q and K)
+  __nv_bfloat16* dst;         // block mode: [T, heads*d]; cache mode: [S][heads][cap][d]
+};
+
+struct EpiArgs {
+  void* out;     // STORE_F32 / STORE_BF16 / RESID / SWIGLU: out[t * ldo + m]
+  int64_t ldo;
+  // heads epilogue
+  int head_dim;
+  float eps;
+  int pos_mode;          // 0: block rows (stream s_begin + t/16, pos lens[s] + t%16); 1: row tables
+  int s_begin;
+  const int* lens;
+  const int* row_stream;
+  const int* row_pos;
+  const float2* rope;    // [pos][d/2] = (cos, sin)
+  HeadSeg seg[kMaxASeg];
+};
+
+struct GemmArgs {
+  CUtensorMap a_map[kMaxASeg];    // weights, one map per stacked projection
+  CUtensorMap a2_map;             // second weight of a dual (gate/up) GEMM
+  CUtensorMap b_map[kMaxBPlane];  // activations, one map per K plane
+  int a_seg_tile[kMaxASeg + 1];   // prefix sum of 128-row tiles per projection
+  int n_aseg;
+  int b_plane_kb;                 // 64-wide reduction blocks per B plane
+  int M, N, K;
+  int m_tiles, n_tiles, kb_total, ksplit, units;
+  float* partial;                 // split-K partial tiles, [units][acc][BN][128]
+  int* counters;                  // [m_tiles * n_tiles], zero before launch
+  int* err;                       // device status word
+  EpiArgs epi;
+};
+
+// Host-side description of a GEMM D[M, N] = A[M, K] * B[N, K]^T (both
+// K-contiguous bf16): A = weights (stacked projections), B = activations
+// (optionally K-split over planes).
+struct GemmPlan {
+  int n_aseg = 0;
+  const CUtensorMap* a_maps[kMaxASeg] = {};
+  int a_rows[kMaxASeg] = {};
+  const CUtensorMap* a2_map = nullptr;  // non-null: dual GEMM
+  int n_b = 0;
+  const void* b_ptr[kMaxBPlane] = {};
+  int64_t ldb = 0;  // elements
+  int Kp = 0;       // reduction length of one B plane
+  int M = 0, N = 0, K = 0;
+  int ksplit = 1;
+  int epi = EPI_STORE_F32;
+  EpiArgs epi_args{};
+};
+
+// Workspace needed by one GEMM launch (partials and counters), bytes.
+size_t gemm_partial_bytes(const GemmPlan& p);
+size_t gemm_counter_count(const GemmPlan& p);
+int gemm_bn_for(int N);
+// Fixed split of the reduction for a weight matrix (independent of N).
+int gemm_choose_ksplit(int m_tiles, int kb_total, int num_sms);
+// Encode the TMA map of a K-contiguous bf16 matrix [rows, cols] (row stride ld
+// elements) with a box of box_rows x 64 and 128-byte swizzle.
+int encode_kmajor_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows);
+int gemm_launch(const GemmPlan& p, float* partial, int* counters, int* err, int num_sms, cudaStream_t st);
+
+// ---------------------------------------------------------------- small kernels (rows.cu)
+int launch_embed(float* X, const __nv_bfloat16* embed, const int* anchors, int S, int H, int V, int mask, int* err,
+                 cudaStream_t st);
+// out[r] = bf16(RMSNorm(x[src_row(r)]) * g); src_row maps mask rows when mask_rows_only.
+int launch_rmsnorm_rows(__nv_bfloat16* out, const float* x, const __nv_bfloat16* g, int rows, int H, float eps,
+                        int mask_rows_only, cudaStream_t st);
+// Row tables (stream, position) of appended segments, and/or the new stream
+// lengths (start + rows of each segment). seg_info_host_packed holds
+// (stream, start, rows) per segment, on the host.
+int launch_prep_rows(int* row_stream, int* row_pos, int* lens, const int* unused, int nseg, int rows,
+                     const int* seg_info_host_packed, cudaStream_t st);
+int launch_hidden_norm(__nv_bfloat16* ring, __nv_bfloat16* fused_tmp, const float* y, const __nv_bfloat16* g,
+                       const int* row_stream, const int* row_pos, int rows, int H, int R, float eps, cudaStream_t st);
+
+// ---------------------------------------------------------------- attention (attention.cu)
+struct AttnArgs {
+  const __nv_bfloat16* Q;   // [T, nq*d]
+  const __nv_bfloat16* Kb;  // [T, nkv*d]
+  const __nv_bfloat16* Vb;  // [T, nkv*d]
+  const __nv_bfloat16* Kc;  // [S][nkv][cap][d]
+  const __nv_bfloat16* Vc;
+  const int* lens;
+  int s_begin;
+  int cap;
+  int window;               // 0: full layer
+  int nq, nkv, d;
+  int chunk;                // context rows per work unit
+  int nchunk;               // chunk slots per (stream, kv head)
+  float* part_o;            // [s][nq][nchunk][16][d]
+  float* part_ml;           // [s][nq][nchunk][16][2]
+  __nv_bfloat16* out;       // [T, nq*d]
+};
+int launch_attention(const AttnArgs& a, int s_count, cudaStream_t st);
+size_t attn_partial_floats(int s_count, int nq, int nchunk, int d);
+
+// ---------------------------------------------------------------- selection (select.cu)
+int launch_topk(const __nv_bfloat16* logits, int rows, int V, int k, float T, const float* uniforms, int* ids,
+                float* vals, int* sampled, cudaStream_t st);
+int launch_verify_greedy(int S, int V, const int* draft, const __nv_bfloat16* tl, int* accept, int* out,
+                         cudaStream_t st);
+int launch_verify_sample(int S, int V, const int* draft, const __nv_bfloat16* tl, const __nv_bfloat16* dl,
+                         const float* u, float T, int* accept, int* out, float* stats, cudaStream_t st);
+
+// launch bookkeeping
+void count_launch(int n = 1);
+int cuda_status(cudaError_t e);
+
+}  // namespace dfl

@@ -1,0 +1,160 @@
+// Row-wise kernels of the hot path: block embedding, RMSNorm of the fp32
+// residual into bf16 GEMM operands, the hidden_norm that turns fc's output
+// into fused ring rows, and the bookkeeping of appended rows.
+//
+// Each row is reduced by one CTA in a fixed order (per-thread strided sums,
+// then a warp tree, then the warps in order), so results do not depend on
+// which other rows share the launch.
+#include "internal.h"
+
+namespace dfl {
+
+namespace {
+
+constexpr int kRowThreads = 256;
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  float t = 0.f;
+  const int nw = blockDim.x >> 5;
+  for (int i = 0; i < nw; ++i) t += red[i];
+  __syncthreads();
+  return t;
+}
+
+// X[t] = embed[token_t] as fp32; token 16s is the anchor of stream s, the
+// other fifteen rows of the block are the mask token [anchor + 15 mask rows].
+__global__ void embed_kernel(float* __restrict__ X, const __nv_bfloat16* __restrict__ E, const int* __restrict__ anchors,
+                             int H, int V, int mask, int* err) {
+  const int t = blockIdx.x;
+  int tok = mask;
+  if ((t & 15) == 0) {
+    tok = anchors[t >> 4];
+    if (tok < 0 || tok >= V) {
+      if (threadIdx.x == 0) atomicOr(err, DFLASH_STATUS_BAD_TOKEN);
+      tok = 0;
+    }
+  }
+  const __nv_bfloat16* e = E + static_cast<int64_t>(tok) * H;
+  float* x = X + static_cast<int64_t>(t) * H;
+  for (int i = threadIdx.x; i < H; i += blockDim.x) x[i] = __bfloat162float(e[i]);
+}
+
+// out[r] = bf16(x[src] / sqrt(mean(x[src]^2) + eps) * g)
+__global__ void rmsnorm_rows_kernel(__nv_bfloat16* __restrict__ out, const float* __restrict__ x,
+                                    const __nv_bfloat16* __restrict__ g, int H, float eps, int mask_rows_only) {
+  __shared__ float red[32];
+  const int r = blockIdx.x;
+  const int src = mask_rows_only ? (r / 15) * 16 + 1 + (r % 15) : r;
+  const float* xr = x + static_cast<int64_t>(src) * H;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < H; i += blockDim.x) {
+    const float v = xr[i];
+    ss += v * v;
+  }
+  const float tot = block_sum(ss, red);
+  const float rstd = rsqrtf(tot / static_cast<float>(H) + eps);
+  __nv_bfloat16* o = out + static_cast<int64_t>(r) * H;
+  for (int i = threadIdx.x; i < H; i += blockDim.x) o[i] = __float2bfloat16_rn(xr[i] * rstd * __bfloat162float(g[i]));
+}
+
+// fused = bf16(RMSNorm(y) * hidden_norm): written to the ring slot of the
+// row's (stream, position) and to a dense staging copy for K/V injection.
+__global__ void hidden_norm_kernel(__nv_bfloat16* __restrict__ ring, __nv_bfloat16* __restrict__ fused_tmp,
+                                   const float* __restrict__ y, const __nv_bfloat16* __restrict__ g,
+                                   const int* __restrict__ row_stream, const int* __restrict__ row_pos, int H, int R,
+                                   float eps) {
+  __shared__ float red[32];
+  const int r = blockIdx.x;
+  const float* yr = y + static_cast<int64_t>(r) * H;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < H; i += blockDim.x) {
+    const float v = yr[i];
+    ss += v * v;
+  }
+  const float tot = block_sum(ss, red);
+  const float rstd = rsqrtf(tot / static_cast<float>(H) + eps);
+  __nv_bfloat16* dr = ring + (static_cast<int64_t>(row_stream[r]) * R + row_pos[r]) * H;
+  __nv_bfloat16* dt = fused_tmp + static_cast<int64_t>(r) * H;
+  for (int i = threadIdx.x; i < H; i += blockDim.x) {
+    const __nv_bfloat16 b = __float2bfloat16_rn(yr[i] * rstd * __bfloat162float(g[i]));
+    dr[i] = b;
+    dt[i] = b;
+  }
+}
+
+struct SegTable {
+  int n;
+  int stream[256];
+  int start[256];
+  int rows[256];
+  int first_row[257];
+};
+
+__global__ void prep_rows_kernel(int* __restrict__ row_stream, int* __restrict__ row_pos, const SegTable tab,
+                                 int total) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= total) return;
+  int s = 0;
+  while (s + 1 < tab.n && r >= tab.first_row[s + 1]) ++s;
+  row_stream[r] = tab.stream[s];
+  row_pos[r] = tab.start[s] + (r - tab.first_row[s]);
+}
+
+__global__ void set_lens_kernel(int* __restrict__ lens, const SegTable tab) {
+  const int i = threadIdx.x;
+  if (i < tab.n) lens[tab.stream[i]] = tab.start[i] + tab.rows[i];
+}
+
+}  // namespace
+
+int launch_embed(float* X, const __nv_bfloat16* embed, const int* anchors, int S, int H, int V, int mask, int* err,
+                 cudaStream_t st) {
+  embed_kernel<<<S * 16, kRowThreads, 0, st>>>(X, embed, anchors, H, V, mask, err);
+  count_launch();
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_rmsnorm_rows(__nv_bfloat16* out, const float* x, const __nv_bfloat16* g, int rows, int H, float eps,
+                        int mask_rows_only, cudaStream_t st) {
+  rmsnorm_rows_kernel<<<rows, kRowThreads, 0, st>>>(out, x, g, H, eps, mask_rows_only);
+  count_launch();
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_hidden_norm(__nv_bfloat16* ring, __nv_bfloat16* fused_tmp, const float* y, const __nv_bfloat16* g,
+                       const int* row_stream, const int* row_pos, int rows, int H, int R, float eps, cudaStream_t st) {
+  hidden_norm_kernel<<<rows, kRowThreads, 0, st>>>(ring, fused_tmp, y, g, row_stream, row_pos, H, R, eps);
+  count_launch();
+  return cuda_status(cudaGetLastError());
+}
+
+// seg_info_host_packed: 3*nseg ints (stream, start, rows) on the host.
+int launch_prep_rows(int* row_stream, int* row_pos, int* lens, const int* /*unused*/, int nseg, int rows,
+                     const int* seg_info_host_packed, cudaStream_t st) {
+  if (nseg < 1 || nseg > 256) return DFLASH_E_INVALID_ARG;
+  SegTable tab{};
+  tab.n = nseg;
+  tab.first_row[0] = 0;
+  for (int i = 0; i < nseg; ++i) {
+    tab.stream[i] = seg_info_host_packed[3 * i];
+    tab.start[i] = seg_info_host_packed[3 * i + 1];
+    tab.rows[i] = seg_info_host_packed[3 * i + 2];
+    tab.first_row[i + 1] = tab.first_row[i] + tab.rows[i];
+  }
+  if (rows > 0) {
+    prep_rows_kernel<<<(rows + 255) / 256, 256, 0, st>>>(row_stream, row_pos, tab, rows);
+    count_launch();
+  }
+  if (lens) {
+    set_lens_kernel<<<1, 256, 0, st>>>(lens, tab);
+    count_launch();
+  }
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace dfl

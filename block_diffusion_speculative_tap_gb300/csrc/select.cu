@@ -1,0 +1,461 @@
+// Vocabulary-wide selection: per-row top-k (ties to the lower id), argmax,
+// inverse-CDF sampling from softmax(logits / T), and target verification
+// (greedy longest-prefix + bonus; speculative sampling with the residual
+// max(p - q, 0)).
+//
+// A row is scanned by one CTA of 16 warps. Warp w owns a contiguous slice of
+// the row and reads it 8 bf16 (16 bytes) per lane per step, lanes interleaved,
+// so loads are coalesced and every warp's elements are visited in ascending
+// id order. Cumulative sums for inverse-CDF draws follow that fixed order
+// (per-lane 8-element sums, a warp scan, then the warps in order), so a draw
+// is deterministic.
+#include <float.h>
+
+#include "internal.h"
+
+namespace dfl {
+
+namespace {
+
+constexpr int kSelThreads = 512;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kKMax = DFLASH_MAX_TOPK;
+
+struct Slice {
+  int g0, g1;  // 8-element groups [g0, g1) owned by this warp
+};
+
+__device__ __forceinline__ Slice warp_slice(int V, int w) {
+  const int ng = V >> 3;
+  return {static_cast<int>(static_cast<long long>(ng) * w / kSelWarps),
+          static_cast<int>(static_cast<long long>(ng) * (w + 1) / kSelWarps)};
+}
+
+__device__ __forceinline__ void load8(const __nv_bfloat16* row, int g, float (&x)[8]) {
+  const uint4 raw = *reinterpret_cast<const uint4*>(row + static_cast<int64_t>(g) * 8);
+  const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(p[i]);
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
+}
+
+// (va, ia) ranks before (vb, ib): larger value, then lower id
+__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// Local sorted top list of one thread; elements arrive in ascending id order,
+// so a strict comparison keeps the lower id ahead on ties.
+template <int KM>
+struct TopList {
+  float v[KM];
+  int i[KM];
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      v[j] = -INFINITY;
+      i[j] = INT_MAX;
+    }
+  }
+  __device__ __forceinline__ void push(float x, int id) {
+    if (!(x > v[KM - 1])) return;
+    v[KM - 1] = x;
+    i[KM - 1] = id;
+#pragma unroll
+    for (int j = KM - 1; j > 0; --j) {
+      if (v[j] > v[j - 1]) {
+        const float tv = v[j];
+        v[j] = v[j - 1];
+        v[j - 1] = tv;
+        const int ti = i[j];
+        i[j] = i[j - 1];
+        i[j - 1] = ti;
+      }
+    }
+  }
+  __device__ __forceinline__ void pop() {
+#pragma unroll
+    for (int j = 0; j < KM - 1; ++j) {
+      v[j] = v[j + 1];
+      i[j] = i[j + 1];
+    }
+    v[KM - 1] = -INFINITY;
+    i[KM - 1] = INT_MAX;
+  }
+};
+
+// Block-wide best of every thread's (v, i); all threads receive it.
+__device__ __forceinline__ void block_best(float v, int i, float* sv, int* si, float& bv, int& bi) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, off);
+    if (better(ov, oi, v, i)) {
+      v = ov;
+      i = oi;
+    }
+  }
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    sv[w] = v;
+    si[w] = i;
+  }
+  __syncthreads();
+  bv = sv[0];
+  bi = si[0];
+  for (int j = 1; j < kSelWarps; ++j)
+    if (better(sv[j], si[j], bv, bi)) {
+      bv = sv[j];
+      bi = si[j];
+    }
+  __syncthreads();
+}
+
+// Top-k (k <= KM) of a row into (ids, vals); also returns the row maximum.
+template <int KM>
+__device__ float row_topk(const __nv_bfloat16* row, int V, int k, int* ids, float* vals, float* sv, int* si) {
+  const int w = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const Slice sl = warp_slice(V, w);
+  TopList<KM> tl;
+  tl.init();
+  for (int g = sl.g0 + lane; g < sl.g1; g += 32) {
+    float x[8];
+    load8(row, g, x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) tl.push(x[e], g * 8 + e);
+  }
+  float mx = -INFINITY;
+  const int rounds = k < 1 ? 1 : k;
+  for (int r = 0; r < rounds; ++r) {
+    float bv;
+    int bi;
+    block_best(tl.v[0], tl.i[0], sv, si, bv, bi);
+    if (r == 0) mx = bv;
+    if (tl.i[0] == bi) tl.pop();
+    if (threadIdx.x == 0 && r < k) {
+      ids[r] = bi;
+      vals[r] = bv;
+    }
+  }
+  return mx;
+}
+
+// Weight of id j for inverse-CDF draws; `mode` 0: exp((x - mx) / T) of one
+// row; mode 1: max(p - q, 0) of two rows with their (max, sum).
+struct Weights {
+  const __nv_bfloat16* a;
+  const __nv_bfloat16* b;
+  float ma, sa, mb, sb, invT;
+  int mode;
+  __device__ __forceinline__ void eval8(int g, float (&w)[8]) const {
+    float x[8];
+    load8(a, g, x);
+    if (mode == 0) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w[e] = expf((x[e] - ma) * invT);
+    } else {
+      float y[8];
+      load8(b, g, y);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float p = expf((x[e] - ma) * invT) / sa;
+        const float q = expf((y[e] - mb) * invT) / sb;
+        w[e] = fmaxf(p - q, 0.f);
+      }
+    }
+  }
+};
+
+__device__ __forceinline__ float warp_incl_scan(float v, int lane) {
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float o = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += o;
+  }
+  return v;
+}
+
+// Sum of the weights in the fixed scan order; every thread gets the total.
+__device__ float weights_total(const Weights& W, int V, float* sw) {
+  __syncthreads();  // sw may still be read by a previous total / draw
+  const int w = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const Slice sl = warp_slice(V, w);
+  float run = 0.f;
+  for (int g0 = sl.g0; g0 < sl.g1; g0 += 32) {
+    const int g = g0 + lane;
+    float s8 = 0.f;
+    if (g < sl.g1) {
+      float x[8];
+      W.eval8(g, x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s8 += x[e];
+    }
+    const float inc = warp_incl_scan(s8, lane);
+    run += __shfl_sync(0xffffffffu, inc, 31);
+  }
+  if (lane == 0) sw[w] = run;
+  __syncthreads();
+  float tot = 0.f;
+  for (int j = 0; j < kSelWarps; ++j) tot += sw[j];
+  return tot;  // sw[] stays valid for weights_draw
+}
+
+// Smallest id whose running sum exceeds thr, summed in the order of
+// weights_total (which must have filled sw). Lane ranges inside a step are
+// [B_{L-1}, B_L) with B_L = run + inclusive_scan_L, computed the same way for
+// every lane, so they tile the step exactly. Rounding can still leave thr at
+// or past the end of a slice or a lane; the draw then falls back to the last
+// id with positive weight there.
+__device__ int weights_draw(const Weights& W, int V, float thr, const float* sw, int* sres) {
+  const int w = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) sres[0] = -1;
+  float pre = 0.f;
+  int ws = -1;
+  float tl = 0.f;
+  for (int j = 0; j < kSelWarps; ++j) {
+    const float t = thr - pre;
+    if (t < sw[j] && sw[j] > 0.f) {
+      ws = j;
+      tl = t;
+      break;
+    }
+    pre += sw[j];
+  }
+  if (ws < 0) {
+    for (int j = kSelWarps - 1; j >= 0 && ws < 0; --j)
+      if (sw[j] > 0.f) ws = j;
+    tl = INFINITY;
+  }
+  __syncthreads();
+  if (w == ws) {
+    const Slice sl = warp_slice(V, w);
+    float run = 0.f;
+    int last_pos = -1;
+    bool done = false;
+    for (int g0 = sl.g0; g0 < sl.g1 && !done; g0 += 32) {
+      const int g = g0 + lane;
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = 0.f;
+      float s8 = 0.f;
+      if (g < sl.g1) {
+        W.eval8(g, x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s8 += x[e];
+      }
+      const float inc = warp_incl_scan(s8, lane);
+      const float tot = __shfl_sync(0xffffffffu, inc, 31);
+      int lp = -1;
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (x[e] > 0.f) lp = g * 8 + e;
+      for (int off = 16; off >= 1; off >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, off));
+      if (lp >= 0) last_pos = lp;
+      if (tl < run + tot) {
+        const float B = run + inc;
+        float Bp = __shfl_up_sync(0xffffffffu, B, 1);
+        const bool mine = (lane == 0 || tl >= Bp) && tl < B;
+        const unsigned who = __ballot_sync(0xffffffffu, mine);
+        const int src = __ffs(who) - 1;  // who != 0: lane 31 has B = run + tot > tl
+        if (lane == src) {
+          float c = lane == 0 ? run : Bp;
+          int pick = -1, lastp = -1;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            if (x[e] > 0.f) lastp = g * 8 + e;
+            c += x[e];
+            if (pick < 0 && tl < c && x[e] > 0.f) pick = g * 8 + e;
+          }
+          if (pick < 0) pick = lastp >= 0 ? lastp : last_pos;
+          sres[0] = pick;
+        }
+        done = true;
+      }
+      run += tot;
+    }
+    __syncwarp();
+    if (lane == 0 && sres[0] < 0) sres[0] = last_pos >= 0 ? last_pos : 0;
+  }
+  __syncthreads();
+  const int r = sres[0];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kSelThreads) topk_kernel(const __nv_bfloat16* __restrict__ logits, int V, int k,
+                                                           float invT, const float* __restrict__ uniforms,
+                                                           int* __restrict__ ids, float* __restrict__ vals,
+                                                           int* __restrict__ sampled) {
+  __shared__ float sv[kSelWarps];
+  __shared__ int si[kSelWarps];
+  __shared__ float sw[kSelWarps];
+  __shared__ int sres[1];
+  __shared__ int sid[kKMax];
+  __shared__ float sval[kKMax];
+  const int r = blockIdx.x;
+  const __nv_bfloat16* row = logits + static_cast<int64_t>(r) * V;
+  const float mx = k <= 8 ? row_topk<8>(row, V, k, sid, sval, sv, si) : row_topk<kKMax>(row, V, k, sid, sval, sv, si);
+  __syncthreads();
+  if (threadIdx.x < k) {
+    ids[static_cast<int64_t>(r) * k + threadIdx.x] = sid[threadIdx.x];
+    vals[static_cast<int64_t>(r) * k + threadIdx.x] = sval[threadIdx.x];
+  }
+  if (uniforms != nullptr) {
+    Weights W{row, nullptr, mx, 1.f, 0.f, 1.f, invT, 0};
+    const float tot = weights_total(W, V, sw);
+    const int j = weights_draw(W, V, uniforms[r] * tot, sw, sres);
+    if (threadIdx.x == 0) sampled[r] = j;
+  }
+}
+
+// greedy, step 1: t_i = argmax of every target row -> out[s][i]
+__global__ void __launch_bounds__(kSelThreads) argmax_kernel(const __nv_bfloat16* __restrict__ tl, int V,
+                                                             int* __restrict__ out) {
+  __shared__ float sv[kSelWarps];
+  __shared__ int si[kSelWarps];
+  __shared__ int sid[1];
+  __shared__ float sval[1];
+  const int r = blockIdx.x;
+  row_topk<1>(tl + static_cast<int64_t>(r) * V, V, 1, sid, sval, sv, si);
+  __syncthreads();
+  if (threadIdx.x == 0) out[r] = sid[0];
+}
+
+// greedy, step 2: longest prefix of drafts equal to the target argmax, then
+// the bonus token; rewrites out[s][*] in place.
+__global__ void greedy_prefix_kernel(int S, int V, const int* __restrict__ draft, int* __restrict__ accept,
+                                     int* __restrict__ out) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= S) return;
+  int t[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) t[i] = out[s * 16 + i];
+  int a = 0;
+  while (a < 15 && draft[s * 15 + a] == t[a]) ++a;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    int v = -1;
+    if (i < a) v = draft[s * 15 + i];
+    if (i == a) v = t[a];
+    out[s * 16 + i] = v;
+  }
+  accept[s] = a;
+}
+
+// sampling, step 1: (max, sum of exp((x - max) / T)) of the 16 target rows
+// (r < 16) and the 15 draft rows (r >= 16) of every stream.
+__global__ void __launch_bounds__(kSelThreads) softmax_stats_kernel(const __nv_bfloat16* __restrict__ tl,
+                                                                    const __nv_bfloat16* __restrict__ dl, int V,
+                                                                    float invT, float* __restrict__ stats) {
+  __shared__ float sv[kSelWarps];
+  __shared__ int si[kSelWarps];
+  __shared__ float sw[kSelWarps];
+  __shared__ int sid[1];
+  __shared__ float sval[1];
+  const int r = blockIdx.x;
+  const int s = blockIdx.y;
+  const __nv_bfloat16* row =
+      r < 16 ? tl + (static_cast<int64_t>(s) * 16 + r) * V : dl + (static_cast<int64_t>(s) * 15 + (r - 16)) * V;
+  const float mx = row_topk<1>(row, V, 1, sid, sval, sv, si);
+  Weights W{row, nullptr, mx, 1.f, 0.f, 1.f, invT, 0};
+  const float tot = weights_total(W, V, sw);
+  if (threadIdx.x == 0) {
+    stats[(s * 31 + r) * 2] = mx;
+    stats[(s * 31 + r) * 2 + 1] = tot;
+  }
+}
+
+// sampling, step 2: the accept chain, then the residual or bonus draw.
+__global__ void __launch_bounds__(kSelThreads) sample_verify_kernel(int V, const int* __restrict__ draft,
+                                                                    const __nv_bfloat16* __restrict__ tl,
+                                                                    const __nv_bfloat16* __restrict__ dl,
+                                                                    const float* __restrict__ u, float invT,
+                                                                    const float* __restrict__ stats,
+                                                                    int* __restrict__ accept, int* __restrict__ out) {
+  __shared__ float sw[kSelWarps];
+  __shared__ int sres[1];
+  const int s = blockIdx.x;
+  const float* st = stats + s * 31 * 2;
+  int a = 15;
+  for (int i = 0; i < 15; ++i) {
+    const int x = draft[s * 15 + i];
+    bool acc = false;
+    if (x >= 0 && x < V) {
+      const float p = expf((__bfloat162float(tl[(static_cast<int64_t>(s) * 16 + i) * V + x]) - st[i * 2]) * invT) /
+                      st[i * 2 + 1];
+      const float q =
+          expf((__bfloat162float(dl[(static_cast<int64_t>(s) * 15 + i) * V + x]) - st[(16 + i) * 2]) * invT) /
+          st[(16 + i) * 2 + 1];
+      acc = u[(s * 16 + i) * 2] * q < p;
+    }
+    if (!acc) {
+      a = i;
+      break;
+    }
+  }
+  int tok;
+  const __nv_bfloat16* trow = tl + (static_cast<int64_t>(s) * 16 + a) * V;
+  const float ud = u[(s * 16 + a) * 2 + 1];
+  if (a < 15) {
+    const __nv_bfloat16* drow = dl + (static_cast<int64_t>(s) * 15 + a) * V;
+    Weights R{trow, drow, st[a * 2], st[a * 2 + 1], st[(16 + a) * 2], st[(16 + a) * 2 + 1], invT, 1};
+    const float tot = weights_total(R, V, sw);
+    __syncthreads();
+    if (tot > 0.f) {
+      tok = weights_draw(R, V, ud * tot, sw, sres);
+    } else {
+      Weights P{trow, nullptr, st[a * 2], 1.f, 0.f, 1.f, invT, 0};
+      const float tp = weights_total(P, V, sw);
+      tok = weights_draw(P, V, ud * tp, sw, sres);
+    }
+  } else {
+    Weights P{trow, nullptr, st[15 * 2], 1.f, 0.f, 1.f, invT, 0};
+    const float tp = weights_total(P, V, sw);
+    tok = weights_draw(P, V, ud * tp, sw, sres);
+  }
+  if (threadIdx.x < 16) {
+    const int i = threadIdx.x;
+    int v = -1;
+    if (i < a) v = draft[s * 15 + i];
+    if (i == a) v = tok;
+    out[s * 16 + i] = v;
+  }
+  if (threadIdx.x == 0) accept[s] = a;
+}
+
+}  // namespace
+
+int launch_topk(const __nv_bfloat16* logits, int rows, int V, int k, float T, const float* uniforms, int* ids,
+                float* vals, int* sampled, cudaStream_t st) {
+  if (rows <= 0) return DFLASH_OK;
+  topk_kernel<<<rows, kSelThreads, 0, st>>>(logits, V, k, 1.0f / T, uniforms, ids, vals, sampled);
+  count_launch();
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_verify_greedy(int S, int V, const int* draft, const __nv_bfloat16* tl, int* accept, int* out,
+                         cudaStream_t st) {
+  argmax_kernel<<<S * 16, kSelThreads, 0, st>>>(tl, V, out);
+  count_launch();
+  greedy_prefix_kernel<<<(S + 127) / 128, 128, 0, st>>>(S, V, draft, accept, out);
+  count_launch();
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_verify_sample(int S, int V, const int* draft, const __nv_bfloat16* tl, const __nv_bfloat16* dl,
+                         const float* u, float T, int* accept, int* out, float* stats, cudaStream_t st) {
+  dim3 g(31, S);
+  softmax_stats_kernel<<<g, kSelThreads, 0, st>>>(tl, dl, V, 1.0f / T, stats);
+  count_launch();
+  sample_verify_kernel<<<S, kSelThreads, 0, st>>>(V, draft, tl, dl, u, 1.0f / T, stats, accept, out);
+  count_launch();
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace dfl

@@ -1,0 +1,300 @@
+/*
+ * dflash.h -- C ABI of libdflash, the GB300 (sm_103a) hot path of DFlash-style
+ * block-diffusion speculative drafting with target taps.
+ *
+ * Three stages, each behind one call:
+ *   dflash_fuse_taps    tap planes -> fc -> hidden_norm -> fused ring rows,
+ *                       then K/V injection into every drafter layer's cache
+ *   dflash_draft_block  the drafter's block forward over anchor + 15 mask rows,
+ *                       final norm, shared LM head, per-position top-k
+ *   dflash_topk         vocab-wide top-k / argmax / temperature sampling
+ *   dflash_verify       greedy longest-prefix + bonus, or speculative sampling
+ *                       with residual correction
+ *
+ * Sources, cited by page title and section:
+ *   [TF1851]  TensorFold pull request #1851, "qwen27 dflash: read and run the
+ *             9B's DFlash drafter beside DFlash2", section "What this changes".
+ *   [ST3457]  Strata pull request #3457, "Metal: opt-in --dflash DFlash2
+ *             drafter in place of the MTP layer", sections "Approach" and
+ *             "Validation".
+ *   [EXPL]    "DFlash 解碼加速：原理、限制與 oMLX 實作" (a DFlash decoding
+ *             explainer), sections 三 (how DFlash works) and 四 (target
+ *             verification).
+ *   [PROT]    "Port the DFlash2 protocol, not its checkpoint", sections
+ *             "What is portable" and "Golden replay before training".
+ *
+ * Conventions
+ *   - Every function returns DFLASH_OK (0) or a negative DFLASH_E_* code, and
+ *     never throws. dflash_strerror() names a code.
+ *   - The caller owns all memory: weights, state memory, workspaces, inputs
+ *     and outputs. The library never allocates device memory. Pointers named
+ *     "device" must be device (or managed) memory of the handle's device;
+ *     pointers named "host" are read on the host during the call and may be
+ *     freed when it returns.
+ *   - Every device-side step is enqueued asynchronously on the caller's
+ *     stream (a cudaStream_t passed as dflash_stream_t; NULL = legacy default
+ *     stream). Arguments are validated on the host before anything is
+ *     enqueued; a call that returns an error has enqueued nothing.
+ *   - bf16 tensors are IEEE bfloat16, row-major, densely packed unless a
+ *     stride is given. Sums are fp32.
+ *   - Faults only the device can see (an anchor id outside the vocabulary, a
+ *     timed-out wait) set bits in the state's device status word; read it with
+ *     dflash_device_status(). No kernel traps.
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dflash_stream_t; /* a cudaStream_t */
+
+/* ---------------------------------------------------------------- status */
+enum {
+  DFLASH_OK = 0,
+  DFLASH_E_INVALID_ARG = -1,   /* NULL pointer, negative size, bad mode */
+  DFLASH_E_TAPS_RANGE = -2,    /* tap count outside 1..8, or a tap past the target [TF1851 item 1] */
+  DFLASH_E_TAPS_REPEATED = -3, /* the same target layer tapped twice [TF1851 item 1] */
+  DFLASH_E_CAUSAL = -4,        /* a causal draft is refused [TF1851 item 1] */
+  DFLASH_E_SHAPE = -5,         /* shapes this drafter cannot run */
+  DFLASH_E_CAPACITY = -6,      /* a position past the ring / served span */
+  DFLASH_E_WORKSPACE = -7,     /* workspace or state memory too small or misaligned */
+  DFLASH_E_CUDA = -8,          /* a CUDA runtime / driver call failed */
+  DFLASH_E_TIMEOUT = -9,       /* a device-side wait ran out (status word) */
+  DFLASH_E_DEVICE_FAULT = -10, /* the device flagged bad data (status word) */
+  DFLASH_E_UNSUPPORTED = -11   /* no sm_100-family device, or a missing driver entry point */
+};
+
+/* bits of the device status word */
+enum {
+  DFLASH_STATUS_BAD_TOKEN = 1,   /* an anchor id outside [0, vocab): row read as id 0 */
+  DFLASH_STATUS_TIMEOUT = 2,     /* a bounded mbarrier wait expired; results invalid */
+  DFLASH_STATUS_BAD_DRAFT = 4    /* a draft id outside [0, vocab) in dflash_verify */
+};
+
+#define DFLASH_MAX_TAPS 8
+#define DFLASH_MAX_LAYERS 64
+#define DFLASH_BLOCK 16 /* anchor + 15 mask rows [TF1851 item 1] */
+#define DFLASH_MAX_TOPK 16
+
+enum { DFLASH_LAYER_FULL = 0, DFLASH_LAYER_SLIDING = 1 };
+enum { DFLASH_VARIANT_V1 = 1, DFLASH_VARIANT_2 = 2 };
+enum { DFLASH_VERIFY_GREEDY = 0, DFLASH_VERIFY_SAMPLE = 1 };
+enum { DFLASH_FUSE_INJECT_KV = 1 }; /* dflash_fuse_taps flags */
+
+/* ---------------------------------------------------------------- config
+ * The drafter's shape. [TF1851 item 1]: taps (up to eight), block, mask
+ * token and layer kinds come from the drafter's config; its body is the qwen3
+ * layer with eleven tensors. */
+typedef struct dflash_config {
+  int32_t variant;        /* DFLASH_VARIANT_V1 (fusing drafter, named "DFlash") or _2 ("DFlash2") */
+  int32_t hidden;         /* H: hidden width of target taps and drafter */
+  int32_t n_taps;         /* N: tap planes, 1..8 */
+  int32_t tap_layers[DFLASH_MAX_TAPS]; /* target layer ids of the taps (first n_taps used) */
+  int32_t target_layers;  /* number of target layers (taps must be < this) */
+  int32_t n_layers;       /* L: drafter layers, 1..DFLASH_MAX_LAYERS */
+  int32_t n_q_heads;      /* query heads */
+  int32_t n_kv_heads;     /* key/value heads; n_q_heads % n_kv_heads == 0 */
+  int32_t head_dim;       /* d: 32, 64 or 128 */
+  int32_t ffn;            /* F: SwiGLU width */
+  int32_t vocab;          /* V: target vocabulary (shared embedding / LM head), multiple of 128 */
+  int32_t block;          /* must be 16 */
+  int32_t mask_token;     /* id of the mask token, in [0, V) */
+  int32_t causal;         /* must be 0: a causal draft is refused */
+  int32_t sliding_window; /* W: window of sliding layers, > 0 if any layer slides */
+  int32_t layer_kind[DFLASH_MAX_LAYERS]; /* DFLASH_LAYER_FULL or _SLIDING per layer */
+  float rope_theta;       /* rotate-half RoPE base */
+  float rms_eps;          /* RMSNorm epsilon */
+} dflash_config;
+
+/* Check a config. Returns DFLASH_OK or the refusal: E_TAPS_RANGE (n_taps
+ * outside 1..8, or a tap id outside [0, target_layers)), E_TAPS_REPEATED,
+ * E_CAUSAL (causal != 0), E_SHAPE (block != 16; n_q_heads % n_kv_heads;
+ * hidden != n_q_heads * head_dim; head_dim not 32/64/128; hidden, ffn or
+ * n_kv_heads*head_dim not a multiple of 128; vocab not a multiple of 128;
+ * mask token outside the vocabulary; a sliding layer with window <= 0;
+ * variant not 1 or 2), E_INVALID_ARG (NULL). [TF1851 item 1] */
+int dflash_config_validate(const dflash_config* cfg);
+
+/* "DFlash" for a v1 drafter, "DFlash2" otherwise, NULL for NULL. [TF1851
+ * item 6: Config.kind() names the layout]. Static string. */
+const char* dflash_kind(const dflash_config* cfg);
+
+/* Prompt-memory price of one prompt row's taps, in bytes [TF1851 item 3]:
+ * a v1 drafter holds its N planes, their row-major copy, fc's row and the
+ * fused row, (2N + 2) * H * 2 (18 * H * 2 for eight taps); a DFlash2 drafter
+ * keeps the N raw planes, N * H * 2. Returns -1 for NULL. (This library's
+ * fc reads the planes in place, so it never builds the row-major copy.) */
+int64_t dflash_tap_row_bytes(const dflash_config* cfg);
+
+/* One fused ring row: H bf16 values, 8 KiB a token at hidden 4096
+ * [TF1851 item 4]. Returns -1 for NULL. */
+int64_t dflash_fused_row_bytes(const dflash_config* cfg);
+
+/* ---------------------------------------------------------------- weights
+ * Device pointers to bf16 tensors, row-major [out_features, in_features].
+ * [TF1851 item 1]: eleven tensors a layer plus fc, hidden_norm and norm; the
+ * embedding / LM head is the target's, shared and frozen [EXPL 三]. All base
+ * addresses must be 16-byte aligned. The pointed-to memory must outlive the
+ * handle. */
+typedef struct dflash_layer_weights {
+  const void* input_norm; /* [H] */
+  const void* q_proj;     /* [n_q*d, H] */
+  const void* k_proj;     /* [n_kv*d, H] */
+  const void* v_proj;     /* [n_kv*d, H] */
+  const void* o_proj;     /* [H, n_q*d] */
+  const void* q_norm;     /* [d] per-head RMSNorm gain */
+  const void* k_norm;     /* [d] */
+  const void* post_norm;  /* [H] post-attention RMSNorm gain */
+  const void* gate_proj;  /* [F, H] */
+  const void* up_proj;    /* [F, H] */
+  const void* down_proj;  /* [H, F] */
+} dflash_layer_weights;
+
+typedef struct dflash_weights {
+  const void* fc;          /* [H, N*H]: concat of the N taps (tap 0 first) -> H */
+  const void* hidden_norm; /* [H] */
+  const void* norm;        /* [H] final norm */
+  const void* embed;       /* [V, H] embedding, also the LM head */
+  const dflash_layer_weights* layers; /* host array of n_layers entries (copied) */
+} dflash_weights;
+
+typedef struct dflash_handle dflash_handle;
+typedef struct dflash_state dflash_state;
+
+/* Create a drafter handle on the current CUDA device. Validates cfg (same
+ * codes as dflash_config_validate) and the weight pointers (E_INVALID_ARG for
+ * NULL or unaligned), checks for an sm_100-family device (E_UNSUPPORTED), and
+ * prepares the TMA descriptors of every weight. Host memory only; *out is set
+ * on success. */
+int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_handle** out);
+int dflash_destroy(dflash_handle* h); /* NULL is fine */
+
+/* ---------------------------------------------------------------- state
+ * Per-stream drafter state in caller-owned device memory: the fused ring
+ * (served span of fused rows, [TF1851 item 4]), each layer's context K/V
+ * cache (a full layer keeps the span, a sliding layer a ring of its window),
+ * the committed length of every stream, RoPE tables and the status word.
+ * ring_capacity R bounds every stream's length; positions >= R are refused
+ * (E_CAPACITY), as a request past the served window is [TF1851 "Exactness"]. */
+int dflash_state_bytes(const dflash_handle* h, int streams, int ring_capacity, size_t* bytes);
+
+/* Carve a state out of dev_mem (>= dflash_state_bytes, 256-byte aligned),
+ * upload its RoPE table (synchronously) and zero the lengths and status on
+ * `stream`. All streams start empty. *out is host memory freed by
+ * dflash_state_free (which does not touch dev_mem). */
+int dflash_state_init(dflash_handle* h, void* dev_mem, size_t bytes, int streams, int ring_capacity,
+                      dflash_stream_t stream, dflash_state** out);
+int dflash_state_free(dflash_state* st);
+
+/* Committed length of stream s as enqueued so far (host mirror). */
+int dflash_state_length(const dflash_state* st, int s, int64_t* len);
+
+/* Roll stream s back to new_len <= its length: rejected or cancelled rows
+ * are dropped [PROT "What is portable": rollback of the rejected suffix].
+ * Sliding-window cache slots that later rows overwrote are rebuilt from the
+ * fused ring (needs ws of dflash_fuse_workspace_bytes(h, W) bytes). */
+int dflash_state_truncate(dflash_handle* h, dflash_state* st, int s, int64_t new_len, void* ws,
+                          size_t ws_bytes, dflash_stream_t stream);
+
+/* Inspection of the state's device buffers (for checkpoints, tests and
+ * tools; writing through them bypasses the length bookkeeping).
+ * Ring: *ring = bf16 [streams][ring_capacity][H]; row p of stream s is the
+ * fused row of position p. Layer l caches: *k, *v = bf16
+ * [streams][n_kv_heads][cap][head_dim]; a full layer has cap = ring_capacity
+ * and slot = position, a sliding layer cap = min(W, ring_capacity) and
+ * slot = position % cap. */
+int dflash_state_ring(const dflash_state* st, void** ring);
+int dflash_state_cache(const dflash_state* st, int layer, void** k, void** v, int* cap);
+
+/* Read and clear the state's device status word (synchronises `stream`).
+ * *out receives DFLASH_STATUS_* bits. Returns E_TIMEOUT / E_DEVICE_FAULT when
+ * the corresponding bits were set, DFLASH_OK when clear. */
+int dflash_device_status(dflash_state* st, dflash_stream_t stream, int32_t* out);
+
+/* ---------------------------------------------------------------- fusion
+ * Tap fusion and context append [TF1851 item 4; ST3457 "Approach": each
+ * prompt chunk and committed window injects its rows' features].
+ * planes: host array of N device pointers; plane p is [rows, H] bf16 with a
+ * row stride of plane_row_stride elements (>= H, multiple of 8); plane
+ * bases 16-byte aligned. The rows are nseg segments in order: segment i holds
+ * seg_rows[i] rows of stream seg_stream[i] at positions seg_start[i] ..
+ * seg_start[i] + seg_rows[i] - 1 (host arrays). Each segment must start at
+ * its stream's committed length (append only; a stream may appear once) and
+ * end at or below the ring capacity (else E_CAPACITY).
+ * For every row: y = concat(planes) * fc^T; fused = bf16(RMSNorm(y) *
+ * hidden_norm) written to the ring. With DFLASH_FUSE_INJECT_KV, every layer l
+ * also gets K = bf16(RoPE(k_norm(fused * k_proj_l^T), pos)) and V =
+ * bf16(fused * v_proj_l^T) in its cache ("k and v only"), and the stream
+ * lengths advance. Without it only the ring is written and lengths stay
+ * (fusion-only timing). ws: >= dflash_fuse_workspace_bytes(h, rows). */
+int dflash_fuse_workspace_bytes(const dflash_handle* h, int rows, size_t* bytes);
+int dflash_fuse_taps(dflash_handle* h, dflash_state* st, const void* const* planes, int64_t plane_row_stride,
+                     int nseg, const int32_t* seg_stream, const int64_t* seg_start, const int32_t* seg_rows,
+                     int flags, void* ws, size_t ws_bytes, dflash_stream_t stream);
+
+/* ---------------------------------------------------------------- drafting
+ * One block forward for streams s_begin .. s_begin + s_count - 1 of the state
+ * [TF1851 item 1; EXPL 三]. For each stream, with C its committed length:
+ * rows = [anchor_ids[i], mask x 15] at positions C..C+15; every layer:
+ * h = RMSNorm(X); Q/K/V projections with per-head q_norm/k_norm and RoPE;
+ * non-causal attention over the layer's visible context (full: positions
+ * 0..C-1; sliding: C-W..C-1) plus the block's 16 rows; O-proj added to the
+ * residual; RMSNorm; SwiGLU MLP added to the residual. Then RMSNorm (norm)
+ * and the shared LM head on the 15 mask rows.
+ * anchor_ids: device int32 [s_count]. logits_out: device bf16
+ * [s_count*15, V] or NULL (then the logits live in ws). topk_ids (int32) and
+ * topk_vals (fp32, the bf16 logit values): device [s_count*15, k], k in
+ * 1..16, descending, ties to the lower id; either may be NULL to skip top-k.
+ * ws: >= dflash_draft_workspace_bytes(h, st, s_count, logits_out == NULL). */
+int dflash_draft_workspace_bytes(const dflash_handle* h, const dflash_state* st, int s_count, int need_logits,
+                                 size_t* bytes);
+int dflash_draft_block(dflash_handle* h, dflash_state* st, int s_begin, int s_count, const int32_t* anchor_ids,
+                       void* logits_out, int32_t* topk_ids, float* topk_vals, int k, void* ws, size_t ws_bytes,
+                       dflash_stream_t stream);
+
+/* ---------------------------------------------------------------- top-k
+ * Per row of a bf16 logit matrix [rows, vocab] (device, rows contiguous):
+ * the k largest logits (descending, ties to the lower id; ids int32, vals fp32
+ * = the bf16 values) ["PROT" top candidates at each position]. With uniforms
+ * (device fp32 [rows]) also one draw per row from softmax(logits / T) by
+ * inverse CDF: the smallest id whose running sum in ascending id order exceeds
+ * u * total (int32 [rows] in `sampled`). ids/vals may be NULL when k == 0;
+ * sampled must be non-NULL iff uniforms is. vocab multiple of 8, T > 0. */
+int dflash_topk(const void* logits, int rows, int vocab, int k, float temperature, const float* uniforms,
+                int32_t* ids, float* vals, int32_t* sampled, dflash_stream_t stream);
+
+/* ---------------------------------------------------------------- verify
+ * Target verification of S drafted blocks [EXPL 四; PROT "What is portable"].
+ * draft_ids: device int32 [S, 15] (d_1..d_15); target_logits: device bf16
+ * [S, 16, V], row i = the target's scores for position C+i+1 (after reading
+ * the anchor and d_1..d_i).
+ * GREEDY: t_i = argmax row i (ties to the lowest id); a = length of the
+ *   longest prefix with d_{i+1} == t_i; tokens = d_1..d_a, t_a.
+ * SAMPLE: p_i = softmax(row i / T), q_{i+1} = softmax(draft_logits row i / T)
+ *   (draft_logits: device bf16 [S, 15, V]); for i = 0..14 accept d_{i+1} iff
+ *   u[s][i][0] * q(d) < p_i(d); at the first rejection draw from
+ *   max(p_i - q_{i+1}, 0) (p_i if that is all zero); if none is rejected draw
+ *   the bonus from p_15; draws use u[s][i][1] by inverse CDF. uniforms: device
+ *   fp32 [S, 16, 2].
+ * Outputs: accept_len device int32 [S] (a in 0..15); out_tokens device int32
+ * [S, 16]: the a+1 committed tokens then -1. A draft id outside [0, V) is
+ * never accepted (and sets nothing else). ws: >= dflash_verify_workspace_bytes. */
+int dflash_verify_workspace_bytes(int mode, int streams, int vocab, size_t* bytes);
+int dflash_verify(int mode, int streams, int vocab, const int32_t* draft_ids, const void* target_logits,
+                  const void* draft_logits, const float* uniforms, float temperature, int32_t* accept_len,
+                  int32_t* out_tokens, void* ws, size_t ws_bytes, dflash_stream_t stream);
+
+/* ---------------------------------------------------------------- misc */
+const char* dflash_strerror(int code);
+/* Kernel launches enqueued by this process so far (all entry points). */
+int64_t dflash_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_H */

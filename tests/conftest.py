@@ -13,6 +13,15 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "slow: long CPU-side oracle run")
 
 
+@pytest.fixture(scope="session", autouse=True)
+def _built_library():
+    """Build libdflash.so (in-tree, sm_103a) once if it is missing or stale."""
+    from block_diffusion_speculative_tap_gb300 import build as B
+
+    B.build()
+    yield
+
+
 def pytest_collection_modifyitems(config, items):
     try:
         import torch

@@ -1,0 +1,160 @@
+"""GPU parity of tap fusion, K/V injection and the block draft against the
+oracle, on small drafters whose GEMMs still span several tiles with ragged
+tails, split-K chunks, sliding rings that wrap, several streams and an empty
+context.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synthetic_inputs as SI
+from parity_util import ATOL, RTOL, assert_close, check_topk_consistent, f64, topk_ids_match
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def D():
+    import block_diffusion_speculative_tap_gb300 as D
+
+    return D
+
+
+def small_model():
+    """A 9B-shaped drafter scaled down: sliding + full layers, d = 128."""
+    return dict(
+        variant=1, hidden=1024, n_taps=4, tap_layers=[2, 9, 17, 25], target_layers=32, n_layers=3,
+        n_q_heads=8, n_kv_heads=2, head_dim=128, ffn=2816, vocab=8192, block=16, mask_token=8191,
+        causal=0, sliding_window=100, layer_kinds=[1, 1, 0], rope_theta=1.0e6, rms_eps=1.0e-6,
+    )
+
+
+def check_state_vs_oracle(st, ref, m, s, upto):
+    ring = st.ring_view()[s, :upto]
+    assert_close(ring.cpu().float().numpy(), ref.fused[s][:upto], "fused ring rows")
+    for l in range(m["n_layers"]):
+        K, V, cap = st.cache_view(l)
+        lo = 0 if m["layer_kinds"][l] == SI.FULL else max(0, upto - cap)
+        pos = np.arange(lo, upto)
+        slots = pos % cap if m["layer_kinds"][l] == SI.SLIDING else pos
+        kg = K[s][:, slots].permute(1, 0, 2).cpu().float().numpy()
+        vg = V[s][:, slots].permute(1, 0, 2).cpu().float().numpy()
+        assert_close(kg, ref.k[s][l][lo:upto], f"K cache layer {l}")
+        assert_close(vg, ref.v[s][l][lo:upto], f"V cache layer {l}")
+
+
+def draft_vs_oracle(D, st, ref, m, anchors, k):
+    S = anchors.numel()
+    logits, ids, vals = st.draft(anchors.cuda(), k=k)
+    torch.cuda.synchronize()
+    rc, bits = st.status()
+    assert rc == 0 and bits == 0, (rc, bits)
+    check_topk_consistent(logits, ids, vals)
+    lg = logits.cpu().float().numpy().reshape(S, 15, -1)
+    ids = ids.cpu().numpy().reshape(S, 15, k)
+    stats = []
+    for s in range(S):
+        ol, _ = ref.draft(s, int(anchors[s]))
+        stats.append(assert_close(lg[s], ol, f"logits stream {s}"))
+        checked, near, bad = topk_ids_match(ids[s], ol, k, margin=2 * (ATOL + RTOL * np.abs(ol).max()))
+        assert bad == 0, (s, checked, near, bad)
+    return logits, stats
+
+
+def test_tiny_preset_fill_append_draft(D):
+    P = SI.preset("tiny")
+    m = P["model"]
+    w = SI.make_weights(m, P["seed"], device="cuda")
+    dr = D.Drafter(m, w)
+    st = dr.new_state(1, P["ring"])
+    ref = O.OracleStreams(m, O.weights_to_f64(w), 1)
+    taps = SI.make_taps(m, 128, P["seed"] + 1, device="cuda")
+    # a ragged 121-row fill then a 7-row append
+    st.fuse_taps([t[:121] for t in taps], [(0, 0, 121)])
+    st.fuse_taps([t[121:] for t in taps], [(0, 121, 7)])
+    ref.append(0, [f64(t[:121]) for t in taps])
+    ref.append(0, [f64(t[121:]) for t in taps])
+    assert st.length(0) == 128
+    check_state_vs_oracle(st, ref, m, 0, 128)
+    anchors = SI.anchor_ids(1, m["vocab"], m["mask_token"], P["seed"] + 2)
+    draft_vs_oracle(D, st, ref, m, anchors, P["topk"])
+
+
+def test_small_multistream_sliding_splitk(D):
+    m = small_model()
+    w = SI.make_weights(m, 77, device="cuda")
+    dr = D.Drafter(m, w)
+    ctx = [300, 57, 1]
+    S = len(ctx)
+    st = dr.new_state(S, 512)
+    ref = O.OracleStreams(m, O.weights_to_f64(w), S)
+    taps = SI.make_taps(m, sum(ctx), 78, device="cuda")
+    segs, r0 = [], 0
+    for s, c in enumerate(ctx):
+        segs.append((s, 0, c))
+        ref.append(s, [f64(t[r0 : r0 + c]) for t in taps])
+        r0 += c
+    st.fuse_taps(taps, segs)
+    for s, c in enumerate(ctx):
+        assert st.length(s) == c
+        check_state_vs_oracle(st, ref, m, s, c)
+    anchors = SI.anchor_ids(S, m["vocab"], m["mask_token"], 79)
+    batch_logits, _ = draft_vs_oracle(D, st, ref, m, anchors, 8)
+    # concurrent == solo: a stream drafted alone gives bit-identical logits
+    solo, _, _ = st.draft(anchors[1:2].cuda(), s_begin=1, k=8)
+    assert torch.equal(solo, batch_logits[15:30])
+
+
+def test_truncate_and_reappend(D):
+    m = small_model()
+    w = SI.make_weights(m, 91, device="cuda")
+    dr = D.Drafter(m, w)
+    st = dr.new_state(1, 512)
+    ref = O.OracleStreams(m, O.weights_to_f64(w), 1)
+    taps = SI.make_taps(m, 300, 92, device="cuda")
+    st.fuse_taps(taps, [(0, 0, 300)])
+    ref.append(0, [f64(t) for t in taps])
+    anchors = SI.anchor_ids(1, m["vocab"], m["mask_token"], 93)
+    fresh, _, _ = st.draft(anchors.cuda(), k=8)
+    fresh = fresh.clone()
+    # roll back 50 rows: the sliding rings lose positions 150..199 to 250..299
+    st.truncate(0, 250)
+    ref.truncate(0, 250)
+    assert st.length(0) == 250
+    check_state_vs_oracle(st, ref, m, 0, 250)
+    draft_vs_oracle(D, st, ref, m, anchors, 8)
+    # re-append the same rows: resumed == fresh
+    st.fuse_taps([t[250:] for t in taps], [(0, 250, 50)])
+    again, _, _ = st.draft(anchors.cuda(), k=8)
+    assert_close(again.cpu().float().numpy(), fresh.cpu().float().numpy(), "resumed vs fresh", atol=0, rtol=0)
+
+
+def test_capacity_and_append_rules(D):
+    m = small_model()
+    w = SI.make_weights(m, 5, device="cuda")
+    dr = D.Drafter(m, w)
+    st = dr.new_state(2, 64)
+    taps = SI.make_taps(m, 70, 6, device="cuda")
+    with pytest.raises(D.DFlashError) as e:
+        st.fuse_taps(taps, [(0, 0, 70)])
+    assert e.value.code == -6  # past the ring
+    with pytest.raises(D.DFlashError) as e:
+        st.fuse_taps([t[:5] for t in taps], [(0, 3, 5)])
+    assert e.value.code == -1  # not an append
+    st.fuse_taps([t[:64] for t in taps], [(0, 0, 64)])
+    assert st.length(0) == 64 and st.length(1) == 0
+
+
+def test_bad_anchor_sets_status(D):
+    m = small_model()
+    w = SI.make_weights(m, 8, device="cuda")
+    dr = D.Drafter(m, w)
+    st = dr.new_state(1, 64)
+    taps = SI.make_taps(m, 20, 9, device="cuda")
+    st.fuse_taps(taps, [(0, 0, 20)])
+    st.draft(torch.tensor([m["vocab"] + 3], dtype=torch.int32, device="cuda"), k=4)
+    rc, bits = st.status()
+    assert rc == -10 and bits == 1
+    rc, bits = st.status()
+    assert rc == 0 and bits == 0

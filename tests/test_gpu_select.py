@@ -1,0 +1,163 @@
+"""GPU parity of top-k, sampling draws and verification against the oracle.
+
+Inputs are seeded synthetic logits fed to both sides. Ids, accept lengths and
+tokens are compared bit for bit; a sampling decision is exempt only when the
+oracle's float64 margin to the other outcome is below 1e-4 (fp32 softmax over
+the vocabulary cannot resolve it), and such cases are counted.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synthetic_inputs as SI
+from parity_util import f64
+
+pytestmark = pytest.mark.gpu
+
+MARGIN = 1e-4
+
+
+@pytest.fixture(scope="module")
+def D():
+    import block_diffusion_speculative_tap_gb300 as D
+
+    return D
+
+
+def _tie_heavy(rows, V, seed):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randint(-4, 5, (rows, V), generator=g).float() * 0.5
+    return x.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("V,k", [(4096, 4), (151936, 8), (5000, 16), (136, 3)])
+def test_topk_matches_oracle(D, V, k):
+    rows = 37
+    lg = SI.make_logits((rows, V), 1.0, seed=V + k)
+    lg[5:9] = _tie_heavy(4, V, 3)  # rows full of exact ties
+    ids, vals, _ = D.topk(lg.cuda(), k)
+    ids, vals = ids.cpu().numpy(), vals.cpu().numpy()
+    ref = f64(lg)
+    for r in range(rows):
+        oi, ov = O.topk(ref[r], k)
+        assert list(ids[r]) == list(oi), r
+        assert np.array_equal(vals[r].astype(np.float64), ov), r
+
+
+def test_topk_empty_and_zero_k(D):
+    lg = SI.make_logits((0, 4096), 1.0, seed=1).cuda()
+    ids, vals, _ = D.topk(lg, 4)
+    assert ids.shape == (0, 4)
+    lg = SI.make_logits((3, 4096), 1.0, seed=1).cuda()
+    ids, vals, s = D.topk(lg, 0, uniforms=torch.rand(3, device="cuda"))
+    assert s.shape == (3,)
+
+
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_sampling_draws_match_oracle(D, T):
+    rows, V = 64, 151936
+    lg = SI.make_logits((rows, V), 2.0, seed=11)
+    u = SI.make_uniforms((rows,), seed=12)
+    _, _, s = D.topk(lg.cuda(), 0, temperature=T, uniforms=u.cuda())
+    s = s.cpu().numpy()
+    ref_ids, margins = O.sample_rows(f64(lg), T, f64(u))
+    clear = margins > MARGIN
+    assert clear.sum() >= rows - 2
+    assert np.array_equal(s[clear], ref_ids[clear])
+
+
+def test_greedy_golden_fixtures(D):
+    with open(os.path.join(os.path.dirname(__file__), "golden", "greedy_verify_cases.json")) as f:
+        cases = json.load(f)["cases"]
+    S = len(cases)
+    V = cases[0]["vocab"]
+    tl = torch.zeros(S, 16, V)
+    draft = torch.zeros(S, 15, dtype=torch.int32)
+    for s, c in enumerate(cases):
+        for i, pk in enumerate(c["peaks"]):
+            for j in pk:
+                tl[s, i, j] = 2.0
+        draft[s] = torch.tensor(c["draft"])
+    a, toks = D.verify_greedy(draft.cuda(), tl.to(torch.bfloat16).cuda())
+    a, toks = a.cpu().tolist(), toks.cpu().tolist()
+    for s, c in enumerate(cases):
+        assert a[s] == c["expect_a"], c["name"]
+        assert toks[s] == c["expect_tokens"], c["name"]
+
+
+@pytest.mark.parametrize("S,V,std", [(32, 151936, 2.0), (5, 4096, 1.0)])
+def test_greedy_planted_matches_oracle(D, S, V, std):
+    tl = SI.make_logits((S, 16, V), std, seed=21)
+    draft = SI.make_token_ids((S, 15), V, seed=22)
+    lengths = SI.make_accept_lengths(S, seed=23)
+    SI.plant_accepts(tl, draft, lengths)
+    a, toks = D.verify_greedy(draft.cuda(), tl.cuda())
+    a, toks = a.cpu().tolist(), toks.cpu().tolist()
+    ref = f64(tl)
+    for s in range(S):
+        oa, ot = O.greedy_verify(draft[s].tolist(), ref[s])
+        assert a[s] == oa == min(lengths[s], 15)
+        assert toks[s] == ot
+
+
+def test_greedy_out_of_range_draft_never_accepted(D):
+    V = 4096
+    tl = torch.zeros(1, 16, V)
+    tl[0, :, 7] = 1.0
+    draft = torch.full((1, 15), 7, dtype=torch.int32)
+    draft[0, 3] = V + 5
+    a, toks = D.verify_greedy(draft.cuda(), tl.to(torch.bfloat16).cuda())
+    assert a.item() == 3 and toks[0, 3].item() == 7
+
+
+def _sampling_inputs(S, V, seed, noise):
+    tl = SI.make_logits((S, 16, V), 1.0, seed)
+    dl = (tl[:, :15].float() + noise * SI.make_logits((S, 15, V), 1.0, seed + 1).float()).to(torch.bfloat16)
+    # drafted tokens: drawn from the drafter's rows (input construction)
+    g = torch.Generator().manual_seed(seed + 2)
+    probs = torch.softmax(dl.float(), dim=-1).view(-1, V)
+    draft = torch.multinomial(probs, 1, generator=g).view(S, 15).to(torch.int32)
+    u = SI.make_uniforms((S, 16, 2), seed + 3)
+    return tl, dl, draft, u
+
+
+@pytest.mark.parametrize("S,V,noise,T", [(8, 151936, 0.3, 1.0), (16, 4096, 1.0, 1.0), (8, 4096, 0.5, 0.6)])
+def test_sampling_verify_matches_oracle(D, S, V, noise, T):
+    tl, dl, draft, u = _sampling_inputs(S, V, 31 + S, noise)
+    a, toks = D.verify_sample(draft.cuda(), tl.cuda(), dl.cuda(), u.cuda(), T)
+    a, toks = a.cpu().tolist(), toks.cpu().tolist()
+    tr, dr, ur = f64(tl), f64(dl), f64(u)
+    checked = 0
+    for s in range(S):
+        oa, ot, margins = O.sampling_verify(draft[s].tolist(), tr[s], dr[s], ur[s], T)
+        if min(margins) <= MARGIN:
+            continue
+        checked += 1
+        assert a[s] == oa, s
+        assert toks[s] == ot, s
+    assert checked >= S - 2
+
+
+def test_sampling_verify_distribution_is_target(D):
+    """Many single-position trials: the first committed token follows p
+    (chi-square), the lossless property of the sampling rule."""
+    from scipy.stats import chisquare
+
+    V, n = 8, 4096
+    tl1 = torch.tensor([[0.5, 1.0, -1.0, 2.0, 0.0, -0.5, 1.5, 0.25]])
+    dl1 = torch.tensor([[1.0, 0.0, 0.5, 1.0, 1.0, -1.0, 0.0, 2.0]])
+    tl = tl1.to(torch.bfloat16).expand(n, V).reshape(n, 1, V).expand(n, 16, V).contiguous()
+    dl = dl1.to(torch.bfloat16).expand(n, V).reshape(n, 1, V).expand(n, 15, V).contiguous()
+    q = torch.softmax(dl1.to(torch.bfloat16).float(), -1)[0]
+    g = torch.Generator().manual_seed(5)
+    draft = torch.multinomial(q.expand(n, V), 15, replacement=True, generator=g).to(torch.int32)
+    u = torch.rand(n, 16, 2, generator=g)
+    a, toks = D.verify_sample(draft.cuda(), tl.cuda(), dl.cuda(), u.cuda(), 1.0)
+    first = toks[:, 0].cpu().numpy()
+    p = torch.softmax(tl1.to(torch.bfloat16).double(), -1)[0].numpy()
+    counts = np.bincount(first, minlength=V)
+    assert chisquare(counts, p * n).pvalue > 1e-3
