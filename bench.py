@@ -1,0 +1,472 @@
+#!/usr/bin/env python
+"""Benchmark of the DFlash drafting hot path on GB300.
+
+Default workload: the 9B-shaped DFlash v1 drafter at batch 1 (8 taps of
+hidden 4096, 6 layers of 32/8 heads x 128, SwiGLU 12288, vocab 151936,
+layers 0-4 sliding over 2048 positions, layer 5 full) over a 4096-token
+context. One step is one decode round of the whole hot path:
+  fuse the round's 16 committed tap rows (fc + hidden_norm + ring + K/V
+  injection into all six layers), draft one block of 16 rows (anchor + 15
+  mask rows), top-8 per position, greedy verification against the target's
+  logits for the 16 verify rows.
+The context grows by 16 rows a step, as a fully accepted decode loop does.
+
+Printed: one JSON line (rank 0). `value` is draft blocks/s over all ranks
+(weak scaling: every rank drafts its own stream; batch 1 does not shard, so
+ranks are replicas). Weights (3.8 GB) exceed L2 (129 MB), so no flush is
+needed between steps.
+
+--impl reference times the CPU oracle (float64 NumPy) on the same workload,
+on the host cores, as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft blocks/s (block 16) and fused tap rows/s; % of HBM/tensor-core roofline"
+UNIT = "blocks/s"
+WORKLOAD = (
+    "9B-shaped DFlash v1 drafter, batch 1: 8 taps x hidden 4096, 6 layers (32q/8kv x 128, SwiGLU 12288), "
+    "vocab 151936, 4096-token context, decode round = 16-row tap fusion + K/V injection, block-16 draft, "
+    "top-8, greedy verify"
+)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = (
+        "index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+        "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+        "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap"
+    )
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True,
+            )
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {
+            "sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "reasons": sorted(reasons),
+            "samples": len(sm),
+        }
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world):
+    import torch
+
+    import block_diffusion_speculative_tap_gb300 as D
+    import synthetic_inputs as SI
+    from block_diffusion_speculative_tap_gb300 import _abi as A
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    P = SI.preset("9b")
+    m = P["model"]
+    C0 = P["context"][0]
+    seed = P["seed"] + rank
+    w = SI.make_weights(m, seed, device=dev)
+    dr = D.Drafter(m, w)
+    total_steps = args.warmup + 2 * args.steps + args.e2e_steps + 2
+    R = C0 + 16 * (total_steps + 2)
+    st = dr.new_state(1, max(R, P["ring"]))
+    ctx = SI.make_taps(m, C0, seed + 1, device=dev)
+    st.fuse_taps(ctx, [(0, 0, C0)])
+    del ctx
+    step_taps = SI.make_taps(m, 16, seed + 2, device=dev)
+    anchor = SI.anchor_ids(1, m["vocab"], m["mask_token"], seed + 3, device=dev)
+    tl = SI.make_logits((1, 16, m["vocab"]), 1.0, seed + 4, device=dev)
+    logits = torch.empty(15, m["vocab"], dtype=torch.bfloat16, device=dev)
+    ids = torch.empty(15, 8, dtype=torch.int32, device=dev)
+    vals = torch.empty(15, 8, dtype=torch.float32, device=dev)
+    acc = torch.empty(1, dtype=torch.int32, device=dev)
+    toks = torch.empty(1, 16, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        C = st.length(0)
+        st.fuse_taps(step_taps, [(0, C, 16)])
+        st.draft(anchor, k=8, logits=logits, ids=ids, vals=vals)
+        D.verify_greedy(ids, tl, accept=acc, tokens=toks)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    def timed(n, trace):
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        if trace:
+            A.lib.dflash_trace_enable(1)
+        l0 = D.launch_count()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if trace:
+            A.lib.dflash_trace_enable(0)
+        if world > 1:
+            torch.distributed.barrier()
+        return e0.elapsed_time(e1), D.launch_count() - l0
+
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    ms, launches = timed(args.steps, trace=False)
+    clk = clocks.stop()
+    ms_tr, _ = timed(args.steps, trace=True)
+    # per-launch durations of the traced region
+    import ctypes as C
+
+    recs = []
+    for i in range(A.lib.dflash_trace_count()):
+        nm, t, b, fl = C.c_char_p(), C.c_float(), C.c_double(), C.c_double()
+        if A.lib.dflash_trace_get(i, C.byref(nm), C.byref(t), C.byref(b), C.byref(fl)) == 0:
+            recs.append((nm.value.decode(), t.value, b.value, fl.value))
+    by = {}
+    for nm, t, b, fl in recs:
+        e = by.setdefault(nm, [0, 0.0, 0.0, 0.0])
+        e[0] += 1
+        e[1] += t
+        e[2] += b
+        e[3] += fl
+    ms_max = ms
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_max = float(tt.item())
+
+    # ---- fused tap rows/s: a 4096-row prompt fill (fc + hidden_norm + K/V injection)
+    fill_rows = 4096
+    st2 = dr.new_state(1, fill_rows)
+    fill_taps = SI.make_taps(m, fill_rows, seed + 5, device=dev)
+    for _ in range(2):
+        st2.fuse_taps(fill_taps, [(0, 0, fill_rows)])
+        st2.truncate(0, 0)
+    torch.cuda.synchronize()
+    A.lib.dflash_trace_enable(1)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nfill = 3
+    f0.record(stream)
+    for _ in range(nfill):
+        st2.fuse_taps(fill_taps, [(0, 0, fill_rows)])
+        st2.truncate(0, 0)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    A.lib.dflash_trace_enable(0)
+    fill_ms = f0.elapsed_time(f1) / nfill
+    fill_recs = {}
+    for i in range(A.lib.dflash_trace_count()):
+        nm, t, b, fl = C.c_char_p(), C.c_float(), C.c_double(), C.c_double()
+        if A.lib.dflash_trace_get(i, C.byref(nm), C.byref(t), C.byref(b), C.byref(fl)) == 0:
+            e = fill_recs.setdefault(nm.value.decode(), [0, 0.0, 0.0, 0.0])
+            e[0] += 1
+            e[1] += t.value
+            e[2] += b.value
+            e[3] += fl.value
+    del st2, fill_taps
+
+    # ---- e2e: host buffers, copies inside the timed region, one readback a step
+    h_taps = [t.cpu().pin_memory() for t in step_taps]
+    h_anchor = anchor.cpu().pin_memory()
+    h_tl = tl.cpu().pin_memory()
+    h_acc = torch.empty(1, dtype=torch.int32).pin_memory()
+    h_toks = torch.empty(1, 16, dtype=torch.int32).pin_memory()
+    h_ids = torch.empty(15, 8, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * 2 for t in h_taps) + 4 + h_tl.numel() * 2
+    d2h = 4 + 64 + 15 * 8 * 4
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        for d_, h_ in zip(step_taps, h_taps):
+            d_.copy_(h_, non_blocking=True)
+        anchor.copy_(h_anchor, non_blocking=True)
+        tl.copy_(h_tl, non_blocking=True)
+        step()
+        h_acc.copy_(acc, non_blocking=True)
+        h_toks.copy_(toks, non_blocking=True)
+        h_ids.copy_(ids, non_blocking=True)
+        stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    rc, bits = st.status()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} bits {bits}")
+
+    pk, src = peaks()
+    gemm = [v for k, v in by.items() if k.startswith("gemm.")]
+    g_ms = sum(v[1] for v in gemm)
+    g_b = sum(v[2] for v in gemm)
+    g_n = sum(v[0] for v in gemm)
+    achieved = (g_b / g_n) / ((g_ms / g_n) * 1e-3) / 1e9 if g_n else None
+    fc = fill_recs.get("gemm.fc", [0, 0.0, 0.0, 0.0])
+    fc_tflops = fc[3] / (fc[1] * 1e-3) / 1e12 if fc[0] else None
+    step_ms = ms_max / args.steps
+    out = {
+        "metric": METRIC,
+        "value": world * args.steps / (ms_max * 1e-3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,0.02) weights, N(0,1) taps, N(0,1) target logits)",
+        "config": {
+            "workload": WORKLOAD,
+            "streams_per_gpu": 1,
+            "context_start": C0,
+            "context_growth_per_step": 16,
+            "ring": st.ring,
+            "l2": "no flush: 3.8 GB of weights stream through a 129 MB L2 every step",
+            "parallelism": f"replicas x{world}",
+        },
+        "fused_tap_rows_per_s": fill_rows / (fill_ms * 1e-3),
+        "fill": {
+            "rows": fill_rows,
+            "ms": fill_ms,
+            "fc_tflops": fc_tflops,
+            "fc_frac_of_bf16_peak": (fc_tflops / pk["bf16_tflops"]) if fc_tflops else None,
+            "peak_source": src,
+            "kernels_ms": {k: v[1] / nfill for k, v in fill_recs.items()},
+        },
+        "roofline": {
+            "kernel": "gemm_kernel (tcgen05, every GEMM launch of the decode step)",
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": pk["hbm_gbs"],
+            "unit": "GB/s",
+            "frac": (achieved / pk["hbm_gbs"]) if achieved else None,
+            "traffic": None,
+            "peak_source": src,
+            "gemm_ms_per_step": g_ms / args.steps,
+            "gemm_bytes_per_step": g_b / args.steps,
+            "gemm_launches_per_step": g_n / args.steps,
+        },
+        "step_kernels_ms": {k: v[1] / args.steps for k, v in sorted(by.items(), key=lambda kv: -kv[1][1])},
+        "ms_per_step_traced": ms_tr / args.steps,
+        "e2e": {
+            "value": args.e2e_steps / e2e_s * world,
+            "unit": UNIT,
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "steps": args.e2e_steps,
+        },
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args, m, w, seed, C0)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return out
+
+
+# ---------------------------------------------------------------- oracle (reference / baseline)
+def oracle_step_setup(m, w64, C0, ctx_planes, step_planes):
+    import oracle as O
+
+    ref = O.OracleStreams(m, w64, 1)
+    ref.append(0, ctx_planes)
+    return ref
+
+
+def cpu_baseline(args, m, w, seed, C0):
+    """Time the oracle on a bounded sample of the same workload: the decode
+    round (16-row fusion + K/V injection, block draft, top-8, greedy verify)
+    at the 4096-row context."""
+    import numpy as np
+
+    import oracle as O
+    import synthetic_inputs as SI
+
+    t_setup = time.perf_counter()
+    w64 = O.weights_to_f64(w)
+    ctx = [O.to_f64(p) for p in SI.make_taps(m, C0, seed + 1, device="cuda")]
+    ref = O.OracleStreams(m, w64, 1)
+    ref.append(0, ctx)
+    del ctx
+    step = [O.to_f64(p) for p in SI.make_taps(m, 16, seed + 2, device="cuda")]
+    anchor = int(SI.anchor_ids(1, m["vocab"], m["mask_token"], seed + 3)[0])
+    tl = O.to_f64(SI.make_logits((1, 16, m["vocab"]), 1.0, seed + 4))[0]
+    setup_s = time.perf_counter() - t_setup
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        ref.append(0, step)
+        logits, _ = ref.draft(0, anchor)
+        ids = [O.topk(logits[r], 8)[0] for r in range(15)]
+        O.greedy_verify([int(i[0]) for i in ids], tl)
+        n += 1
+        if time.perf_counter() - t0 > args.cpu_seconds or n >= 50:
+            break
+    dt = time.perf_counter() - t0
+    threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+    return {
+        "value": n / dt,
+        "unit": UNIT,
+        "cores": threads,
+        "kind": "oracle",
+        "sample": f"{n} decode rounds of the same workload (float64 NumPy oracle, BLAS threads={threads}); "
+        f"context set-up {setup_s:.1f} s not timed",
+    }
+
+
+def run_reference(args):
+    import numpy as np
+
+    import oracle as O
+    import synthetic_inputs as SI
+
+    P = SI.preset("9b")
+    m = P["model"]
+    C0 = P["context"][0]
+    seed = P["seed"]
+    w = SI.make_weights(m, seed, device="cpu")
+    w64 = O.weights_to_f64(w)
+    del w
+    ref = O.OracleStreams(m, w64, 1)
+    ref.append(0, [O.to_f64(p) for p in SI.make_taps(m, C0, seed + 1)])
+    step = [O.to_f64(p) for p in SI.make_taps(m, 16, seed + 2)]
+    anchor = int(SI.anchor_ids(1, m["vocab"], m["mask_token"], seed + 3)[0])
+    tl = O.to_f64(SI.make_logits((1, 16, m["vocab"]), 1.0, seed + 4))[0]
+
+    def one():
+        ref.append(0, step)
+        logits, _ = ref.draft(0, anchor)
+        ids = [O.topk(logits[r], 8)[0] for r in range(15)]
+        O.greedy_verify([int(i[0]) for i in ids], tl)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = time.perf_counter() - t0
+    threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+    v = args.steps / dt
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": v,
+        "unit": UNIT,
+        "n_gpus": 0,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "context_start": C0, "context_growth_per_step": 16},
+        "cpu_baseline": {
+            "value": v,
+            "unit": UNIT,
+            "cores": threads,
+            "kind": "oracle",
+            "sample": f"{args.steps} timed decode rounds after {args.warmup} untimed ones (float64 NumPy oracle)",
+        },
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    out = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

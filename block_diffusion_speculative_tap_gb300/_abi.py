@@ -129,9 +129,14 @@ def _load():
     fn("dflash_fuse_taps", C.c_int, vp, vp, P(vp), i64, C.c_int, P(i32), P(i64), P(i32), C.c_int, vp, sz, vp)
     fn("dflash_draft_workspace_bytes", C.c_int, vp, vp, C.c_int, C.c_int, P(sz))
     fn("dflash_draft_block", C.c_int, vp, vp, C.c_int, C.c_int, vp, vp, vp, vp, C.c_int, vp, sz, vp)
+    fn("dflash_draft_layers", C.c_int, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, vp, vp, sz, vp)
+    fn("dflash_draft_head", C.c_int, vp, vp, C.c_int, vp, vp, vp, vp, C.c_int, vp, sz, vp)
     fn("dflash_topk", C.c_int, vp, C.c_int, C.c_int, C.c_int, C.c_float, vp, vp, vp, vp, vp)
     fn("dflash_verify_workspace_bytes", C.c_int, C.c_int, C.c_int, C.c_int, P(sz))
-    fn("dflash_verify", C.c_int, C.c_int, C.c_int, C.c_int, vp, vp, vp, vp, C.c_float, vp, vp, vp, sz, vp)
+    fn("dflash_verify", C.c_int, C.c_int, C.c_int, C.c_int, vp, C.c_int, vp, vp, vp, C.c_float, vp, vp, vp, sz, vp)
+    fn("dflash_trace_enable", C.c_int, C.c_int)
+    fn("dflash_trace_count", C.c_int)
+    fn("dflash_trace_get", C.c_int, C.c_int, P(C.c_char_p), P(C.c_float), P(C.c_double), P(C.c_double))
     return lib
 
 
@@ -158,9 +163,14 @@ EXPORTED = [
     "dflash_fuse_taps",
     "dflash_draft_workspace_bytes",
     "dflash_draft_block",
+    "dflash_draft_layers",
+    "dflash_draft_head",
     "dflash_topk",
     "dflash_verify_workspace_bytes",
     "dflash_verify",
+    "dflash_trace_enable",
+    "dflash_trace_count",
+    "dflash_trace_get",
 ]
 
 

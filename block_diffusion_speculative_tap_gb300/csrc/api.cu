@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -16,6 +17,44 @@ namespace dfl {
 static std::atomic<long long> g_launches{0};
 void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? DFLASH_OK : DFLASH_E_CUDA; }
+
+namespace {
+struct TraceRec {
+  const char* name;
+  cudaEvent_t a, b;
+  double bytes, flops;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace;
+std::vector<cudaEvent_t> g_event_pool;
+size_t g_event_next = 0;
+
+cudaEvent_t next_event() {
+  if (g_event_next == g_event_pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    g_event_pool.push_back(e);
+  }
+  return g_event_pool[g_event_next++];
+}
+}  // namespace
+
+TraceScope::TraceScope(cudaStream_t s, const char* name, double bytes, double flops) : st(s), idx(-1) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (!g_trace_on) return;
+  cudaEvent_t a = next_event(), b = next_event();
+  if (!a || !b) return;
+  if (cudaEventRecord(a, s) != cudaSuccess) return;
+  g_trace.push_back(TraceRec{name, a, b, bytes, flops});
+  idx = static_cast<int>(g_trace.size()) - 1;
+}
+
+TraceScope::~TraceScope() {
+  if (idx < 0) return;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (idx < static_cast<int>(g_trace.size())) cudaEventRecord(g_trace[idx].b, st);
+}
 
 // Bump allocator over caller-owned memory; with base == nullptr it only sizes.
 struct Carver {
@@ -108,6 +147,38 @@ const char* dflash_strerror(int code) {
 }
 
 int64_t dflash_launch_count(void) { return g_launches.load(); }
+
+int dflash_trace_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (on) {
+    g_trace.clear();
+    g_event_next = 0;
+  }
+  g_trace_on = on != 0;
+  return DFLASH_OK;
+}
+
+int dflash_trace_count(void) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  return static_cast<int>(g_trace.size());
+}
+
+int dflash_trace_get(int i, const char** name, float* ms, double* bytes, double* flops) {
+  TraceRec r;
+  {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (i < 0 || i >= static_cast<int>(g_trace.size())) return DFLASH_E_INVALID_ARG;
+    r = g_trace[i];
+  }
+  if (cudaEventSynchronize(r.b) != cudaSuccess) return DFLASH_E_CUDA;
+  float t = 0.f;
+  if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) return DFLASH_E_CUDA;
+  if (name) *name = r.name;
+  if (ms) *ms = t;
+  if (bytes) *bytes = r.bytes;
+  if (flops) *flops = r.flops;
+  return DFLASH_OK;
+}
 
 int dflash_config_validate(const dflash_config* c) {
   if (!c) return DFLASH_E_INVALID_ARG;
@@ -336,6 +407,7 @@ struct FuseWs {
   int* counters;
   int* row_stream;
   int* row_pos;
+  int* row_end;
   float* y;
   __nv_bfloat16* fused;
   float* partial;
@@ -358,6 +430,7 @@ GemmPlan fc_plan(const dflash_handle* h, int rows) {
   p.ksplit = ksplit_for(h, p.M, p.K, rows);
   p.epi = EPI_STORE_F32;
   p.epi_args.ldo = c.hidden;
+  p.name = "gemm.fc";
   return p;
 }
 
@@ -392,6 +465,7 @@ GemmPlan kv_plan(const dflash_handle* h, const dflash_state* st, int rows, int l
   p.epi_args.head_dim = c.head_dim;
   p.epi_args.eps = c.rms_eps;
   p.epi_args.pos_mode = 1;
+  p.name = "gemm.kv_inject";
   return p;
 }
 
@@ -412,6 +486,7 @@ size_t fuse_ws_layout(const dflash_handle* h, int rows, void* base, FuseWs* ws) 
   w.counters = cv.take<int>(counters * ((rows + pass - 1) / pass + 1));
   w.row_stream = cv.take<int>(std::max(rows, 1));
   w.row_pos = cv.take<int>(std::max(rows, 1));
+  w.row_end = cv.take<int>(std::max(rows, 1));
   w.y = cv.take<float>(static_cast<size_t>(pass) * c.hidden);
   w.fused = cv.take<__nv_bfloat16>(static_cast<size_t>(pass) * c.hidden);
   w.partial = cv.take<float>(partial / sizeof(float) + 1);
@@ -422,7 +497,8 @@ size_t fuse_ws_layout(const dflash_handle* h, int rows, void* base, FuseWs* ws) 
 
 // K/V injection for `rows` fused rows already in `fused` (rows tables in ws).
 int inject_kv(dflash_handle* h, dflash_state* st, const __nv_bfloat16* fused, const int* row_stream,
-              const int* row_pos, int rows, bool sliding_only, int*& counters, float* partial, cudaStream_t s) {
+              const int* row_pos, const int* row_end, int rows, bool sliding_only, int*& counters, float* partial,
+              cudaStream_t s) {
   const dflash_config& c = h->cfg;
   for (int l0 = 0; l0 < c.n_layers; l0 += layers_per_kv_pass()) {
     GemmPlan kp = kv_plan(h, st, rows, l0, std::min(c.n_layers, l0 + layers_per_kv_pass()), sliding_only);
@@ -431,6 +507,7 @@ int inject_kv(dflash_handle* h, dflash_state* st, const __nv_bfloat16* fused, co
     kp.ldb = c.hidden;
     kp.epi_args.row_stream = row_stream;
     kp.epi_args.row_pos = row_pos;
+    kp.epi_args.row_end = row_end;
     kp.epi_args.rope = st->rope;
     const int rc = gemm_launch(kp, partial, counters, st->status, h->num_sms, s);
     if (rc) return rc;
@@ -476,7 +553,7 @@ int dflash_fuse_taps(dflash_handle* h, dflash_state* st, const void* const* plan
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool inject = (flags & DFLASH_FUSE_INJECT_KV) != 0;
 
-  int rc = launch_prep_rows(w.row_stream, w.row_pos, nullptr, nullptr, nseg, rows, packed.data(), s);
+  int rc = launch_prep_rows(w.row_stream, w.row_pos, w.row_end, nullptr, nseg, rows, packed.data(), s);
   if (rc) return rc;
   // zero every split-K counter of this call at once
   const size_t counters_bytes = reinterpret_cast<char*>(w.row_stream) - reinterpret_cast<char*>(w.counters);
@@ -496,12 +573,13 @@ int dflash_fuse_taps(dflash_handle* h, dflash_state* st, const void* const* plan
                             st->R, c.rms_eps, s);
     if (rc) return rc;
     if (inject) {
-      rc = inject_kv(h, st, w.fused, w.row_stream + r0, w.row_pos + r0, n, false, counters, w.partial, s);
+      rc = inject_kv(h, st, w.fused, w.row_stream + r0, w.row_pos + r0, w.row_end + r0, n, false, counters,
+                     w.partial, s);
       if (rc) return rc;
     }
   }
   if (inject) {
-    rc = launch_prep_rows(nullptr, nullptr, st->lens, nullptr, nseg, 0, packed.data(), s);
+    rc = launch_prep_rows(nullptr, nullptr, nullptr, st->lens, nseg, 0, packed.data(), s);
     if (rc) return rc;
     for (int i = 0; i < nseg; ++i) st->host_len[seg_stream[i]] = seg_start[i] + seg_rows[i];
   }
@@ -531,17 +609,18 @@ int dflash_state_truncate(dflash_handle* h, dflash_state* st, int s_id, int64_t 
     const size_t counters_bytes = reinterpret_cast<char*>(w.row_stream) - reinterpret_cast<char*>(w.counters);
     if (cudaMemsetAsync(w.counters, 0, counters_bytes, s) != cudaSuccess) return DFLASH_E_CUDA;
     int seg[3] = {s_id, static_cast<int>(lo), n};
-    int rc = launch_prep_rows(w.row_stream, w.row_pos, nullptr, nullptr, 1, n, seg, s);
+    int rc = launch_prep_rows(w.row_stream, w.row_pos, w.row_end, nullptr, 1, n, seg, s);
     if (rc) return rc;
     int* counters = w.counters;
     for (int r0 = 0; r0 < n; r0 += kFusePass) {
       const int m = std::min(kFusePass, n - r0);
       const __nv_bfloat16* rows = st->ring + (static_cast<int64_t>(s_id) * st->R + lo + r0) * c.hidden;
-      rc = inject_kv(h, st, rows, w.row_stream + r0, w.row_pos + r0, m, true, counters, w.partial, s);
+      rc = inject_kv(h, st, rows, w.row_stream + r0, w.row_pos + r0, w.row_end + r0, m, true, counters,
+                     w.partial, s);
       if (rc) return rc;
     }
   }
-  const int rc = launch_prep_rows(nullptr, nullptr, st->lens, nullptr, 1, 0, packed, s);
+  const int rc = launch_prep_rows(nullptr, nullptr, nullptr, st->lens, 1, 0, packed, s);
   if (rc) return rc;
   st->host_len[s_id] = new_len;
   return DFLASH_OK;
@@ -591,6 +670,7 @@ void layer_plans(const dflash_handle* h, int l, int T, GemmPlan& qkv, GemmPlan& 
   qkv.K = c.hidden;
   qkv.ksplit = ksplit_for(h, qkv.M, qkv.K, T);
   qkv.epi = EPI_HEADS;
+  qkv.name = "gemm.qkv";
   o = GemmPlan();
   o.n_aseg = 1;
   o.a_maps[0] = &m.o;
@@ -602,6 +682,7 @@ void layer_plans(const dflash_handle* h, int l, int T, GemmPlan& qkv, GemmPlan& 
   o.K = qd;
   o.ksplit = ksplit_for(h, o.M, o.K, T);
   o.epi = EPI_RESID;
+  o.name = "gemm.o";
   gu = GemmPlan();
   gu.n_aseg = 1;
   gu.a_maps[0] = &m.gate;
@@ -614,6 +695,7 @@ void layer_plans(const dflash_handle* h, int l, int T, GemmPlan& qkv, GemmPlan& 
   gu.K = c.hidden;
   gu.ksplit = ksplit_for(h, gu.M, gu.K, T);
   gu.epi = EPI_SWIGLU;
+  gu.name = "gemm.gate_up";
   dn = GemmPlan();
   dn.n_aseg = 1;
   dn.a_maps[0] = &m.down;
@@ -625,6 +707,7 @@ void layer_plans(const dflash_handle* h, int l, int T, GemmPlan& qkv, GemmPlan& 
   dn.K = c.ffn;
   dn.ksplit = ksplit_for(h, dn.M, dn.K, T);
   dn.epi = EPI_RESID;
+  dn.name = "gemm.down";
 }
 
 GemmPlan lm_plan(const dflash_handle* h, int rows) {
@@ -641,6 +724,7 @@ GemmPlan lm_plan(const dflash_handle* h, int rows) {
   p.ksplit = ksplit_for(h, p.M, p.K, rows);
   p.epi = EPI_STORE_BF16;
   p.epi_args.ldo = c.vocab;
+  p.name = "gemm.lm_head";
   return p;
 }
 
@@ -690,36 +774,22 @@ int dflash_draft_workspace_bytes(const dflash_handle* h, const dflash_state* st,
   return DFLASH_OK;
 }
 
-int dflash_draft_block(dflash_handle* h, dflash_state* st, int s_begin, int s_count, const int32_t* anchor_ids,
-                       void* logits_out, int32_t* topk_ids, float* topk_vals, int k, void* ws, size_t ws_bytes,
-                       dflash_stream_t stream) {
-  if (!h || !st || st->h != h || !anchor_ids || !ws) return DFLASH_E_INVALID_ARG;
-  if (s_count < 1 || s_begin < 0 || s_begin + s_count > st->S) return DFLASH_E_INVALID_ARG;
-  const bool do_topk = topk_ids != nullptr || topk_vals != nullptr;
-  if (do_topk && (!topk_ids || !topk_vals || k < 1 || k > DFLASH_MAX_TOPK)) return DFLASH_E_INVALID_ARG;
-  if (logits_out && !aligned16(logits_out)) return DFLASH_E_INVALID_ARG;
-  for (int i = 0; i < s_count; ++i)
-    if (st->host_len[s_begin + i] + DFLASH_BLOCK > st->R + DFLASH_BLOCK) return DFLASH_E_CAPACITY;
-  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return DFLASH_E_WORKSPACE;
+namespace {
+
+// Layers [l0, l1) of the block forward on the fp32 residual X [16*s_count, H].
+int run_layers(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int l0, int l1, float* X,
+               const DraftWs& w, int*& counters, cudaStream_t s) {
   const dflash_config& c = h->cfg;
-  DraftWs w{};
-  if (draft_ws_layout(h, st, s_count, logits_out == nullptr, ws, &w) > ws_bytes) return DFLASH_E_WORKSPACE;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int T = s_count * DFLASH_BLOCK;
   const int qd = c.n_q_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim;
-  __nv_bfloat16* logits = logits_out ? static_cast<__nv_bfloat16*>(logits_out) : w.logits;
-
-  if (cudaMemsetAsync(w.counters, 0, w.n_counters * sizeof(int), s) != cudaSuccess) return DFLASH_E_CUDA;
-  int rc = launch_embed(w.X, h->embed, anchor_ids, s_count, c.hidden, c.vocab, c.mask_token, st->status, s);
-  if (rc) return rc;
-  int* counters = w.counters;
   const int nch = max_nchunk(st);
-  for (int l = 0; l < c.n_layers; ++l) {
+  int rc = DFLASH_OK;
+  for (int l = l0; l < l1; ++l) {
     const dflash_layer_weights& L = h->layers[l];
     GemmPlan qkv, o, gu, dn;
     layer_plans(h, l, T, qkv, o, gu, dn);
     // input RMSNorm -> QKV with q_norm / k_norm + RoPE at positions C..C+15
-    rc = launch_rmsnorm_rows(w.hbuf, w.X, static_cast<const __nv_bfloat16*>(L.input_norm), T, c.hidden, c.rms_eps, 0, s);
+    rc = launch_rmsnorm_rows(w.hbuf, X, static_cast<const __nv_bfloat16*>(L.input_norm), T, c.hidden, c.rms_eps, 0, s);
     if (rc) return rc;
     qkv.b_ptr[0] = w.hbuf;
     qkv.ldb = c.hidden;
@@ -755,20 +825,26 @@ int dflash_draft_block(dflash_handle* h, dflash_state* st, int s_begin, int s_co
     a.part_o = w.part_o;
     a.part_ml = w.part_ml;
     a.out = w.attn;
-    // units beyond this layer's capacity exit at once; the combine reads only
-    // the chunks that hold context
+    {
+      double keys = 0.0;
+      for (int i = 0; i < s_count; ++i) {
+        const int64_t C = st->host_len[s_begin + i];
+        keys += static_cast<double>(st->window[l] > 0 ? std::min<int64_t>(C, st->window[l]) : C) + DFLASH_BLOCK;
+      }
+      a.trace_bytes = keys * kvd * 2.0 * 2.0 + 2.0 * T * qd * 2.0;
+    }
     rc = launch_attention(a, s_count, s);
     if (rc) return rc;
     // O projection added to the residual
     o.b_ptr[0] = w.attn;
     o.ldb = qd;
-    o.epi_args.out = w.X;
+    o.epi_args.out = X;
     o.epi_args.ldo = c.hidden;
     rc = gemm_launch(o, w.partial, counters, st->status, h->num_sms, s);
     if (rc) return rc;
     counters += gemm_counter_count(o);
     // post-attention RMSNorm -> SwiGLU -> down projection added to the residual
-    rc = launch_rmsnorm_rows(w.hbuf, w.X, static_cast<const __nv_bfloat16*>(L.post_norm), T, c.hidden, c.rms_eps, 0, s);
+    rc = launch_rmsnorm_rows(w.hbuf, X, static_cast<const __nv_bfloat16*>(L.post_norm), T, c.hidden, c.rms_eps, 0, s);
     if (rc) return rc;
     gu.b_ptr[0] = w.hbuf;
     gu.ldb = c.hidden;
@@ -779,30 +855,97 @@ int dflash_draft_block(dflash_handle* h, dflash_state* st, int s_begin, int s_co
     counters += gemm_counter_count(gu);
     dn.b_ptr[0] = w.mid;
     dn.ldb = c.ffn;
-    dn.epi_args.out = w.X;
+    dn.epi_args.out = X;
     dn.epi_args.ldo = c.hidden;
     rc = gemm_launch(dn, w.partial, counters, st->status, h->num_sms, s);
     if (rc) return rc;
     counters += gemm_counter_count(dn);
   }
-  (void)kvd;
-  // final norm on the 15 mask rows of every stream, shared LM head
+  return DFLASH_OK;
+}
+
+// Final norm on the 15 mask rows of every stream, shared LM head, top-k.
+int run_head(dflash_handle* h, int* status, int s_count, const float* X, const DraftWs& w, __nv_bfloat16* logits,
+             int32_t* topk_ids, float* topk_vals, int k, int*& counters, cudaStream_t s) {
+  const dflash_config& c = h->cfg;
   const int rows = s_count * (DFLASH_BLOCK - 1);
-  rc = launch_rmsnorm_rows(w.hbuf, w.X, h->norm, rows, c.hidden, c.rms_eps, 1, s);
+  int rc = launch_rmsnorm_rows(w.hbuf, X, h->norm, rows, c.hidden, c.rms_eps, 1, s);
   if (rc) return rc;
   GemmPlan lp = lm_plan(h, rows);
   lp.b_ptr[0] = w.hbuf;
   lp.ldb = c.hidden;
   lp.epi_args.out = logits;
-  rc = gemm_launch(lp, w.partial, counters, st->status, h->num_sms, s);
+  rc = gemm_launch(lp, w.partial, counters, status, h->num_sms, s);
   if (rc) return rc;
-  if (do_topk) rc = launch_topk(logits, rows, c.vocab, k, 1.0f, nullptr, topk_ids, topk_vals, nullptr, s);
+  counters += gemm_counter_count(lp);
+  if (topk_ids) rc = launch_topk(logits, rows, c.vocab, k, 1.0f, nullptr, topk_ids, topk_vals, nullptr, s);
   return rc;
+}
+
+int check_draft_args(dflash_handle* h, dflash_state* st, int s_begin, int s_count, const void* ws, int32_t* topk_ids,
+                     float* topk_vals, int k, const void* logits_out) {
+  if (!h || !st || st->h != h || !ws) return DFLASH_E_INVALID_ARG;
+  if (s_count < 1 || s_begin < 0 || s_begin + s_count > st->S) return DFLASH_E_INVALID_ARG;
+  const bool do_topk = topk_ids != nullptr || topk_vals != nullptr;
+  if (do_topk && (!topk_ids || !topk_vals || k < 1 || k > DFLASH_MAX_TOPK)) return DFLASH_E_INVALID_ARG;
+  if (logits_out && !aligned16(logits_out)) return DFLASH_E_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return DFLASH_E_WORKSPACE;
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+int dflash_draft_block(dflash_handle* h, dflash_state* st, int s_begin, int s_count, const int32_t* anchor_ids,
+                       void* logits_out, int32_t* topk_ids, float* topk_vals, int k, void* ws, size_t ws_bytes,
+                       dflash_stream_t stream) {
+  int rc = check_draft_args(h, st, s_begin, s_count, ws, topk_ids, topk_vals, k, logits_out);
+  if (rc) return rc;
+  if (!anchor_ids) return DFLASH_E_INVALID_ARG;
+  const dflash_config& c = h->cfg;
+  DraftWs w{};
+  if (draft_ws_layout(h, st, s_count, logits_out == nullptr, ws, &w) > ws_bytes) return DFLASH_E_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  __nv_bfloat16* logits = logits_out ? static_cast<__nv_bfloat16*>(logits_out) : w.logits;
+  if (cudaMemsetAsync(w.counters, 0, w.n_counters * sizeof(int), s) != cudaSuccess) return DFLASH_E_CUDA;
+  rc = launch_embed(w.X, h->embed, anchor_ids, s_count, c.hidden, c.vocab, c.mask_token, st->status, s);
+  if (rc) return rc;
+  int* counters = w.counters;
+  rc = run_layers(h, st, s_begin, s_count, 0, c.n_layers, w.X, w, counters, s);
+  if (rc) return rc;
+  return run_head(h, st->status, s_count, w.X, w, logits, topk_ids, topk_vals, k, counters, s);
+}
+
+int dflash_draft_layers(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int l0, int l1, float* X,
+                        void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  int rc = check_draft_args(h, st, s_begin, s_count, ws, nullptr, nullptr, 0, nullptr);
+  if (rc) return rc;
+  if (!X || !aligned16(X) || l0 < 0 || l1 < l0 || l1 > h->cfg.n_layers) return DFLASH_E_INVALID_ARG;
+  DraftWs w{};
+  if (draft_ws_layout(h, st, s_count, false, ws, &w) > ws_bytes) return DFLASH_E_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(w.counters, 0, w.n_counters * sizeof(int), s) != cudaSuccess) return DFLASH_E_CUDA;
+  int* counters = w.counters;
+  return run_layers(h, st, s_begin, s_count, l0, l1, X, w, counters, s);
+}
+
+int dflash_draft_head(dflash_handle* h, dflash_state* st, int s_count, const float* X, void* logits_out,
+                      int32_t* topk_ids, float* topk_vals, int k, void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  int rc = check_draft_args(h, st, 0, s_count, ws, topk_ids, topk_vals, k, logits_out);
+  if (rc) return rc;
+  if (!X || !aligned16(X) || !logits_out) return DFLASH_E_INVALID_ARG;
+  DraftWs w{};
+  if (draft_ws_layout(h, st, s_count, false, ws, &w) > ws_bytes) return DFLASH_E_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(w.counters, 0, w.n_counters * sizeof(int), s) != cudaSuccess) return DFLASH_E_CUDA;
+  int* counters = w.counters;
+  return run_head(h, st->status, s_count, X, w, static_cast<__nv_bfloat16*>(logits_out), topk_ids, topk_vals, k,
+                  counters, s);
 }
 
 // ---------------------------------------------------------------- top-k / verify
 int dflash_topk(const void* logits, int rows, int vocab, int k, float temperature, const float* uniforms,
                 int32_t* ids, float* vals, int32_t* sampled, dflash_stream_t stream) {
+  if (rows == 0 && vocab >= 8 && vocab % 8 == 0 && k >= 0 && k <= DFLASH_MAX_TOPK) return DFLASH_OK;
   if (!logits || rows < 0 || vocab < 8 || vocab % 8 || k < 0 || k > DFLASH_MAX_TOPK) return DFLASH_E_INVALID_ARG;
   if (k > 0 && (!ids || !vals)) return DFLASH_E_INVALID_ARG;
   if ((uniforms == nullptr) != (sampled == nullptr)) return DFLASH_E_INVALID_ARG;
@@ -821,16 +964,17 @@ int dflash_verify_workspace_bytes(int mode, int streams, int vocab, size_t* byte
   return DFLASH_OK;
 }
 
-int dflash_verify(int mode, int streams, int vocab, const int32_t* draft_ids, const void* target_logits,
+int dflash_verify(int mode, int streams, int vocab, const int32_t* draft_ids, int draft_ld, const void* target_logits,
                   const void* draft_logits, const float* uniforms, float temperature, int32_t* accept_len,
                   int32_t* out_tokens, void* ws, size_t ws_bytes, dflash_stream_t stream) {
-  if (streams < 0 || vocab < 8 || vocab % 8 || !draft_ids || !target_logits || !accept_len || !out_tokens)
+  if (streams < 0 || vocab < 8 || vocab % 8 || !draft_ids || draft_ld < 1 || !target_logits || !accept_len ||
+      !out_tokens)
     return DFLASH_E_INVALID_ARG;
   if (!aligned16(target_logits)) return DFLASH_E_INVALID_ARG;
   if (streams == 0) return DFLASH_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (mode == DFLASH_VERIFY_GREEDY) {
-    return launch_verify_greedy(streams, vocab, draft_ids, static_cast<const __nv_bfloat16*>(target_logits),
+    return launch_verify_greedy(streams, vocab, draft_ids, draft_ld, static_cast<const __nv_bfloat16*>(target_logits),
                                 accept_len, out_tokens, s);
   }
   if (mode != DFLASH_VERIFY_SAMPLE) return DFLASH_E_INVALID_ARG;
@@ -838,7 +982,7 @@ int dflash_verify(int mode, int streams, int vocab, const int32_t* draft_ids, co
   size_t need = 0;
   dflash_verify_workspace_bytes(mode, streams, vocab, &need);
   if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 15u)) return DFLASH_E_WORKSPACE;
-  return launch_verify_sample(streams, vocab, draft_ids, static_cast<const __nv_bfloat16*>(target_logits),
+  return launch_verify_sample(streams, vocab, draft_ids, draft_ld, static_cast<const __nv_bfloat16*>(target_logits),
                               static_cast<const __nv_bfloat16*>(draft_logits), uniforms, temperature, accept_len,
                               out_tokens, static_cast<float*>(ws), s);
 }

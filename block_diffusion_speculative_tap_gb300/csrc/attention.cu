@@ -7,12 +7,14 @@
 // heads that share the kv head (4 for 32/8 heads) is one warp each, 16 query
 // rows per warp, so one K/V tile staged in shared memory serves the whole
 // group. Scores and P*V run on the tensor cores (mma.sync m16n8k16 bf16,
-// fp32 accumulate) with an online softmax; chunk 0 also covers the block's
+// fp32 accumulate; P enters as a bf16 hi + lo pair so P*V keeps fp32-level
+// accuracy) with an online softmax; chunk 0 also covers the block's
 // 16 rows. Each unit writes its unnormalised output and (max, sum); a second
 // kernel merges the chunks with their log-sum-exp weights. Chunk sizes depend
 // only on the layer's cache capacity, so a stream's result does not depend on
 // the other streams in the batch.
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace dfl {
 
@@ -43,9 +45,13 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
+// (a, b) -> bf16 pairs hi = bf16(x), lo = bf16(x - hi)
+__device__ __forceinline__ void split_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 template <int D>
@@ -90,6 +96,8 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a) {
   __nv_bfloat16* buf = reinterpret_cast<__nv_bfloat16*>(smem_raw);
   constexpr int kLd = AttnSmem<D>::kLd;
   constexpr int kTE = AttnSmem<D>::kTileElems;
+  pdl_trigger();
+  pdl_wait();
 
   const int c = blockIdx.x;
   const int kvh = blockIdx.y;
@@ -208,14 +216,15 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a) {
         o[n][2] *= alpha[1];
         o[n][3] *= alpha[1];
       }
-      // O += P V: P from the score accumulators, V via transposed ldmatrix
+      // O += P V with P split into bf16 hi + lo parts (P = hi + lo to ~2^-17),
+      // so the product keeps fp32-level accuracy; V via transposed ldmatrix
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        uint32_t pa[4];
-        pa[0] = pack_bf16(sacc[2 * kk][0], sacc[2 * kk][1]);
-        pa[1] = pack_bf16(sacc[2 * kk][2], sacc[2 * kk][3]);
-        pa[2] = pack_bf16(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
-        pa[3] = pack_bf16(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
+        uint32_t ph[4], pl[4];
+        split_bf16(sacc[2 * kk][0], sacc[2 * kk][1], ph[0], pl[0]);
+        split_bf16(sacc[2 * kk][2], sacc[2 * kk][3], ph[1], pl[1]);
+        split_bf16(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1], ph[2], pl[2]);
+        split_bf16(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3], ph[3], pl[3]);
         const int mi = lane >> 3;
         const int key = kk * 16 + (mi & 1) * 8 + (lane & 7);
 #pragma unroll
@@ -223,8 +232,10 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a) {
           const int dim = n2 * 16 + (mi >> 1) * 8;
           uint32_t vb[4];
           ldmatrix_x4_trans(vb, static_cast<uint32_t>(__cvta_generic_to_shared(Vs + key * kLd + dim)));
-          mma_bf16_16816(o[2 * n2], pa, vb[0], vb[1]);
-          mma_bf16_16816(o[2 * n2 + 1], pa, vb[2], vb[3]);
+          mma_bf16_16816(o[2 * n2], ph, vb[0], vb[1]);
+          mma_bf16_16816(o[2 * n2 + 1], ph, vb[2], vb[3]);
+          mma_bf16_16816(o[2 * n2], pl, vb[0], vb[1]);
+          mma_bf16_16816(o[2 * n2 + 1], pl, vb[2], vb[3]);
         }
       }
     }
@@ -255,6 +266,8 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a) {
 // sum_c 2^(m_c - M) l_c, in chunk order.
 template <int D>
 __global__ void attn_combine_kernel(const AttnArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int h = blockIdx.x;
   const int si = blockIdx.y;
   const int s = a.s_begin + si;
@@ -288,11 +301,19 @@ int launch_d(const AttnArgs& a, int s_count, cudaStream_t st) {
     configured = true;
   }
   dim3 grid(a.nchunk, a.nkv, s_count);
-  attn_kernel<D><<<grid, 32 * G, smem, st>>>(a);
-  count_launch();
+  {
+    TraceScope ts(st, "attention", a.trace_bytes, 0.0);
+    const cudaError_t e = launch_pdl(attn_kernel<D>, grid, dim3(32 * G), smem, st, a);
+    count_launch();
+    if (e != cudaSuccess) return DFLASH_E_CUDA;
+  }
   dim3 g2(a.nq, s_count);
-  attn_combine_kernel<D><<<g2, 256, 0, st>>>(a);
-  count_launch();
+  {
+    TraceScope ts(st, "attention.combine", static_cast<double>(s_count) * a.nq * 16 * D * 2, 0.0);
+    const cudaError_t e = launch_pdl(attn_combine_kernel<D>, g2, dim3(256), 0, st, a);
+    count_launch();
+    if (e != cudaSuccess) return DFLASH_E_CUDA;
+  }
   return cuda_status(cudaGetLastError());
 }
 

@@ -170,6 +170,8 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
       if (a.epi.pos_mode == 0) {
         o = static_cast<int64_t>(t) * (sg.heads * d) + f;
       } else {
+        // a later row of the same segment owns this ring slot
+        if (sg.window > 0 && pos[j] < a.epi.row_end[t] - sg.window) continue;
         const int slot = sg.window > 0 ? (pos[j] % sg.window) : pos[j];
         o = ((static_cast<int64_t>(strm[j]) * sg.heads + head) * sg.cap + slot) * d + dim;
       }
@@ -221,6 +223,7 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -232,6 +235,7 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
+      bool first = true;
       for (int u = blockIdx.x; u < args.units && ok; u += gridDim.x) {
         int m_tile, kc, n_tile;
         decode_unit(args, u, m_tile, kc, n_tile);
@@ -239,7 +243,32 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
         const int kb1 = static_cast<int>(static_cast<long long>(kc + 1) * args.kb_total / args.ksplit);
         const int sidx = seg_of_tile(args, m_tile);
         const int arow = (m_tile - args.a_seg_tile[sidx]) * kTileM;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        int kb = kb0;
+        if (first) {
+          // Weights do not depend on the previous kernel: fill every stage
+          // with its weight tile before waiting for the activations.
+          first = false;
+          const int npre = kb1 - kb0 < STAGES ? kb1 - kb0 : STAGES;
+          for (int i = 0; i < npre; ++i) {
+            uint8_t* st = tiles + i * Tr::kStageBytes;
+            mbar_arrive_expect_tx(&full[i], Tr::kStageBytes);
+            tma_load_2d(st, &args.a_map[sidx], &full[i], (kb0 + i) * kTileK, arow, pol_w);
+            if constexpr (DUAL) tma_load_2d(st + Tr::kABytes, &args.a2_map, &full[i], (kb0 + i) * kTileK, arow, pol_w);
+          }
+          pdl_wait();
+          for (int i = 0; i < npre; ++i) {
+            const int kbi = kb0 + i;
+            const int pl = kbi / args.b_plane_kb;
+            const int kin = kbi - pl * args.b_plane_kb;
+            tma_load_2d(tiles + i * Tr::kStageBytes + Tr::kABytes * (DUAL ? 2 : 1), &args.b_map[pl], &full[i],
+                        kin * kTileK, n_tile * BN, pol_x);
+          }
+          issued = npre;
+          kb = kb0 + npre;
+          stage = npre % STAGES;
+          phase = npre == STAGES ? 1u : 0u;
+        }
+        for (; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, args.err, DFLASH_STATUS_TIMEOUT, abort_word)) {
             ok = false;
             break;
@@ -327,6 +356,7 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
     int acc = 0;
     uint32_t acc_phase = 0;
     const bool epi_leader = (warp == 2 && lane == 0);
+    pdl_wait();  // the epilogue reads and writes buffers of earlier kernels
     for (int u = blockIdx.x; u < args.units; u += gridDim.x) {
       int m_tile, kc, n_tile;
       decode_unit(args, u, m_tile, kc, n_tile);
@@ -433,9 +463,9 @@ int launch_inst(const GemmArgs& a, int num_sms, cudaStream_t st) {
     configured = true;
   }
   const int grid = std::max(1, std::min(a.units, num_sms * MINB));
-  kern<<<grid, kGemmThreads, Tr::kSmemBytes, st>>>(a);
+  const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kGemmThreads), Tr::kSmemBytes, st, a);
   count_launch();
-  return cuda_status(cudaGetLastError());
+  return cuda_status(e);
 }
 
 template <int BN, bool DUAL, int STAGES, int MINB>
@@ -553,6 +583,15 @@ int gemm_launch(const GemmPlan& p, float* partial, int* counters, int* err, int 
   a.err = err;
   if (a.ksplit > 1 && (partial == nullptr || counters == nullptr)) return DFLASH_E_WORKSPACE;
   const bool dual = p.a2_map != nullptr;
+  // algorithmic traffic: weights once, activations once, outputs once
+  // (a residual add reads and writes its fp32 row)
+  const double M = p.M, N = p.N, K = p.K;
+  double out_b = 2.0;
+  if (p.epi == EPI_STORE_F32) out_b = 4.0;
+  if (p.epi == EPI_RESID) out_b = 8.0;
+  const double bytes = (dual ? 2.0 : 1.0) * M * K * 2.0 + N * K * 2.0 + N * M * out_b;
+  const double flops = (dual ? 2.0 : 1.0) * 2.0 * M * N * K;
+  TraceScope ts(st, p.name, bytes, flops);
   if (BN == 16) {
     return dual ? launch_epi<16, true, 3, 2>(a, p.epi, num_sms, st) : launch_epi<16, false, 5, 2>(a, p.epi, num_sms, st);
   } else if (BN == 128) {

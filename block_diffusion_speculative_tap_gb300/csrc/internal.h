@@ -41,6 +41,8 @@ struct EpiArgs {
   const int* lens;
   const int* row_stream;
   const int* row_pos;
+  const int* row_end;    // rows mode: end position of the row's segment; a sliding-ring
+                         // slot is written only by the last W positions of a segment
   const float2* rope;    // [pos][d/2] = (cos, sin)
   HeadSeg seg[kMaxASeg];
 };
@@ -76,6 +78,7 @@ struct GemmPlan {
   int ksplit = 1;
   int epi = EPI_STORE_F32;
   EpiArgs epi_args{};
+  const char* name = "gemm";  // trace label
 };
 
 // Workspace needed by one GEMM launch (partials and counters), bytes.
@@ -98,7 +101,7 @@ int launch_rmsnorm_rows(__nv_bfloat16* out, const float* x, const __nv_bfloat16*
 // Row tables (stream, position) of appended segments, and/or the new stream
 // lengths (start + rows of each segment). seg_info_host_packed holds
 // (stream, start, rows) per segment, on the host.
-int launch_prep_rows(int* row_stream, int* row_pos, int* lens, const int* unused, int nseg, int rows,
+int launch_prep_rows(int* row_stream, int* row_pos, int* row_end, int* lens, int nseg, int rows,
                      const int* seg_info_host_packed, cudaStream_t st);
 int launch_hidden_norm(__nv_bfloat16* ring, __nv_bfloat16* fused_tmp, const float* y, const __nv_bfloat16* g,
                        const int* row_stream, const int* row_pos, int rows, int H, int R, float eps, cudaStream_t st);
@@ -120,6 +123,7 @@ struct AttnArgs {
   float* part_o;            // [s][nq][nchunk][16][d]
   float* part_ml;           // [s][nq][nchunk][16][2]
   __nv_bfloat16* out;       // [T, nq*d]
+  double trace_bytes;       // algorithmic K/V + Q + O bytes (host estimate, for the trace)
 };
 int launch_attention(const AttnArgs& a, int s_count, cudaStream_t st);
 size_t attn_partial_floats(int s_count, int nq, int nchunk, int d);
@@ -127,13 +131,40 @@ size_t attn_partial_floats(int s_count, int nq, int nchunk, int d);
 // ---------------------------------------------------------------- selection (select.cu)
 int launch_topk(const __nv_bfloat16* logits, int rows, int V, int k, float T, const float* uniforms, int* ids,
                 float* vals, int* sampled, cudaStream_t st);
-int launch_verify_greedy(int S, int V, const int* draft, const __nv_bfloat16* tl, int* accept, int* out,
+int launch_verify_greedy(int S, int V, const int* draft, int dld, const __nv_bfloat16* tl, int* accept, int* out,
                          cudaStream_t st);
-int launch_verify_sample(int S, int V, const int* draft, const __nv_bfloat16* tl, const __nv_bfloat16* dl,
+int launch_verify_sample(int S, int V, const int* draft, int dld, const __nv_bfloat16* tl, const __nv_bfloat16* dl,
                          const float* u, float T, int* accept, int* out, float* stats, cudaStream_t st);
+
+// Launch a kernel with programmatic stream serialization (PDL) on `st`.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // launch bookkeeping
 void count_launch(int n = 1);
 int cuda_status(cudaError_t e);
+
+// Per-launch timing trace: while enabled, a scope records a CUDA event on
+// its stream when it opens and when it closes, with the launch's algorithmic
+// bytes and flops.
+struct TraceScope {
+  TraceScope(cudaStream_t st, const char* name, double bytes, double flops);
+  ~TraceScope();
+  cudaStream_t st;
+  int idx;
+};
 
 }  // namespace dfl

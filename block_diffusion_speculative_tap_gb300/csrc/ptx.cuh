@@ -184,6 +184,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start while its predecessor is still running; it must
+// call pdl_wait() before touching anything the predecessor (or any earlier
+// kernel of the chain) writes. pdl_trigger() lets the successor launch once
+// every CTA of this grid has issued it. Both are no-ops without the launch
+// attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Named barrier over `nthreads` threads (multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

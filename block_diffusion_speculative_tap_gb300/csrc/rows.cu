@@ -6,6 +6,7 @@
 // then a warp tree, then the warps in order), so results do not depend on
 // which other rows share the launch.
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace dfl {
 
@@ -30,6 +31,8 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 // other fifteen rows of the block are the mask token [anchor + 15 mask rows].
 __global__ void embed_kernel(float* __restrict__ X, const __nv_bfloat16* __restrict__ E, const int* __restrict__ anchors,
                              int H, int V, int mask, int* err) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x;
   int tok = mask;
   if ((t & 15) == 0) {
@@ -48,6 +51,8 @@ __global__ void embed_kernel(float* __restrict__ X, const __nv_bfloat16* __restr
 __global__ void rmsnorm_rows_kernel(__nv_bfloat16* __restrict__ out, const float* __restrict__ x,
                                     const __nv_bfloat16* __restrict__ g, int H, float eps, int mask_rows_only) {
   __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   const int src = mask_rows_only ? (r / 15) * 16 + 1 + (r % 15) : r;
   const float* xr = x + static_cast<int64_t>(src) * H;
@@ -69,6 +74,8 @@ __global__ void hidden_norm_kernel(__nv_bfloat16* __restrict__ ring, __nv_bfloat
                                    const int* __restrict__ row_stream, const int* __restrict__ row_pos, int H, int R,
                                    float eps) {
   __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   const float* yr = y + static_cast<int64_t>(r) * H;
   float ss = 0.f;
@@ -95,17 +102,22 @@ struct SegTable {
   int first_row[257];
 };
 
-__global__ void prep_rows_kernel(int* __restrict__ row_stream, int* __restrict__ row_pos, const SegTable tab,
-                                 int total) {
+__global__ void prep_rows_kernel(int* __restrict__ row_stream, int* __restrict__ row_pos, int* __restrict__ row_end,
+                                 const SegTable tab, int total) {
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= total) return;
   int s = 0;
   while (s + 1 < tab.n && r >= tab.first_row[s + 1]) ++s;
   row_stream[r] = tab.stream[s];
   row_pos[r] = tab.start[s] + (r - tab.first_row[s]);
+  row_end[r] = tab.start[s] + tab.rows[s];
 }
 
 __global__ void set_lens_kernel(int* __restrict__ lens, const SegTable tab) {
+  pdl_trigger();
+  pdl_wait();
   const int i = threadIdx.x;
   if (i < tab.n) lens[tab.stream[i]] = tab.start[i] + tab.rows[i];
 }
@@ -114,27 +126,32 @@ __global__ void set_lens_kernel(int* __restrict__ lens, const SegTable tab) {
 
 int launch_embed(float* X, const __nv_bfloat16* embed, const int* anchors, int S, int H, int V, int mask, int* err,
                  cudaStream_t st) {
-  embed_kernel<<<S * 16, kRowThreads, 0, st>>>(X, embed, anchors, H, V, mask, err);
+  TraceScope ts(st, "embed", static_cast<double>(S) * 16 * H * 6, 0.0);
+  const cudaError_t e = launch_pdl(embed_kernel, dim3(S * 16), dim3(kRowThreads), 0, st, X, embed, anchors, H, V, mask, err);
   count_launch();
-  return cuda_status(cudaGetLastError());
+  return cuda_status(e);
 }
 
 int launch_rmsnorm_rows(__nv_bfloat16* out, const float* x, const __nv_bfloat16* g, int rows, int H, float eps,
                         int mask_rows_only, cudaStream_t st) {
-  rmsnorm_rows_kernel<<<rows, kRowThreads, 0, st>>>(out, x, g, H, eps, mask_rows_only);
+  TraceScope ts(st, "rmsnorm", static_cast<double>(rows) * H * 6, 0.0);
+  const cudaError_t e =
+      launch_pdl(rmsnorm_rows_kernel, dim3(rows), dim3(kRowThreads), 0, st, out, x, g, H, eps, mask_rows_only);
   count_launch();
-  return cuda_status(cudaGetLastError());
+  return cuda_status(e);
 }
 
 int launch_hidden_norm(__nv_bfloat16* ring, __nv_bfloat16* fused_tmp, const float* y, const __nv_bfloat16* g,
                        const int* row_stream, const int* row_pos, int rows, int H, int R, float eps, cudaStream_t st) {
-  hidden_norm_kernel<<<rows, kRowThreads, 0, st>>>(ring, fused_tmp, y, g, row_stream, row_pos, H, R, eps);
+  TraceScope ts(st, "hidden_norm", static_cast<double>(rows) * H * 8, 0.0);
+  const cudaError_t e = launch_pdl(hidden_norm_kernel, dim3(rows), dim3(kRowThreads), 0, st, ring, fused_tmp, y, g,
+                                   row_stream, row_pos, H, R, eps);
   count_launch();
-  return cuda_status(cudaGetLastError());
+  return cuda_status(e);
 }
 
 // seg_info_host_packed: 3*nseg ints (stream, start, rows) on the host.
-int launch_prep_rows(int* row_stream, int* row_pos, int* lens, const int* /*unused*/, int nseg, int rows,
+int launch_prep_rows(int* row_stream, int* row_pos, int* row_end, int* lens, int nseg, int rows,
                      const int* seg_info_host_packed, cudaStream_t st) {
   if (nseg < 1 || nseg > 256) return DFLASH_E_INVALID_ARG;
   SegTable tab{};
@@ -147,12 +164,17 @@ int launch_prep_rows(int* row_stream, int* row_pos, int* lens, const int* /*unus
     tab.first_row[i + 1] = tab.first_row[i] + tab.rows[i];
   }
   if (rows > 0) {
-    prep_rows_kernel<<<(rows + 255) / 256, 256, 0, st>>>(row_stream, row_pos, tab, rows);
+    TraceScope ts(st, "prep_rows", rows * 8.0, 0.0);
+    const cudaError_t e =
+        launch_pdl(prep_rows_kernel, dim3((rows + 255) / 256), dim3(256), 0, st, row_stream, row_pos, row_end, tab, rows);
     count_launch();
+    if (e != cudaSuccess) return DFLASH_E_CUDA;
   }
   if (lens) {
-    set_lens_kernel<<<1, 256, 0, st>>>(lens, tab);
+    TraceScope ts(st, "set_lens", nseg * 4.0, 0.0);
+    const cudaError_t e = launch_pdl(set_lens_kernel, dim3(1), dim3(256), 0, st, lens, tab);
     count_launch();
+    if (e != cudaSuccess) return DFLASH_E_CUDA;
   }
   return cuda_status(cudaGetLastError());
 }

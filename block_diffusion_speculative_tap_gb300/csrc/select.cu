@@ -12,6 +12,7 @@
 #include <float.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace dfl {
 
@@ -292,6 +293,8 @@ __global__ void __launch_bounds__(kSelThreads) topk_kernel(const __nv_bfloat16* 
                                                            float invT, const float* __restrict__ uniforms,
                                                            int* __restrict__ ids, float* __restrict__ vals,
                                                            int* __restrict__ sampled) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float sv[kSelWarps];
   __shared__ int si[kSelWarps];
   __shared__ float sw[kSelWarps];
@@ -317,6 +320,8 @@ __global__ void __launch_bounds__(kSelThreads) topk_kernel(const __nv_bfloat16* 
 // greedy, step 1: t_i = argmax of every target row -> out[s][i]
 __global__ void __launch_bounds__(kSelThreads) argmax_kernel(const __nv_bfloat16* __restrict__ tl, int V,
                                                              int* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float sv[kSelWarps];
   __shared__ int si[kSelWarps];
   __shared__ int sid[1];
@@ -329,19 +334,21 @@ __global__ void __launch_bounds__(kSelThreads) argmax_kernel(const __nv_bfloat16
 
 // greedy, step 2: longest prefix of drafts equal to the target argmax, then
 // the bonus token; rewrites out[s][*] in place.
-__global__ void greedy_prefix_kernel(int S, int V, const int* __restrict__ draft, int* __restrict__ accept,
-                                     int* __restrict__ out) {
+__global__ void greedy_prefix_kernel(int S, int V, const int* __restrict__ draft, int dld,
+                                     int* __restrict__ accept, int* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= S) return;
   int t[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) t[i] = out[s * 16 + i];
   int a = 0;
-  while (a < 15 && draft[s * 15 + a] == t[a]) ++a;
+  while (a < 15 && draft[(s * 15 + a) * dld] == t[a]) ++a;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     int v = -1;
-    if (i < a) v = draft[s * 15 + i];
+    if (i < a) v = draft[(s * 15 + i) * dld];
     if (i == a) v = t[a];
     out[s * 16 + i] = v;
   }
@@ -353,6 +360,8 @@ __global__ void greedy_prefix_kernel(int S, int V, const int* __restrict__ draft
 __global__ void __launch_bounds__(kSelThreads) softmax_stats_kernel(const __nv_bfloat16* __restrict__ tl,
                                                                     const __nv_bfloat16* __restrict__ dl, int V,
                                                                     float invT, float* __restrict__ stats) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float sv[kSelWarps];
   __shared__ int si[kSelWarps];
   __shared__ float sw[kSelWarps];
@@ -372,19 +381,21 @@ __global__ void __launch_bounds__(kSelThreads) softmax_stats_kernel(const __nv_b
 }
 
 // sampling, step 2: the accept chain, then the residual or bonus draw.
-__global__ void __launch_bounds__(kSelThreads) sample_verify_kernel(int V, const int* __restrict__ draft,
+__global__ void __launch_bounds__(kSelThreads) sample_verify_kernel(int V, const int* __restrict__ draft, int dld,
                                                                     const __nv_bfloat16* __restrict__ tl,
                                                                     const __nv_bfloat16* __restrict__ dl,
                                                                     const float* __restrict__ u, float invT,
                                                                     const float* __restrict__ stats,
                                                                     int* __restrict__ accept, int* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float sw[kSelWarps];
   __shared__ int sres[1];
   const int s = blockIdx.x;
   const float* st = stats + s * 31 * 2;
   int a = 15;
   for (int i = 0; i < 15; ++i) {
-    const int x = draft[s * 15 + i];
+    const int x = draft[(s * 15 + i) * dld];
     bool acc = false;
     if (x >= 0 && x < V) {
       const float p = expf((__bfloat162float(tl[(static_cast<int64_t>(s) * 16 + i) * V + x]) - st[i * 2]) * invT) /
@@ -422,7 +433,7 @@ __global__ void __launch_bounds__(kSelThreads) sample_verify_kernel(int V, const
   if (threadIdx.x < 16) {
     const int i = threadIdx.x;
     int v = -1;
-    if (i < a) v = draft[s * 15 + i];
+    if (i < a) v = draft[(s * 15 + i) * dld];
     if (i == a) v = tok;
     out[s * 16 + i] = v;
   }
@@ -434,27 +445,47 @@ __global__ void __launch_bounds__(kSelThreads) sample_verify_kernel(int V, const
 int launch_topk(const __nv_bfloat16* logits, int rows, int V, int k, float T, const float* uniforms, int* ids,
                 float* vals, int* sampled, cudaStream_t st) {
   if (rows <= 0) return DFLASH_OK;
-  topk_kernel<<<rows, kSelThreads, 0, st>>>(logits, V, k, 1.0f / T, uniforms, ids, vals, sampled);
+  TraceScope ts(st, "topk", static_cast<double>(rows) * V * 2, 0.0);
+  const cudaError_t e = launch_pdl(topk_kernel, dim3(rows), dim3(kSelThreads), 0, st, logits, V, k, 1.0f / T, uniforms,
+                                   ids, vals, sampled);
   count_launch();
-  return cuda_status(cudaGetLastError());
+  return cuda_status(e);
 }
 
-int launch_verify_greedy(int S, int V, const int* draft, const __nv_bfloat16* tl, int* accept, int* out,
+int launch_verify_greedy(int S, int V, const int* draft, int dld, const __nv_bfloat16* tl, int* accept, int* out,
                          cudaStream_t st) {
-  argmax_kernel<<<S * 16, kSelThreads, 0, st>>>(tl, V, out);
-  count_launch();
-  greedy_prefix_kernel<<<(S + 127) / 128, 128, 0, st>>>(S, V, draft, accept, out);
-  count_launch();
+  {
+    TraceScope ts(st, "verify.argmax", static_cast<double>(S) * 16 * V * 2, 0.0);
+    const cudaError_t e = launch_pdl(argmax_kernel, dim3(S * 16), dim3(kSelThreads), 0, st, tl, V, out);
+    count_launch();
+    if (e != cudaSuccess) return DFLASH_E_CUDA;
+  }
+  {
+    TraceScope ts(st, "verify.prefix", S * 31.0 * 4, 0.0);
+    const cudaError_t e =
+        launch_pdl(greedy_prefix_kernel, dim3((S + 127) / 128), dim3(128), 0, st, S, V, draft, dld, accept, out);
+    count_launch();
+    if (e != cudaSuccess) return DFLASH_E_CUDA;
+  }
   return cuda_status(cudaGetLastError());
 }
 
-int launch_verify_sample(int S, int V, const int* draft, const __nv_bfloat16* tl, const __nv_bfloat16* dl,
+int launch_verify_sample(int S, int V, const int* draft, int dld, const __nv_bfloat16* tl, const __nv_bfloat16* dl,
                          const float* u, float T, int* accept, int* out, float* stats, cudaStream_t st) {
   dim3 g(31, S);
-  softmax_stats_kernel<<<g, kSelThreads, 0, st>>>(tl, dl, V, 1.0f / T, stats);
-  count_launch();
-  sample_verify_kernel<<<S, kSelThreads, 0, st>>>(V, draft, tl, dl, u, 1.0f / T, stats, accept, out);
-  count_launch();
+  {
+    TraceScope ts(st, "verify.softmax_stats", static_cast<double>(S) * 31 * V * 2, 0.0);
+    const cudaError_t e = launch_pdl(softmax_stats_kernel, g, dim3(kSelThreads), 0, st, tl, dl, V, 1.0f / T, stats);
+    count_launch();
+    if (e != cudaSuccess) return DFLASH_E_CUDA;
+  }
+  {
+    TraceScope ts(st, "verify.sample", static_cast<double>(S) * 2 * V * 2, 0.0);
+    const cudaError_t e = launch_pdl(sample_verify_kernel, dim3(S), dim3(kSelThreads), 0, st, V, draft, dld, tl, dl, u,
+                                     1.0f / T, stats, accept, out);
+    count_launch();
+    if (e != cudaSuccess) return DFLASH_E_CUDA;
+  }
   return cuda_status(cudaGetLastError());
 }
 

@@ -289,6 +289,38 @@ class State:
         return logits, ids, vals
 
 
+    def draft_layers(self, X, l0, l1, s_begin=0):
+        """Run layers [l0, l1) on the fp32 residual X [S*16, H] in place."""
+        _need(X, torch.float32, "X")
+        S = X.shape[0] // 16
+        ws = self.ws_draft.get(self.draft_workspace_bytes(S, False))
+        check(
+            lib.dflash_draft_layers(
+                self.drafter.handle, self.st, s_begin, S, l0, l1, _ptr(X), _ptr(ws), ws.numel(), _stream()
+            ),
+            "dflash_draft_layers",
+        )
+        return X
+
+    def draft_head(self, X, k=8):
+        """Final norm + LM head (+ top-k) of the fp32 residual X [S*16, H]."""
+        _need(X, torch.float32, "X")
+        S = X.shape[0] // 16
+        dev = self.drafter.device
+        logits = torch.empty(S * 15, self.drafter.model["vocab"], dtype=torch.bfloat16, device=dev)
+        ids = torch.empty(S * 15, k, dtype=torch.int32, device=dev) if k > 0 else None
+        vals = torch.empty(S * 15, k, dtype=torch.float32, device=dev) if k > 0 else None
+        ws = self.ws_draft.get(self.draft_workspace_bytes(S, False))
+        check(
+            lib.dflash_draft_head(
+                self.drafter.handle, self.st, S, _ptr(X), _ptr(logits), _ptr(ids), _ptr(vals), k, _ptr(ws),
+                ws.numel(), _stream(),
+            ),
+            "dflash_draft_head",
+        )
+        return logits, ids, vals
+
+
 # ---------------------------------------------------------------- free functions
 
 
@@ -321,9 +353,21 @@ def topk(logits, k, temperature=1.0, uniforms=None, ids=None, vals=None, sampled
     return ids, vals, sampled
 
 
+def _draft_ld(draft_ids):
+    """Elements between consecutive draft positions: 1 for [S, 15], k for the
+    top-1 column of a [S*15, k] top-k tensor."""
+    if draft_ids.dtype != torch.int32 or draft_ids.device.type != "cuda" or not draft_ids.is_contiguous():
+        raise ValueError("draft_ids: contiguous int32 CUDA tensor")
+    if draft_ids.dim() == 2 and draft_ids.shape[1] != 15:
+        return draft_ids.shape[1]
+    return 1
+
+
 def verify_greedy(draft_ids, target_logits, accept=None, tokens=None):
-    """draft_ids [S, 15] int32; target_logits [S, 16, V] bf16 -> (accept [S], tokens [S, 16])."""
-    _need(draft_ids, torch.int32, "draft_ids")
+    """draft_ids [S, 15] int32 (or a [S*15, k] top-k id tensor: its top-1
+    column is read in place); target_logits [S, 16, V] bf16 -> (accept [S],
+    tokens [S, 16])."""
+    dld = _draft_ld(draft_ids)
     _need(target_logits, torch.bfloat16, "target_logits")
     S, _, V = target_logits.shape
     dev = target_logits.device
@@ -331,7 +375,7 @@ def verify_greedy(draft_ids, target_logits, accept=None, tokens=None):
     tokens = tokens if tokens is not None else torch.empty(S, 16, dtype=torch.int32, device=dev)
     check(
         lib.dflash_verify(
-            A.VERIFY_GREEDY, S, V, _ptr(draft_ids), _ptr(target_logits), C.c_void_p(0), C.c_void_p(0), 1.0,
+            A.VERIFY_GREEDY, S, V, _ptr(draft_ids), dld, _ptr(target_logits), C.c_void_p(0), C.c_void_p(0), 1.0,
             _ptr(accept), _ptr(tokens), C.c_void_p(0), 0, _stream(),
         ),
         "dflash_verify",
@@ -342,7 +386,7 @@ def verify_greedy(draft_ids, target_logits, accept=None, tokens=None):
 def verify_sample(draft_ids, target_logits, draft_logits, uniforms, temperature=1.0, accept=None, tokens=None,
                   ws=None):
     """Speculative sampling verification; uniforms [S, 16, 2] fp32."""
-    _need(draft_ids, torch.int32, "draft_ids")
+    dld = _draft_ld(draft_ids)
     _need(target_logits, torch.bfloat16, "target_logits")
     _need(draft_logits, torch.bfloat16, "draft_logits")
     _need(uniforms, torch.float32, "uniforms")
@@ -356,7 +400,7 @@ def verify_sample(draft_ids, target_logits, draft_logits, uniforms, temperature=
         ws = torch.empty(max(nb.value, 256), dtype=torch.uint8, device=dev)
     check(
         lib.dflash_verify(
-            A.VERIFY_SAMPLE, S, V, _ptr(draft_ids), _ptr(target_logits), _ptr(draft_logits), _ptr(uniforms),
+            A.VERIFY_SAMPLE, S, V, _ptr(draft_ids), dld, _ptr(target_logits), _ptr(draft_logits), _ptr(uniforms),
             float(temperature), _ptr(accept), _ptr(tokens), _ptr(ws), ws.numel(), _stream(),
         ),
         "dflash_verify",

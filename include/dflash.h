@@ -257,6 +257,20 @@ int dflash_draft_block(dflash_handle* h, dflash_state* st, int s_begin, int s_co
                        void* logits_out, int32_t* topk_ids, float* topk_vals, int k, void* ws, size_t ws_bytes,
                        dflash_stream_t stream);
 
+/* The same block forward in stages, for layer-by-layer execution and for
+ * stage-isolated checks (each stage fed a reference input, so errors do not
+ * compound). X is the fp32 residual stream, device [s_count*16, H], row
+ * 16*i + j = row j (0 = anchor) of stream s_begin + i; it must be 16-byte
+ * aligned. dflash_draft_layers runs layers l0 .. l1-1 on X in place (with the
+ * streams' K/V caches and lengths as dflash_draft_block would);
+ * dflash_draft_head applies the final norm to the 15 mask rows of every
+ * stream, the LM head (logits_out required) and the optional top-k. Both take
+ * the workspace of dflash_draft_workspace_bytes(h, st, s_count, 0). */
+int dflash_draft_layers(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int l0, int l1, float* X,
+                        void* ws, size_t ws_bytes, dflash_stream_t stream);
+int dflash_draft_head(dflash_handle* h, dflash_state* st, int s_count, const float* X, void* logits_out,
+                      int32_t* topk_ids, float* topk_vals, int k, void* ws, size_t ws_bytes, dflash_stream_t stream);
+
 /* ---------------------------------------------------------------- top-k
  * Per row of a bf16 logit matrix [rows, vocab] (device, rows contiguous):
  * the k largest logits (descending, ties to the lower id; ids int32, vals fp32
@@ -270,7 +284,9 @@ int dflash_topk(const void* logits, int rows, int vocab, int k, float temperatur
 
 /* ---------------------------------------------------------------- verify
  * Target verification of S drafted blocks [EXPL 四; PROT "What is portable"].
- * draft_ids: device int32 [S, 15] (d_1..d_15); target_logits: device bf16
+ * draft_ids: device int32, d_{i+1} of stream s at draft_ids[(s*15 + i) * draft_ld]
+ * (draft_ld = 1 for a dense [S, 15] array, k to read the top-1 column of a
+ * [S*15, k] top-k output); target_logits: device bf16
  * [S, 16, V], row i = the target's scores for position C+i+1 (after reading
  * the anchor and d_1..d_i).
  * GREEDY: t_i = argmax row i (ties to the lowest id); a = length of the
@@ -285,7 +301,7 @@ int dflash_topk(const void* logits, int rows, int vocab, int k, float temperatur
  * [S, 16]: the a+1 committed tokens then -1. A draft id outside [0, V) is
  * never accepted (and sets nothing else). ws: >= dflash_verify_workspace_bytes. */
 int dflash_verify_workspace_bytes(int mode, int streams, int vocab, size_t* bytes);
-int dflash_verify(int mode, int streams, int vocab, const int32_t* draft_ids, const void* target_logits,
+int dflash_verify(int mode, int streams, int vocab, const int32_t* draft_ids, int draft_ld, const void* target_logits,
                   const void* draft_logits, const float* uniforms, float temperature, int32_t* accept_len,
                   int32_t* out_tokens, void* ws, size_t ws_bytes, dflash_stream_t stream);
 
@@ -293,6 +309,18 @@ int dflash_verify(int mode, int streams, int vocab, const int32_t* draft_ids, co
 const char* dflash_strerror(int code);
 /* Kernel launches enqueued by this process so far (all entry points). */
 int64_t dflash_launch_count(void);
+
+/* Per-launch timing trace (process-wide). dflash_trace_enable(1) clears the
+ * trace and starts recording: every kernel launch is then bracketed by two
+ * CUDA events on its stream, with the launch's algorithmic bytes (each
+ * weight, activation and output touched once) and flops. enable(0) stops.
+ * dflash_trace_get waits for record i's end event and returns its label
+ * (static string, e.g. "gemm.lm_head", "attention"), its duration in ms,
+ * bytes and flops. Events cost a little GPU time; leave the trace off for
+ * production timing. */
+int dflash_trace_enable(int on);
+int dflash_trace_count(void);
+int dflash_trace_get(int i, const char** name, float* ms, double* bytes, double* flops);
 
 #ifdef __cplusplus
 }

@@ -75,6 +75,9 @@ __all__ = [
     "visible_positions",
     "block_attention",
     "silu",
+    "block_embed",
+    "draft_layer",
+    "draft_head",
     "draft_block",
     "OracleStreams",
     "topk",
@@ -226,7 +229,53 @@ def block_attention(q, k, v):
     return out
 
 
-def draft_block(model, w, ctx_k, ctx_v, C, anchor):
+def block_embed(model, w, anchor):
+    """Residual rows of the block: the anchor token then fifteen mask tokens
+    (TensorFold #1851 item 1: the fifteen mask rows), float64 copies of the
+    shared embedding rows."""
+    tokens = [int(anchor)] + [model["mask_token"]] * (BLOCK - 1)
+    return w["embed"][tokens].astype(np.float64)
+
+
+def draft_layer(model, w, l, X, ctx_k, ctx_v, C):
+    """One drafter layer on the block's residual X [16, H] (qwen3 body:
+    TensorFold #1851 item 1, "two residual adds a layer").
+
+    ctx_k, ctx_v: [C, n_kv, d] bf16 K/V of this layer for positions 0..C-1.
+    Returns the residual after the attention and MLP adds.
+    """
+    nq, nkv, d = model["n_q_heads"], model["n_kv_heads"], model["head_dim"]
+    eps, theta = model["rms_eps"], model["rope_theta"]
+    lw = w["layers"][l]
+    pos = C + np.arange(BLOCK)
+    h = round_bf16(rms_norm(X, lw["input_layernorm"], eps))
+    q = (h @ lw["q_proj"].T).reshape(BLOCK, nq, d)
+    k = (h @ lw["k_proj"].T).reshape(BLOCK, nkv, d)
+    v = (h @ lw["v_proj"].T).reshape(BLOCK, nkv, d)
+    q = round_bf16(rope(rms_norm(q, lw["q_norm"], eps), pos[:, None], theta))
+    k = round_bf16(rope(rms_norm(k, lw["k_norm"], eps), pos[:, None], theta))
+    v = round_bf16(v)
+    vis = visible_positions(model["layer_kinds"][l], C, model["sliding_window"])
+    keys = np.concatenate([ctx_k[vis], k], axis=0)
+    vals = np.concatenate([ctx_v[vis], v], axis=0)
+    att = round_bf16(block_attention(q, keys, vals).reshape(BLOCK, nq * d))
+    X = X + att @ lw["o_proj"].T
+    h2 = round_bf16(rms_norm(X, lw["post_attention_layernorm"], eps))
+    gate = h2 @ lw["gate_proj"].T
+    up = h2 @ lw["up_proj"].T
+    mid = round_bf16(silu(gate) * up)
+    return X + mid @ lw["down_proj"].T
+
+
+def draft_head(model, w, X):
+    """Final norm of the 15 mask rows and the shared LM head (the explainer's
+    section 三: embedding and LM head are the target's). Returns bf16 logits
+    [15, V] as float64."""
+    z = round_bf16(rms_norm(X[1:], w["norm"], model["rms_eps"]))
+    return round_bf16(z @ w["embed"].T)
+
+
+def draft_block(model, w, ctx_k, ctx_v, C, anchor, keep_residuals=False):
     """One block forward of the drafter for one stream.
 
     TensorFold #1851 item 1 (qwen3 body; each layer adds attention and its MLP
@@ -236,37 +285,17 @@ def draft_block(model, w, ctx_k, ctx_v, C, anchor):
 
     ctx_k[l], ctx_v[l]: [C, n_kv, d] bf16 context K/V of layer l for positions
     0..C-1. anchor: token id at position C. Returns (logits [15, V] bf16 values
-    of the mask rows, X final residual [16, H]).
+    of the mask rows, X final residual [16, H]); with keep_residuals, X is the
+    list of residuals before layer 0, ..., after the last layer.
     """
-    H = model["hidden"]
-    nq, nkv, d = model["n_q_heads"], model["n_kv_heads"], model["head_dim"]
-    eps, theta = model["rms_eps"], model["rope_theta"]
-    W = model["sliding_window"]
-    tokens = [int(anchor)] + [model["mask_token"]] * (BLOCK - 1)
-    pos = C + np.arange(BLOCK)
-    X = w["embed"][tokens].astype(np.float64)  # residual stream, float64 here
-    for l, lw in enumerate(w["layers"]):
-        h = round_bf16(rms_norm(X, lw["input_layernorm"], eps))
-        q = (h @ lw["q_proj"].T).reshape(BLOCK, nq, d)
-        k = (h @ lw["k_proj"].T).reshape(BLOCK, nkv, d)
-        v = (h @ lw["v_proj"].T).reshape(BLOCK, nkv, d)
-        q = round_bf16(rope(rms_norm(q, lw["q_norm"], eps), pos[:, None], theta))
-        k = round_bf16(rope(rms_norm(k, lw["k_norm"], eps), pos[:, None], theta))
-        v = round_bf16(v)
-        vis = visible_positions(model["layer_kinds"][l], C, W)
-        keys = np.concatenate([ctx_k[l][vis], k], axis=0)
-        vals = np.concatenate([ctx_v[l][vis], v], axis=0)
-        att = round_bf16(block_attention(q, keys, vals).reshape(BLOCK, nq * d))
-        X = X + att @ lw["o_proj"].T
-        h2 = round_bf16(rms_norm(X, lw["post_attention_layernorm"], eps))
-        gate = h2 @ lw["gate_proj"].T
-        up = h2 @ lw["up_proj"].T
-        mid = round_bf16(silu(gate) * up)
-        X = X + mid @ lw["down_proj"].T
-    z = round_bf16(rms_norm(X[1:], w["norm"], eps))
-    logits = round_bf16(z @ w["embed"].T)
-    assert logits.shape == (BLOCK - 1, w["embed"].shape[0]) and X.shape == (BLOCK, H)
-    return logits, X
+    X = block_embed(model, w, anchor)
+    Xs = [X]
+    for l in range(model["n_layers"]):
+        X = draft_layer(model, w, l, X, ctx_k[l], ctx_v[l], C)
+        Xs.append(X)
+    logits = draft_head(model, w, X)
+    assert logits.shape == (BLOCK - 1, w["embed"].shape[0]) and X.shape == (BLOCK, model["hidden"])
+    return logits, (Xs if keep_residuals else X)
 
 
 class OracleStreams:
@@ -309,8 +338,8 @@ class OracleStreams:
             self.k[s][l] = self.k[s][l][:new_len]
             self.v[s][l] = self.v[s][l][:new_len]
 
-    def draft(self, s, anchor):
-        return draft_block(self.model, self.w, self.k[s], self.v[s], self.length(s), anchor)
+    def draft(self, s, anchor, keep_residuals=False):
+        return draft_block(self.model, self.w, self.k[s], self.v[s], self.length(s), anchor, keep_residuals)
 
 
 # ----------------------------------------------------------------------------

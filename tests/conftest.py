@@ -16,9 +16,9 @@ def pytest_configure(config):
 @pytest.fixture(scope="session", autouse=True)
 def _built_library():
     """Build libdflash.so (in-tree, sm_103a) once if it is missing or stale."""
-    from block_diffusion_speculative_tap_gb300 import build as B
+    import __graft_entry__
 
-    B.build()
+    __graft_entry__.build()
     yield
 
 

@@ -21,10 +21,12 @@ def tol_report(gpu, ref, atol=ATOL, rtol=RTOL):
     bound = atol + rtol * np.abs(r)
     bad = err > bound
     return {
+        "mean_abs": float(err.mean()) if err.size else 0.0,
+        "p999_ratio": float(np.quantile(err / bound, 0.999)) if err.size else 0.0,
         "max_abs": float(err.max()) if err.size else 0.0,
         "n_bad": int(bad.sum()),
         "n": int(err.size),
-        "worst": float((err / bound).max()) if err.size else 0.0,
+        "worst": float((err / bound).max()) if err.size and np.all(bound > 0) else (0.0 if not err.any() else float("inf")),
     }
 
 

@@ -57,6 +57,7 @@ def draft_vs_oracle(D, st, ref, m, anchors, k):
     for s in range(S):
         ol, _ = ref.draft(s, int(anchors[s]))
         stats.append(assert_close(lg[s], ol, f"logits stream {s}"))
+        print(f"logits stream {s}: {stats[-1]}")
         checked, near, bad = topk_ids_match(ids[s], ol, k, margin=2 * (ATOL + RTOL * np.abs(ol).max()))
         assert bad == 0, (s, checked, near, bad)
     return logits, stats

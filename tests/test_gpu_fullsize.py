@@ -1,0 +1,250 @@
+"""Full-size parity on the four large workloads, in the launch shapes the bench
+times. The oracle computes sampled outputs one by one: sampled fused rows and
+K/V rows of a fill, and the full draft of sampled streams (it fuses only
+those streams' contexts). Everything else is checked by properties that hold
+at any size (top-k consistent with the logits, planted acceptance lengths,
+valid sampling outcomes).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synthetic_inputs as SI
+from parity_util import ATOL, RTOL, assert_close, check_topk_consistent, f64, topk_ids_match
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+@pytest.fixture(scope="module")
+def D():
+    import block_diffusion_speculative_tap_gb300 as D
+
+    return D
+
+
+def sampled_rows(n, k, seed):
+    rng = np.random.default_rng(seed)
+    idx = set(rng.choice(n, size=min(k, n), replace=False).tolist())
+    idx |= {0, n - 1}
+    return np.array(sorted(idx))
+
+
+def check_rows(st, m, w64, taps_host, s, base, rows):
+    """Fused rows and K/V cache rows of positions base + rows (oracle on those rows only)."""
+    planes = [p[rows] for p in taps_host]
+    fused = O.fuse_taps(planes, w64["fc"], w64["hidden_norm"], m["rms_eps"])
+    ring = st.ring_view()[s, base + rows].cpu().float().numpy()
+    assert_close(ring, fused, "sampled fused rows")
+    pos = base + rows
+    for l, lw in enumerate(w64["layers"]):
+        K, V, cap = st.cache_view(l)
+        k, v = O.context_kv(fused, pos, lw, m)
+        if m["layer_kinds"][l] == SI.SLIDING:
+            keep = pos >= st.length(s) - cap
+            slots = pos[keep] % cap
+            k, v = k[keep], v[keep]
+        else:
+            slots = pos
+        if len(slots) == 0:
+            continue
+        kg = K[s][:, slots].permute(1, 0, 2).cpu().float().numpy()
+        vg = V[s][:, slots].permute(1, 0, 2).cpu().float().numpy()
+        assert_close(kg, k, f"K rows layer {l}")
+        assert_close(vg, v, f"V rows layer {l}")
+
+
+# End to end, six bf16-activation layers amplify fp32-sized differences:
+# the oracle's own arithmetic run in float32 lands at mean |d logit| 6.7e-3
+# (max ~5e-2) from float64 at the 9B shape, doubling about every layer
+# through bf16 rounding flips. The stated tolerance is therefore enforced
+# stage by stage (each layer and the head fed the oracle's input and K/V, so
+# errors cannot compound); end to end the mean error must stay below the
+# tolerance's absolute term and every clearly separated candidate must agree.
+E2E_MEAN = 2e-2
+E2E_ID_MARGIN = 0.25
+
+
+def oracle_stream(m, w64, planes_host):
+    ref = O.OracleStreams(m, w64, 1)
+    ref.append(0, planes_host)
+    return ref
+
+
+def compare_draft(lg_gpu, ids_gpu, ol, k):
+    from parity_util import tol_report
+
+    rep = tol_report(lg_gpu, ol)
+    print(f"end-to-end draft logits: {rep}")
+    assert rep["mean_abs"] < E2E_MEAN, rep
+    checked, near, bad = topk_ids_match(ids_gpu, ol, k, E2E_ID_MARGIN)
+    print(f"top-{k} ids: checked {checked}, near ties {near}, mismatches {bad}")
+    assert bad == 0 and checked > 0, (checked, near, bad)
+    return rep
+
+
+def staged_parity(st, ref, rs, m, s, anchor, k):
+    """Every layer and the head on the oracle's input, within the tolerance.
+
+    rs: stream index inside the oracle state `ref`; s: stream in the GPU state.
+    The GPU caches of stream s are overwritten with the oracle's K/V so the
+    attention reads identical context."""
+    C = ref.length(rs)
+    assert st.length(s) == C
+    ol, Xs = ref.draft(rs, anchor, keep_residuals=True)
+    for l in range(m["n_layers"]):
+        K, V, cap = st.cache_view(l)
+        if m["layer_kinds"][l] == SI.SLIDING:
+            pos = np.arange(max(0, C - cap), C)
+            slots = torch.from_numpy(pos % cap)
+        else:
+            pos = np.arange(C)
+            slots = torch.from_numpy(pos)
+        kk = torch.from_numpy(ref.k[rs][l][pos].transpose(1, 0, 2).copy()).to(torch.bfloat16).cuda()
+        vv = torch.from_numpy(ref.v[rs][l][pos].transpose(1, 0, 2).copy()).to(torch.bfloat16).cuda()
+        K[s][:, slots.cuda()] = kk
+        V[s][:, slots.cuda()] = vv
+    for l in range(m["n_layers"]):
+        X = torch.from_numpy(Xs[l].astype(np.float32)).cuda()
+        st.draft_layers(X, l, l + 1, s_begin=s)
+        rep = assert_close(X.cpu().numpy(), Xs[l + 1], f"layer {l} residual")
+        print(f"stage layer {l}: {rep}")
+    X = torch.from_numpy(Xs[-1].astype(np.float32)).cuda()
+    logits, ids, vals = st.draft_head(X, k=k)
+    rep = assert_close(logits.cpu().float().numpy(), ol, "head logits")
+    print(f"stage head: {rep}")
+    check_topk_consistent(logits, ids, vals)
+    checked, near, bad = topk_ids_match(ids.cpu().numpy(), ol, k, 2 * (ATOL + RTOL * np.abs(ol).max()))
+    assert bad == 0, (checked, near, bad)
+    return ol
+
+
+@pytest.fixture(scope="module")
+def nine_b(D):
+    P = SI.preset("9b")
+    m = P["model"]
+    w = SI.make_weights(m, P["seed"], device="cuda")
+    dr = D.Drafter(m, w)
+    yield P, m, w, dr, O.weights_to_f64(w)
+    dr.close()
+
+
+def test_9b_batch1_decode_round(D, nine_b):
+    P, m, w, dr, w64 = nine_b
+    C0 = P["context"][0]
+    st = dr.new_state(1, P["ring"])
+    ctx = SI.make_taps(m, C0 + 16, P["seed"] + 1, device="cuda")
+    st.fuse_taps([t[:C0] for t in ctx], [(0, 0, C0)])  # prompt fill (4096 rows)
+    st.fuse_taps([t[C0:] for t in ctx], [(0, C0, 16)])  # the round's 16 committed rows
+    host = [f64(t) for t in ctx]
+    check_rows(st, m, w64, [h[:C0] for h in host], 0, 0, sampled_rows(C0, 40, 1))
+    check_rows(st, m, w64, [h[C0:] for h in host], 0, C0, np.arange(16))
+    anchor = SI.anchor_ids(1, m["vocab"], m["mask_token"], P["seed"] + 2, device="cuda")
+    logits, ids, vals = st.draft(anchor, k=P["topk"])
+    check_topk_consistent(logits, ids, vals)
+    ref = oracle_stream(m, w64, host)
+    ol = staged_parity(st, ref, 0, m, 0, int(anchor[0]), P["topk"])
+    compare_draft(logits.cpu().float().numpy(), ids.cpu().numpy(), ol, P["topk"])
+    # verification on the drafted top-1 ids: planted acceptance is recovered
+    tl = SI.make_logits((1, 16, m["vocab"]), P["target_logit_std"], P["seed"] + 3)
+    L = 9
+    SI.plant_accepts(tl, ids[:, 0].reshape(1, 15).cpu(), [L])
+    a, toks = D.verify_greedy(ids, tl.cuda())
+    assert int(a[0]) == L
+    assert toks[0, :L].tolist() == ids[:L, 0].tolist()
+    assert int(toks[0, L]) == int(torch.argmax(tl[0, L].float()))
+    rc, bits = st.status()
+    assert rc == 0 and bits == 0
+
+
+def test_long32k_append_and_windowed_draft(D, nine_b):
+    P0, m, w, dr, w64 = nine_b
+    P = SI.preset("long32k")
+    C0 = P["context"][0]
+    st = dr.new_state(1, P["ring"])
+    ctx = SI.make_taps(m, C0 + 16, P["seed"] + 1, device="cuda")
+    st.fuse_taps([t[:C0] for t in ctx], [(0, 0, C0)])
+    st.fuse_taps([t[C0:] for t in ctx], [(0, C0, 16)])
+    host = [f64(t) for t in ctx]
+    check_rows(st, m, w64, [h[:C0] for h in host], 0, 0, sampled_rows(C0, 24, 2))
+    check_rows(st, m, w64, [h[C0:] for h in host], 0, C0, np.arange(16))
+    anchor = SI.anchor_ids(1, m["vocab"], m["mask_token"], P["seed"] + 2, device="cuda")
+    logits, ids, vals = st.draft(anchor, k=P["topk"])
+    check_topk_consistent(logits, ids, vals)
+    ref = oracle_stream(m, w64, host)
+    ol = staged_parity(st, ref, 0, m, 0, int(anchor[0]), P["topk"])
+    compare_draft(logits.cpu().float().numpy(), ids.cpu().numpy(), ol, P["topk"])
+    rc, bits = st.status()
+    assert rc == 0 and bits == 0
+
+
+def test_serve32_shared_round(D, nine_b):
+    P0, m, w, dr, w64 = nine_b
+    P = SI.preset("serve32")
+    ctx = P["context"]
+    S = len(ctx)
+    st = dr.new_state(S, P["ring"])
+    taps = SI.make_taps(m, sum(ctx), P["seed"] + 1, device="cuda")
+    offs = np.concatenate([[0], np.cumsum(ctx)])
+    st.fuse_taps(taps, [(s, 0, ctx[s]) for s in range(S)])
+    anchors = SI.anchor_ids(S, m["vocab"], m["mask_token"], P["seed"] + 2, device="cuda")
+    logits, ids, vals = st.draft(anchors, k=P["topk"])
+    check_topk_consistent(logits, ids, vals)
+    lg = logits.cpu().float().numpy().reshape(S, 15, -1)
+    idn = ids.cpu().numpy().reshape(S, 15, -1)
+    # concurrent == solo: one stream drafted alone is bit-identical
+    solo, _, _ = st.draft(anchors[5:6].contiguous(), s_begin=5, k=P["topk"])
+    assert torch.equal(solo, logits[5 * 15 : 6 * 15])
+    for s in sorted({int(np.argmin(ctx)), int(np.argmax(ctx))}):
+        host = [f64(t[offs[s] : offs[s + 1]]) for t in taps]
+        ref = oracle_stream(m, w64, host)
+        ol = staged_parity(st, ref, 0, m, s, int(anchors[s]), P["topk"])
+        compare_draft(lg[s], idn[s], ol, P["topk"])
+    # greedy verification of every stream against planted target logits
+    tl = SI.make_logits((S, 16, m["vocab"]), P["target_logit_std"], P["seed"] + 3)
+    lengths = SI.make_accept_lengths(S, P["seed"] + 4)
+    SI.plant_accepts(tl, ids[:, 0].reshape(S, 15).cpu(), lengths)
+    a, toks = D.verify_greedy(ids, tl.cuda())
+    assert a.cpu().tolist() == [min(L, 15) for L in lengths]
+    rc, bits = st.status()
+    assert rc == 0 and bits == 0
+
+
+def test_dflash2_geometry_sampling_round(D):
+    P = SI.preset("dflash2geom")
+    m = P["model"]
+    w = SI.make_weights(m, P["seed"], device="cuda")
+    dr = D.Drafter(m, w)
+    ctx = P["context"]
+    S = len(ctx)
+    st = dr.new_state(S, P["ring"])
+    taps = SI.make_taps(m, sum(ctx), P["seed"] + 1, device="cuda")
+    offs = np.concatenate([[0], np.cumsum(ctx)])
+    st.fuse_taps(taps, [(s, 0, ctx[s]) for s in range(S)])
+    anchors = SI.anchor_ids(S, m["vocab"], m["mask_token"], P["seed"] + 2, device="cuda")
+    logits, ids, vals = st.draft(anchors, k=P["topk"])
+    check_topk_consistent(logits, ids, vals)
+    w64 = O.weights_to_f64(w)
+    lg = logits.cpu().float().numpy().reshape(S, 15, -1)
+    idn = ids.cpu().numpy().reshape(S, 15, -1)
+    # drafted tokens sampled from the drafter's rows, then sampling verification
+    T = P["temperature"]
+    ud = SI.make_uniforms((S * 15,), P["seed"] + 3, device="cuda")
+    _, _, draft = D.topk(logits, 0, temperature=T, uniforms=ud)
+    tl = SI.make_logits((S, 16, m["vocab"]), P["target_logit_std"], P["seed"] + 4, device="cuda")
+    u = SI.make_uniforms((S, 16, 2), P["seed"] + 5, device="cuda")
+    a, toks = D.verify_sample(draft.view(S, 15), tl, logits.view(S, 15, -1), u, T)
+    a, toks, dd = a.cpu().tolist(), toks.cpu().tolist(), draft.view(S, 15).cpu().tolist()
+    for s in range(S):
+        assert 0 <= a[s] <= 15
+        assert toks[s][: a[s]] == dd[s][: a[s]]
+        assert 0 <= toks[s][a[s]] < m["vocab"]
+        assert all(t == -1 for t in toks[s][a[s] + 1 :])
+    rc, bits = st.status()
+    assert rc == 0 and bits == 0
+    s = S - 1
+    host = [f64(t[offs[s] : offs[s + 1]]) for t in taps]
+    ref = oracle_stream(m, w64, host)
+    ol = staged_parity(st, ref, 0, m, s, int(anchors[s]), P["topk"])
+    compare_draft(lg[s], idn[s], ol, P["topk"])
+    dr.close()

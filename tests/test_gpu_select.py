@@ -2,8 +2,14 @@
 
 Inputs are seeded synthetic logits fed to both sides. Ids, accept lengths and
 tokens are compared bit for bit; a sampling decision is exempt only when the
-oracle's float64 margin to the other outcome is below 1e-4 (fp32 softmax over
-the vocabulary cannot resolve it), and such cases are counted.
+oracle's float64 margin to the other outcome is below 1e-5 of the total, and
+such cases are counted and checked for validity instead.
+
+The 1e-5 bound is the kernel's fp32 error budget: each weight exp((x-m)/T)
+carries <= 2 ulp from expf plus |x-m|/T * 2^-24 from rounding its argument
+(<= 2e-6 for |x-m|/T <= 30), and the running sums add <= 8 + 5 + 37 + 16
+fp32 roundings along any path (lane, warp scan, warp-slice steps, warps),
+about 4e-6 of the total; probabilities divide two such sums.
 """
 import json
 import os
@@ -18,7 +24,7 @@ from parity_util import f64
 
 pytestmark = pytest.mark.gpu
 
-MARGIN = 1e-4
+MARGIN = 1e-5
 
 
 @pytest.fixture(scope="module")
@@ -57,17 +63,25 @@ def test_topk_empty_and_zero_k(D):
     assert s.shape == (3,)
 
 
-@pytest.mark.parametrize("T", [1.0, 0.7])
-def test_sampling_draws_match_oracle(D, T):
-    rows, V = 64, 151936
-    lg = SI.make_logits((rows, V), 2.0, seed=11)
+@pytest.mark.parametrize("T,V,std", [(1.0, 151936, 3.0), (0.7, 151936, 3.0), (1.0, 4096, 2.0)])
+def test_sampling_draws_match_oracle(D, T, V, std):
+    rows = 64
+    lg = SI.make_logits((rows, V), std, seed=11)
     u = SI.make_uniforms((rows,), seed=12)
     _, _, s = D.topk(lg.cuda(), 0, temperature=T, uniforms=u.cuda())
     s = s.cpu().numpy()
     ref_ids, margins = O.sample_rows(f64(lg), T, f64(u))
     clear = margins > MARGIN
-    assert clear.sum() >= rows - 2
+    assert clear.sum() >= rows // 4, clear.sum()
     assert np.array_equal(s[clear], ref_ids[clear])
+    # a near-tie draw must still sit within the error budget of u on the CDF
+    uu = f64(u)
+    for r in np.nonzero(~clear)[0]:
+        p = O.softmax_t(f64(lg[r]), T)
+        c = np.cumsum(p)
+        j = int(s[r])
+        lo = c[j - 1] if j > 0 else 0.0
+        assert p[j] > 0 and lo - 2 * MARGIN <= uu[r] <= c[j] + 2 * MARGIN, r
 
 
 def test_greedy_golden_fixtures(D):
@@ -114,8 +128,8 @@ def test_greedy_out_of_range_draft_never_accepted(D):
     assert a.item() == 3 and toks[0, 3].item() == 7
 
 
-def _sampling_inputs(S, V, seed, noise):
-    tl = SI.make_logits((S, 16, V), 1.0, seed)
+def _sampling_inputs(S, V, seed, noise, std):
+    tl = SI.make_logits((S, 16, V), std, seed)
     dl = (tl[:, :15].float() + noise * SI.make_logits((S, 15, V), 1.0, seed + 1).float()).to(torch.bfloat16)
     # drafted tokens: drawn from the drafter's rows (input construction)
     g = torch.Generator().manual_seed(seed + 2)
@@ -125,9 +139,11 @@ def _sampling_inputs(S, V, seed, noise):
     return tl, dl, draft, u
 
 
-@pytest.mark.parametrize("S,V,noise,T", [(8, 151936, 0.3, 1.0), (16, 4096, 1.0, 1.0), (8, 4096, 0.5, 0.6)])
-def test_sampling_verify_matches_oracle(D, S, V, noise, T):
-    tl, dl, draft, u = _sampling_inputs(S, V, 31 + S, noise)
+@pytest.mark.parametrize(
+    "S,V,noise,T,std", [(8, 151936, 0.3, 1.0, 3.0), (16, 4096, 1.0, 1.0, 2.0), (16, 4096, 0.5, 0.6, 2.0)]
+)
+def test_sampling_verify_matches_oracle(D, S, V, noise, T, std):
+    tl, dl, draft, u = _sampling_inputs(S, V, 31 + S, noise, std)
     a, toks = D.verify_sample(draft.cuda(), tl.cuda(), dl.cuda(), u.cuda(), T)
     a, toks = a.cpu().tolist(), toks.cpu().tolist()
     tr, dr, ur = f64(tl), f64(dl), f64(u)
@@ -135,11 +151,15 @@ def test_sampling_verify_matches_oracle(D, S, V, noise, T):
     for s in range(S):
         oa, ot, margins = O.sampling_verify(draft[s].tolist(), tr[s], dr[s], ur[s], T)
         if min(margins) <= MARGIN:
+            # near tie somewhere in the chain: the result must still be valid
+            assert 0 <= a[s] <= 15
+            assert toks[s][: a[s]] == draft[s].tolist()[: a[s]]
+            assert 0 <= toks[s][a[s]] < V and all(t == -1 for t in toks[s][a[s] + 1 :])
             continue
         checked += 1
         assert a[s] == oa, s
         assert toks[s] == ot, s
-    assert checked >= S - 2
+    assert checked >= max(2, S // 4), checked
 
 
 def test_sampling_verify_distribution_is_target(D):
