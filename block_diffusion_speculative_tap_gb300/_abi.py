@@ -129,7 +129,7 @@ def _load():
     fn("dflash_fuse_taps", C.c_int, vp, vp, P(vp), i64, C.c_int, P(i32), P(i64), P(i32), C.c_int, vp, sz, vp)
     fn("dflash_draft_workspace_bytes", C.c_int, vp, vp, C.c_int, C.c_int, P(sz))
     fn("dflash_draft_block", C.c_int, vp, vp, C.c_int, C.c_int, vp, vp, vp, vp, C.c_int, vp, sz, vp)
-    fn("dflash_draft_layers", C.c_int, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, vp, vp, sz, vp)
+    fn("dflash_draft_stages", C.c_int, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, vp, vp, sz, vp)
     fn("dflash_draft_head", C.c_int, vp, vp, C.c_int, vp, vp, vp, vp, C.c_int, vp, sz, vp)
     fn("dflash_topk", C.c_int, vp, C.c_int, C.c_int, C.c_int, C.c_float, vp, vp, vp, vp, vp)
     fn("dflash_verify_workspace_bytes", C.c_int, C.c_int, C.c_int, C.c_int, P(sz))
@@ -163,7 +163,7 @@ EXPORTED = [
     "dflash_fuse_taps",
     "dflash_draft_workspace_bytes",
     "dflash_draft_block",
-    "dflash_draft_layers",
+    "dflash_draft_stages",
     "dflash_draft_head",
     "dflash_topk",
     "dflash_verify_workspace_bytes",

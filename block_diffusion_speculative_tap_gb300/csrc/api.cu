@@ -776,18 +776,42 @@ int dflash_draft_workspace_bytes(const dflash_handle* h, const dflash_state* st,
 
 namespace {
 
-// Layers [l0, l1) of the block forward on the fp32 residual X [16*s_count, H].
-int run_layers(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int l0, int l1, float* X,
+// Stages [g0, g1) of the block forward on the fp32 residual X [16*s_count, H]:
+// stage 2l is layer l's attention half (input norm, QKV, attention, O-proj
+// added to X), stage 2l+1 its MLP half (post norm, SwiGLU, down added to X).
+int run_stages(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int g0, int g1, float* X,
                const DraftWs& w, int*& counters, cudaStream_t s) {
   const dflash_config& c = h->cfg;
   const int T = s_count * DFLASH_BLOCK;
   const int qd = c.n_q_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim;
   const int nch = max_nchunk(st);
   int rc = DFLASH_OK;
-  for (int l = l0; l < l1; ++l) {
+  for (int g = g0; g < g1; ++g) {
+    const int l = g >> 1;
     const dflash_layer_weights& L = h->layers[l];
     GemmPlan qkv, o, gu, dn;
     layer_plans(h, l, T, qkv, o, gu, dn);
+    if (g & 1) {
+      // post-attention RMSNorm -> SwiGLU -> down projection added to the residual
+      rc = launch_rmsnorm_rows(w.hbuf, X, static_cast<const __nv_bfloat16*>(L.post_norm), T, c.hidden, c.rms_eps, 0,
+                               s);
+      if (rc) return rc;
+      gu.b_ptr[0] = w.hbuf;
+      gu.ldb = c.hidden;
+      gu.epi_args.out = w.mid;
+      gu.epi_args.ldo = c.ffn;
+      rc = gemm_launch(gu, w.partial, counters, st->status, h->num_sms, s);
+      if (rc) return rc;
+      counters += gemm_counter_count(gu);
+      dn.b_ptr[0] = w.mid;
+      dn.ldb = c.ffn;
+      dn.epi_args.out = X;
+      dn.epi_args.ldo = c.hidden;
+      rc = gemm_launch(dn, w.partial, counters, st->status, h->num_sms, s);
+      if (rc) return rc;
+      counters += gemm_counter_count(dn);
+      continue;
+    }
     // input RMSNorm -> QKV with q_norm / k_norm + RoPE at positions C..C+15
     rc = launch_rmsnorm_rows(w.hbuf, X, static_cast<const __nv_bfloat16*>(L.input_norm), T, c.hidden, c.rms_eps, 0, s);
     if (rc) return rc;
@@ -843,23 +867,6 @@ int run_layers(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int
     rc = gemm_launch(o, w.partial, counters, st->status, h->num_sms, s);
     if (rc) return rc;
     counters += gemm_counter_count(o);
-    // post-attention RMSNorm -> SwiGLU -> down projection added to the residual
-    rc = launch_rmsnorm_rows(w.hbuf, X, static_cast<const __nv_bfloat16*>(L.post_norm), T, c.hidden, c.rms_eps, 0, s);
-    if (rc) return rc;
-    gu.b_ptr[0] = w.hbuf;
-    gu.ldb = c.hidden;
-    gu.epi_args.out = w.mid;
-    gu.epi_args.ldo = c.ffn;
-    rc = gemm_launch(gu, w.partial, counters, st->status, h->num_sms, s);
-    if (rc) return rc;
-    counters += gemm_counter_count(gu);
-    dn.b_ptr[0] = w.mid;
-    dn.ldb = c.ffn;
-    dn.epi_args.out = X;
-    dn.epi_args.ldo = c.hidden;
-    rc = gemm_launch(dn, w.partial, counters, st->status, h->num_sms, s);
-    if (rc) return rc;
-    counters += gemm_counter_count(dn);
   }
   return DFLASH_OK;
 }
@@ -910,22 +917,23 @@ int dflash_draft_block(dflash_handle* h, dflash_state* st, int s_begin, int s_co
   rc = launch_embed(w.X, h->embed, anchor_ids, s_count, c.hidden, c.vocab, c.mask_token, st->status, s);
   if (rc) return rc;
   int* counters = w.counters;
-  rc = run_layers(h, st, s_begin, s_count, 0, c.n_layers, w.X, w, counters, s);
+  rc = run_stages(h, st, s_begin, s_count, 0, 2 * c.n_layers, w.X, w, counters, s);
   if (rc) return rc;
   return run_head(h, st->status, s_count, w.X, w, logits, topk_ids, topk_vals, k, counters, s);
 }
 
-int dflash_draft_layers(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int l0, int l1, float* X,
-                        void* ws, size_t ws_bytes, dflash_stream_t stream) {
+int dflash_draft_stages(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int stage0, int stage1,
+                        float* X, void* ws, size_t ws_bytes, dflash_stream_t stream) {
   int rc = check_draft_args(h, st, s_begin, s_count, ws, nullptr, nullptr, 0, nullptr);
   if (rc) return rc;
-  if (!X || !aligned16(X) || l0 < 0 || l1 < l0 || l1 > h->cfg.n_layers) return DFLASH_E_INVALID_ARG;
+  if (!X || !aligned16(X) || stage0 < 0 || stage1 < stage0 || stage1 > 2 * h->cfg.n_layers)
+    return DFLASH_E_INVALID_ARG;
   DraftWs w{};
   if (draft_ws_layout(h, st, s_count, false, ws, &w) > ws_bytes) return DFLASH_E_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(w.counters, 0, w.n_counters * sizeof(int), s) != cudaSuccess) return DFLASH_E_CUDA;
   int* counters = w.counters;
-  return run_layers(h, st, s_begin, s_count, l0, l1, X, w, counters, s);
+  return run_stages(h, st, s_begin, s_count, stage0, stage1, X, w, counters, s);
 }
 
 int dflash_draft_head(dflash_handle* h, dflash_state* st, int s_count, const float* X, void* logits_out,

@@ -289,16 +289,17 @@ class State:
         return logits, ids, vals
 
 
-    def draft_layers(self, X, l0, l1, s_begin=0):
-        """Run layers [l0, l1) on the fp32 residual X [S*16, H] in place."""
+    def draft_stages(self, X, g0, g1, s_begin=0):
+        """Run stages [g0, g1) on the fp32 residual X [S*16, H] in place;
+        stage 2l = layer l's attention half, 2l+1 = its MLP half."""
         _need(X, torch.float32, "X")
         S = X.shape[0] // 16
         ws = self.ws_draft.get(self.draft_workspace_bytes(S, False))
         check(
-            lib.dflash_draft_layers(
-                self.drafter.handle, self.st, s_begin, S, l0, l1, _ptr(X), _ptr(ws), ws.numel(), _stream()
+            lib.dflash_draft_stages(
+                self.drafter.handle, self.st, s_begin, S, g0, g1, _ptr(X), _ptr(ws), ws.numel(), _stream()
             ),
-            "dflash_draft_layers",
+            "dflash_draft_stages",
         )
         return X
 

@@ -257,17 +257,21 @@ int dflash_draft_block(dflash_handle* h, dflash_state* st, int s_begin, int s_co
                        void* logits_out, int32_t* topk_ids, float* topk_vals, int k, void* ws, size_t ws_bytes,
                        dflash_stream_t stream);
 
-/* The same block forward in stages, for layer-by-layer execution and for
+/* The same block forward in stages, for staged execution and for
  * stage-isolated checks (each stage fed a reference input, so errors do not
- * compound). X is the fp32 residual stream, device [s_count*16, H], row
- * 16*i + j = row j (0 = anchor) of stream s_begin + i; it must be 16-byte
- * aligned. dflash_draft_layers runs layers l0 .. l1-1 on X in place (with the
- * streams' K/V caches and lengths as dflash_draft_block would);
- * dflash_draft_head applies the final norm to the 15 mask rows of every
- * stream, the LM head (logits_out required) and the optional top-k. Both take
- * the workspace of dflash_draft_workspace_bytes(h, st, s_count, 0). */
-int dflash_draft_layers(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int l0, int l1, float* X,
-                        void* ws, size_t ws_bytes, dflash_stream_t stream);
+ * compound). A layer is two stages, one per residual add [TF1851 item 1]:
+ * stage 2l = layer l's input norm, Q/K/V, attention and O projection added
+ * to the residual; stage 2l+1 = its post-attention norm and SwiGLU MLP added
+ * to the residual. X is the fp32 residual stream, device [s_count*16, H],
+ * row 16*i + j = row j (0 = anchor) of stream s_begin + i; 16-byte aligned.
+ * dflash_draft_stages runs stages stage0 .. stage1-1 (0 <= stage0 <= stage1
+ * <= 2L) on X in place, with the streams' K/V caches and lengths as
+ * dflash_draft_block would; dflash_draft_head applies the final norm to the
+ * 15 mask rows of every stream, the LM head (logits_out required) and the
+ * optional top-k. Both take the workspace of
+ * dflash_draft_workspace_bytes(h, st, s_count, 0). */
+int dflash_draft_stages(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int stage0, int stage1,
+                        float* X, void* ws, size_t ws_bytes, dflash_stream_t stream);
 int dflash_draft_head(dflash_handle* h, dflash_state* st, int s_count, const float* X, void* logits_out,
                       int32_t* topk_ids, float* topk_vals, int k, void* ws, size_t ws_bytes, dflash_stream_t stream);
 

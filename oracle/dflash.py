@@ -76,6 +76,8 @@ __all__ = [
     "block_attention",
     "silu",
     "block_embed",
+    "attention_half",
+    "mlp_half",
     "draft_layer",
     "draft_head",
     "draft_block",
@@ -237,12 +239,13 @@ def block_embed(model, w, anchor):
     return w["embed"][tokens].astype(np.float64)
 
 
-def draft_layer(model, w, l, X, ctx_k, ctx_v, C):
-    """One drafter layer on the block's residual X [16, H] (qwen3 body:
-    TensorFold #1851 item 1, "two residual adds a layer").
+def attention_half(model, w, l, X, ctx_k, ctx_v, C):
+    """First half of drafter layer l: input RMSNorm, Q/K/V with per-head
+    norms and RoPE, non-causal attention over the layer's visible context
+    plus the block, O projection added to the residual (TensorFold #1851
+    item 1: each layer adds attention to the residual).
 
     ctx_k, ctx_v: [C, n_kv, d] bf16 K/V of this layer for positions 0..C-1.
-    Returns the residual after the attention and MLP adds.
     """
     nq, nkv, d = model["n_q_heads"], model["n_kv_heads"], model["head_dim"]
     eps, theta = model["rms_eps"], model["rope_theta"]
@@ -259,12 +262,25 @@ def draft_layer(model, w, l, X, ctx_k, ctx_v, C):
     keys = np.concatenate([ctx_k[vis], k], axis=0)
     vals = np.concatenate([ctx_v[vis], v], axis=0)
     att = round_bf16(block_attention(q, keys, vals).reshape(BLOCK, nq * d))
-    X = X + att @ lw["o_proj"].T
-    h2 = round_bf16(rms_norm(X, lw["post_attention_layernorm"], eps))
+    return X + att @ lw["o_proj"].T
+
+
+def mlp_half(model, w, l, X):
+    """Second half of drafter layer l: post-attention RMSNorm, SwiGLU MLP
+    added to the residual (TensorFold #1851 item 1: each layer adds its MLP
+    to the residual)."""
+    lw = w["layers"][l]
+    h2 = round_bf16(rms_norm(X, lw["post_attention_layernorm"], model["rms_eps"]))
     gate = h2 @ lw["gate_proj"].T
     up = h2 @ lw["up_proj"].T
     mid = round_bf16(silu(gate) * up)
     return X + mid @ lw["down_proj"].T
+
+
+def draft_layer(model, w, l, X, ctx_k, ctx_v, C):
+    """One drafter layer on the block's residual X [16, H] (qwen3 body:
+    TensorFold #1851 item 1, "two residual adds a layer")."""
+    return mlp_half(model, w, l, attention_half(model, w, l, X, ctx_k, ctx_v, C))
 
 
 def draft_head(model, w, X):
@@ -286,12 +302,16 @@ def draft_block(model, w, ctx_k, ctx_v, C, anchor, keep_residuals=False):
     ctx_k[l], ctx_v[l]: [C, n_kv, d] bf16 context K/V of layer l for positions
     0..C-1. anchor: token id at position C. Returns (logits [15, V] bf16 values
     of the mask rows, X final residual [16, H]); with keep_residuals, X is the
-    list of residuals before layer 0, ..., after the last layer.
+    list of residuals at every stage boundary: before layer 0, after layer
+    0's attention add, after its MLP add, ..., after the last layer's MLP add
+    (2L + 1 entries).
     """
     X = block_embed(model, w, anchor)
     Xs = [X]
     for l in range(model["n_layers"]):
-        X = draft_layer(model, w, l, X, ctx_k[l], ctx_v[l], C)
+        X = attention_half(model, w, l, X, ctx_k[l], ctx_v[l], C)
+        Xs.append(X)
+        X = mlp_half(model, w, l, X)
         Xs.append(X)
     logits = draft_head(model, w, X)
     assert logits.shape == (BLOCK - 1, w["embed"].shape[0]) and X.shape == (BLOCK, model["hidden"])
