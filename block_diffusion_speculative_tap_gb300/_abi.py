@@ -134,6 +134,7 @@ def _load():
     fn("dflash_topk", C.c_int, vp, C.c_int, C.c_int, C.c_int, C.c_float, vp, vp, vp, vp, vp)
     fn("dflash_verify_workspace_bytes", C.c_int, C.c_int, C.c_int, C.c_int, P(sz))
     fn("dflash_verify", C.c_int, C.c_int, C.c_int, C.c_int, vp, C.c_int, vp, vp, vp, C.c_float, vp, vp, vp, sz, vp)
+    fn("dflash_verify_sample_noalloc", C.c_int, C.c_int, C.c_int, vp, C.c_int, vp, vp, vp, C.c_float, vp, vp, vp)
     fn("dflash_trace_enable", C.c_int, C.c_int)
     fn("dflash_trace_count", C.c_int)
     fn("dflash_trace_get", C.c_int, C.c_int, P(C.c_char_p), P(C.c_float), P(C.c_double), P(C.c_double))
@@ -168,6 +169,7 @@ EXPORTED = [
     "dflash_topk",
     "dflash_verify_workspace_bytes",
     "dflash_verify",
+    "dflash_verify_sample_noalloc",
     "dflash_trace_enable",
     "dflash_trace_count",
     "dflash_trace_get",

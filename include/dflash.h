@@ -309,6 +309,30 @@ int dflash_verify(int mode, int streams, int vocab, const int32_t* draft_ids, in
                   const void* draft_logits, const float* uniforms, float temperature, int32_t* accept_len,
                   int32_t* out_tokens, void* ws, size_t ws_bytes, dflash_stream_t stream);
 
+/* ---------------------------------------------------------------- no-allocation variant
+ * Sampling verification for callers that cannot allocate device memory (a
+ * host framework that owns every allocation through its own pool, a plugin
+ * inside another runtime, a serving loop that must not call the allocator
+ * once running). Same arguments, rule and outputs as
+ * dflash_verify(DFLASH_VERIFY_SAMPLE, ...), but the scratch lives in a
+ * 248 KiB array inside the library (held on every GPU that loads it until
+ * the process exits), so no workspace is passed. The pages have no
+ * counterpart: this is an interface for such callers only.
+ * - At most DFLASH_NOALLOC_MAX_STREAMS streams; more returns
+ *   DFLASH_E_WORKSPACE and enqueues nothing.
+ * - The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture.
+ * - All calls share the array: calls that overlap on the GPU (issued on
+ *   different streams or from several host threads with nothing ordering
+ *   them) race on it. Nothing in it needs to start at zero; each call writes
+ *   every value it reads before reading it. */
+#define DFLASH_NOALLOC_MAX_STREAMS 1024
+int dflash_verify_sample_noalloc(int streams, int vocab, const int32_t* draft_ids, int draft_ld,
+                                 const void* target_logits, const void* draft_logits, const float* uniforms,
+                                 float temperature, int32_t* accept_len, int32_t* out_tokens,
+                                 dflash_stream_t stream);
+
 /* ---------------------------------------------------------------- misc */
 const char* dflash_strerror(int code);
 /* Kernel launches enqueued by this process so far (all entry points). */
