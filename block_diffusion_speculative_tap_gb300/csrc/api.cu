@@ -103,6 +103,7 @@ struct dflash_state {
   __nv_bfloat16* ring = nullptr;
   std::vector<__nv_bfloat16*> kc, vc;
   std::vector<int> cap, window;
+  std::vector<CUtensorMap> kmap, vmap;  // per-layer cache maps of the cluster attention
   std::vector<int64_t> host_len;
 };
 
@@ -337,6 +338,18 @@ int dflash_state_init(dflash_handle* h, void* dev_mem, size_t bytes, int streams
   st->R = ring_capacity;
   state_layout(h, streams, ring_capacity, dev_mem, st);
   st->host_len.assign(streams, 0);
+  st->kmap.resize(h->cfg.n_layers);
+  st->vmap.resize(h->cfg.n_layers);
+  if (h->cfg.head_dim == 128) {
+    for (int l = 0; l < h->cfg.n_layers; ++l) {
+      const int rc = attention_cluster_maps(&st->kmap[l], &st->vmap[l], st->kc[l], st->vc[l],
+                                            streams * h->cfg.n_kv_heads, st->cap[l]);
+      if (rc) {
+        delete st;
+        return rc;
+      }
+    }
+  }
   // RoPE table: angle pos * theta^(-2i/d), evaluated in double precision
   const int d = h->cfg.head_dim, half = d / 2;
   const size_t npos = static_cast<size_t>(ring_capacity) + DFLASH_BLOCK;
@@ -352,6 +365,12 @@ int dflash_state_init(dflash_handle* h, void* dev_mem, size_t bytes, int streams
   cudaError_t e = cudaMemcpyAsync(st->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(st->lens, 0, sizeof(int) * streams, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(st->status, 0, sizeof(int) * 4, s);
+  // caches start at zero: attention tiles may read (and mask) slots not yet written
+  for (int l = 0; l < h->cfg.n_layers && e == cudaSuccess; ++l) {
+    const size_t n = static_cast<size_t>(streams) * h->cfg.n_kv_heads * st->cap[l] * h->cfg.head_dim * 2;
+    e = cudaMemsetAsync(st->kc[l], 0, n, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(st->vc[l], 0, n, s);
+  }
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);  // the host table goes out of scope
   if (e != cudaSuccess) {
     delete st;
@@ -857,7 +876,9 @@ int run_stages(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int
       }
       a.trace_bytes = keys * kvd * 2.0 * 2.0 + 2.0 * T * qd * 2.0;
     }
-    rc = launch_attention(a, s_count, s);
+    a.err = st->status;
+    rc = attention_cluster_supported(a) ? launch_attention_cluster(a, st->kmap[l], st->vmap[l], s_count, s)
+                                        : launch_attention(a, s_count, s);
     if (rc) return rc;
     // O projection added to the residual
     o.b_ptr[0] = w.attn;

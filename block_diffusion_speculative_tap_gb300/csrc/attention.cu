@@ -262,32 +262,54 @@ __global__ void __launch_bounds__(256) attn_kernel(const AttnArgs a) {
   }
 }
 
-// Merge the chunks of one (stream, query head): O = sum_c 2^(m_c - M) O_c /
-// sum_c 2^(m_c - M) l_c, in chunk order.
+// Merge the chunks of one (stream, query head, row): O = sum_c 2^(m_c - M) O_c
+// / sum_c 2^(m_c - M) l_c, in chunk order. One warp per output row vector,
+// each lane owning D/32 consecutive dims.
 template <int D>
-__global__ void attn_combine_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a, int s_count) {
   pdl_trigger();
   pdl_wait();
-  const int h = blockIdx.x;
-  const int si = blockIdx.y;
+  constexpr int kPer = D / 32;
+  const int wg = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wg >= s_count * a.nq * 16) return;
+  const int r = wg & 15;
+  const int h = (wg >> 4) % a.nq;
+  const int si = (wg >> 4) / a.nq;
   const int s = a.s_begin + si;
   const int C = a.lens[s];
   const int nvis = a.window > 0 ? min(C, a.window) : C;
   const int nu = max(1, (nvis + a.chunk - 1) / a.chunk);
   const size_t unit0 = (static_cast<size_t>(si) * a.nq + h) * a.nchunk;
-  for (int idx = threadIdx.x; idx < 16 * D; idx += blockDim.x) {
-    const int r = idx / D;
-    const int dim = idx - r * D;
-    float M = -INFINITY;
-    for (int u = 0; u < nu; ++u) M = fmaxf(M, a.part_ml[(unit0 + u) * 32 + r * 2]);
-    float num = 0.f, den = 0.f;
-    for (int u = 0; u < nu; ++u) {
-      const float w = exp2f(a.part_ml[(unit0 + u) * 32 + r * 2] - M);
-      num += w * a.part_o[(unit0 + u) * 16 * D + r * D + dim];
-      den += w * a.part_ml[(unit0 + u) * 32 + r * 2 + 1];
+  const float* ml = a.part_ml + unit0 * 32 + r * 2;
+  float M = -INFINITY;
+  for (int u = lane; u < nu; u += 32) M = fmaxf(M, ml[u * 32]);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float acc[kPer];
+#pragma unroll
+  for (int p = 0; p < kPer; ++p) acc[p] = 0.f;
+  float den = 0.f;
+  const float* po = a.part_o + (unit0 * 16 + r) * D + lane * kPer;
+#pragma unroll 4
+  for (int u = 0; u < nu; ++u) {
+    const float w = exp2f(ml[u * 32] - M);
+    den += w * ml[u * 32 + 1];
+    const float* pu = po + static_cast<size_t>(u) * 16 * D;
+    if constexpr (kPer == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(pu);
+      acc[0] += w * v.x;
+      acc[1] += w * v.y;
+      acc[2] += w * v.z;
+      acc[3] += w * v.w;
+    } else {
+#pragma unroll
+      for (int p = 0; p < kPer; ++p) acc[p] += w * pu[p];
     }
-    a.out[(static_cast<int64_t>(si) * 16 + r) * (a.nq * D) + h * D + dim] = __float2bfloat16_rn(num / den);
   }
+  __nv_bfloat16* out = a.out + (static_cast<int64_t>(si) * 16 + r) * (a.nq * D) + h * D + lane * kPer;
+#pragma unroll
+  for (int p = 0; p < kPer; ++p) out[p] = __float2bfloat16_rn(acc[p] / den);
 }
 
 template <int D>
@@ -307,10 +329,11 @@ int launch_d(const AttnArgs& a, int s_count, cudaStream_t st) {
     count_launch();
     if (e != cudaSuccess) return DFLASH_E_CUDA;
   }
-  dim3 g2(a.nq, s_count);
+  const int warps = s_count * a.nq * 16;
+  dim3 g2((warps + 7) / 8);
   {
     TraceScope ts(st, "attention.combine", static_cast<double>(s_count) * a.nq * 16 * D * 2, 0.0);
-    const cudaError_t e = launch_pdl(attn_combine_kernel<D>, g2, dim3(256), 0, st, a);
+    const cudaError_t e = launch_pdl(attn_combine_kernel<D>, g2, dim3(256), 0, st, a, s_count);
     count_launch();
     if (e != cudaSuccess) return DFLASH_E_CUDA;
   }

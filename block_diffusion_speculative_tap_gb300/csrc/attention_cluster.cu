@@ -1,0 +1,496 @@
+// Block attention for head dimension 128 as one thread-block cluster per
+// (stream, kv head).
+//
+// The visible context keys of a (stream, kv head) are split evenly over the
+// kClusterCtas CTAs of a cluster; the last CTA also takes the block's own 16
+// rows. Inside a CTA one producer thread streams 64-key tiles of K and V from
+// the head-major cache with TMA (3-D tensor maps, 128-byte swizzle) through
+// a ring of kStages shared-memory stages; 2G consumer warps (G = query heads
+// per kv head, two key-tile parities each) compute scores and P*V on the
+// tensor cores (mma.sync m16n8k16, P as a bf16 hi + lo pair) with an online
+// softmax. The two parities of a head merge in shared memory, then the CTAs
+// of the cluster reduce-scatter their partial (max, sum, output) through
+// distributed shared memory, in rank order, and write the bf16 attention
+// output: no partials in global memory and no second kernel. The split
+// depends only on the stream's visible length, so a stream's result does
+// not depend on the batch.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dfl {
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kKeys = 64;             // keys per tile
+constexpr int kStages = 4;
+constexpr int kClusterCtas = 8;
+constexpr int kSubBytes = kKeys * 128;   // 64 rows x 64 dims (128 B) per swizzled sub-tile
+constexpr int kTileBytes = 4 * kSubBytes;  // K lo, K hi, V lo, V hi = 32 KiB
+
+struct ClusterAttnSmem {
+  static constexpr int kStageOff = 0;
+  static constexpr int kBlockOff = kStages * kTileBytes;       // block tile (rows 16..63 zero)
+  static constexpr int kBarOff = kBlockOff + kTileBytes;
+  static constexpr int kBytes = kBarOff + 8 * (2 * kStages + 1) + 64;
+};
+
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t saddr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr));
+}
+
+__device__ __forceinline__ void split_hi_lo(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// Byte offset of (row, 16-byte chunk) in a 128-byte-swizzled sub-tile.
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void tma3d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma2d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t crank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void csync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cmap(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float cld(uint32_t a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 cld4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a)
+               : "memory");
+  return v;
+}
+
+struct AttnState {
+  float o[kD / 8][4];
+  float m[2];
+  float l[2];
+};
+
+// One 64-key tile at shared address `t` (K lo/hi, V lo/hi sub-tiles) for
+// keys [0, nvalid); scores use `sc` = log2(e) / sqrt(d).
+__device__ __forceinline__ void attend_tile(AttnState& S, const uint32_t (&qa)[kD / 16][4], uint32_t t, int nvalid,
+                                            float sc, int lane) {
+  float sacc[8][4];
+#pragma unroll
+  for (int n = 0; n < 8; ++n) {
+    sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
+    const int key = n * 8 + (lane >> 2);
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+      const uint32_t sub = t + static_cast<uint32_t>((kk >> 2) * kSubBytes);
+      const int kq = kk & 3;
+      uint32_t b0, b1;
+      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b0) : "r"(sub + swz(key, 2 * kq) + (lane & 3) * 4));
+      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b1) : "r"(sub + swz(key, 2 * kq + 1) + (lane & 3) * 4));
+      mma16816(sacc[n], qa[kk], b0, b1);
+    }
+  }
+  float tmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int n = 0; n < 8; ++n) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int key = n * 8 + (lane & 3) * 2 + (e & 1);
+      const float v = key < nvalid ? sacc[n][e] * sc : -INFINITY;
+      sacc[n][e] = v;
+      tmax[e >> 1] = fmaxf(tmax[e >> 1], v);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    tmax[r] = fmaxf(tmax[r], __shfl_xor_sync(0xffffffffu, tmax[r], 1));
+    tmax[r] = fmaxf(tmax[r], __shfl_xor_sync(0xffffffffu, tmax[r], 2));
+  }
+  float mnew[2], alpha[2], psum[2] = {0.f, 0.f};
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    mnew[r] = fmaxf(S.m[r], tmax[r]);
+    alpha[r] = mnew[r] == -INFINITY ? 1.f : exp2f(S.m[r] - mnew[r]);
+    S.m[r] = mnew[r];
+  }
+#pragma unroll
+  for (int n = 0; n < 8; ++n) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float p = mnew[e >> 1] == -INFINITY ? 0.f : exp2f(sacc[n][e] - mnew[e >> 1]);
+      sacc[n][e] = p;
+      psum[e >> 1] += p;
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    psum[r] += __shfl_xor_sync(0xffffffffu, psum[r], 1);
+    psum[r] += __shfl_xor_sync(0xffffffffu, psum[r], 2);
+    S.l[r] = S.l[r] * alpha[r] + psum[r];
+  }
+#pragma unroll
+  for (int n = 0; n < kD / 8; ++n) {
+    S.o[n][0] *= alpha[0];
+    S.o[n][1] *= alpha[0];
+    S.o[n][2] *= alpha[1];
+    S.o[n][3] *= alpha[1];
+  }
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    uint32_t ph[4], pl[4];
+    split_hi_lo(sacc[2 * kk][0], sacc[2 * kk][1], ph[0], pl[0]);
+    split_hi_lo(sacc[2 * kk][2], sacc[2 * kk][3], ph[1], pl[1]);
+    split_hi_lo(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1], ph[2], pl[2]);
+    split_hi_lo(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3], ph[3], pl[3]);
+    const int mi = lane >> 3;
+    const int key = kk * 16 + (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+    for (int n2 = 0; n2 < kD / 16; ++n2) {
+      const int dim = n2 * 16 + (mi >> 1) * 8;
+      const uint32_t sub = t + static_cast<uint32_t>((2 + (dim >> 6)) * kSubBytes);
+      uint32_t vb[4];
+      ldsm_x4_trans(vb, sub + swz(key, (dim & 63) >> 3));
+      mma16816(S.o[2 * n2], ph, vb[0], vb[1]);
+      mma16816(S.o[2 * n2 + 1], ph, vb[2], vb[3]);
+      mma16816(S.o[2 * n2], pl, vb[0], vb[1]);
+      mma16816(S.o[2 * n2 + 1], pl, vb[2], vb[3]);
+    }
+  }
+}
+
+struct ClusterAttnArgs {
+  CUtensorMap kmap;  // cache K: 3-D [S*nkv][cap][128], box {64, 64, 1}
+  CUtensorMap vmap;
+  CUtensorMap kbmap;  // block K: 2-D [T][nkv*128], box {64, 16}
+  CUtensorMap vbmap;
+  AttnArgs a;
+};
+
+template <int G>
+__global__ void __launch_bounds__(32 * (2 * G + 1), 1) attn_cluster_kernel(const __grid_constant__ ClusterAttnArgs P) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const AttnArgs& a = P.a;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + ClusterAttnSmem::kBarOff);
+  uint64_t* empty = full + kStages;
+  uint64_t* blkbar = empty + kStages;
+  const uint32_t sbase = smem_u32(smem);
+
+  const int ncons = 2 * G;  // consumer warps
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = crank();
+  const int kvh = blockIdx.y;
+  const int si = blockIdx.z;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], G);
+    }
+    mbar_init(blkbar, 1);
+    fence_barrier_init();
+  }
+  // zero rows 16..63 of the block tile (only rows 0..15 are loaded)
+  for (int i = threadIdx.x; i < 4 * 48 * 128 / 16; i += blockDim.x) {
+    const int sub = i / (48 * 8), rem = i - sub * 48 * 8;
+    *reinterpret_cast<uint4*>(smem + ClusterAttnSmem::kBlockOff + sub * kSubBytes + 16 * 128 + rem * 16) =
+        make_uint4(0u, 0u, 0u, 0u);
+  }
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();
+
+  const int s = a.s_begin + si;
+  const int C = a.lens[s];
+  const int nvis = a.window > 0 ? min(C, a.window) : C;
+  const int k0 = static_cast<int>(static_cast<long long>(nvis) * rank / kClusterCtas);
+  const int k1 = static_cast<int>(static_cast<long long>(nvis) * (rank + 1) / kClusterCtas);
+  const int nt = (k1 - k0 + kKeys - 1) / kKeys;
+  const bool has_block = rank == kClusterCtas - 1;
+  const int slab = s * a.nkv + kvh;
+  int* err = a.err;
+
+  if (warp == ncons) {
+    if (lane == 0) {
+      if (has_block) {
+        mbar_arrive_expect_tx(blkbar, 4 * 16 * 128);
+        const uint32_t b = sbase + ClusterAttnSmem::kBlockOff;
+        tma2d(b, &P.kbmap, blkbar, kvh * kD, 16 * si);
+        tma2d(b + kSubBytes, &P.kbmap, blkbar, kvh * kD + 64, 16 * si);
+        tma2d(b + 2 * kSubBytes, &P.vbmap, blkbar, kvh * kD, 16 * si);
+        tma2d(b + 3 * kSubBytes, &P.vbmap, blkbar, kvh * kD + 64, 16 * si);
+      }
+      for (int t = 0; t < nt; ++t) {
+        const int st = t % kStages;
+        if (!mbar_wait(&empty[st], ((t / kStages) & 1) ^ 1u, err, DFLASH_STATUS_TIMEOUT, nullptr)) break;
+        mbar_arrive_expect_tx(&full[st], kTileBytes);
+        const uint32_t d = sbase + ClusterAttnSmem::kStageOff + st * kTileBytes;
+        const int row = k0 + t * kKeys;
+        tma3d(d, &P.kmap, &full[st], 0, row, slab);
+        tma3d(d + kSubBytes, &P.kmap, &full[st], 64, row, slab);
+        tma3d(d + 2 * kSubBytes, &P.vmap, &full[st], 0, row, slab);
+        tma3d(d + 3 * kSubBytes, &P.vmap, &full[st], 64, row, slab);
+      }
+      // no copy may still be landing when the stage memory is reused below
+      for (int st = 0; st < kStages && st < nt; ++st) {
+        const int last = st + ((nt - 1 - st) / kStages) * kStages;
+        mbar_wait(&full[st], (last / kStages) & 1, err, DFLASH_STATUS_TIMEOUT, nullptr);
+      }
+      if (has_block) mbar_wait(blkbar, 0, err, DFLASH_STATUS_TIMEOUT, nullptr);
+    }
+  }
+
+  AttnState S;
+  const int hq = warp >> 1;
+  const int par = warp & 1;
+  const bool consumer = warp < ncons;
+  if (consumer) {
+#pragma unroll
+    for (int n = 0; n < kD / 8; ++n) S.o[n][0] = S.o[n][1] = S.o[n][2] = S.o[n][3] = 0.f;
+    S.m[0] = S.m[1] = -INFINITY;
+    S.l[0] = S.l[1] = 0.f;
+    const int h = kvh * G + hq;
+    uint32_t qa[kD / 16][4];
+    {
+      const __nv_bfloat16* Q = a.Q + static_cast<int64_t>(si) * 16 * (a.nq * kD) + static_cast<int64_t>(h) * kD;
+      const int qr = lane >> 2, qc = (lane & 3) * 2, ld = a.nq * kD;
+#pragma unroll
+      for (int kk = 0; kk < kD / 16; ++kk) {
+        qa[kk][0] = *reinterpret_cast<const uint32_t*>(Q + qr * ld + kk * 16 + qc);
+        qa[kk][1] = *reinterpret_cast<const uint32_t*>(Q + (qr + 8) * ld + kk * 16 + qc);
+        qa[kk][2] = *reinterpret_cast<const uint32_t*>(Q + qr * ld + kk * 16 + qc + 8);
+        qa[kk][3] = *reinterpret_cast<const uint32_t*>(Q + (qr + 8) * ld + kk * 16 + qc + 8);
+      }
+    }
+    const float sc = rsqrtf(static_cast<float>(kD)) * 1.4426950408889634f;
+    for (int t = par; t < nt; t += 2) {
+      const int st = t % kStages;
+      if (!mbar_wait(&full[st], (t / kStages) & 1, err, DFLASH_STATUS_TIMEOUT, nullptr)) break;
+      attend_tile(S, qa, sbase + ClusterAttnSmem::kStageOff + st * kTileBytes, min(kKeys, k1 - k0 - t * kKeys), sc,
+                  lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    if (has_block && par == 1) {
+      if (mbar_wait(blkbar, 0, err, DFLASH_STATUS_TIMEOUT, nullptr))
+        attend_tile(S, qa, sbase + ClusterAttnSmem::kBlockOff, 16, sc, lane);
+    }
+  }
+  __syncthreads();  // every tile consumed: the stage memory is free
+
+  // merge the two parities of each head; the CTA partial goes to
+  // part[hq][16][128] (fp32) and ml[hq][16][2], at the start of stage memory
+  float* part = reinterpret_cast<float*>(smem + ClusterAttnSmem::kStageOff);
+  float* ml = part + G * 16 * kD;
+  float* xch = ml + G * 16 * 2;  // odd-parity warps' states, 68 floats a lane
+  if (consumer && par == 1) {
+    float* x = xch + (hq * 32 + lane) * 68;
+#pragma unroll
+    for (int n = 0; n < kD / 8; ++n) {
+      x[4 * n] = S.o[n][0];
+      x[4 * n + 1] = S.o[n][1];
+      x[4 * n + 2] = S.o[n][2];
+      x[4 * n + 3] = S.o[n][3];
+    }
+    x[64] = S.m[0];
+    x[65] = S.m[1];
+    x[66] = S.l[0];
+    x[67] = S.l[1];
+  }
+  __syncthreads();
+  if (consumer && par == 0) {
+    const float* x = xch + (hq * 32 + lane) * 68;
+    float w0[2], w1[2], M[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      M[r] = fmaxf(S.m[r], x[64 + r]);
+      w0[r] = M[r] == -INFINITY ? 0.f : exp2f(S.m[r] - M[r]);
+      w1[r] = M[r] == -INFINITY ? 0.f : exp2f(x[64 + r] - M[r]);
+    }
+    const int r0 = lane >> 2;
+#pragma unroll
+    for (int n = 0; n < kD / 8; ++n) {
+      const int col = n * 8 + (lane & 3) * 2;
+      float* p0 = part + (hq * 16 + r0) * kD + col;
+      float* p1 = part + (hq * 16 + r0 + 8) * kD + col;
+      p0[0] = S.o[n][0] * w0[0] + x[4 * n] * w1[0];
+      p0[1] = S.o[n][1] * w0[0] + x[4 * n + 1] * w1[0];
+      p1[0] = S.o[n][2] * w0[1] + x[4 * n + 2] * w1[1];
+      p1[1] = S.o[n][3] * w0[1] + x[4 * n + 3] * w1[1];
+    }
+    if ((lane & 3) == 0) {
+      ml[(hq * 16 + r0) * 2] = M[0];
+      ml[(hq * 16 + r0) * 2 + 1] = S.l[0] * w0[0] + x[66] * w1[0];
+      ml[(hq * 16 + r0 + 8) * 2] = M[1];
+      ml[(hq * 16 + r0 + 8) * 2 + 1] = S.l[1] * w0[1] + x[67] * w1[1];
+    }
+  }
+  csync();  // every CTA's partial is ready
+
+  // reduce-scatter: this rank owns (head, row) vectors [v0, v1) of the G*16
+  {
+    const int nvec = G * 16;
+    const int v0 = static_cast<int>(rank) * nvec / kClusterCtas;
+    const int v1 = (static_cast<int>(rank) + 1) * nvec / kClusterCtas;
+    const uint32_t pbase = smem_u32(part), mlbase = smem_u32(ml);
+    for (int idx = threadIdx.x; idx < (v1 - v0) * 32; idx += blockDim.x) {
+      const int vec = v0 + idx / 32;
+      const int d4 = (idx & 31) * 4;
+      float M = -INFINITY;
+#pragma unroll
+      for (int r2 = 0; r2 < kClusterCtas; ++r2) M = fmaxf(M, cld(cmap(mlbase, r2) + vec * 8));
+      float den = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int r2 = 0; r2 < kClusterCtas; ++r2) {
+        const float m = cld(cmap(mlbase, r2) + vec * 8);
+        const float w = M == -INFINITY ? 0.f : exp2f(m - M);
+        den += w * cld(cmap(mlbase, r2) + vec * 8 + 4);
+        const float4 v = cld4(cmap(pbase, r2) + (vec * kD + d4) * 4);
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
+      }
+      const int hq2 = vec >> 4, row = vec & 15;
+      __nv_bfloat16* out =
+          a.out + (static_cast<int64_t>(si) * 16 + row) * (a.nq * kD) + (kvh * G + hq2) * kD + d4;
+      const float inv = 1.f / den;
+      *reinterpret_cast<__nv_bfloat162*>(out) = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      *reinterpret_cast<__nv_bfloat162*>(out + 2) = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    }
+  }
+  csync();  // partials stay alive until every rank has read them
+}
+
+int encode_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+               const cuuint32_t* box) {
+  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return DFLASH_E_UNSUPPORTED;
+    fn = reinterpret_cast<EncodeFn>(p);
+  }
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_E_CUDA;
+}
+
+}  // namespace
+
+bool attention_cluster_supported(const AttnArgs& a) {
+  const int G = a.nq / a.nkv;
+  return a.d == kD && (G == 1 || G == 2 || G == 4 || G == 5 || G == 8);
+}
+
+int attention_cluster_maps(CUtensorMap* kmap, CUtensorMap* vmap, const void* kc, const void* vc, int slabs, int cap) {
+  const cuuint64_t dims[3] = {kD, static_cast<cuuint64_t>(cap), static_cast<cuuint64_t>(slabs)};
+  const cuuint64_t strides[2] = {kD * 2, static_cast<cuuint64_t>(cap) * kD * 2};
+  const cuuint32_t box[3] = {64, kKeys, 1};
+  int rc = encode_map(kmap, kc, 3, dims, strides, box);
+  if (!rc) rc = encode_map(vmap, vc, 3, dims, strides, box);
+  return rc;
+}
+
+int launch_attention_cluster(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap, int s_count,
+                             cudaStream_t st) {
+  static thread_local ClusterAttnArgs P;
+  P.a = a;
+  P.kmap = kmap;
+  P.vmap = vmap;
+  const int T = s_count * 16;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.nkv) * kD, static_cast<cuuint64_t>(T)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.nkv) * kD * 2};
+  const cuuint32_t box[2] = {64, 16};
+  int rc = encode_map(&P.kbmap, a.Kb, 2, dims, strides, box);
+  if (!rc) rc = encode_map(&P.vbmap, a.Vb, 2, dims, strides, box);
+  if (rc) return rc;
+  const int G = a.nq / a.nkv;
+  const int threads = 32 * (2 * G + 1);
+  const int smem = ClusterAttnSmem::kBytes + 1024;
+  void (*kern)(ClusterAttnArgs) = nullptr;
+  switch (G) {
+    case 1: kern = attn_cluster_kernel<1>; break;
+    case 2: kern = attn_cluster_kernel<2>; break;
+    case 4: kern = attn_cluster_kernel<4>; break;
+    case 5: kern = attn_cluster_kernel<5>; break;
+    case 8: kern = attn_cluster_kernel<8>; break;
+    default: return DFLASH_E_SHAPE;
+  }
+  static bool configured[9] = {};
+  if (!configured[G]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return DFLASH_E_CUDA;
+    configured[G] = true;
+  }
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kClusterCtas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(kClusterCtas, a.nkv, s_count);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  TraceScope ts(st, "attention", a.trace_bytes, 0.0);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, P);
+  count_launch();
+  return cuda_status(e);
+}
+
+}  // namespace dfl

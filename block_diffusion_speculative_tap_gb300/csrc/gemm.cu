@@ -50,15 +50,48 @@ struct GemmTraits {
   static constexpr int kSmemBytes =
       1024 /*alignment slack*/ + STAGES * kStageBytes + kBarBytes + 4 * (kXchFloats + kRedFloats) + 64;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, BN);
+  // cluster split-K parks each CTA's fp32 partial in its (idle) stage memory
+  static constexpr bool kClusterFits = kAcc * BN * kTileM * 4 <= STAGES * kStageBytes;
 };
+
+// ---------------------------------------------------------------- cluster helpers
+__device__ __forceinline__ uint32_t gemm_cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void gemm_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t gemm_mapa(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float gemm_ld_dsmem(uint32_t a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
+// Work-unit order. Global split-K: ((m_tile * ksplit + kc) * n_tiles + n_tile),
+// so concurrent CTAs share weight slabs across n-tiles. Cluster split-K:
+// (tile * ksplit + kc), the chunks of a tile being one cluster.
+template <bool CLU>
 __device__ __forceinline__ void decode_unit(const GemmArgs& a, int u, int& m_tile, int& kc, int& n_tile) {
-  n_tile = u % a.n_tiles;
-  const int r = u / a.n_tiles;
-  kc = r % a.ksplit;
-  m_tile = r / a.ksplit;
+  if constexpr (CLU) {
+    kc = u % a.ksplit;
+    const int tile = u / a.ksplit;
+    m_tile = tile / a.n_tiles;
+    n_tile = tile - m_tile * a.n_tiles;
+  } else {
+    n_tile = u % a.n_tiles;
+    const int r = u / a.n_tiles;
+    kc = r % a.ksplit;
+    m_tile = r / a.ksplit;
+  }
 }
 
 __device__ __forceinline__ int seg_of_tile(const GemmArgs& a, int m_tile) {
@@ -72,13 +105,14 @@ __device__ __forceinline__ int seg_of_tile(const GemmArgs& a, int m_tile) {
 // m = m_tile*128 + row for tokens t = n0 + j, j = 0..15.
 template <int EPI>
 __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0, int row, int q, int lane,
-                                          const float (&v0)[16], const float (&v1)[16], float* xch, float* red) {
+                                          const float (&v0)[16], const float (&v1)[16], float* xch, float* red,
+                                          int nvalid = 16) {
   const int m = m_tile * kTileM + row;
   if constexpr (EPI == EPI_STORE_F32 || EPI == EPI_STORE_BF16 || EPI == EPI_RESID || EPI == EPI_SWIGLU) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int t = n0 + j;
-      if (t >= a.N) break;
+      if (j >= nvalid || t >= a.N) break;
       const int64_t o = static_cast<int64_t>(t) * a.epi.ldo + m;
       if constexpr (EPI == EPI_STORE_F32) {
         static_cast<float*>(a.epi.out)[o] = v0[j];
@@ -107,7 +141,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
       const int t = n0 + j;
       pos[j] = 0;
       strm[j] = 0;
-      if (t < a.N) {
+      if (j < nvalid && t < a.N) {
         if (a.epi.pos_mode == 0) {
           strm[j] = a.epi.s_begin + t / 16;
           pos[j] = a.epi.lens[strm[j]] + (t & 15);
@@ -165,7 +199,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int t = n0 + j;
-      if (t >= a.N) break;
+      if (j >= nvalid || t >= a.N) break;
       int64_t o;
       if (a.epi.pos_mode == 0) {
         o = static_cast<int64_t>(t) * (sg.heads * d) + f;
@@ -181,7 +215,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
 }
 
 // ---------------------------------------------------------------- kernel
-template <int BN, bool DUAL, int STAGES, int EPI, int MINB>
+template <int BN, bool DUAL, int STAGES, int EPI, int MINB, bool CLU>
 __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_constant__ GemmArgs args) {
   using Tr = GemmTraits<BN, DUAL, STAGES, EPI>;
   extern __shared__ uint8_t smem_raw[];
@@ -200,6 +234,7 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  int clu_tile = -1;  // cluster split-K: this CTA's unit, once its partial is parked
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -238,7 +273,7 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
       bool first = true;
       for (int u = blockIdx.x; u < args.units && ok; u += gridDim.x) {
         int m_tile, kc, n_tile;
-        decode_unit(args, u, m_tile, kc, n_tile);
+        decode_unit<CLU>(args, u, m_tile, kc, n_tile);
         const int kb0 = static_cast<int>(static_cast<long long>(kc) * args.kb_total / args.ksplit);
         const int kb1 = static_cast<int>(static_cast<long long>(kc + 1) * args.kb_total / args.ksplit);
         const int sidx = seg_of_tile(args, m_tile);
@@ -307,7 +342,7 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
       bool any = false;
       for (int u = blockIdx.x; u < args.units && ok; u += gridDim.x) {
         int m_tile, kc, n_tile;
-        decode_unit(args, u, m_tile, kc, n_tile);
+        decode_unit<CLU>(args, u, m_tile, kc, n_tile);
         const int kb0 = static_cast<int>(static_cast<long long>(kc) * args.kb_total / args.ksplit);
         const int kb1 = static_cast<int>(static_cast<long long>(kc + 1) * args.kb_total / args.ksplit);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, args.err, DFLASH_STATUS_TIMEOUT, abort_word)) break;
@@ -359,14 +394,30 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
     pdl_wait();  // the epilogue reads and writes buffers of earlier kernels
     for (int u = blockIdx.x; u < args.units; u += gridDim.x) {
       int m_tile, kc, n_tile;
-      decode_unit(args, u, m_tile, kc, n_tile);
+      decode_unit<CLU>(args, u, m_tile, kc, n_tile);
       const bool ok = mbar_wait(&tfull[acc], acc_phase, args.err, DFLASH_STATUS_TIMEOUT, abort_word);
       // the four epilogue warps leave together, so none is left at a named barrier
       if (named_bar_or(1, 128, ok ? 0 : 1)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * Tr::kAccCols);
       float v0[16], v1[16];
-      if (args.ksplit == 1) {
+      if constexpr (CLU) {
+        // park this chunk's fp32 partial in the idle stage memory, [acc][col][row]
+        float* part = reinterpret_cast<float*>(tiles);
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          tmem_ld16(tbase + c0, v0);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) part[(c0 + j) * kTileM + row] = v0[j];
+          if constexpr (DUAL) {
+            tmem_ld16(tbase + BN + c0, v1);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) part[(BN + c0 + j) * kTileM + row] = v1[j];
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+        clu_tile = u;  // reduced after the cluster barrier below
+      } else if (args.ksplit == 1) {
         for (int c0 = 0; c0 < BN; c0 += 16) {
           tmem_ld16(tbase + c0, v0);
           if constexpr (DUAL) tmem_ld16(tbase + BN + c0, v1);
@@ -424,6 +475,47 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
     }
   }
 
+  if constexpr (CLU) {
+    // every chunk's partial is parked: rank r reduces columns
+    // [r*BN/ks, (r+1)*BN/ks) over the cluster, in rank order, and runs the
+    // epilogue on them; the second barrier keeps the partials alive until
+    // every rank has read them
+    __syncwarp();
+    gemm_cluster_sync();
+    if (warp >= 2 && named_bar_or(1, 128, clu_tile < 0 ? 1 : 0) == 0) {
+      int m_tile, kc, n_tile;
+      decode_unit<CLU>(args, clu_tile, m_tile, kc, n_tile);
+      const int q = warp & 3;
+      const int row = q * 32 + lane;
+      const int ks = args.ksplit;
+      const int rk = static_cast<int>(gemm_cluster_rank());
+      const int cb = rk * BN / ks, ce = (rk + 1) * BN / ks;
+      const uint32_t pbase = smem_u32(tiles);
+      float v0[16], v1[16];
+      for (int c0 = cb; c0 < ce; c0 += 16) {
+        const int nv = ce - c0 < 16 ? ce - c0 : 16;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          v0[j] = 0.f;
+          v1[j] = 0.f;
+        }
+        for (int r2 = 0; r2 < ks; ++r2) {
+          const uint32_t rb = gemm_mapa(pbase, static_cast<uint32_t>(r2));
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (j < nv) {
+              v0[j] += gemm_ld_dsmem(rb + static_cast<uint32_t>(((c0 + j) * kTileM + row) * 4));
+              if constexpr (DUAL) v1[j] += gemm_ld_dsmem(rb + static_cast<uint32_t>(((BN + c0 + j) * kTileM + row) * 4));
+            }
+          }
+        }
+        epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red, nv);
+      }
+    }
+    __syncwarp();
+    gemm_cluster_sync();
+  }
+
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -452,39 +544,68 @@ EncodeFn get_encode() {
   return fn;
 }
 
-template <int BN, bool DUAL, int STAGES, int EPI, int MINB>
+template <int BN, bool DUAL, int STAGES, int EPI, int MINB, bool CLU>
 int launch_inst(const GemmArgs& a, int num_sms, cudaStream_t st) {
   using Tr = GemmTraits<BN, DUAL, STAGES, EPI>;
-  auto kern = gemm_kernel<BN, DUAL, STAGES, EPI, MINB>;
+  auto kern = gemm_kernel<BN, DUAL, STAGES, EPI, MINB, CLU>;
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kSmemBytes) != cudaSuccess)
       return DFLASH_E_CUDA;
     configured = true;
   }
-  const int grid = std::max(1, std::min(a.units, num_sms * MINB));
-  const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kGemmThreads), Tr::kSmemBytes, st, a);
+  cudaError_t e;
+  if constexpr (CLU) {
+    // one unit per CTA, the ksplit chunks of a tile form one cluster
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(a.ksplit);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(a.units);
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = Tr::kSmemBytes;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, kern, a);
+  } else {
+    const int grid = std::max(1, std::min(a.units, num_sms * MINB));
+    e = launch_pdl(kern, dim3(grid), dim3(kGemmThreads), Tr::kSmemBytes, st, a);
+  }
   count_launch();
   return cuda_status(e);
+}
+
+template <int BN, bool DUAL, int STAGES, int MINB, int EPI>
+int launch_mode(const GemmArgs& a, int num_sms, cudaStream_t st) {
+  using Tr = GemmTraits<BN, DUAL, STAGES, EPI>;
+  if (a.ksplit > 1 && a.ksplit <= kMaxClusterSplit) {
+    if constexpr (Tr::kClusterFits) return launch_inst<BN, DUAL, STAGES, EPI, MINB, true>(a, num_sms, st);
+  }
+  return launch_inst<BN, DUAL, STAGES, EPI, MINB, false>(a, num_sms, st);
 }
 
 template <int BN, bool DUAL, int STAGES, int MINB>
 int launch_epi(const GemmArgs& a, int epi, int num_sms, cudaStream_t st) {
   switch (epi) {
     case EPI_STORE_F32:
-      if constexpr (!DUAL) return launch_inst<BN, DUAL, STAGES, EPI_STORE_F32, MINB>(a, num_sms, st);
+      if constexpr (!DUAL) return launch_mode<BN, DUAL, STAGES, MINB, EPI_STORE_F32>(a, num_sms, st);
       break;
     case EPI_STORE_BF16:
-      if constexpr (!DUAL) return launch_inst<BN, DUAL, STAGES, EPI_STORE_BF16, MINB>(a, num_sms, st);
+      if constexpr (!DUAL) return launch_mode<BN, DUAL, STAGES, MINB, EPI_STORE_BF16>(a, num_sms, st);
       break;
     case EPI_RESID:
-      if constexpr (!DUAL) return launch_inst<BN, DUAL, STAGES, EPI_RESID, MINB>(a, num_sms, st);
+      if constexpr (!DUAL) return launch_mode<BN, DUAL, STAGES, MINB, EPI_RESID>(a, num_sms, st);
       break;
     case EPI_HEADS:
-      if constexpr (!DUAL) return launch_inst<BN, DUAL, STAGES, EPI_HEADS, MINB>(a, num_sms, st);
+      if constexpr (!DUAL) return launch_mode<BN, DUAL, STAGES, MINB, EPI_HEADS>(a, num_sms, st);
       break;
     case EPI_SWIGLU:
-      if constexpr (DUAL) return launch_inst<BN, DUAL, STAGES, EPI_SWIGLU, MINB>(a, num_sms, st);
+      if constexpr (DUAL) return launch_mode<BN, DUAL, STAGES, MINB, EPI_SWIGLU>(a, num_sms, st);
       break;
     default:
       break;
@@ -518,9 +639,10 @@ int gemm_bn_for(int N) {
 int gemm_choose_ksplit(int m_tiles, int kb_total, int num_sms) {
   // Fill the 2-CTA-per-SM batch-1 configuration as evenly as possible: the
   // smallest split whose wave efficiency is within 5% of the best one, with
-  // at least 4 reduction blocks per chunk and at most 16 chunks.
+  // at least 4 reduction blocks per chunk and at most kMaxClusterSplit chunks
+  // (the chunks of a tile run as one portable-size cluster).
   const int slots = 2 * num_sms;
-  const int kmax = std::max(1, std::min(16, kb_total / 4));
+  const int kmax = std::max(1, std::min(kMaxClusterSplit, kb_total / 4));
   double eff[17] = {0.0};
   double best = 0.0;
   for (int ks = 1; ks <= kmax; ++ks) {

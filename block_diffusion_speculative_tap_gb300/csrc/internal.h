@@ -16,6 +16,7 @@ constexpr int kMaxBPlane = 8;  // tap planes stacked along the reduction
 constexpr int kTileM = 128;    // output features per tile (TMEM lanes)
 constexpr int kTileK = 64;     // reduction per pipeline stage (one 128-byte swizzle row)
 constexpr int kGemmThreads = 192;
+constexpr int kMaxClusterSplit = 8;  // split-K chunks of a tile = one portable cluster
 
 enum EpiKind { EPI_STORE_F32 = 0, EPI_STORE_BF16 = 1, EPI_RESID = 2, EPI_SWIGLU = 3, EPI_HEADS = 4 };
 enum HeadKind { HEAD_Q = 0, HEAD_K = 1, HEAD_V = 2 };
@@ -124,8 +125,15 @@ struct AttnArgs {
   float* part_ml;           // [s][nq][nchunk][16][2]
   __nv_bfloat16* out;       // [T, nq*d]
   double trace_bytes;       // algorithmic K/V + Q + O bytes (host estimate, for the trace)
+  int* err;                 // device status word (bounded waits)
 };
 int launch_attention(const AttnArgs& a, int s_count, cudaStream_t st);
+// Cluster variant for head dimension 128 (attention_cluster.cu): TMA-fed,
+// reduce-scatter over distributed shared memory, no partials in global memory.
+bool attention_cluster_supported(const AttnArgs& a);
+int attention_cluster_maps(CUtensorMap* kmap, CUtensorMap* vmap, const void* kc, const void* vc, int slabs, int cap);
+int launch_attention_cluster(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap, int s_count,
+                             cudaStream_t st);
 size_t attn_partial_floats(int s_count, int nq, int nchunk, int d);
 
 // ---------------------------------------------------------------- selection (select.cu)

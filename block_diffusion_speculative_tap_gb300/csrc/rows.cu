@@ -47,24 +47,58 @@ __global__ void embed_kernel(float* __restrict__ X, const __nv_bfloat16* __restr
   for (int i = threadIdx.x; i < H; i += blockDim.x) x[i] = __bfloat162float(e[i]);
 }
 
-// out[r] = bf16(x[src] / sqrt(mean(x[src]^2) + eps) * g)
-__global__ void rmsnorm_rows_kernel(__nv_bfloat16* __restrict__ out, const float* __restrict__ x,
-                                    const __nv_bfloat16* __restrict__ g, int H, float eps, int mask_rows_only) {
+// out[r] = bf16(x[src] / sqrt(mean(x[src]^2) + eps) * g). The row is held in
+// registers (up to kNormVec float4 per thread), all loads issued up front,
+// so a row costs one memory round trip. Rows wider than
+// kNormVec * 4 * blockDim fall back to a strided second pass.
+constexpr int kNormThreads = 512;
+constexpr int kNormVec = 4;
+
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_rows_kernel(__nv_bfloat16* __restrict__ out,
+                                                                    const float* __restrict__ x,
+                                                                    const __nv_bfloat16* __restrict__ g, int H,
+                                                                    float eps, int mask_rows_only) {
   __shared__ float red[32];
   pdl_trigger();
   pdl_wait();
   const int r = blockIdx.x;
   const int src = mask_rows_only ? (r / 15) * 16 + 1 + (r % 15) : r;
-  const float* xr = x + static_cast<int64_t>(src) * H;
+  const float4* xr = reinterpret_cast<const float4*>(x + static_cast<int64_t>(src) * H);
+  const int nv = H >> 2;
+  float4 v[kNormVec];
   float ss = 0.f;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) {
-    const float v = xr[i];
-    ss += v * v;
+#pragma unroll
+  for (int i = 0; i < kNormVec; ++i) {
+    const int j = threadIdx.x + i * kNormThreads;
+    v[i] = j < nv ? xr[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int i = 0; i < kNormVec; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+  for (int j = threadIdx.x + kNormVec * kNormThreads; j < nv; j += kNormThreads) {
+    const float4 t = xr[j];
+    ss += t.x * t.x + t.y * t.y + t.z * t.z + t.w * t.w;
   }
   const float tot = block_sum(ss, red);
   const float rstd = rsqrtf(tot / static_cast<float>(H) + eps);
-  __nv_bfloat16* o = out + static_cast<int64_t>(r) * H;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) o[i] = __float2bfloat16_rn(xr[i] * rstd * __bfloat162float(g[i]));
+  __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(out + static_cast<int64_t>(r) * H);
+  const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(g);
+#pragma unroll
+  for (int i = 0; i < kNormVec; ++i) {
+    const int j = threadIdx.x + i * kNormThreads;
+    if (j < nv) {
+      const float2 ga = __bfloat1622float2(g2[2 * j]);
+      const float2 gb = __bfloat1622float2(g2[2 * j + 1]);
+      o[2 * j] = __floats2bfloat162_rn(v[i].x * rstd * ga.x, v[i].y * rstd * ga.y);
+      o[2 * j + 1] = __floats2bfloat162_rn(v[i].z * rstd * gb.x, v[i].w * rstd * gb.y);
+    }
+  }
+  for (int j = threadIdx.x + kNormVec * kNormThreads; j < nv; j += kNormThreads) {
+    const float4 t = xr[j];
+    const float2 ga = __bfloat1622float2(g2[2 * j]);
+    const float2 gb = __bfloat1622float2(g2[2 * j + 1]);
+    o[2 * j] = __floats2bfloat162_rn(t.x * rstd * ga.x, t.y * rstd * ga.y);
+    o[2 * j + 1] = __floats2bfloat162_rn(t.z * rstd * gb.x, t.w * rstd * gb.y);
+  }
 }
 
 // fused = bf16(RMSNorm(y) * hidden_norm): written to the ring slot of the
@@ -136,7 +170,7 @@ int launch_rmsnorm_rows(__nv_bfloat16* out, const float* x, const __nv_bfloat16*
                         int mask_rows_only, cudaStream_t st) {
   TraceScope ts(st, "rmsnorm", static_cast<double>(rows) * H * 6, 0.0);
   const cudaError_t e =
-      launch_pdl(rmsnorm_rows_kernel, dim3(rows), dim3(kRowThreads), 0, st, out, x, g, H, eps, mask_rows_only);
+      launch_pdl(rmsnorm_rows_kernel, dim3(rows), dim3(kNormThreads), 0, st, out, x, g, H, eps, mask_rows_only);
   count_launch();
   return cuda_status(e);
 }

@@ -115,15 +115,20 @@ __device__ __forceinline__ void block_best(float v, int i, float* sv, int* si, f
   __syncthreads();
 }
 
-// Top-k (k <= KM) of a row into (ids, vals); also returns the row maximum.
+// Top-k (k <= KM) of the 8-element groups [g_begin, g_end) of a row into
+// (ids, vals) (thread 0 writes them); also returns the range maximum. The
+// 16 warps split the range into contiguous pieces, lanes interleave inside.
 template <int KM>
-__device__ float row_topk(const __nv_bfloat16* row, int V, int k, int* ids, float* vals, float* sv, int* si) {
+__device__ float range_topk(const __nv_bfloat16* row, int g_begin, int g_end, int k, int* ids, float* vals,
+                            float* sv, int* si) {
   const int w = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const Slice sl = warp_slice(V, w);
+  const int ng = g_end - g_begin;
+  const int wg0 = g_begin + static_cast<int>(static_cast<long long>(ng) * w / kSelWarps);
+  const int wg1 = g_begin + static_cast<int>(static_cast<long long>(ng) * (w + 1) / kSelWarps);
   TopList<KM> tl;
   tl.init();
-  for (int g = sl.g0 + lane; g < sl.g1; g += 32) {
+  for (int g = wg0 + lane; g < wg1; g += 32) {
     float x[8];
     load8(row, g, x);
 #pragma unroll
@@ -143,6 +148,121 @@ __device__ float row_topk(const __nv_bfloat16* row, int V, int k, int* ids, floa
     }
   }
   return mx;
+}
+
+template <int KM>
+__device__ float row_topk(const __nv_bfloat16* row, int V, int k, int* ids, float* vals, float* sv, int* si) {
+  return range_topk<KM>(row, 0, V >> 3, k, ids, vals, sv, si);
+}
+
+// ---------------------------------------------------------------- cluster top-k
+// A row split over a cluster of kSlices CTAs: each CTA ranks its slice, rank
+// 0 merges the kSlices sorted lists read through distributed shared memory.
+constexpr int kSlices = 8;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float dsmem_ld_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int dsmem_ld_s32(uint32_t a) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+
+template <int KM>
+__global__ void __launch_bounds__(kSelThreads) topk_cluster_kernel(const __nv_bfloat16* __restrict__ logits, int V,
+                                                                   int k, int* __restrict__ ids,
+                                                                   float* __restrict__ vals) {
+  __shared__ float sv[kSelWarps];
+  __shared__ int si[kSelWarps];
+  __shared__ int cid[kKMax];
+  __shared__ float cval[kKMax];
+  pdl_trigger();
+  pdl_wait();
+  const int row = blockIdx.y;
+  const uint32_t rank = cluster_rank();
+  const int ng = V >> 3;
+  const int g0 = static_cast<int>(static_cast<long long>(ng) * rank / kSlices);
+  const int g1 = static_cast<int>(static_cast<long long>(ng) * (rank + 1) / kSlices);
+  range_topk<KM>(logits + static_cast<int64_t>(row) * V, g0, g1, k, cid, cval, sv, si);
+  __syncthreads();
+  cluster_sync_all();
+  if (rank == 0) {
+    // gather every slice's sorted list with one parallel round of DSMEM loads
+    __shared__ float gv[kSlices * kKMax];
+    __shared__ int gi[kSlices * kKMax];
+    const int t = threadIdx.x;
+    if (t < kSlices * k) {
+      const int c = t / k, j = t - c * k;
+      gv[c * kKMax + j] = dsmem_ld_f32(dsmem_addr(cval + j, c));
+      gi[c * kKMax + j] = dsmem_ld_s32(dsmem_addr(cid + j, c));
+    }
+    __syncthreads();
+    if (t == 0) {
+      int pos[kSlices];
+#pragma unroll
+      for (int c = 0; c < kSlices; ++c) pos[c] = 0;
+      for (int r = 0; r < k; ++r) {
+        int b = -1;
+        float bv = -INFINITY;
+        int bi = INT_MAX;
+#pragma unroll
+        for (int c = 0; c < kSlices; ++c) {
+          if (pos[c] >= k) continue;
+          const float v = gv[c * kKMax + pos[c]];
+          const int i = gi[c * kKMax + pos[c]];
+          if (b < 0 || better(v, i, bv, bi)) {
+            b = c;
+            bv = v;
+            bi = i;
+          }
+        }
+        ids[static_cast<int64_t>(row) * k + r] = bi;
+        if (vals) vals[static_cast<int64_t>(row) * k + r] = bv;
+        ++pos[b];
+      }
+    }
+  }
+  cluster_sync_all();  // every slice's shared memory stays alive until rank 0 has read it
+}
+
+template <int KM>
+cudaError_t launch_topk_cluster(const __nv_bfloat16* logits, int rows, int V, int k, int* ids, float* vals,
+                                cudaStream_t st) {
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kSlices;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(kSlices, rows);
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<KM>, logits, V, k, ids, vals);
 }
 
 // Weight of id j for inverse-CDF draws; `mode` 0: exp((x - mx) / T) of one
@@ -317,20 +437,8 @@ __global__ void __launch_bounds__(kSelThreads) topk_kernel(const __nv_bfloat16* 
   }
 }
 
-// greedy, step 1: t_i = argmax of every target row -> out[s][i]
-__global__ void __launch_bounds__(kSelThreads) argmax_kernel(const __nv_bfloat16* __restrict__ tl, int V,
-                                                             int* __restrict__ out) {
-  pdl_trigger();
-  pdl_wait();
-  __shared__ float sv[kSelWarps];
-  __shared__ int si[kSelWarps];
-  __shared__ int sid[1];
-  __shared__ float sval[1];
-  const int r = blockIdx.x;
-  row_topk<1>(tl + static_cast<int64_t>(r) * V, V, 1, sid, sval, sv, si);
-  __syncthreads();
-  if (threadIdx.x == 0) out[r] = sid[0];
-}
+// greedy, step 1 (t_i = argmax of every target row -> out[s][i]) is the
+// cluster top-k with k = 1.
 
 // greedy, step 2: longest prefix of drafts equal to the target argmax, then
 // the bonus token; rewrites out[s][*] in place.
@@ -446,8 +554,14 @@ int launch_topk(const __nv_bfloat16* logits, int rows, int V, int k, float T, co
                 float* vals, int* sampled, cudaStream_t st) {
   if (rows <= 0) return DFLASH_OK;
   TraceScope ts(st, "topk", static_cast<double>(rows) * V * 2, 0.0);
-  const cudaError_t e = launch_pdl(topk_kernel, dim3(rows), dim3(kSelThreads), 0, st, logits, V, k, 1.0f / T, uniforms,
-                                   ids, vals, sampled);
+  cudaError_t e;
+  if (uniforms == nullptr && k >= 1) {
+    e = k <= 8 ? launch_topk_cluster<8>(logits, rows, V, k, ids, vals, st)
+               : launch_topk_cluster<kKMax>(logits, rows, V, k, ids, vals, st);
+  } else {
+    e = launch_pdl(topk_kernel, dim3(rows), dim3(kSelThreads), 0, st, logits, V, k, 1.0f / T, uniforms, ids, vals,
+                   sampled);
+  }
   count_launch();
   return cuda_status(e);
 }
@@ -456,7 +570,7 @@ int launch_verify_greedy(int S, int V, const int* draft, int dld, const __nv_bfl
                          cudaStream_t st) {
   {
     TraceScope ts(st, "verify.argmax", static_cast<double>(S) * 16 * V * 2, 0.0);
-    const cudaError_t e = launch_pdl(argmax_kernel, dim3(S * 16), dim3(kSelThreads), 0, st, tl, V, out);
+    const cudaError_t e = launch_topk_cluster<1>(tl, S * 16, V, 1, out, nullptr, st);
     count_launch();
     if (e != cudaSuccess) return DFLASH_E_CUDA;
   }

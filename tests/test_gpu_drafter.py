@@ -9,7 +9,16 @@ import torch
 
 import oracle as O
 import synthetic_inputs as SI
-from parity_util import ATOL, RTOL, assert_close, check_topk_consistent, f64, topk_ids_match
+from parity_util import (
+    ATOL,
+    RTOL,
+    assert_close,
+    check_topk_consistent,
+    compare_draft,
+    f64,
+    staged_parity,
+    topk_ids_match,
+)
 
 pytestmark = pytest.mark.gpu
 
@@ -45,6 +54,10 @@ def check_state_vs_oracle(st, ref, m, s, upto):
 
 
 def draft_vs_oracle(D, st, ref, m, anchors, k):
+    """Draft every stream and compare with the oracle: element-wise within
+    the tolerance for drafters of at most two layers; deeper drafters stage
+    by stage (within the tolerance) and end to end on the mean (see
+    parity_util)."""
     S = anchors.numel()
     logits, ids, vals = st.draft(anchors.cuda(), k=k)
     torch.cuda.synchronize()
@@ -52,15 +65,25 @@ def draft_vs_oracle(D, st, ref, m, anchors, k):
     assert rc == 0 and bits == 0, (rc, bits)
     check_topk_consistent(logits, ids, vals)
     lg = logits.cpu().float().numpy().reshape(S, 15, -1)
-    ids = ids.cpu().numpy().reshape(S, 15, k)
+    idn = ids.cpu().numpy().reshape(S, 15, k)
     stats = []
     for s in range(S):
         ol, _ = ref.draft(s, int(anchors[s]))
-        stats.append(assert_close(lg[s], ol, f"logits stream {s}"))
-        print(f"logits stream {s}: {stats[-1]}")
-        checked, near, bad = topk_ids_match(ids[s], ol, k, margin=2 * (ATOL + RTOL * np.abs(ol).max()))
-        assert bad == 0, (s, checked, near, bad)
+        if m["n_layers"] <= 2:
+            stats.append(assert_close(lg[s], ol, f"logits stream {s}"))
+            print(f"logits stream {s}: {stats[-1]}")
+            checked, near, bad = topk_ids_match(idn[s], ol, k, margin=2 * (ATOL + RTOL * np.abs(ol).max()))
+            assert bad == 0, (s, checked, near, bad)
+        else:
+            stats.append(compare_draft(lg[s], idn[s], ol, k))
     return logits, stats
+
+
+def staged_vs_oracle(st, ref, m, anchors, k):
+    """Stage-isolated parity of every stream (overwrites the GPU caches with
+    the oracle's K/V, so run it after the end-to-end checks)."""
+    for s in range(anchors.numel()):
+        staged_parity(st, ref, s, m, s, int(anchors[s]), k)
 
 
 def test_tiny_preset_fill_append_draft(D):
@@ -105,6 +128,7 @@ def test_small_multistream_sliding_splitk(D):
     # concurrent == solo: a stream drafted alone gives bit-identical logits
     solo, _, _ = st.draft(anchors[1:2].cuda(), s_begin=1, k=8)
     assert torch.equal(solo, batch_logits[15:30])
+    staged_vs_oracle(st, ref, m, anchors, 8)
 
 
 def test_truncate_and_reappend(D):
@@ -129,6 +153,8 @@ def test_truncate_and_reappend(D):
     st.fuse_taps([t[250:] for t in taps], [(0, 250, 50)])
     again, _, _ = st.draft(anchors.cuda(), k=8)
     assert_close(again.cpu().float().numpy(), fresh.cpu().float().numpy(), "resumed vs fresh", atol=0, rtol=0)
+    ref.append(0, [f64(t[250:]) for t in taps])
+    staged_vs_oracle(st, ref, m, anchors, 8)
 
 
 def test_capacity_and_append_rules(D):
