@@ -3,10 +3,13 @@
 //
 // The visible context keys of a (stream, kv head) are split evenly over the
 // kClusterCtas CTAs of a cluster; the last CTA also takes the block's own 16
-// rows. Inside a CTA one producer thread streams 64-key tiles of K and V from
-// the head-major cache with TMA (3-D tensor maps, 128-byte swizzle) through
-// a ring of kStages shared-memory stages; 2G consumer warps (G = query heads
-// per kv head, two key-tile parities each) compute scores and P*V on the
+// rows. When the query heads of a kv head are an even number, two clusters
+// share the kv head, each taking half of its query heads (K/V tiles are read
+// by both, the second read mostly from L2), so twice as many SMs stream.
+// Inside a CTA one producer thread streams 64-key tiles of K and V from the
+// head-major cache with TMA (3-D tensor maps, 128-byte swizzle) through a
+// ring of kStages shared-memory stages; 2G consumer warps (G = query heads
+// of the CTA, two key-tile parities each) compute scores and P*V on the
 // tensor cores (mma.sync m16n8k16, P as a bf16 hi + lo pair) with an online
 // softmax. The two parities of a head merge in shared memory, then the CTAs
 // of the cluster reduce-scatter their partial (max, sum, output) through
@@ -206,7 +209,9 @@ struct ClusterAttnArgs {
   AttnArgs a;
 };
 
-template <int G>
+// G: query heads handled by this CTA (of the kv head's group); HS: CTAs
+// (clusters) sharing a kv head.
+template <int G, int HS>
 __global__ void __launch_bounds__(32 * (2 * G + 1), 1) attn_cluster_kernel(const __grid_constant__ ClusterAttnArgs P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -220,7 +225,9 @@ __global__ void __launch_bounds__(32 * (2 * G + 1), 1) attn_cluster_kernel(const
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = crank();
-  const int kvh = blockIdx.y;
+  const int kvh = blockIdx.y / HS;
+  const int hs = blockIdx.y - kvh * HS;
+  const int head0 = kvh * (G * HS) + hs * G;  // first query head of this CTA
   const int si = blockIdx.z;
 
   if (threadIdx.x == 0) {
@@ -290,7 +297,7 @@ __global__ void __launch_bounds__(32 * (2 * G + 1), 1) attn_cluster_kernel(const
     for (int n = 0; n < kD / 8; ++n) S.o[n][0] = S.o[n][1] = S.o[n][2] = S.o[n][3] = 0.f;
     S.m[0] = S.m[1] = -INFINITY;
     S.l[0] = S.l[1] = 0.f;
-    const int h = kvh * G + hq;
+    const int h = head0 + hq;
     uint32_t qa[kD / 16][4];
     {
       const __nv_bfloat16* Q = a.Q + static_cast<int64_t>(si) * 16 * (a.nq * kD) + static_cast<int64_t>(h) * kD;
@@ -395,7 +402,7 @@ __global__ void __launch_bounds__(32 * (2 * G + 1), 1) attn_cluster_kernel(const
       }
       const int hq2 = vec >> 4, row = vec & 15;
       __nv_bfloat16* out =
-          a.out + (static_cast<int64_t>(si) * 16 + row) * (a.nq * kD) + (kvh * G + hq2) * kD + d4;
+          a.out + (static_cast<int64_t>(si) * 16 + row) * (a.nq * kD) + (head0 + hq2) * kD + d4;
       const float inv = 1.f / den;
       *reinterpret_cast<__nv_bfloat162*>(out) = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
       *reinterpret_cast<__nv_bfloat162*>(out + 2) = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
@@ -433,6 +440,21 @@ bool attention_cluster_supported(const AttnArgs& a) {
   return a.d == kD && (G == 1 || G == 2 || G == 4 || G == 5 || G == 8);
 }
 
+namespace {
+// (kernel, CTAs per kv head) for a query-head group of G
+void pick_cluster_kernel(int G, void (**kern)(ClusterAttnArgs), int* HS, int* GH) {
+  switch (G) {
+    case 1: *kern = attn_cluster_kernel<1, 1>; *HS = 1; break;
+    case 2: *kern = attn_cluster_kernel<1, 2>; *HS = 2; break;
+    case 4: *kern = attn_cluster_kernel<2, 2>; *HS = 2; break;
+    case 5: *kern = attn_cluster_kernel<5, 1>; *HS = 1; break;
+    case 8: *kern = attn_cluster_kernel<4, 2>; *HS = 2; break;
+    default: *kern = nullptr; *HS = 1; break;
+  }
+  *GH = G / *HS;
+}
+}  // namespace
+
 int attention_cluster_maps(CUtensorMap* kmap, CUtensorMap* vmap, const void* kc, const void* vc, int slabs, int cap) {
   const cuuint64_t dims[3] = {kD, static_cast<cuuint64_t>(cap), static_cast<cuuint64_t>(slabs)};
   const cuuint64_t strides[2] = {kD * 2, static_cast<cuuint64_t>(cap) * kD * 2};
@@ -456,17 +478,12 @@ int launch_attention_cluster(const AttnArgs& a, const CUtensorMap& kmap, const C
   if (!rc) rc = encode_map(&P.vbmap, a.Vb, 2, dims, strides, box);
   if (rc) return rc;
   const int G = a.nq / a.nkv;
-  const int threads = 32 * (2 * G + 1);
   const int smem = ClusterAttnSmem::kBytes + 1024;
   void (*kern)(ClusterAttnArgs) = nullptr;
-  switch (G) {
-    case 1: kern = attn_cluster_kernel<1>; break;
-    case 2: kern = attn_cluster_kernel<2>; break;
-    case 4: kern = attn_cluster_kernel<4>; break;
-    case 5: kern = attn_cluster_kernel<5>; break;
-    case 8: kern = attn_cluster_kernel<8>; break;
-    default: return DFLASH_E_SHAPE;
-  }
+  int HS = 1, GH = G;
+  pick_cluster_kernel(G, &kern, &HS, &GH);
+  if (!kern) return DFLASH_E_SHAPE;
+  const int threads = 32 * (2 * GH + 1);
   static bool configured[9] = {};
   if (!configured[G]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -481,7 +498,7 @@ int launch_attention_cluster(const AttnArgs& a, const CUtensorMap& kmap, const C
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(kClusterCtas, a.nkv, s_count);
+  cfg.gridDim = dim3(kClusterCtas, a.nkv * HS, s_count);
   cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;

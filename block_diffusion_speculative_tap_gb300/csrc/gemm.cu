@@ -550,7 +550,9 @@ int launch_inst(const GemmArgs& a, int num_sms, cudaStream_t st) {
   auto kern = gemm_kernel<BN, DUAL, STAGES, EPI, MINB, CLU>;
   static bool configured = false;
   if (!configured) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kSmemBytes) != cudaSuccess)
+    // two CTAs of the batch-1 variants share an SM only with the full carveout
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
       return DFLASH_E_CUDA;
     configured = true;
   }
@@ -637,23 +639,18 @@ int gemm_bn_for(int N) {
 }
 
 int gemm_choose_ksplit(int m_tiles, int kb_total, int num_sms) {
-  // Fill the 2-CTA-per-SM batch-1 configuration as evenly as possible: the
-  // smallest split whose wave efficiency is within 5% of the best one, with
-  // at least 4 reduction blocks per chunk and at most kMaxClusterSplit chunks
-  // (the chunks of a tile run as one portable-size cluster).
-  const int slots = 2 * num_sms;
-  const int kmax = std::max(1, std::min(kMaxClusterSplit, kb_total / 4));
-  double eff[17] = {0.0};
-  double best = 0.0;
-  for (int ks = 1; ks <= kmax; ++ks) {
-    const long long units = static_cast<long long>(m_tiles) * ks;
-    const long long waves = (units + slots - 1) / slots;
-    eff[ks] = static_cast<double>(units) / static_cast<double>(waves * slots);
-    best = std::max(best, eff[ks]);
+  // The largest split (<= kMaxClusterSplit, >= 4 reduction blocks a chunk)
+  // whose CTAs all fit in one wave of clusters at two CTAs an SM. Cluster
+  // placement inside GPCs leaves some SMs unused, so the wave is taken as
+  // 85% of 2 x SMs (measured on GB300: 48 tiles x 5 splits runs in one wave,
+  // x 6 in two).
+  const int budget = (2 * num_sms * 85) / 100;
+  int best = 1;
+  for (int ks = 2; ks <= kMaxClusterSplit; ++ks) {
+    if (kb_total / ks < 4) break;
+    if (m_tiles * ks <= budget) best = ks;
   }
-  for (int ks = 1; ks <= kmax; ++ks)
-    if (eff[ks] >= 0.95 * best) return ks;
-  return 1;
+  return best;
 }
 
 static void fill_args(const GemmPlan& p, GemmArgs& a, int BN) {

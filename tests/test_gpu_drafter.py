@@ -185,3 +185,27 @@ def test_bad_anchor_sets_status(D):
     assert rc == -10 and bits == 1
     rc, bits = st.status()
     assert rc == 0 and bits == 0
+
+
+@pytest.mark.parametrize("nq,nkv", [(8, 8), (8, 4), (8, 2), (8, 1), (10, 2)])
+def test_query_group_sizes(D, nq, nkv):
+    """Every query-group size the d = 128 attention kernel handles (1, 2, 4,
+    8 and 5 query heads per kv head), on a one-layer full-attention drafter
+    (element-wise parity)."""
+    m = small_model()
+    m.update(hidden=nq * 128, n_q_heads=nq, n_kv_heads=nkv, n_layers=1, layer_kinds=[0], ffn=1536)
+    w = SI.make_weights(m, 300 + nq * 10 + nkv, device="cuda")
+    dr = D.Drafter(m, w)
+    ctx = [333, 16]
+    S = len(ctx)
+    st = dr.new_state(S, 512)
+    ref = O.OracleStreams(m, O.weights_to_f64(w), S)
+    taps = SI.make_taps(m, sum(ctx), 301, device="cuda")
+    segs, r0 = [], 0
+    for s, c in enumerate(ctx):
+        segs.append((s, 0, c))
+        ref.append(s, [f64(t[r0 : r0 + c]) for t in taps])
+        r0 += c
+    st.fuse_taps(taps, segs)
+    anchors = SI.anchor_ids(S, m["vocab"], m["mask_token"], 302)
+    draft_vs_oracle(D, st, ref, m, anchors, 4)
