@@ -25,16 +25,20 @@ namespace dfl {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kKeys = 64;             // keys per tile
-constexpr int kStages = 4;
+constexpr int kKeys = 64;             // keys per context tile
+constexpr int kBlockKeys = 16;        // the block's own keys
+constexpr int kStages = 3;
 constexpr int kClusterCtas = 8;
 constexpr int kSubBytes = kKeys * 128;   // 64 rows x 64 dims (128 B) per swizzled sub-tile
 constexpr int kTileBytes = 4 * kSubBytes;  // K lo, K hi, V lo, V hi = 32 KiB
+constexpr int kBlockSubBytes = kBlockKeys * 128;
+constexpr int kPartLd = kD + 8;       // fp32 partial row stride (conflict-free float2 stores)
 
+// Under 113 KiB, so two CTAs fit an SM and a cluster of 8 spans four SMs.
 struct ClusterAttnSmem {
   static constexpr int kStageOff = 0;
-  static constexpr int kBlockOff = kStages * kTileBytes;       // block tile (rows 16..63 zero)
-  static constexpr int kBarOff = kBlockOff + kTileBytes;
+  static constexpr int kBlockOff = kStages * kTileBytes;       // block tile: 16 keys
+  static constexpr int kBarOff = kBlockOff + 4 * kBlockSubBytes;
   static constexpr int kBytes = kBarOff + 8 * (2 * kStages + 1) + 64;
 };
 
@@ -44,6 +48,12 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
       "{%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t saddr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr));
 }
 
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t saddr) {
@@ -114,28 +124,30 @@ struct AttnState {
   float l[2];
 };
 
-// One 64-key tile at shared address `t` (K lo/hi, V lo/hi sub-tiles) for
-// keys [0, nvalid); scores use `sc` = log2(e) / sqrt(d).
+// One tile of NK keys at shared address `t` (K lo/hi, V lo/hi sub-tiles of
+// NK rows each) for keys [0, nvalid); scores use `sc` = log2(e) / sqrt(d).
+template <int NK>
 __device__ __forceinline__ void attend_tile(AttnState& S, const uint32_t (&qa)[kD / 16][4], uint32_t t, int nvalid,
                                             float sc, int lane) {
-  float sacc[8][4];
+  constexpr uint32_t kSub = NK * 128;
+  constexpr int kN = NK / 8;  // 8-key score tiles
+  float sacc[kN][4];
 #pragma unroll
-  for (int n = 0; n < 8; ++n) {
+  for (int n = 0; n < kN; ++n) {
     sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
-    const int key = n * 8 + (lane >> 2);
+    const int key = n * 8 + (lane & 7);
 #pragma unroll
-    for (int kk = 0; kk < kD / 16; ++kk) {
-      const uint32_t sub = t + static_cast<uint32_t>((kk >> 2) * kSubBytes);
-      const int kq = kk & 3;
-      uint32_t b0, b1;
-      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b0) : "r"(sub + swz(key, 2 * kq) + (lane & 3) * 4));
-      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b1) : "r"(sub + swz(key, 2 * kq + 1) + (lane & 3) * 4));
-      mma16816(sacc[n], qa[kk], b0, b1);
+    for (int kp = 0; kp < kD / 32; ++kp) {
+      // four 8x8 matrices: dims [32kp, 32kp + 32) of keys n*8 .. n*8+7
+      uint32_t kb[4];
+      ldsm_x4(kb, t + static_cast<uint32_t>((kp >> 1) * kSub) + swz(key, 4 * (kp & 1) + (lane >> 3)));
+      mma16816(sacc[n], qa[2 * kp], kb[0], kb[1]);
+      mma16816(sacc[n], qa[2 * kp + 1], kb[2], kb[3]);
     }
   }
   float tmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-  for (int n = 0; n < 8; ++n) {
+  for (int n = 0; n < kN; ++n) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int key = n * 8 + (lane & 3) * 2 + (e & 1);
@@ -157,7 +169,7 @@ __device__ __forceinline__ void attend_tile(AttnState& S, const uint32_t (&qa)[k
     S.m[r] = mnew[r];
   }
 #pragma unroll
-  for (int n = 0; n < 8; ++n) {
+  for (int n = 0; n < kN; ++n) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float p = mnew[e >> 1] == -INFINITY ? 0.f : exp2f(sacc[n][e] - mnew[e >> 1]);
@@ -179,7 +191,7 @@ __device__ __forceinline__ void attend_tile(AttnState& S, const uint32_t (&qa)[k
     S.o[n][3] *= alpha[1];
   }
 #pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
+  for (int kk = 0; kk < NK / 16; ++kk) {
     uint32_t ph[4], pl[4];
     split_hi_lo(sacc[2 * kk][0], sacc[2 * kk][1], ph[0], pl[0]);
     split_hi_lo(sacc[2 * kk][2], sacc[2 * kk][3], ph[1], pl[1]);
@@ -190,7 +202,7 @@ __device__ __forceinline__ void attend_tile(AttnState& S, const uint32_t (&qa)[k
 #pragma unroll
     for (int n2 = 0; n2 < kD / 16; ++n2) {
       const int dim = n2 * 16 + (mi >> 1) * 8;
-      const uint32_t sub = t + static_cast<uint32_t>((2 + (dim >> 6)) * kSubBytes);
+      const uint32_t sub = t + static_cast<uint32_t>((2 + (dim >> 6)) * kSub);
       uint32_t vb[4];
       ldsm_x4_trans(vb, sub + swz(key, (dim & 63) >> 3));
       mma16816(S.o[2 * n2], ph, vb[0], vb[1]);
@@ -212,7 +224,7 @@ struct ClusterAttnArgs {
 // G: query heads handled by this CTA (of the kv head's group); HS: CTAs
 // (clusters) sharing a kv head.
 template <int G, int HS>
-__global__ void __launch_bounds__(32 * (2 * G + 1), 1) attn_cluster_kernel(const __grid_constant__ ClusterAttnArgs P) {
+__global__ void __launch_bounds__(32 * (2 * G + 1), G <= 2 ? 2 : 1) attn_cluster_kernel(const __grid_constant__ ClusterAttnArgs P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const AttnArgs& a = P.a;
@@ -238,12 +250,6 @@ __global__ void __launch_bounds__(32 * (2 * G + 1), 1) attn_cluster_kernel(const
     mbar_init(blkbar, 1);
     fence_barrier_init();
   }
-  // zero rows 16..63 of the block tile (only rows 0..15 are loaded)
-  for (int i = threadIdx.x; i < 4 * 48 * 128 / 16; i += blockDim.x) {
-    const int sub = i / (48 * 8), rem = i - sub * 48 * 8;
-    *reinterpret_cast<uint4*>(smem + ClusterAttnSmem::kBlockOff + sub * kSubBytes + 16 * 128 + rem * 16) =
-        make_uint4(0u, 0u, 0u, 0u);
-  }
   __syncthreads();
   pdl_trigger();
   pdl_wait();
@@ -261,12 +267,12 @@ __global__ void __launch_bounds__(32 * (2 * G + 1), 1) attn_cluster_kernel(const
   if (warp == ncons) {
     if (lane == 0) {
       if (has_block) {
-        mbar_arrive_expect_tx(blkbar, 4 * 16 * 128);
+        mbar_arrive_expect_tx(blkbar, 4 * kBlockSubBytes);
         const uint32_t b = sbase + ClusterAttnSmem::kBlockOff;
         tma2d(b, &P.kbmap, blkbar, kvh * kD, 16 * si);
-        tma2d(b + kSubBytes, &P.kbmap, blkbar, kvh * kD + 64, 16 * si);
-        tma2d(b + 2 * kSubBytes, &P.vbmap, blkbar, kvh * kD, 16 * si);
-        tma2d(b + 3 * kSubBytes, &P.vbmap, blkbar, kvh * kD + 64, 16 * si);
+        tma2d(b + kBlockSubBytes, &P.kbmap, blkbar, kvh * kD + 64, 16 * si);
+        tma2d(b + 2 * kBlockSubBytes, &P.vbmap, blkbar, kvh * kD, 16 * si);
+        tma2d(b + 3 * kBlockSubBytes, &P.vbmap, blkbar, kvh * kD + 64, 16 * si);
       }
       for (int t = 0; t < nt; ++t) {
         const int st = t % kStages;
@@ -314,63 +320,66 @@ __global__ void __launch_bounds__(32 * (2 * G + 1), 1) attn_cluster_kernel(const
     for (int t = par; t < nt; t += 2) {
       const int st = t % kStages;
       if (!mbar_wait(&full[st], (t / kStages) & 1, err, DFLASH_STATUS_TIMEOUT, nullptr)) break;
-      attend_tile(S, qa, sbase + ClusterAttnSmem::kStageOff + st * kTileBytes, min(kKeys, k1 - k0 - t * kKeys), sc,
-                  lane);
+      attend_tile<kKeys>(S, qa, sbase + ClusterAttnSmem::kStageOff + st * kTileBytes,
+                         min(kKeys, k1 - k0 - t * kKeys), sc, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
     if (has_block && par == 1) {
       if (mbar_wait(blkbar, 0, err, DFLASH_STATUS_TIMEOUT, nullptr))
-        attend_tile(S, qa, sbase + ClusterAttnSmem::kBlockOff, 16, sc, lane);
+        attend_tile<kBlockKeys>(S, qa, sbase + ClusterAttnSmem::kBlockOff, kBlockKeys, sc, lane);
     }
   }
   __syncthreads();  // every tile consumed: the stage memory is free
 
   // merge the two parities of each head; the CTA partial goes to
-  // part[hq][16][128] (fp32) and ml[hq][16][2], at the start of stage memory
+  // part[hq][16][kPartLd] (fp32) and ml[hq][16][2], at the start of stage
+  // memory; the odd-parity states pass through xch[hq][68][32] (lane-minor)
   float* part = reinterpret_cast<float*>(smem + ClusterAttnSmem::kStageOff);
-  float* ml = part + G * 16 * kD;
-  float* xch = ml + G * 16 * 2;  // odd-parity warps' states, 68 floats a lane
+  float* ml = part + G * 16 * kPartLd;
+  float* xch = ml + G * 16 * 2;
+  static_assert(sizeof(float) * G * (16 * (kPartLd + 2) + 68 * 32) <= kStages * kTileBytes,
+                "merge scratch exceeds the stage memory");
   if (consumer && par == 1) {
-    float* x = xch + (hq * 32 + lane) * 68;
+    float* x = xch + hq * 68 * 32 + lane;
 #pragma unroll
     for (int n = 0; n < kD / 8; ++n) {
-      x[4 * n] = S.o[n][0];
-      x[4 * n + 1] = S.o[n][1];
-      x[4 * n + 2] = S.o[n][2];
-      x[4 * n + 3] = S.o[n][3];
+      x[(4 * n) * 32] = S.o[n][0];
+      x[(4 * n + 1) * 32] = S.o[n][1];
+      x[(4 * n + 2) * 32] = S.o[n][2];
+      x[(4 * n + 3) * 32] = S.o[n][3];
     }
-    x[64] = S.m[0];
-    x[65] = S.m[1];
-    x[66] = S.l[0];
-    x[67] = S.l[1];
+    x[64 * 32] = S.m[0];
+    x[65 * 32] = S.m[1];
+    x[66 * 32] = S.l[0];
+    x[67 * 32] = S.l[1];
   }
   __syncthreads();
   if (consumer && par == 0) {
-    const float* x = xch + (hq * 32 + lane) * 68;
+    const float* x = xch + hq * 68 * 32 + lane;
     float w0[2], w1[2], M[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      M[r] = fmaxf(S.m[r], x[64 + r]);
+      const float mx = x[(64 + r) * 32];
+      M[r] = fmaxf(S.m[r], mx);
       w0[r] = M[r] == -INFINITY ? 0.f : exp2f(S.m[r] - M[r]);
-      w1[r] = M[r] == -INFINITY ? 0.f : exp2f(x[64 + r] - M[r]);
+      w1[r] = M[r] == -INFINITY ? 0.f : exp2f(mx - M[r]);
     }
     const int r0 = lane >> 2;
 #pragma unroll
     for (int n = 0; n < kD / 8; ++n) {
       const int col = n * 8 + (lane & 3) * 2;
-      float* p0 = part + (hq * 16 + r0) * kD + col;
-      float* p1 = part + (hq * 16 + r0 + 8) * kD + col;
-      p0[0] = S.o[n][0] * w0[0] + x[4 * n] * w1[0];
-      p0[1] = S.o[n][1] * w0[0] + x[4 * n + 1] * w1[0];
-      p1[0] = S.o[n][2] * w0[1] + x[4 * n + 2] * w1[1];
-      p1[1] = S.o[n][3] * w0[1] + x[4 * n + 3] * w1[1];
+      float2* p0 = reinterpret_cast<float2*>(part + (hq * 16 + r0) * kPartLd + col);
+      float2* p1 = reinterpret_cast<float2*>(part + (hq * 16 + r0 + 8) * kPartLd + col);
+      *p0 = make_float2(S.o[n][0] * w0[0] + x[(4 * n) * 32] * w1[0], S.o[n][1] * w0[0] + x[(4 * n + 1) * 32] * w1[0]);
+      *p1 = make_float2(S.o[n][2] * w0[1] + x[(4 * n + 2) * 32] * w1[1],
+                        S.o[n][3] * w0[1] + x[(4 * n + 3) * 32] * w1[1]);
     }
     if ((lane & 3) == 0) {
       ml[(hq * 16 + r0) * 2] = M[0];
-      ml[(hq * 16 + r0) * 2 + 1] = S.l[0] * w0[0] + x[66] * w1[0];
+      ml[(hq * 16 + r0) * 2 + 1] = S.l[0] * w0[0] + x[66 * 32] * w1[0];
       ml[(hq * 16 + r0 + 8) * 2] = M[1];
-      ml[(hq * 16 + r0 + 8) * 2 + 1] = S.l[1] * w0[1] + x[67] * w1[1];
+      ml[(hq * 16 + r0 + 8) * 2 + 1] = S.l[1] * w0[1] + x[67 * 32] * w1[1];
     }
   }
   csync();  // every CTA's partial is ready
@@ -394,7 +403,7 @@ __global__ void __launch_bounds__(32 * (2 * G + 1), 1) attn_cluster_kernel(const
         const float m = cld(cmap(mlbase, r2) + vec * 8);
         const float w = M == -INFINITY ? 0.f : exp2f(m - M);
         den += w * cld(cmap(mlbase, r2) + vec * 8 + 4);
-        const float4 v = cld4(cmap(pbase, r2) + (vec * kD + d4) * 4);
+        const float4 v = cld4(cmap(pbase, r2) + (vec * kPartLd + d4) * 4);
         acc.x += w * v.x;
         acc.y += w * v.y;
         acc.z += w * v.z;
@@ -486,7 +495,8 @@ int launch_attention_cluster(const AttnArgs& a, const CUtensorMap& kmap, const C
   const int threads = 32 * (2 * GH + 1);
   static bool configured[9] = {};
   if (!configured[G]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
       return DFLASH_E_CUDA;
     configured[G] = true;
   }
