@@ -652,7 +652,8 @@ struct DraftWs {
   int* counters;
   size_t n_counters;
   float* X;
-  __nv_bfloat16* hbuf;
+  __nv_bfloat16* hbuf;  // bf16 normalised rows, the B operand after each RMSNorm
+  float* ss;            // [H/128][T] per-part sums of squares of the residual rows (every writer of X publishes them)
   __nv_bfloat16* Q;
   __nv_bfloat16* Kb;
   __nv_bfloat16* Vb;
@@ -771,6 +772,7 @@ size_t draft_ws_layout(const dflash_handle* h, const dflash_state* st, int S, bo
   w.n_counters = counters;
   w.X = cv.take<float>(static_cast<size_t>(T) * c.hidden);
   w.hbuf = cv.take<__nv_bfloat16>(static_cast<size_t>(T) * c.hidden);
+  w.ss = cv.take<float>(static_cast<size_t>(T) * (c.hidden / kTileM));
   w.Q = cv.take<__nv_bfloat16>(static_cast<size_t>(T) * qd);
   w.Kb = cv.take<__nv_bfloat16>(static_cast<size_t>(T) * kvd);
   w.Vb = cv.take<__nv_bfloat16>(static_cast<size_t>(T) * kvd);
@@ -795,9 +797,36 @@ int dflash_draft_workspace_bytes(const dflash_handle* h, const dflash_state* st,
 
 namespace {
 
-// Stages [g0, g1) of the block forward on the fp32 residual X [16*s_count, H]:
-// stage 2l is layer l's attention half (input norm, QKV, attention, O-proj
-// added to X), stage 2l+1 its MLP half (post norm, SwiGLU, down added to X).
+// The RMSNorm gain of stage g's input norm (input_norm of layer g/2 for an
+// attention half, post_norm for an MLP half).
+const __nv_bfloat16* stage_gain(const dflash_handle* h, int g) {
+  const dflash_layer_weights& L = h->layers[g >> 1];
+  return static_cast<const __nv_bfloat16*>((g & 1) ? L.post_norm : L.input_norm);
+}
+
+// Stage g's input RMSNorm of X into w.hbuf (rstd from the sums in w.ss),
+// which the stage's first GEMM `p` reads.
+int stage_norm(dflash_handle* h, int g, GemmPlan& p, const float* X, const DraftWs& w, int T, cudaStream_t s) {
+  const dflash_config& c = h->cfg;
+  p.n_b = 1;
+  p.ldb = c.hidden;
+  p.b_ptr[0] = w.hbuf;
+  return launch_rmsnorm_rows(w.hbuf, X, stage_gain(h, g), w.ss, T, T, c.hidden, c.rms_eps, 0, s);
+}
+
+// A residual add that also leaves the new rows' sums of squares in w.ss.
+void resid_add(EpiArgs& e, float* X, const dflash_config& c, const DraftWs& w, int T) {
+  e.out = X;
+  e.ldo = c.hidden;
+  e.ss_out = w.ss;
+  e.ss_ld = T;
+}
+
+// Stages [g0, g1) of the block forward on the fp32 residual X [16*s_count, H]
+// whose per-part sums of squares are in w.ss: stage 2l is layer l's
+// attention half (input norm, QKV, attention, O-proj added to X), stage 2l+1
+// its MLP half (post norm, SwiGLU, down added to X). Each residual add
+// leaves the sums of squares of the new rows for the next stage's norm.
 int run_stages(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int g0, int g1, float* X,
                const DraftWs& w, int*& counters, cudaStream_t s) {
   const dflash_config& c = h->cfg;
@@ -812,11 +841,8 @@ int run_stages(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int
     layer_plans(h, l, T, qkv, o, gu, dn);
     if (g & 1) {
       // post-attention RMSNorm -> SwiGLU -> down projection added to the residual
-      rc = launch_rmsnorm_rows(w.hbuf, X, static_cast<const __nv_bfloat16*>(L.post_norm), T, c.hidden, c.rms_eps, 0,
-                               s);
+      rc = stage_norm(h, g, gu, X, w, T, s);
       if (rc) return rc;
-      gu.b_ptr[0] = w.hbuf;
-      gu.ldb = c.hidden;
       gu.epi_args.out = w.mid;
       gu.epi_args.ldo = c.ffn;
       rc = gemm_launch(gu, w.partial, counters, st->status, h->num_sms, s);
@@ -824,18 +850,15 @@ int run_stages(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int
       counters += gemm_counter_count(gu);
       dn.b_ptr[0] = w.mid;
       dn.ldb = c.ffn;
-      dn.epi_args.out = X;
-      dn.epi_args.ldo = c.hidden;
+      resid_add(dn.epi_args, X, c, w, T);
       rc = gemm_launch(dn, w.partial, counters, st->status, h->num_sms, s);
       if (rc) return rc;
       counters += gemm_counter_count(dn);
       continue;
     }
     // input RMSNorm -> QKV with q_norm / k_norm + RoPE at positions C..C+15
-    rc = launch_rmsnorm_rows(w.hbuf, X, static_cast<const __nv_bfloat16*>(L.input_norm), T, c.hidden, c.rms_eps, 0, s);
+    rc = stage_norm(h, g, qkv, X, w, T, s);
     if (rc) return rc;
-    qkv.b_ptr[0] = w.hbuf;
-    qkv.ldb = c.hidden;
     EpiArgs& e = qkv.epi_args;
     e.head_dim = c.head_dim;
     e.eps = c.rms_eps;
@@ -883,8 +906,7 @@ int run_stages(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int
     // O projection added to the residual
     o.b_ptr[0] = w.attn;
     o.ldb = qd;
-    o.epi_args.out = X;
-    o.epi_args.ldo = c.hidden;
+    resid_add(o.epi_args, X, c, w, T);
     rc = gemm_launch(o, w.partial, counters, st->status, h->num_sms, s);
     if (rc) return rc;
     counters += gemm_counter_count(o);
@@ -892,12 +914,13 @@ int run_stages(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int
   return DFLASH_OK;
 }
 
-// Final norm on the 15 mask rows of every stream, shared LM head, top-k.
+// Final norm on the 15 mask rows of every stream (sums of squares of X in
+// w.ss), shared LM head, top-k.
 int run_head(dflash_handle* h, int* status, int s_count, const float* X, const DraftWs& w, __nv_bfloat16* logits,
              int32_t* topk_ids, float* topk_vals, int k, int*& counters, cudaStream_t s) {
   const dflash_config& c = h->cfg;
   const int rows = s_count * (DFLASH_BLOCK - 1);
-  int rc = launch_rmsnorm_rows(w.hbuf, X, h->norm, rows, c.hidden, c.rms_eps, 1, s);
+  int rc = launch_rmsnorm_rows(w.hbuf, X, h->norm, w.ss, s_count * DFLASH_BLOCK, rows, c.hidden, c.rms_eps, 1, s);
   if (rc) return rc;
   GemmPlan lp = lm_plan(h, rows);
   lp.b_ptr[0] = w.hbuf;
@@ -935,7 +958,7 @@ int dflash_draft_block(dflash_handle* h, dflash_state* st, int s_begin, int s_co
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   __nv_bfloat16* logits = logits_out ? static_cast<__nv_bfloat16*>(logits_out) : w.logits;
   if (cudaMemsetAsync(w.counters, 0, w.n_counters * sizeof(int), s) != cudaSuccess) return DFLASH_E_CUDA;
-  rc = launch_embed(w.X, h->embed, anchor_ids, s_count, c.hidden, c.vocab, c.mask_token, st->status, s);
+  rc = launch_embed(w.X, w.ss, h->embed, anchor_ids, s_count, c.hidden, c.vocab, c.mask_token, st->status, s);
   if (rc) return rc;
   int* counters = w.counters;
   rc = run_stages(h, st, s_begin, s_count, 0, 2 * c.n_layers, w.X, w, counters, s);
@@ -954,6 +977,9 @@ int dflash_draft_stages(dflash_handle* h, dflash_state* st, int s_begin, int s_c
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(w.counters, 0, w.n_counters * sizeof(int), s) != cudaSuccess) return DFLASH_E_CUDA;
   int* counters = w.counters;
+  if (stage1 == stage0) return DFLASH_OK;
+  rc = launch_row_sumsq(w.ss, X, s_count * DFLASH_BLOCK, h->cfg.hidden, s);
+  if (rc) return rc;
   return run_stages(h, st, s_begin, s_count, stage0, stage1, X, w, counters, s);
 }
 
@@ -967,6 +993,8 @@ int dflash_draft_head(dflash_handle* h, dflash_state* st, int s_count, const flo
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(w.counters, 0, w.n_counters * sizeof(int), s) != cudaSuccess) return DFLASH_E_CUDA;
   int* counters = w.counters;
+  rc = launch_row_sumsq(w.ss, X, s_count * DFLASH_BLOCK, h->cfg.hidden, s);
+  if (rc) return rc;
   return run_head(h, st->status, s_count, X, w, static_cast<__nv_bfloat16*>(logits_out), topk_ids, topk_vals, k,
                   counters, s);
 }

@@ -393,21 +393,28 @@ __global__ void __launch_bounds__(32 * (2 * G + 1), G <= 2 ? 2 : 1) attn_cluster
     for (int idx = threadIdx.x; idx < (v1 - v0) * 32; idx += blockDim.x) {
       const int vec = v0 + idx / 32;
       const int d4 = (idx & 31) * 4;
+      // every rank's (max, sum, partial) loaded before any is used
+      float mr[kClusterCtas], lr[kClusterCtas];
+      float4 pr[kClusterCtas];
+#pragma unroll
+      for (int r2 = 0; r2 < kClusterCtas; ++r2) {
+        mr[r2] = cld(cmap(mlbase, r2) + vec * 8);
+        lr[r2] = cld(cmap(mlbase, r2) + vec * 8 + 4);
+        pr[r2] = cld4(cmap(pbase, r2) + (vec * kPartLd + d4) * 4);
+      }
       float M = -INFINITY;
 #pragma unroll
-      for (int r2 = 0; r2 < kClusterCtas; ++r2) M = fmaxf(M, cld(cmap(mlbase, r2) + vec * 8));
+      for (int r2 = 0; r2 < kClusterCtas; ++r2) M = fmaxf(M, mr[r2]);
       float den = 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int r2 = 0; r2 < kClusterCtas; ++r2) {
-        const float m = cld(cmap(mlbase, r2) + vec * 8);
-        const float w = M == -INFINITY ? 0.f : exp2f(m - M);
-        den += w * cld(cmap(mlbase, r2) + vec * 8 + 4);
-        const float4 v = cld4(cmap(pbase, r2) + (vec * kPartLd + d4) * 4);
-        acc.x += w * v.x;
-        acc.y += w * v.y;
-        acc.z += w * v.z;
-        acc.w += w * v.w;
+        const float w = M == -INFINITY ? 0.f : exp2f(mr[r2] - M);
+        den += w * lr[r2];
+        acc.x += w * pr[r2].x;
+        acc.y += w * pr[r2].y;
+        acc.z += w * pr[r2].z;
+        acc.w += w * pr[r2].w;
       }
       const int hq2 = vec >> 4, row = vec & 15;
       __nv_bfloat16* out =

@@ -46,7 +46,7 @@ struct GemmTraits {
                                                             : kTmemNeed <= 256 ? 256 : 512;
   static constexpr int kBarBytes = 8 * (2 * STAGES + 2 * kAccBufs + 1) + 16;
   static constexpr int kXchFloats = EPI == EPI_HEADS ? kTileM * 17 : 0;  // rope partner exchange
-  static constexpr int kRedFloats = EPI == EPI_HEADS ? 4 * 16 : 0;       // per-warp sums of squares
+  static constexpr int kRedFloats = (EPI == EPI_HEADS || EPI == EPI_RESID) ? 4 * 16 : 0;  // per-warp sums of squares
   static constexpr int kSmemBytes =
       1024 /*alignment slack*/ + STAGES * kStageBytes + kBarBytes + 4 * (kXchFloats + kRedFloats) + 64;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, BN);
@@ -101,6 +101,28 @@ __device__ __forceinline__ int seg_of_tile(const GemmArgs& a, int m_tile) {
 }
 
 // ---------------------------------------------------------------- epilogues
+
+// Sum v[j] over the 32 lanes for all 16 j at once: four halving exchanges
+// then one pairwise add (16 shuffles). Lane L (and L ^ 1) ends with the total
+// of column j = 8*b4 + 4*b3 + 2*b2 + b1 of L's bits; the order of the
+// additions is fixed.
+__device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane, int& j_out) {
+  float a[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) a[j] = v[j];
+#pragma unroll
+  for (int h = 8, off = 16; h >= 1; h >>= 1, off >>= 1) {
+    const bool up = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float send = up ? a[i] : a[i + h];
+      const float keep = up ? a[i + h] : a[i];
+      a[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  j_out = 8 * ((lane >> 4) & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) + ((lane >> 1) & 1);
+  return a[0] + __shfl_xor_sync(0xffffffffu, a[0], 1);
+}
 // v0 (and v1 for the dual GEMM) hold the accumulator of output feature
 // m = m_tile*128 + row for tokens t = n0 + j, j = 0..15.
 template <int EPI>
@@ -108,7 +130,32 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
                                           const float (&v0)[16], const float (&v1)[16], float* xch, float* red,
                                           int nvalid = 16) {
   const int m = m_tile * kTileM + row;
-  if constexpr (EPI == EPI_STORE_F32 || EPI == EPI_STORE_BF16 || EPI == EPI_RESID || EPI == EPI_SWIGLU) {
+  if constexpr (EPI == EPI_RESID) {
+    // X += v, and the tile's per-column sums of squares of the new X
+    float ss[16];
+    float* X = static_cast<float*>(a.epi.out);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int t = n0 + j;
+      ss[j] = 0.f;
+      if (j < nvalid && t < a.N && m < a.M) {
+        const int64_t o = static_cast<int64_t>(t) * a.epi.ldo + m;
+        const float xn = X[o] + v0[j];
+        X[o] = xn;
+        ss[j] = xn * xn;
+      }
+    }
+    if (a.epi.ss_out) {
+      int jj;
+      const float w = warp_sum16(ss, lane, jj);
+      if ((lane & 1) == 0) red[q * 16 + jj] = w;
+      named_bar_sync(1, 128);
+      if (row < 16 && row < nvalid && n0 + row < a.N)
+        a.epi.ss_out[static_cast<int64_t>(m_tile) * a.epi.ss_ld + n0 + row] =
+            ((red[row] + red[16 + row]) + red[32 + row]) + red[48 + row];
+      named_bar_sync(1, 128);  // red reusable by the next chunk
+    }
+  } else if constexpr (EPI == EPI_STORE_F32 || EPI == EPI_STORE_BF16 || EPI == EPI_SWIGLU) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int t = n0 + j;
@@ -118,9 +165,6 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
         static_cast<float*>(a.epi.out)[o] = v0[j];
       } else if constexpr (EPI == EPI_STORE_BF16) {
         static_cast<__nv_bfloat16*>(a.epi.out)[o] = __float2bfloat16_rn(v0[j]);
-      } else if constexpr (EPI == EPI_RESID) {
-        float* X = static_cast<float*>(a.epi.out);
-        X[o] = X[o] + v0[j];
       } else {
         static_cast<__nv_bfloat16*>(a.epi.out)[o] = __float2bfloat16_rn(silu_f(v0[j]) * v1[j]);
       }
@@ -153,32 +197,26 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
     }
     float y[16];
     if (sg.kind != HEAD_V) {
-      float ss[16];
+      // per-head sums of squares: warp partials (transpose reduction), then
+      // the head's warps in order
+      float sq[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) ss[j] = v0[j] * v0[j];
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) ss[j] += __shfl_xor_sync(0xffffffffu, ss[j], off);
-      }
+      for (int j = 0; j < 16; ++j) sq[j] = v0[j] * v0[j];
+      int jj;
+      const float w = warp_sum16(sq, lane, jj);
+      if ((lane & 1) == 0) red[q * 16 + jj] = w;
+      named_bar_sync(1, 128);
       const int wph = d >> 5;  // warps per head (1, 2 or 4)
-      if (wph > 1) {
-        if (lane == 0) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) red[q * 16 + j] = ss[j];
-        }
-        named_bar_sync(1, 128);
-        const int q0 = (q / wph) * wph;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          float s = 0.f;
-          for (int qq = 0; qq < wph; ++qq) s += red[(q0 + qq) * 16 + j];
-          ss[j] = s;
-        }
-      }
+      const int q0 = (q / wph) * wph;
+      // d is a power of two, so * (1/d) is exactly / d
+      const float inv_d = 1.0f / static_cast<float>(d);
       const float g = __bfloat162float(sg.gain[dim]);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) y[j] = v0[j] * rsqrtf(ss[j] / static_cast<float>(d) + a.epi.eps) * g;
+      for (int j = 0; j < 16; ++j) {
+        float s = red[q0 * 16 + j];
+        for (int qq = 1; qq < wph; ++qq) s += red[(q0 + qq) * 16 + j];
+        y[j] = v0[j] * rsqrtf(s * inv_d + a.epi.eps) * g;
+      }
       // partner value (dim +- d/2) via shared memory
 #pragma unroll
       for (int j = 0; j < 16; ++j) xch[row * 17 + j] = y[j];
@@ -395,6 +433,25 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
     for (int u = blockIdx.x; u < args.units; u += gridDim.x) {
       int m_tile, kc, n_tile;
       decode_unit<CLU>(args, u, m_tile, kc, n_tile);
+      if constexpr (EPI == EPI_HEADS) {
+        // the epilogue's per-head gain and RoPE rows are read once, long after
+        // the weight stream has evicted them: pull them into L2 now
+        if (args.epi.pos_mode == 0) {
+          const int sidx = seg_of_tile(args, m_tile);
+          const HeadSeg& sg = args.epi.seg[sidx];
+          const int half = args.epi.head_dim >> 1;
+          const int lpr = (half * 8 + 127) / 128;  // 128-byte lines per RoPE row
+          for (int i = row; i < BN * lpr; i += 128) {
+            const int t = n_tile * BN + i / lpr;
+            if (t < args.N) {
+              const int p = args.epi.lens[args.epi.s_begin + t / 16] + (t & 15);
+              prefetch_l2(reinterpret_cast<const char*>(args.epi.rope + static_cast<int64_t>(p) * half) +
+                          (i % lpr) * 128);
+            }
+          }
+          if (sg.gain != nullptr && row * 64 < args.epi.head_dim) prefetch_l2(sg.gain + row * 64);
+        }
+      }
       const bool ok = mbar_wait(&tfull[acc], acc_phase, args.err, DFLASH_STATUS_TIMEOUT, abort_word);
       // the four epilogue warps leave together, so none is left at a named barrier
       if (named_bar_or(1, 128, ok ? 0 : 1)) break;
@@ -499,13 +556,30 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
           v0[j] = 0.f;
           v1[j] = 0.f;
         }
-        for (int r2 = 0; r2 < ks; ++r2) {
-          const uint32_t rb = gemm_mapa(pbase, static_cast<uint32_t>(r2));
+        // rank order; the loads of two ranks are issued before their adds
+        for (int r2 = 0; r2 < ks; r2 += 2) {
+          const bool two = r2 + 1 < ks;
+          const uint32_t ra = gemm_mapa(pbase, static_cast<uint32_t>(r2));
+          const uint32_t rb = gemm_mapa(pbase, static_cast<uint32_t>(two ? r2 + 1 : r2));
+          float a0[16], b0[16], a1[16], b1[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            if (j < nv) {
-              v0[j] += gemm_ld_dsmem(rb + static_cast<uint32_t>(((c0 + j) * kTileM + row) * 4));
-              if constexpr (DUAL) v1[j] += gemm_ld_dsmem(rb + static_cast<uint32_t>(((BN + c0 + j) * kTileM + row) * 4));
+            const uint32_t o0 = static_cast<uint32_t>(((c0 + j) * kTileM + row) * 4);
+            const uint32_t o1 = static_cast<uint32_t>(((BN + c0 + j) * kTileM + row) * 4);
+            a0[j] = j < nv ? gemm_ld_dsmem(ra + o0) : 0.f;
+            b0[j] = (j < nv && two) ? gemm_ld_dsmem(rb + o0) : 0.f;
+            if constexpr (DUAL) {
+              a1[j] = j < nv ? gemm_ld_dsmem(ra + o1) : 0.f;
+              b1[j] = (j < nv && two) ? gemm_ld_dsmem(rb + o1) : 0.f;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            v0[j] += a0[j];
+            if (two) v0[j] += b0[j];
+            if constexpr (DUAL) {
+              v1[j] += a1[j];
+              if (two) v1[j] += b1[j];
             }
           }
         }

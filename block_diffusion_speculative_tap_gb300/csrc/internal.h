@@ -46,6 +46,11 @@ struct EpiArgs {
                          // slot is written only by the last W positions of a segment
   const float2* rope;    // [pos][d/2] = (cos, sin)
   HeadSeg seg[kMaxASeg];
+  // RESID: per-tile sums of squares of the updated rows,
+  // ss_out[m_tile * ss_ld + t] (null: not published), for the RMSNorm that
+  // reads the rows next
+  float* ss_out;
+  int ss_ld;
 };
 
 struct GemmArgs {
@@ -94,11 +99,18 @@ int encode_kmajor_map(CUtensorMap* map, const void* base, int64_t rows, int64_t 
 int gemm_launch(const GemmPlan& p, float* partial, int* counters, int* err, int num_sms, cudaStream_t st);
 
 // ---------------------------------------------------------------- small kernels (rows.cu)
-int launch_embed(float* X, const __nv_bfloat16* embed, const int* anchors, int S, int H, int V, int mask, int* err,
-                 cudaStream_t st);
-// out[r] = bf16(RMSNorm(x[src_row(r)]) * g); src_row maps mask rows when mask_rows_only.
-int launch_rmsnorm_rows(__nv_bfloat16* out, const float* x, const __nv_bfloat16* g, int rows, int H, float eps,
-                        int mask_rows_only, cudaStream_t st);
+// X = embedding rows of [anchor + 15 mask] per stream, with the per-128-
+// feature sums of squares of every row, ss[p][T], for a fused input norm.
+int launch_embed(float* X, float* ss, const __nv_bfloat16* embed, const int* anchors, int S, int H, int V, int mask,
+                 int* err, cudaStream_t st);
+// The same sums of squares for rows of a caller-given X [rows, H].
+int launch_row_sumsq(float* ss, const float* X, int rows, int H, cudaStream_t st);
+// out[r] = bf16(x[src] * rstd * g) with rstd = rsqrt(sum_p ss[p][src] / H +
+// eps) from the rows' published per-128-feature sums of squares (parts summed
+// in order); src = r, or the r-th mask row (block rows 1..15) when
+// mask_rows_only. Elementwise: 8 features a thread.
+int launch_rmsnorm_rows(__nv_bfloat16* out, const float* x, const __nv_bfloat16* g, const float* ss, int ss_ld,
+                        int rows, int H, float eps, int mask_rows_only, cudaStream_t st);
 // Row tables (stream, position) of appended segments, and/or the new stream
 // lengths (start + rows of each segment). seg_info_host_packed holds
 // (stream, start, rows) per segment, on the host.

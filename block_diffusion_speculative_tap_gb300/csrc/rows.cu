@@ -27,10 +27,31 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return t;
 }
 
+// Per-128-feature sums of squares of one row, ss[p * ss_ld + t], for an
+// input norm fused into the GEMM that reads the row next (lane sums of four
+// in order, then a fixed warp tree). Warp w of the CTA takes parts w, w + 4,
+// ...; `x4(i)` yields float4 i of the row.
+constexpr int kStatThreads = 128;
+
+template <typename Load>
+__device__ __forceinline__ void row_sumsq(float* __restrict__ ss, int ss_ld, int t, int H, Load x4) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int p = warp; p * 128 < H; p += kStatThreads / 32) {
+    const float4 v = x4(p * 32 + lane);
+    float q = ((v.x * v.x + v.y * v.y) + v.z * v.z) + v.w * v.w;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) q += __shfl_xor_sync(0xffffffffu, q, off);
+    if (lane == 0) ss[static_cast<int64_t>(p) * ss_ld + t] = q;
+  }
+}
+
 // X[t] = embed[token_t] as fp32; token 16s is the anchor of stream s, the
 // other fifteen rows of the block are the mask token [anchor + 15 mask rows].
-__global__ void embed_kernel(float* __restrict__ X, const __nv_bfloat16* __restrict__ E, const int* __restrict__ anchors,
-                             int H, int V, int mask, int* err) {
+// The row's sums of squares go to ss for the first layer's input norm.
+__global__ void __launch_bounds__(kStatThreads) embed_kernel(float* __restrict__ X, float* __restrict__ ss,
+                                                             const __nv_bfloat16* __restrict__ E,
+                                                             const int* __restrict__ anchors, int H, int V, int mask,
+                                                             int ss_ld, int* err) {
   pdl_trigger();
   pdl_wait();
   const int t = blockIdx.x;
@@ -42,63 +63,62 @@ __global__ void embed_kernel(float* __restrict__ X, const __nv_bfloat16* __restr
       tok = 0;
     }
   }
-  const __nv_bfloat16* e = E + static_cast<int64_t>(tok) * H;
-  float* x = X + static_cast<int64_t>(t) * H;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) x[i] = __bfloat162float(e[i]);
+  const uint2* e = reinterpret_cast<const uint2*>(E + static_cast<int64_t>(tok) * H);
+  float4* x = reinterpret_cast<float4*>(X + static_cast<int64_t>(t) * H);
+  row_sumsq(ss, ss_ld, t, H, [&](int i) {
+    const uint2 r = e[i];
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.y));
+    const float4 v = make_float4(a.x, a.y, b.x, b.y);
+    x[i] = v;
+    return v;
+  });
 }
 
-// out[r] = bf16(x[src] / sqrt(mean(x[src]^2) + eps) * g). The row is held in
-// registers (up to kNormVec float4 per thread), all loads issued up front,
-// so a row costs one memory round trip. Rows wider than
-// kNormVec * 4 * blockDim fall back to a strided second pass.
-constexpr int kNormThreads = 512;
-constexpr int kNormVec = 4;
+// Sums of squares of rows of a caller-given residual X.
+__global__ void __launch_bounds__(kStatThreads) row_sumsq_kernel(float* __restrict__ ss, const float* __restrict__ X,
+                                                                 int H, int ss_ld) {
+  pdl_trigger();
+  pdl_wait();
+  const int t = blockIdx.x;
+  const float4* x = reinterpret_cast<const float4*>(X + static_cast<int64_t>(t) * H);
+  row_sumsq(ss, ss_ld, t, H, [&](int i) { return x[i]; });
+}
+
+// out[r] = bf16(x[src] * rstd * g), rstd = 1 / sqrt(sum_p ss[p][src] / H +
+// eps): the row's sum of squares comes as per-128-feature parts published by
+// the kernel that wrote the row (summed here in part order), so the norm is
+// elementwise. A CTA covers 1024 features of one row, 8 a thread.
+constexpr int kNormThreads = 128;
 
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_rows_kernel(__nv_bfloat16* __restrict__ out,
                                                                     const float* __restrict__ x,
-                                                                    const __nv_bfloat16* __restrict__ g, int H,
-                                                                    float eps, int mask_rows_only) {
-  __shared__ float red[32];
+                                                                    const __nv_bfloat16* __restrict__ g,
+                                                                    const float* __restrict__ ss, int ss_ld, int H,
+                                                                    float inv_h, float eps, int mask_rows_only) {
   pdl_trigger();
   pdl_wait();
-  const int r = blockIdx.x;
+  const int r = blockIdx.y;
   const int src = mask_rows_only ? (r / 15) * 16 + 1 + (r % 15) : r;
-  const float4* xr = reinterpret_cast<const float4*>(x + static_cast<int64_t>(src) * H);
-  const int nv = H >> 2;
-  float4 v[kNormVec];
-  float ss = 0.f;
+  const int i = (blockIdx.x * kNormThreads + threadIdx.x) * 8;  // first feature
+  float sum = 0.f;
+  for (int p = 0; p * 128 < H; ++p) sum += ss[static_cast<int64_t>(p) * ss_ld + src];
+  const float rstd = rsqrtf(__fmaf_rn(sum, inv_h, eps));
+  if (i >= H) return;
+  const float4* xr = reinterpret_cast<const float4*>(x + static_cast<int64_t>(src) * H + i);
+  const float4 a = xr[0], b = xr[1];
+  const uint4 gr = *reinterpret_cast<const uint4*>(g + i);
+  const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gr);
+  const float xs[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint4 o;
+  uint32_t* o2 = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
-  for (int i = 0; i < kNormVec; ++i) {
-    const int j = threadIdx.x + i * kNormThreads;
-    v[i] = j < nv ? xr[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < 4; ++k) {
+    const float2 gf = __bfloat1622float2(g2[k]);
+    const __nv_bfloat162 y = __floats2bfloat162_rn(xs[2 * k] * rstd * gf.x, xs[2 * k + 1] * rstd * gf.y);
+    o2[k] = *reinterpret_cast<const uint32_t*>(&y);
   }
-#pragma unroll
-  for (int i = 0; i < kNormVec; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
-  for (int j = threadIdx.x + kNormVec * kNormThreads; j < nv; j += kNormThreads) {
-    const float4 t = xr[j];
-    ss += t.x * t.x + t.y * t.y + t.z * t.z + t.w * t.w;
-  }
-  const float tot = block_sum(ss, red);
-  const float rstd = rsqrtf(tot / static_cast<float>(H) + eps);
-  __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(out + static_cast<int64_t>(r) * H);
-  const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(g);
-#pragma unroll
-  for (int i = 0; i < kNormVec; ++i) {
-    const int j = threadIdx.x + i * kNormThreads;
-    if (j < nv) {
-      const float2 ga = __bfloat1622float2(g2[2 * j]);
-      const float2 gb = __bfloat1622float2(g2[2 * j + 1]);
-      o[2 * j] = __floats2bfloat162_rn(v[i].x * rstd * ga.x, v[i].y * rstd * ga.y);
-      o[2 * j + 1] = __floats2bfloat162_rn(v[i].z * rstd * gb.x, v[i].w * rstd * gb.y);
-    }
-  }
-  for (int j = threadIdx.x + kNormVec * kNormThreads; j < nv; j += kNormThreads) {
-    const float4 t = xr[j];
-    const float2 ga = __bfloat1622float2(g2[2 * j]);
-    const float2 gb = __bfloat1622float2(g2[2 * j + 1]);
-    o[2 * j] = __floats2bfloat162_rn(t.x * rstd * ga.x, t.y * rstd * ga.y);
-    o[2 * j + 1] = __floats2bfloat162_rn(t.z * rstd * gb.x, t.w * rstd * gb.y);
-  }
+  *reinterpret_cast<uint4*>(out + static_cast<int64_t>(r) * H + i) = o;
 }
 
 // fused = bf16(RMSNorm(y) * hidden_norm): written to the ring slot of the
@@ -158,19 +178,29 @@ __global__ void set_lens_kernel(int* __restrict__ lens, const SegTable tab) {
 
 }  // namespace
 
-int launch_embed(float* X, const __nv_bfloat16* embed, const int* anchors, int S, int H, int V, int mask, int* err,
-                 cudaStream_t st) {
-  TraceScope ts(st, "embed", static_cast<double>(S) * 16 * H * 6, 0.0);
-  const cudaError_t e = launch_pdl(embed_kernel, dim3(S * 16), dim3(kRowThreads), 0, st, X, embed, anchors, H, V, mask, err);
+int launch_embed(float* X, float* ss, const __nv_bfloat16* embed, const int* anchors, int S, int H, int V, int mask,
+                 int* err, cudaStream_t st) {
+  TraceScope ts(st, "embed", static_cast<double>(S) * 16 * H * 6 + static_cast<double>(S) * 16 * (H / 128) * 4, 0.0);
+  const cudaError_t e =
+      launch_pdl(embed_kernel, dim3(S * 16), dim3(kStatThreads), 0, st, X, ss, embed, anchors, H, V, mask, S * 16, err);
   count_launch();
   return cuda_status(e);
 }
 
-int launch_rmsnorm_rows(__nv_bfloat16* out, const float* x, const __nv_bfloat16* g, int rows, int H, float eps,
-                        int mask_rows_only, cudaStream_t st) {
-  TraceScope ts(st, "rmsnorm", static_cast<double>(rows) * H * 6, 0.0);
-  const cudaError_t e =
-      launch_pdl(rmsnorm_rows_kernel, dim3(rows), dim3(kNormThreads), 0, st, out, x, g, H, eps, mask_rows_only);
+int launch_row_sumsq(float* ss, const float* X, int rows, int H, cudaStream_t st) {
+  TraceScope ts(st, "row_sumsq", static_cast<double>(rows) * H * 4 + static_cast<double>(rows) * (H / 128) * 4, 0.0);
+  const cudaError_t e = launch_pdl(row_sumsq_kernel, dim3(rows), dim3(kStatThreads), 0, st, ss, X, H, rows);
+  count_launch();
+  return cuda_status(e);
+}
+
+int launch_rmsnorm_rows(__nv_bfloat16* out, const float* x, const __nv_bfloat16* g, const float* ss, int ss_ld,
+                        int rows, int H, float eps, int mask_rows_only, cudaStream_t st) {
+  if (H % 8) return DFLASH_E_SHAPE;
+  TraceScope ts(st, "rmsnorm", static_cast<double>(rows) * H * 6 + static_cast<double>(rows) * (H / 128) * 4, 0.0);
+  const dim3 grid((H + kNormThreads * 8 - 1) / (kNormThreads * 8), rows);
+  const cudaError_t e = launch_pdl(rmsnorm_rows_kernel, grid, dim3(kNormThreads), 0, st, out, x, g, ss, ss_ld, H,
+                                   1.0f / static_cast<float>(H), eps, mask_rows_only);
   count_launch();
   return cuda_status(e);
 }
