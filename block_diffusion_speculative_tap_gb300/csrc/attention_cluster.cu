@@ -10,8 +10,7 @@
 // head-major cache with TMA (3-D tensor maps, 128-byte swizzle) through a
 // ring of kStages shared-memory stages; 2G consumer warps (G = query heads
 // of the CTA, two key-tile parities each) compute scores and P*V on the
-// tensor cores (mma.sync m16n8k16, P as a bf16 hi + lo pair) with an online
-// softmax. The two parities of a head merge in shared memory, then the CTAs
+// tensor cores (mma.sync m16n8k16, P in bf16) with an online softmax. The two parities of a head merge in shared memory, then the CTAs
 // of the cluster reduce-scatter their partial (max, sum, output) through
 // distributed shared memory, in rank order, and write the bf16 attention
 // output: no partials in global memory and no second kernel. The split
@@ -62,12 +61,11 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t saddr) 
                : "r"(saddr));
 }
 
-__device__ __forceinline__ void split_hi_lo(float a, float b, uint32_t& hi, uint32_t& lo) {
+// P (probabilities in [0, 1]) enters P*V as bf16; the row sum l uses the
+// unrounded fp32 values.
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // Byte offset of (row, 16-byte chunk) in a 128-byte-swizzled sub-tile.
@@ -192,11 +190,11 @@ __device__ __forceinline__ void attend_tile(AttnState& S, const uint32_t (&qa)[k
   }
 #pragma unroll
   for (int kk = 0; kk < NK / 16; ++kk) {
-    uint32_t ph[4], pl[4];
-    split_hi_lo(sacc[2 * kk][0], sacc[2 * kk][1], ph[0], pl[0]);
-    split_hi_lo(sacc[2 * kk][2], sacc[2 * kk][3], ph[1], pl[1]);
-    split_hi_lo(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1], ph[2], pl[2]);
-    split_hi_lo(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3], ph[3], pl[3]);
+    uint32_t ph[4];
+    ph[0] = pack_bf16(sacc[2 * kk][0], sacc[2 * kk][1]);
+    ph[1] = pack_bf16(sacc[2 * kk][2], sacc[2 * kk][3]);
+    ph[2] = pack_bf16(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
+    ph[3] = pack_bf16(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
     const int mi = lane >> 3;
     const int key = kk * 16 + (mi & 1) * 8 + (lane & 7);
 #pragma unroll
@@ -207,8 +205,6 @@ __device__ __forceinline__ void attend_tile(AttnState& S, const uint32_t (&qa)[k
       ldsm_x4_trans(vb, sub + swz(key, (dim & 63) >> 3));
       mma16816(S.o[2 * n2], ph, vb[0], vb[1]);
       mma16816(S.o[2 * n2 + 1], ph, vb[2], vb[3]);
-      mma16816(S.o[2 * n2], pl, vb[0], vb[1]);
-      mma16816(S.o[2 * n2 + 1], pl, vb[2], vb[3]);
     }
   }
 }

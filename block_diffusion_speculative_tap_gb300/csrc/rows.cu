@@ -101,8 +101,17 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_rows_kernel(__nv_bfloat1
   const int r = blockIdx.y;
   const int src = mask_rows_only ? (r / 15) * 16 + 1 + (r % 15) : r;
   const int i = (blockIdx.x * kNormThreads + threadIdx.x) * 8;  // first feature
+  // the parts load in parallel (lane p holds parts p, p + 32, ...) and are
+  // added in part order through shuffles
+  const int lane = threadIdx.x & 31;
+  const int parts = H / 128;
   float sum = 0.f;
-  for (int p = 0; p * 128 < H; ++p) sum += ss[static_cast<int64_t>(p) * ss_ld + src];
+  for (int p0 = 0; p0 < parts; p0 += 32) {
+    const int p = p0 + lane;
+    const float v = p < parts ? __ldcg(&ss[static_cast<int64_t>(p) * ss_ld + src]) : 0.f;
+    const int n = parts - p0 < 32 ? parts - p0 : 32;
+    for (int q = 0; q < n; ++q) sum += __shfl_sync(0xffffffffu, v, q);
+  }
   const float rstd = rsqrtf(__fmaf_rn(sum, inv_h, eps));
   if (i >= H) return;
   const float4* xr = reinterpret_cast<const float4*>(x + static_cast<int64_t>(src) * H + i);
