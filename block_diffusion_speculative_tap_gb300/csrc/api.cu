@@ -428,6 +428,7 @@ struct FuseWs {
   int* row_pos;
   int* row_end;
   float* y;
+  float* ss;  // [H/128][rows of the pass]: sums of squares of y, published by the fc GEMM
   __nv_bfloat16* fused;
   float* partial;
   size_t bytes;
@@ -507,6 +508,7 @@ size_t fuse_ws_layout(const dflash_handle* h, int rows, void* base, FuseWs* ws) 
   w.row_pos = cv.take<int>(std::max(rows, 1));
   w.row_end = cv.take<int>(std::max(rows, 1));
   w.y = cv.take<float>(static_cast<size_t>(pass) * c.hidden);
+  w.ss = cv.take<float>(static_cast<size_t>(pass) * (c.hidden / kTileM));
   w.fused = cv.take<__nv_bfloat16>(static_cast<size_t>(pass) * c.hidden);
   w.partial = cv.take<float>(partial / sizeof(float) + 1);
   w.bytes = cv.off;
@@ -585,11 +587,13 @@ int dflash_fuse_taps(dflash_handle* h, dflash_state* st, const void* const* plan
       fp.b_ptr[i] = static_cast<const __nv_bfloat16*>(planes[i]) + static_cast<int64_t>(r0) * plane_row_stride;
     fp.ldb = plane_row_stride;
     fp.epi_args.out = w.y;
+    fp.epi_args.ss_out = w.ss;
+    fp.epi_args.ss_ld = n;
     rc = gemm_launch(fp, w.partial, counters, st->status, h->num_sms, s);
     if (rc) return rc;
     counters += gemm_counter_count(fp);
-    rc = launch_hidden_norm(st->ring, w.fused, w.y, h->hidden_norm, w.row_stream + r0, w.row_pos + r0, n, c.hidden,
-                            st->R, c.rms_eps, s);
+    rc = launch_hidden_norm(st->ring, w.fused, w.y, w.ss, h->hidden_norm, w.row_stream + r0, w.row_pos + r0, n,
+                            c.hidden, st->R, c.rms_eps, s);
     if (rc) return rc;
     if (inject) {
       rc = inject_kv(h, st, w.fused, w.row_stream + r0, w.row_pos + r0, w.row_end + r0, n, false, counters,
@@ -663,6 +667,8 @@ struct DraftWs {
   float* part_ml;
   float* partial;
   __nv_bfloat16* logits;
+  float* cand_v;  // LM-head per-tile top-k candidates, [rows][V/128][8]
+  int* cand_i;
 };
 
 int max_nchunk(const dflash_state* st) {
@@ -782,6 +788,9 @@ size_t draft_ws_layout(const dflash_handle* h, const dflash_state* st, int S, bo
   w.part_ml = cv.take<float>(static_cast<size_t>(S) * c.n_q_heads * nch * 16 * 2);
   w.partial = cv.take<float>(partial / sizeof(float) + 1);
   w.logits = need_logits ? cv.take<__nv_bfloat16>(static_cast<size_t>(S) * (DFLASH_BLOCK - 1) * c.vocab) : nullptr;
+  const size_t ncand = static_cast<size_t>(S) * (DFLASH_BLOCK - 1) * (c.vocab / kTileM) * 8;
+  w.cand_v = cv.take<float>(ncand);
+  w.cand_i = cv.take<int>(ncand);
   if (out) *out = w;
   return cv.off;
 }
@@ -926,10 +935,21 @@ int run_head(dflash_handle* h, int* status, int s_count, const float* X, const D
   lp.b_ptr[0] = w.hbuf;
   lp.ldb = c.hidden;
   lp.epi_args.out = logits;
+  // top-k up to 8: the LM head's epilogue ranks each 128-id tile, a small
+  // kernel merges the tiles' lists
+  const bool fused_topk = topk_ids != nullptr && k <= 8;
+  if (fused_topk) {
+    lp.epi_args.cand_k = k;
+    lp.epi_args.cand_v = w.cand_v;
+    lp.epi_args.cand_i = w.cand_i;
+  }
   rc = gemm_launch(lp, w.partial, counters, status, h->num_sms, s);
   if (rc) return rc;
   counters += gemm_counter_count(lp);
-  if (topk_ids) rc = launch_topk(logits, rows, c.vocab, k, 1.0f, nullptr, topk_ids, topk_vals, nullptr, s);
+  if (fused_topk)
+    rc = launch_topk_merge(w.cand_v, w.cand_i, rows, c.vocab / kTileM, k, topk_ids, topk_vals, s);
+  else if (topk_ids)
+    rc = launch_topk(logits, rows, c.vocab, k, 1.0f, nullptr, topk_ids, topk_vals, nullptr, s);
   return rc;
 }
 

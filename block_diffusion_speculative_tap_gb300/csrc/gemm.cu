@@ -45,8 +45,10 @@ struct GemmTraits {
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                                             : kTmemNeed <= 256 ? 256 : 512;
   static constexpr int kBarBytes = 8 * (2 * STAGES + 2 * kAccBufs + 1) + 16;
-  static constexpr int kXchFloats = EPI == EPI_HEADS ? kTileM * 17 : 0;  // rope partner exchange
-  static constexpr int kRedFloats = (EPI == EPI_HEADS || EPI == EPI_RESID) ? 4 * 16 : 0;  // per-warp sums of squares
+  // rope partner exchange (heads) / the chunk's bf16 outputs for candidate ranking (store bf16)
+  static constexpr int kXchFloats = EPI == EPI_HEADS ? kTileM * 17 : EPI == EPI_STORE_BF16 ? 16 * (kTileM + 1) : 0;
+  static constexpr int kRedFloats =
+      (EPI == EPI_HEADS || EPI == EPI_RESID || EPI == EPI_STORE_F32) ? 4 * 16 : 0;  // per-warp sums of squares
   static constexpr int kSmemBytes =
       1024 /*alignment slack*/ + STAGES * kStageBytes + kBarBytes + 4 * (kXchFloats + kRedFloats) + 64;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, BN);
@@ -125,6 +127,20 @@ __device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane, int&
 }
 // v0 (and v1 for the dual GEMM) hold the accumulator of output feature
 // m = m_tile*128 + row for tokens t = n0 + j, j = 0..15.
+// ss_out[m_tile][t] = sum over the tile's 128 rows of sq (per column t of the
+// chunk): warp partials by the transpose reduction, then the 4 warps in order.
+__device__ __forceinline__ void publish_ss(const GemmArgs& a, const float (&sq)[16], int m_tile, int n0, int row,
+                                           int q, int lane, float* red, int nvalid) {
+  int jj;
+  const float w = warp_sum16(sq, lane, jj);
+  if ((lane & 1) == 0) red[q * 16 + jj] = w;
+  named_bar_sync(1, 128);
+  if (row < 16 && row < nvalid && n0 + row < a.N)
+    a.epi.ss_out[static_cast<int64_t>(m_tile) * a.epi.ss_ld + n0 + row] =
+        ((red[row] + red[16 + row]) + red[32 + row]) + red[48 + row];
+  named_bar_sync(1, 128);  // red reusable by the next chunk
+}
+
 template <int EPI>
 __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0, int row, int q, int lane,
                                           const float (&v0)[16], const float (&v1)[16], float* xch, float* red,
@@ -145,29 +161,80 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
         ss[j] = xn * xn;
       }
     }
-    if (a.epi.ss_out) {
-      int jj;
-      const float w = warp_sum16(ss, lane, jj);
-      if ((lane & 1) == 0) red[q * 16 + jj] = w;
-      named_bar_sync(1, 128);
-      if (row < 16 && row < nvalid && n0 + row < a.N)
-        a.epi.ss_out[static_cast<int64_t>(m_tile) * a.epi.ss_ld + n0 + row] =
-            ((red[row] + red[16 + row]) + red[32 + row]) + red[48 + row];
-      named_bar_sync(1, 128);  // red reusable by the next chunk
+    if (a.epi.ss_out) publish_ss(a, ss, m_tile, n0, row, q, lane, red, nvalid);
+  } else if constexpr (EPI == EPI_STORE_F32) {
+    // y = v, and (optionally) the tile's per-column sums of squares of y
+    float ss[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int t = n0 + j;
+      ss[j] = 0.f;
+      if (j < nvalid && t < a.N && m < a.M) {
+        static_cast<float*>(a.epi.out)[static_cast<int64_t>(t) * a.epi.ldo + m] = v0[j];
+        ss[j] = v0[j] * v0[j];
+      }
     }
-  } else if constexpr (EPI == EPI_STORE_F32 || EPI == EPI_STORE_BF16 || EPI == EPI_SWIGLU) {
+    if (a.epi.ss_out) publish_ss(a, ss, m_tile, n0, row, q, lane, red, nvalid);
+  } else if constexpr (EPI == EPI_STORE_BF16) {
+    float y[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int t = n0 + j;
+      const __nv_bfloat16 b = __float2bfloat16_rn(v0[j]);
+      y[j] = __bfloat162float(b);
+      if (j < nvalid && t < a.N && m < a.M) static_cast<__nv_bfloat16*>(a.epi.out)[static_cast<int64_t>(t) * a.epi.ldo + m] = b;
+    }
+    if (a.epi.cand_k > 0) {
+      // per column: the tile's top cand_k rows, one column at a time per warp
+      // (warp q takes columns q, q + 4, ...), lane l holding rows l + 32i
+#pragma unroll
+      for (int j = 0; j < 16; ++j) xch[j * (kTileM + 1) + row] = m < a.M ? y[j] : -INFINITY;
+      named_bar_sync(1, 128);
+      for (int j = q; j < 16; j += 4) {
+        const int t = n0 + j;
+        if (j >= nvalid || t >= a.N) continue;
+        float lv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) lv[i] = xch[j * (kTileM + 1) + lane + 32 * i];
+        uint32_t used = 0;
+        float* cv = a.epi.cand_v + (static_cast<int64_t>(t) * a.m_tiles + m_tile) * a.epi.cand_k;
+        int* ci = a.epi.cand_i + (static_cast<int64_t>(t) * a.m_tiles + m_tile) * a.epi.cand_k;
+        for (int r = 0; r < a.epi.cand_k; ++r) {
+          // lane-local best unused (rows ascend with i, so strict > keeps the lower row)
+          float bv = -INFINITY;
+          int bi = 0x7fffffff;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (!(used >> i & 1u) && (lv[i] > bv || bi == 0x7fffffff)) {
+              bv = lv[i];
+              bi = lane + 32 * i;
+            }
+          }
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (ov > bv || (ov == bv && oi < bi)) {
+              bv = ov;
+              bi = oi;
+            }
+          }
+          if (bi != 0x7fffffff && (bi & 31) == lane) used |= 1u << (bi >> 5);
+          if (lane == 0) {
+            cv[r] = bv;
+            ci[r] = bi == 0x7fffffff ? 0x7fffffff : m_tile * kTileM + bi;
+          }
+        }
+      }
+      named_bar_sync(1, 128);  // xch reusable by the next chunk
+    }
+  } else if constexpr (EPI == EPI_SWIGLU) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int t = n0 + j;
       if (j >= nvalid || t >= a.N) break;
       const int64_t o = static_cast<int64_t>(t) * a.epi.ldo + m;
-      if constexpr (EPI == EPI_STORE_F32) {
-        static_cast<float*>(a.epi.out)[o] = v0[j];
-      } else if constexpr (EPI == EPI_STORE_BF16) {
-        static_cast<__nv_bfloat16*>(a.epi.out)[o] = __float2bfloat16_rn(v0[j]);
-      } else {
-        static_cast<__nv_bfloat16*>(a.epi.out)[o] = __float2bfloat16_rn(silu_f(v0[j]) * v1[j]);
-      }
+      static_cast<__nv_bfloat16*>(a.epi.out)[o] = __float2bfloat16_rn(silu_f(v0[j]) * v1[j]);
     }
   } else {
     // heads: per-head RMSNorm over d (q_norm / k_norm), rotate-half RoPE, bf16

@@ -46,11 +46,17 @@ struct EpiArgs {
                          // slot is written only by the last W positions of a segment
   const float2* rope;    // [pos][d/2] = (cos, sin)
   HeadSeg seg[kMaxASeg];
-  // RESID: per-tile sums of squares of the updated rows,
+  // RESID / STORE_F32: per-tile sums of squares of the written rows,
   // ss_out[m_tile * ss_ld + t] (null: not published), for the RMSNorm that
   // reads the rows next
   float* ss_out;
   int ss_ld;
+  // STORE_BF16: per 128-row tile and output column t, the top cand_k of the
+  // tile's bf16-rounded outputs (larger value first, ties to the lower row):
+  // cand_v / cand_i[(t * m_tiles + m_tile) * cand_k + r]. 0: none.
+  int cand_k;
+  float* cand_v;
+  int* cand_i;
 };
 
 struct GemmArgs {
@@ -116,8 +122,9 @@ int launch_rmsnorm_rows(__nv_bfloat16* out, const float* x, const __nv_bfloat16*
 // (stream, start, rows) per segment, on the host.
 int launch_prep_rows(int* row_stream, int* row_pos, int* row_end, int* lens, int nseg, int rows,
                      const int* seg_info_host_packed, cudaStream_t st);
-int launch_hidden_norm(__nv_bfloat16* ring, __nv_bfloat16* fused_tmp, const float* y, const __nv_bfloat16* g,
-                       const int* row_stream, const int* row_pos, int rows, int H, int R, float eps, cudaStream_t st);
+int launch_hidden_norm(__nv_bfloat16* ring, __nv_bfloat16* fused_tmp, const float* y, const float* ss,
+                       const __nv_bfloat16* g, const int* row_stream, const int* row_pos, int rows, int H, int R,
+                       float eps, cudaStream_t st);
 
 // ---------------------------------------------------------------- attention (attention.cu)
 struct AttnArgs {
@@ -149,6 +156,10 @@ int launch_attention_cluster(const AttnArgs& a, const CUtensorMap& kmap, const C
 size_t attn_partial_floats(int s_count, int nq, int nchunk, int d);
 
 // ---------------------------------------------------------------- selection (select.cu)
+// Row-wise top-k (k <= 8) from per-tile candidate lists written by a GEMM
+// epilogue (EpiArgs::cand_*): rows x tiles lists of k, each sorted.
+int launch_topk_merge(const float* cand_v, const int* cand_i, int rows, int tiles, int k, int* ids, float* vals,
+                      cudaStream_t st);
 int launch_topk(const __nv_bfloat16* logits, int rows, int V, int k, float T, const float* uniforms, int* ids,
                 float* vals, int* sampled, cudaStream_t st);
 int launch_verify_greedy(int S, int V, const int* draft, int dld, const __nv_bfloat16* tl, int* accept, int* out,

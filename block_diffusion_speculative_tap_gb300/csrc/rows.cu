@@ -85,6 +85,22 @@ __global__ void __launch_bounds__(kStatThreads) row_sumsq_kernel(float* __restri
   row_sumsq(ss, ss_ld, t, H, [&](int i) { return x[i]; });
 }
 
+// rstd of row r from its per-128-feature sums of squares ss[p][r]: lane p
+// loads parts p, p + 32, ...; they are added in part order through shuffles.
+__device__ __forceinline__ float parts_rstd(const float* __restrict__ ss, int ss_ld, int r, int H, float inv_h,
+                                            float eps) {
+  const int lane = threadIdx.x & 31;
+  const int parts = H / 128;
+  float sum = 0.f;
+  for (int p0 = 0; p0 < parts; p0 += 32) {
+    const int p = p0 + lane;
+    const float v = p < parts ? __ldcg(&ss[static_cast<int64_t>(p) * ss_ld + r]) : 0.f;
+    const int n = parts - p0 < 32 ? parts - p0 : 32;
+    for (int q = 0; q < n; ++q) sum += __shfl_sync(0xffffffffu, v, q);
+  }
+  return rsqrtf(__fmaf_rn(sum, inv_h, eps));
+}
+
 // out[r] = bf16(x[src] * rstd * g), rstd = 1 / sqrt(sum_p ss[p][src] / H +
 // eps): the row's sum of squares comes as per-128-feature parts published by
 // the kernel that wrote the row (summed here in part order), so the norm is
@@ -101,18 +117,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_rows_kernel(__nv_bfloat1
   const int r = blockIdx.y;
   const int src = mask_rows_only ? (r / 15) * 16 + 1 + (r % 15) : r;
   const int i = (blockIdx.x * kNormThreads + threadIdx.x) * 8;  // first feature
-  // the parts load in parallel (lane p holds parts p, p + 32, ...) and are
-  // added in part order through shuffles
-  const int lane = threadIdx.x & 31;
-  const int parts = H / 128;
-  float sum = 0.f;
-  for (int p0 = 0; p0 < parts; p0 += 32) {
-    const int p = p0 + lane;
-    const float v = p < parts ? __ldcg(&ss[static_cast<int64_t>(p) * ss_ld + src]) : 0.f;
-    const int n = parts - p0 < 32 ? parts - p0 : 32;
-    for (int q = 0; q < n; ++q) sum += __shfl_sync(0xffffffffu, v, q);
-  }
-  const float rstd = rsqrtf(__fmaf_rn(sum, inv_h, eps));
+  const float rstd = parts_rstd(ss, ss_ld, src, H, inv_h, eps);
   if (i >= H) return;
   const float4* xr = reinterpret_cast<const float4*>(x + static_cast<int64_t>(src) * H + i);
   const float4 a = xr[0], b = xr[1];
@@ -130,31 +135,38 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_rows_kernel(__nv_bfloat1
   *reinterpret_cast<uint4*>(out + static_cast<int64_t>(r) * H + i) = o;
 }
 
-// fused = bf16(RMSNorm(y) * hidden_norm): written to the ring slot of the
-// row's (stream, position) and to a dense staging copy for K/V injection.
-__global__ void hidden_norm_kernel(__nv_bfloat16* __restrict__ ring, __nv_bfloat16* __restrict__ fused_tmp,
-                                   const float* __restrict__ y, const __nv_bfloat16* __restrict__ g,
-                                   const int* __restrict__ row_stream, const int* __restrict__ row_pos, int H, int R,
-                                   float eps) {
-  __shared__ float red[32];
+// fused = bf16(RMSNorm(y) * hidden_norm), rstd from the sums of squares the
+// fc GEMM published: written to the ring slot of the row's (stream,
+// position) and to a dense staging copy for K/V injection. Elementwise: a CTA
+// covers 1024 features of one row, 8 a thread.
+__global__ void __launch_bounds__(128) hidden_norm_kernel(__nv_bfloat16* __restrict__ ring,
+                                                          __nv_bfloat16* __restrict__ fused_tmp,
+                                                          const float* __restrict__ y, const float* __restrict__ ss,
+                                                          const __nv_bfloat16* __restrict__ g,
+                                                          const int* __restrict__ row_stream,
+                                                          const int* __restrict__ row_pos, int rows, int H, int R,
+                                                          float inv_h, float eps) {
   pdl_trigger();
   pdl_wait();
-  const int r = blockIdx.x;
-  const float* yr = y + static_cast<int64_t>(r) * H;
-  float ss = 0.f;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) {
-    const float v = yr[i];
-    ss += v * v;
+  const int r = blockIdx.y;
+  const float rstd = parts_rstd(ss, rows, r, H, inv_h, eps);
+  const int i = (blockIdx.x * 128 + threadIdx.x) * 8;
+  if (i >= H) return;
+  const float4* yr = reinterpret_cast<const float4*>(y + static_cast<int64_t>(r) * H + i);
+  const float4 a = yr[0], b = yr[1];
+  const uint4 gr = *reinterpret_cast<const uint4*>(g + i);
+  const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gr);
+  const float xs[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint4 o;
+  uint32_t* o2 = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 gf = __bfloat1622float2(g2[k]);
+    const __nv_bfloat162 v = __floats2bfloat162_rn(xs[2 * k] * rstd * gf.x, xs[2 * k + 1] * rstd * gf.y);
+    o2[k] = *reinterpret_cast<const uint32_t*>(&v);
   }
-  const float tot = block_sum(ss, red);
-  const float rstd = rsqrtf(tot / static_cast<float>(H) + eps);
-  __nv_bfloat16* dr = ring + (static_cast<int64_t>(row_stream[r]) * R + row_pos[r]) * H;
-  __nv_bfloat16* dt = fused_tmp + static_cast<int64_t>(r) * H;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) {
-    const __nv_bfloat16 b = __float2bfloat16_rn(yr[i] * rstd * __bfloat162float(g[i]));
-    dr[i] = b;
-    dt[i] = b;
-  }
+  *reinterpret_cast<uint4*>(ring + (static_cast<int64_t>(row_stream[r]) * R + row_pos[r]) * H + i) = o;
+  *reinterpret_cast<uint4*>(fused_tmp + static_cast<int64_t>(r) * H + i) = o;
 }
 
 struct SegTable {
@@ -214,11 +226,14 @@ int launch_rmsnorm_rows(__nv_bfloat16* out, const float* x, const __nv_bfloat16*
   return cuda_status(e);
 }
 
-int launch_hidden_norm(__nv_bfloat16* ring, __nv_bfloat16* fused_tmp, const float* y, const __nv_bfloat16* g,
-                       const int* row_stream, const int* row_pos, int rows, int H, int R, float eps, cudaStream_t st) {
+int launch_hidden_norm(__nv_bfloat16* ring, __nv_bfloat16* fused_tmp, const float* y, const float* ss,
+                       const __nv_bfloat16* g, const int* row_stream, const int* row_pos, int rows, int H, int R,
+                       float eps, cudaStream_t st) {
+  if (H % 8) return DFLASH_E_SHAPE;
   TraceScope ts(st, "hidden_norm", static_cast<double>(rows) * H * 8, 0.0);
-  const cudaError_t e = launch_pdl(hidden_norm_kernel, dim3(rows), dim3(kRowThreads), 0, st, ring, fused_tmp, y, g,
-                                   row_stream, row_pos, H, R, eps);
+  const dim3 grid((H + 1023) / 1024, rows);
+  const cudaError_t e = launch_pdl(hidden_norm_kernel, grid, dim3(128), 0, st, ring, fused_tmp, y, ss, g, row_stream,
+                                   row_pos, rows, H, R, 1.0f / static_cast<float>(H), eps);
   count_launch();
   return cuda_status(e);
 }

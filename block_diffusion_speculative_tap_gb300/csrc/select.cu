@@ -115,6 +115,85 @@ __device__ __forceinline__ void block_best(float v, int i, float* sv, int* si, f
   __syncthreads();
 }
 
+// Inserts (x, xi) into a thread's sorted list (larger value, then lower id).
+template <int KM>
+__device__ __forceinline__ void list_insert(float (&v)[KM], int (&id)[KM], float x, int xi) {
+  if (!better(x, xi, v[KM - 1], id[KM - 1])) return;
+  v[KM - 1] = x;
+  id[KM - 1] = xi;
+#pragma unroll
+  for (int j = KM - 1; j > 0; --j) {
+    if (better(v[j], id[j], v[j - 1], id[j - 1])) {
+      const float tv = v[j];
+      v[j] = v[j - 1];
+      v[j - 1] = tv;
+      const int ti = id[j];
+      id[j] = id[j - 1];
+      id[j - 1] = ti;
+    }
+  }
+}
+
+// The best of every lane's (v, i) over the warp; all lanes receive it.
+__device__ __forceinline__ void warp_best(float& v, int& i) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, off);
+    if (better(ov, oi, v, i)) {
+      v = ov;
+      i = oi;
+    }
+  }
+}
+
+// Block top-k (k <= KM) from every thread's sorted list, by warp shuffles:
+// each warp takes its own best k in k rounds (the winner pops its head), the
+// 16 warp lists meet in shared memory, and warp 0 merges them in k rounds
+// (lane w walks warp w's list). Thread 0 writes ids / vals[r] for r < k; the
+// block maximum is returned to every thread.
+template <int KM>
+__device__ float block_topk(float (&v)[KM], int (&id)[KM], int k, int* ids, float* vals, float* wv, int* wi) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = 0; r < k; ++r) {
+    float bv = v[0];
+    int bi = id[0];
+    warp_best(bv, bi);
+    if (id[0] == bi) {
+#pragma unroll
+      for (int j = 0; j < KM - 1; ++j) {
+        v[j] = v[j + 1];
+        id[j] = id[j + 1];
+      }
+      v[KM - 1] = -INFINITY;
+      id[KM - 1] = INT_MAX;
+    }
+    if (lane == 0) {
+      wv[w * KM + r] = bv;
+      wi[w * KM + r] = bi;
+    }
+  }
+  __syncthreads();
+  __shared__ float smx;
+  if (w == 0) {
+    int pos = 0;
+    for (int r = 0; r < k; ++r) {
+      float bv = lane < kSelWarps && pos < k ? wv[lane * KM + pos] : -INFINITY;
+      int bi = lane < kSelWarps && pos < k ? wi[lane * KM + pos] : INT_MAX;
+      const int mine = bi;
+      warp_best(bv, bi);
+      if (r == 0 && lane == 0) smx = bv;
+      if (mine == bi && lane < kSelWarps) ++pos;
+      if (lane == 0) {
+        ids[r] = bi;
+        if (vals) vals[r] = bv;
+      }
+    }
+  }
+  __syncthreads();
+  return smx;
+}
+
 // Top-k (k <= KM) of the 8-element groups [g_begin, g_end) of a row into
 // (ids, vals) (thread 0 writes them); also returns the range maximum. The
 // 16 warps split the range into contiguous pieces, lanes interleave inside.
@@ -128,11 +207,32 @@ __device__ float range_topk(const __nv_bfloat16* row, int g_begin, int g_end, in
   const int wg1 = g_begin + static_cast<int>(static_cast<long long>(ng) * (w + 1) / kSelWarps);
   TopList<KM> tl;
   tl.init();
-  for (int g = wg0 + lane; g < wg1; g += 32) {
-    float x[8];
-    load8(row, g, x);
+  // four 16-byte loads in flight before any is ranked
+  for (int g0 = wg0 + lane; g0 < wg1; g0 += 4 * 32) {
+    float x[4][8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) tl.push(x[e], g * 8 + e);
+    for (int u = 0; u < 4; ++u) {
+      const int g = g0 + u * 32;
+      if (g < wg1) {
+        load8(row, g, x[u]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[u][e] = -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int g = g0 + u * 32;
+      if (g < wg1) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) tl.push(x[u][e], g * 8 + e);
+      }
+    }
+  }
+  if (k >= 1 && k <= KM && KM <= 16) {
+    __shared__ float wv[kSelWarps * KM];
+    __shared__ int wi[kSelWarps * KM];
+    return block_topk<KM>(tl.v, tl.i, k, ids, vals, wv, wi);
   }
   float mx = -INFINITY;
   const int rounds = k < 1 ? 1 : k;
@@ -243,6 +343,46 @@ __global__ void __launch_bounds__(kSelThreads) topk_cluster_kernel(const __nv_bf
     }
   }
   cluster_sync_all();  // every slice's shared memory stays alive until rank 0 has read it
+}
+
+// ---------------------------------------------------------------- merge of per-tile candidates
+// Row `blockIdx.x`: `tiles` sorted lists of k (value, id) written by a GEMM
+// epilogue. Thread j keeps the best KM of candidates j, j + 512, ...; then k
+// block-wide rounds pick the winners (larger value, then lower id).
+template <int KM>
+__global__ void __launch_bounds__(kSelThreads) topk_merge_kernel(const float* __restrict__ cand_v,
+                                                                 const int* __restrict__ cand_i, int tiles, int k,
+                                                                 int* __restrict__ ids, float* __restrict__ vals) {
+  pdl_trigger();
+  pdl_wait();
+  const int row = blockIdx.x;
+  const int n = tiles * k;
+  const float* cv = cand_v + static_cast<int64_t>(row) * n;
+  const int* ci = cand_i + static_cast<int64_t>(row) * n;
+  float v[KM];
+  int id[KM];
+#pragma unroll
+  for (int j = 0; j < KM; ++j) {
+    v[j] = -INFINITY;
+    id[j] = INT_MAX;
+  }
+  // eight candidates in flight before any is ranked
+  for (int c0 = threadIdx.x; c0 < n; c0 += 8 * kSelThreads) {
+    float x[8];
+    int xi[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int c = c0 + u * kSelThreads;
+      x[u] = c < n ? __ldcg(cv + c) : -INFINITY;
+      xi[u] = c < n ? __ldcg(ci + c) : INT_MAX;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) list_insert<KM>(v, id, x[u], xi[u]);
+  }
+  __shared__ float wv[kSelWarps * KM];
+  __shared__ int wi[kSelWarps * KM];
+  block_topk<KM>(v, id, k, ids + static_cast<int64_t>(row) * k, vals ? vals + static_cast<int64_t>(row) * k : nullptr,
+                 wv, wi);
 }
 
 template <int KM>
@@ -549,6 +689,17 @@ __global__ void __launch_bounds__(kSelThreads) sample_verify_kernel(int V, const
 }
 
 }  // namespace
+
+int launch_topk_merge(const float* cand_v, const int* cand_i, int rows, int tiles, int k, int* ids, float* vals,
+                      cudaStream_t st) {
+  if (rows <= 0) return DFLASH_OK;
+  if (k < 1 || k > 8) return DFLASH_E_INVALID_ARG;
+  TraceScope ts(st, "topk_merge", static_cast<double>(rows) * tiles * k * 8, 0.0);
+  const cudaError_t e = launch_pdl(topk_merge_kernel<8>, dim3(rows), dim3(kSelThreads), 0, st, cand_v, cand_i, tiles,
+                                   k, ids, vals);
+  count_launch();
+  return cuda_status(e);
+}
 
 int launch_topk(const __nv_bfloat16* logits, int rows, int V, int k, float T, const float* uniforms, int* ids,
                 float* vals, int* sampled, cudaStream_t st) {
