@@ -16,6 +16,10 @@
 // output: no partials in global memory and no second kernel. The split
 // depends only on the stream's visible length, so a stream's result does
 // not depend on the batch.
+#include <mutex>
+#include <utility>
+#include <vector>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -453,17 +457,57 @@ bool attention_cluster_supported(const AttnArgs& a) {
 }
 
 namespace {
-// (kernel, CTAs per kv head) for a query-head group of G
-void pick_cluster_kernel(int G, void (**kern)(ClusterAttnArgs), int* HS, int* GH) {
+// One way to cut a kv head's G query heads over HS clusters of GH heads each.
+struct Split {
+  void (*kern)(ClusterAttnArgs);
+  int GH, HS;
+};
+
+// The splits of a group of G, most parallel first.
+int splits_for(int G, Split* out) {
+  using K = void (*)(ClusterAttnArgs);
+  int n = 0;
+  auto add = [&](K k, int gh) { out[n++] = Split{k, gh, G / gh}; };
   switch (G) {
-    case 1: *kern = attn_cluster_kernel<1, 1>; *HS = 1; break;
-    case 2: *kern = attn_cluster_kernel<1, 2>; *HS = 2; break;
-    case 4: *kern = attn_cluster_kernel<2, 2>; *HS = 2; break;
-    case 5: *kern = attn_cluster_kernel<5, 1>; *HS = 1; break;
-    case 8: *kern = attn_cluster_kernel<4, 2>; *HS = 2; break;
-    default: *kern = nullptr; *HS = 1; break;
+    case 1: add(attn_cluster_kernel<1, 1>, 1); break;
+    case 2: add(attn_cluster_kernel<1, 2>, 1); break;
+    case 4: add(attn_cluster_kernel<1, 4>, 1); add(attn_cluster_kernel<2, 2>, 2); break;
+    case 5: add(attn_cluster_kernel<1, 5>, 1); add(attn_cluster_kernel<5, 1>, 5); break;
+    case 8: add(attn_cluster_kernel<1, 8>, 1); add(attn_cluster_kernel<2, 4>, 2); add(attn_cluster_kernel<4, 2>, 4); break;
+    default: break;
   }
-  *GH = G / *HS;
+  return n;
+}
+
+constexpr int kSmemLaunch = ClusterAttnSmem::kBytes + 1024;
+
+// Clusters of this kernel that can be resident at once on this device
+// (queried once per kernel; 0 if the query fails).
+int resident_clusters(void (*kern)(ClusterAttnArgs), int threads) {
+  static std::mutex mu;
+  static std::vector<std::pair<void (*)(ClusterAttnArgs), int>> memo;
+  std::lock_guard<std::mutex> lk(mu);
+  for (auto& m : memo)
+    if (m.first == kern) return m.second;
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLaunch) == cudaSuccess &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kClusterCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(kClusterCtas, 1, 1);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = kSmemLaunch;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  memo.emplace_back(kern, n);
+  return n;
 }
 }  // namespace
 
@@ -489,20 +533,25 @@ int launch_attention_cluster(const AttnArgs& a, const CUtensorMap& kmap, const C
   int rc = encode_map(&P.kbmap, a.Kb, 2, dims, strides, box);
   if (!rc) rc = encode_map(&P.vbmap, a.Vb, 2, dims, strides, box);
   if (rc) return rc;
+  // the most parallel split whose clusters are all resident at once; the
+  // split only regroups query heads, so every split gives the same results
   const int G = a.nq / a.nkv;
-  const int smem = ClusterAttnSmem::kBytes + 1024;
-  void (*kern)(ClusterAttnArgs) = nullptr;
-  int HS = 1, GH = G;
-  pick_cluster_kernel(G, &kern, &HS, &GH);
-  if (!kern) return DFLASH_E_SHAPE;
-  const int threads = 32 * (2 * GH + 1);
-  static bool configured[9] = {};
-  if (!configured[G]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
-      return DFLASH_E_CUDA;
-    configured[G] = true;
+  Split sp[4];
+  const int ns = splits_for(G, sp);
+  if (ns == 0) return DFLASH_E_SHAPE;
+  int pick = ns - 1;
+  for (int i = 0; i < ns; ++i) {
+    const int cap = resident_clusters(sp[i].kern, 32 * (2 * sp[i].GH + 1));
+    if (cap > 0 && a.nkv * sp[i].HS * s_count <= cap) {
+      pick = i;
+      break;
+    }
   }
+  void (*kern)(ClusterAttnArgs) = sp[pick].kern;
+  const int HS = sp[pick].HS, GH = sp[pick].GH;
+  const int threads = 32 * (2 * GH + 1);
+  if (resident_clusters(kern, threads) == 0) return DFLASH_E_CUDA;  // also sets the smem attributes
+  const int smem = kSmemLaunch;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kClusterCtas;
