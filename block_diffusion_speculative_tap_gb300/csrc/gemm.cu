@@ -141,10 +141,52 @@ __device__ __forceinline__ void publish_ss(const GemmArgs& a, const float (&sq)[
   named_bar_sync(1, 128);  // red reusable by the next chunk
 }
 
+// Heads-epilogue operands of one thread's columns, loaded while the main
+// loop runs (batch-1 cluster launches: one tile a CTA, at most kPre columns
+// a rank): positions, streams, the RoPE (cos, sin) of the thread's feature at
+// each position, and the feature's norm gain.
+constexpr int kPre = 8;
+struct HeadPre {
+  int pos[kPre];
+  int strm[kPre];
+  float2 cs[kPre];
+  float g;
+};
+
+__device__ __forceinline__ void head_pre_load(const GemmArgs& a, int m_tile, int n0, int nvalid, int row,
+                                              HeadPre& pre) {
+  const int sidx = seg_of_tile(a, m_tile);
+  const HeadSeg& sg = a.epi.seg[sidx];
+  const int d = a.epi.head_dim;
+  const int f = (m_tile - a.a_seg_tile[sidx]) * kTileM + row;
+  const int dim = f % d;
+  const int half = d >> 1;
+  const int fi = dim < half ? dim : dim - half;
+  const bool rot = sg.kind != HEAD_V;
+#pragma unroll
+  for (int j = 0; j < kPre; ++j) {
+    const int t = n0 + j;
+    int p = 0, sm = 0;
+    if (j < nvalid && t < a.N) {
+      if (a.epi.pos_mode == 0) {
+        sm = a.epi.s_begin + t / 16;
+        p = a.epi.lens[sm] + (t & 15);
+      } else {
+        sm = a.epi.row_stream[t];
+        p = a.epi.row_pos[t];
+      }
+    }
+    pre.pos[j] = p;
+    pre.strm[j] = sm;
+    pre.cs[j] = rot && j < nvalid && t < a.N ? a.epi.rope[static_cast<int64_t>(p) * half + fi] : make_float2(1.f, 0.f);
+  }
+  pre.g = rot ? __bfloat162float(sg.gain[dim]) : 1.f;
+}
+
 template <int EPI>
 __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0, int row, int q, int lane,
                                           const float (&v0)[16], const float (&v1)[16], float* xch, float* red,
-                                          int nvalid = 16) {
+                                          int nvalid = 16, const HeadPre* pre = nullptr) {
   const int m = m_tile * kTileM + row;
   if constexpr (EPI == EPI_RESID) {
     // X += v, and the tile's per-column sums of squares of the new X
@@ -252,7 +294,12 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
       const int t = n0 + j;
       pos[j] = 0;
       strm[j] = 0;
-      if (j < nvalid && t < a.N) {
+      if (pre != nullptr) {
+        if (j < kPre) {
+          pos[j] = pre->pos[j];
+          strm[j] = pre->strm[j];
+        }
+      } else if (j < nvalid && t < a.N) {
         if (a.epi.pos_mode == 0) {
           strm[j] = a.epi.s_begin + t / 16;
           pos[j] = a.epi.lens[strm[j]] + (t & 15);
@@ -277,7 +324,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
       const int q0 = (q / wph) * wph;
       // d is a power of two, so * (1/d) is exactly / d
       const float inv_d = 1.0f / static_cast<float>(d);
-      const float g = __bfloat162float(sg.gain[dim]);
+      const float g = pre != nullptr ? pre->g : __bfloat162float(sg.gain[dim]);
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         float s = red[q0 * 16 + j];
@@ -293,7 +340,8 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const float yp = xch[prow * 17 + j];
-        const float2 cs = a.epi.rope[static_cast<int64_t>(pos[j]) * half + fi];
+        const float2 cs = pre != nullptr ? (j < kPre ? pre->cs[j] : make_float2(1.f, 0.f))
+                                         : a.epi.rope[static_cast<int64_t>(pos[j]) * half + fi];
         y[j] = dim < half ? (y[j] * cs.x - yp * cs.y) : (y[j] * cs.x + yp * cs.y);
       }
       named_bar_sync(1, 128);  // xch / red reusable by the next chunk
@@ -340,6 +388,8 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   int clu_tile = -1;  // cluster split-K: this CTA's unit, once its partial is parked
+  HeadPre hpre;       // heads epilogue operands, preloaded (cluster launches)
+  bool have_pre = false;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -500,7 +550,17 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
     for (int u = blockIdx.x; u < args.units; u += gridDim.x) {
       int m_tile, kc, n_tile;
       decode_unit<CLU>(args, u, m_tile, kc, n_tile);
-      if constexpr (EPI == EPI_HEADS) {
+      if constexpr (EPI == EPI_HEADS && CLU && BN == 16) {
+        // the epilogue's gain, positions and RoPE values, loaded while the
+        // MMAs run (under a full-rate weight stream they miss L2)
+        const int ks = args.ksplit;
+        const int rk = static_cast<int>(gemm_cluster_rank());
+        const int cb = rk * BN / ks, ce = (rk + 1) * BN / ks;
+        if (ce - cb <= kPre) {
+          head_pre_load(args, m_tile, n_tile * BN + cb, ce - cb, row, hpre);
+          have_pre = true;
+        }
+      } else if constexpr (EPI == EPI_HEADS) {
         // the epilogue's per-head gain and RoPE rows are read once, long after
         // the weight stream has evicted them: pull them into L2 now
         if (args.epi.pos_mode == 0) {
@@ -650,7 +710,8 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
             }
           }
         }
-        epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red, nv);
+        epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red, nv,
+                       have_pre ? &hpre : nullptr);
       }
     }
     __syncwarp();
