@@ -319,7 +319,7 @@ def run_ours(args, rank, world):
         h_acc.copy_(acc, non_blocking=True)
         h_toks.copy_(toks, non_blocking=True)
         h_ids.copy_(ids, non_blocking=True)
-        stream.synchronize()
+        stream.synchronize()  # the next round's anchor depends on this round's result
     e2e_s = time.perf_counter() - t0
     rc, bits = st.status()
     if rc != 0:
@@ -522,7 +522,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=60)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -346,17 +346,26 @@ __global__ void __launch_bounds__(kSelThreads) topk_cluster_kernel(const __nv_bf
 }
 
 // ---------------------------------------------------------------- merge of per-tile candidates
-// Row `blockIdx.x`: `tiles` sorted lists of k (value, id) written by a GEMM
-// epilogue. Thread j keeps the best KM of candidates j, j + 512, ...; then k
-// block-wide rounds pick the winners (larger value, then lower id).
+// Row `blockIdx.y`: `tiles` sorted lists of k (value, id) written by a GEMM
+// epilogue, split over a cluster of kSlices CTAs. Thread j of a CTA keeps the
+// best KM of its slice's candidates j, j + 512, ...; the CTA's top k comes
+// from warp-shuffle rounds (block_topk); rank 0 merges the kSlices sorted
+// lists read through distributed shared memory (larger value, then lower id).
 template <int KM>
 __global__ void __launch_bounds__(kSelThreads) topk_merge_kernel(const float* __restrict__ cand_v,
                                                                  const int* __restrict__ cand_i, int tiles, int k,
                                                                  int* __restrict__ ids, float* __restrict__ vals) {
+  __shared__ int cid[kKMax];
+  __shared__ float cval[kKMax];
+  __shared__ float wv[kSelWarps * KM];
+  __shared__ int wi[kSelWarps * KM];
   pdl_trigger();
   pdl_wait();
-  const int row = blockIdx.x;
+  const int row = blockIdx.y;
+  const uint32_t rank = cluster_rank();
   const int n = tiles * k;
+  const int c_begin = static_cast<int>(static_cast<long long>(n) * rank / kSlices);
+  const int c_end = static_cast<int>(static_cast<long long>(n) * (rank + 1) / kSlices);
   const float* cv = cand_v + static_cast<int64_t>(row) * n;
   const int* ci = cand_i + static_cast<int64_t>(row) * n;
   float v[KM];
@@ -366,23 +375,48 @@ __global__ void __launch_bounds__(kSelThreads) topk_merge_kernel(const float* __
     v[j] = -INFINITY;
     id[j] = INT_MAX;
   }
-  // eight candidates in flight before any is ranked
-  for (int c0 = threadIdx.x; c0 < n; c0 += 8 * kSelThreads) {
-    float x[8];
-    int xi[8];
+  // four candidates in flight before any is ranked
+  for (int c0 = c_begin + static_cast<int>(threadIdx.x); c0 < c_end; c0 += 4 * kSelThreads) {
+    float x[4];
+    int xi[4];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < 4; ++u) {
       const int c = c0 + u * kSelThreads;
-      x[u] = c < n ? __ldcg(cv + c) : -INFINITY;
-      xi[u] = c < n ? __ldcg(ci + c) : INT_MAX;
+      x[u] = c < c_end ? __ldcg(cv + c) : -INFINITY;
+      xi[u] = c < c_end ? __ldcg(ci + c) : INT_MAX;
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) list_insert<KM>(v, id, x[u], xi[u]);
+    for (int u = 0; u < 4; ++u) list_insert<KM>(v, id, x[u], xi[u]);
   }
-  __shared__ float wv[kSelWarps * KM];
-  __shared__ int wi[kSelWarps * KM];
-  block_topk<KM>(v, id, k, ids + static_cast<int64_t>(row) * k, vals ? vals + static_cast<int64_t>(row) * k : nullptr,
-                 wv, wi);
+  block_topk<KM>(v, id, k, cid, cval, wv, wi);
+  cluster_sync_all();
+  if (rank == 0) {
+    __shared__ float gv[kSlices * kKMax];
+    __shared__ int gi[kSlices * kKMax];
+    const int t = threadIdx.x;
+    if (t < kSlices * k) {
+      const int c = t / k, j = t - c * k;
+      gv[c * kKMax + j] = dsmem_ld_f32(dsmem_addr(cval + j, c));
+      gi[c * kKMax + j] = dsmem_ld_s32(dsmem_addr(cid + j, c));
+    }
+    __syncthreads();
+    if (t < 32) {
+      // lane c walks slice c's list; k rounds of a warp arg-max
+      int pos = 0;
+      for (int r = 0; r < k; ++r) {
+        float bv = t < kSlices && pos < k ? gv[t * kKMax + pos] : -INFINITY;
+        int bi = t < kSlices && pos < k ? gi[t * kKMax + pos] : INT_MAX;
+        const int mine = bi;
+        warp_best(bv, bi);
+        if (mine == bi && t < kSlices) ++pos;
+        if (t == 0) {
+          ids[static_cast<int64_t>(row) * k + r] = bi;
+          if (vals) vals[static_cast<int64_t>(row) * k + r] = bv;
+        }
+      }
+    }
+  }
+  cluster_sync_all();  // every slice's shared memory stays alive until rank 0 has read it
 }
 
 template <int KM>
@@ -695,8 +729,20 @@ int launch_topk_merge(const float* cand_v, const int* cand_i, int rows, int tile
   if (rows <= 0) return DFLASH_OK;
   if (k < 1 || k > 8) return DFLASH_E_INVALID_ARG;
   TraceScope ts(st, "topk_merge", static_cast<double>(rows) * tiles * k * 8, 0.0);
-  const cudaError_t e = launch_pdl(topk_merge_kernel<8>, dim3(rows), dim3(kSelThreads), 0, st, cand_v, cand_i, tiles,
-                                   k, ids, vals);
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kSlices;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(kSlices, rows);
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, topk_merge_kernel<8>, cand_v, cand_i, tiles, k, ids, vals);
   count_launch();
   return cuda_status(e);
 }
