@@ -288,6 +288,19 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     A.lib.dflash_trace_enable(0)
     fill_ms = f0.elapsed_time(f1) / nfill
+    # the same fill without K/V injection (fc + hidden_norm + ring only)
+    for _ in range(2):
+        st2.fuse_taps(fill_taps, [(0, 0, fill_rows)], inject=False)
+        st2.truncate(0, 0)
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(nfill):
+        st2.fuse_taps(fill_taps, [(0, 0, fill_rows)], inject=False)
+        st2.truncate(0, 0)
+    g1.record(stream)
+    torch.cuda.synchronize()
+    fill_noinj_ms = g0.elapsed_time(g1) / nfill
     fill_recs = {}
     for i in range(A.lib.dflash_trace_count()):
         nm, t, b, fl = C.c_char_p(), C.c_float(), C.c_double(), C.c_double()
@@ -358,9 +371,11 @@ def run_ours(args, rank, world):
             "settle_steps": settle,
         },
         "fused_tap_rows_per_s": fill_rows / (fill_ms * 1e-3),
+        "fused_tap_rows_per_s_without_kv_injection": fill_rows / (fill_noinj_ms * 1e-3),
         "fill": {
             "rows": fill_rows,
             "ms": fill_ms,
+            "ms_without_kv_injection": fill_noinj_ms,
             "fc_tflops": fc_tflops,
             "fc_frac_of_bf16_peak": (fc_tflops / pk["bf16_tflops"]) if fc_tflops else None,
             "peak_source": src,

@@ -428,7 +428,8 @@ struct FuseWs {
   int* row_pos;
   int* row_end;
   float* y;
-  float* ss;  // [H/128][rows of the pass]: sums of squares of y, published by the fc GEMM
+  float* ss;      // [H/128][rows of the pass]: sums of squares of y, published by the fc GEMM
+  float* kv_raw;  // [rows of the pass][2 * layers of a K/V pass * n_kv * d]: raw K/V of wide fills
   __nv_bfloat16* fused;
   float* partial;
   size_t bytes;
@@ -509,6 +510,10 @@ size_t fuse_ws_layout(const dflash_handle* h, int rows, void* base, FuseWs* ws) 
   w.row_end = cv.take<int>(std::max(rows, 1));
   w.y = cv.take<float>(static_cast<size_t>(pass) * c.hidden);
   w.ss = cv.take<float>(static_cast<size_t>(pass) * (c.hidden / kTileM));
+  w.kv_raw = pass > kDecodeRegimeN
+                 ? cv.take<float>(static_cast<size_t>(pass) * 2 * std::min(c.n_layers, layers_per_kv_pass()) *
+                                  c.n_kv_heads * c.head_dim)
+                 : nullptr;
   w.fused = cv.take<__nv_bfloat16>(static_cast<size_t>(pass) * c.hidden);
   w.partial = cv.take<float>(partial / sizeof(float) + 1);
   w.bytes = cv.off;
@@ -517,22 +522,53 @@ size_t fuse_ws_layout(const dflash_handle* h, int rows, void* base, FuseWs* ws) 
 }
 
 // K/V injection for `rows` fused rows already in `fused` (rows tables in ws).
+// Up to kDecodeRegimeN rows the GEMM's epilogue applies k_norm, RoPE and the
+// cache scatter; wider passes (no split-K, many tiles a CTA) write the raw
+// projections to kv_raw and an elementwise kernel does that work with the
+// whole GPU, with the same arithmetic.
 int inject_kv(dflash_handle* h, dflash_state* st, const __nv_bfloat16* fused, const int* row_stream,
               const int* row_pos, const int* row_end, int rows, bool sliding_only, int*& counters, float* partial,
-              cudaStream_t s) {
+              float* kv_raw, cudaStream_t s) {
   const dflash_config& c = h->cfg;
   for (int l0 = 0; l0 < c.n_layers; l0 += layers_per_kv_pass()) {
     GemmPlan kp = kv_plan(h, st, rows, l0, std::min(c.n_layers, l0 + layers_per_kv_pass()), sliding_only);
     if (kp.n_aseg == 0) continue;
     kp.b_ptr[0] = fused;
     kp.ldb = c.hidden;
-    kp.epi_args.row_stream = row_stream;
-    kp.epi_args.row_pos = row_pos;
-    kp.epi_args.row_end = row_end;
-    kp.epi_args.rope = st->rope;
-    const int rc = gemm_launch(kp, partial, counters, st->status, h->num_sms, s);
+    const bool split = kv_raw != nullptr && rows > kDecodeRegimeN;
+    KvSegs segs{};
+    if (split) {
+      segs.n = kp.n_aseg;
+      int64_t col = 0;
+      segs.head0[0] = 0;
+      for (int i = 0; i < kp.n_aseg; ++i) {
+        const HeadSeg& sg = kp.epi_args.seg[i];
+        segs.col0[i] = col;
+        segs.heads[i] = sg.heads;
+        segs.cap[i] = sg.cap;
+        segs.window[i] = sg.window;
+        segs.gain[i] = sg.kind == HEAD_V ? nullptr : sg.gain;
+        segs.dst[i] = sg.dst;
+        segs.head0[i + 1] = segs.head0[i] + sg.heads;
+        col += kp.a_rows[i];
+      }
+      kp.epi = EPI_STORE_F32;
+      kp.epi_args.out = kv_raw;
+      kp.epi_args.ldo = kp.M;
+      kp.name = "gemm.kv_inject";
+    } else {
+      kp.epi_args.row_stream = row_stream;
+      kp.epi_args.row_pos = row_pos;
+      kp.epi_args.row_end = row_end;
+      kp.epi_args.rope = st->rope;
+    }
+    int rc = gemm_launch(kp, partial, counters, st->status, h->num_sms, s);
     if (rc) return rc;
     counters += gemm_counter_count(kp);
+    if (split) {
+      rc = launch_kv_rows(kv_raw, kp.M, segs, row_stream, row_pos, row_end, st->rope, c.head_dim, c.rms_eps, rows, s);
+      if (rc) return rc;
+    }
   }
   return DFLASH_OK;
 }
@@ -597,7 +633,7 @@ int dflash_fuse_taps(dflash_handle* h, dflash_state* st, const void* const* plan
     if (rc) return rc;
     if (inject) {
       rc = inject_kv(h, st, w.fused, w.row_stream + r0, w.row_pos + r0, w.row_end + r0, n, false, counters,
-                     w.partial, s);
+                     w.partial, w.kv_raw, s);
       if (rc) return rc;
     }
   }
@@ -639,7 +675,7 @@ int dflash_state_truncate(dflash_handle* h, dflash_state* st, int s_id, int64_t 
       const int m = std::min(kFusePass, n - r0);
       const __nv_bfloat16* rows = st->ring + (static_cast<int64_t>(s_id) * st->R + lo + r0) * c.hidden;
       rc = inject_kv(h, st, rows, w.row_stream + r0, w.row_pos + r0, w.row_end + r0, m, true, counters,
-                     w.partial, s);
+                     w.partial, w.kv_raw, s);
       if (rc) return rc;
     }
   }

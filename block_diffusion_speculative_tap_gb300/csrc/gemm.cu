@@ -49,8 +49,9 @@ struct GemmTraits {
   static constexpr int kXchFloats = EPI == EPI_HEADS ? kTileM * 17 : EPI == EPI_STORE_BF16 ? 16 * (kTileM + 1) : 0;
   static constexpr int kRedFloats =
       (EPI == EPI_HEADS || EPI == EPI_RESID || EPI == EPI_STORE_F32) ? 4 * 16 : 0;  // per-warp sums of squares
+  static constexpr int kMetaInts = EPI == EPI_HEADS ? 4 * BN : 0;  // per-token (pos, stream, segment end)
   static constexpr int kSmemBytes =
-      1024 /*alignment slack*/ + STAGES * kStageBytes + kBarBytes + 4 * (kXchFloats + kRedFloats) + 64;
+      1024 /*alignment slack*/ + STAGES * kStageBytes + kBarBytes + 4 * (kXchFloats + kRedFloats + kMetaInts) + 64;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, BN);
   // cluster split-K parks each CTA's fp32 partial in its (idle) stage memory
   static constexpr bool kClusterFits = kAcc * BN * kTileM * 4 <= STAGES * kStageBytes;
@@ -183,10 +184,38 @@ __device__ __forceinline__ void head_pre_load(const GemmArgs& a, int m_tile, int
   pre.g = rot ? __bfloat162float(sg.gain[dim]) : 1.f;
 }
 
-template <int EPI>
+// Heads epilogue of a whole tile (row-table mode or block mode): the
+// position, stream and segment end of its n tokens go to shared memory once,
+// meta[4 * c + {0, 1, 2}], instead of being loaded per chunk by every thread.
+__device__ __forceinline__ void stage_token_meta(const GemmArgs& a, int t0, int n, int row, int* meta) {
+  named_bar_sync(1, 128);  // the previous tile's chunks are done with meta
+  for (int c = row; c < n; c += 128) {
+    const int t = t0 + c;
+    int p = 0, sm = 0, e = 0;
+    if (t < a.N) {
+      if (a.epi.pos_mode == 0) {
+        sm = a.epi.s_begin + t / 16;
+        p = a.epi.lens[sm] + (t & 15);
+      } else {
+        sm = a.epi.row_stream[t];
+        p = a.epi.row_pos[t];
+        e = a.epi.row_end[t];
+      }
+    }
+    meta[4 * c] = p;
+    meta[4 * c + 1] = sm;
+    meta[4 * c + 2] = e;
+  }
+  named_bar_sync(1, 128);
+}
+
+// HOIST (wide tiles, whose kernels have the registers): the heads epilogue
+// issues its RoPE and gain loads before the reductions that precede their use.
+template <int EPI, bool HOIST = false>
 __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0, int row, int q, int lane,
                                           const float (&v0)[16], const float (&v1)[16], float* xch, float* red,
-                                          int nvalid = 16, const HeadPre* pre = nullptr) {
+                                          int nvalid = 16, const HeadPre* pre = nullptr,
+                                          const int* tmeta = nullptr) {
   const int m = m_tile * kTileM + row;
   if constexpr (EPI == EPI_RESID) {
     // X += v, and the tile's per-column sums of squares of the new X
@@ -299,6 +328,11 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
           pos[j] = pre->pos[j];
           strm[j] = pre->strm[j];
         }
+      } else if (tmeta != nullptr) {
+        if (j < nvalid && t < a.N) {
+          pos[j] = tmeta[4 * j];
+          strm[j] = tmeta[4 * j + 1];
+        }
       } else if (j < nvalid && t < a.N) {
         if (a.epi.pos_mode == 0) {
           strm[j] = a.epi.s_begin + t / 16;
@@ -310,6 +344,21 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
       }
     }
     float y[16];
+    const int fi = dim < half ? dim : dim - half;
+    // RoPE values and the norm gain, issued before the reductions they wait for
+    float2 csv[HOIST ? 16 : 1];
+    float gval = 1.f;
+    if constexpr (HOIST) {
+      if (sg.kind != HEAD_V) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int t = n0 + j;
+          csv[j] = (j < nvalid && t < a.N) ? a.epi.rope[static_cast<int64_t>(pos[j]) * half + fi]
+                                           : make_float2(1.f, 0.f);
+        }
+        gval = __bfloat162float(sg.gain[dim]);
+      }
+    }
     if (sg.kind != HEAD_V) {
       // per-head sums of squares: warp partials (transpose reduction), then
       // the head's warps in order
@@ -324,25 +373,28 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
       const int q0 = (q / wph) * wph;
       // d is a power of two, so * (1/d) is exactly / d
       const float inv_d = 1.0f / static_cast<float>(d);
-      const float g = pre != nullptr ? pre->g : __bfloat162float(sg.gain[dim]);
+      const float g = HOIST ? gval : (pre != nullptr ? pre->g : __bfloat162float(sg.gain[dim]));
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         float s = red[q0 * 16 + j];
         for (int qq = 1; qq < wph; ++qq) s += red[(q0 + qq) * 16 + j];
-        y[j] = v0[j] * rsqrtf(s * inv_d + a.epi.eps) * g;
+        y[j] = head_norm_apply(v0[j], head_norm_scale(s, inv_d, a.epi.eps), g);
       }
       // partner value (dim +- d/2) via shared memory
 #pragma unroll
       for (int j = 0; j < 16; ++j) xch[row * 17 + j] = y[j];
       named_bar_sync(1, 128);
       const int prow = dim < half ? row + half : row - half;
-      const int fi = dim < half ? dim : dim - half;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const float yp = xch[prow * 17 + j];
-        const float2 cs = pre != nullptr ? (j < kPre ? pre->cs[j] : make_float2(1.f, 0.f))
-                                         : a.epi.rope[static_cast<int64_t>(pos[j]) * half + fi];
-        y[j] = dim < half ? (y[j] * cs.x - yp * cs.y) : (y[j] * cs.x + yp * cs.y);
+        float2 cs;
+        if constexpr (HOIST)
+          cs = csv[j];
+        else
+          cs = pre != nullptr ? (j < kPre ? pre->cs[j] : make_float2(1.f, 0.f))
+                              : a.epi.rope[static_cast<int64_t>(pos[j]) * half + fi];
+        y[j] = rope_rotate(y[j], yp, cs, dim < half);
       }
       named_bar_sync(1, 128);  // xch / red reusable by the next chunk
     } else {
@@ -358,7 +410,8 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
         o = static_cast<int64_t>(t) * (sg.heads * d) + f;
       } else {
         // a later row of the same segment owns this ring slot
-        if (sg.window > 0 && pos[j] < a.epi.row_end[t] - sg.window) continue;
+        const int rend = tmeta != nullptr ? tmeta[4 * j + 2] : a.epi.row_end[t];
+        if (sg.window > 0 && pos[j] < rend - sg.window) continue;
         const int slot = sg.window > 0 ? (pos[j] % sg.window) : pos[j];
         o = ((static_cast<int64_t>(strm[j]) * sg.heads + head) * sg.cap + slot) * d + dim;
       }
@@ -384,6 +437,7 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
   volatile int* last_word = abort_word + 1;
   float* xch = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + Tr::kBarBytes);
   float* red = xch + Tr::kXchFloats;
+  int* tmeta = reinterpret_cast<int*>(red + Tr::kRedFloats);  // heads: the tile's token metadata
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -602,10 +656,16 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
         mbar_arrive(&tempty[acc]);
         clu_tile = u;  // reduced after the cluster barrier below
       } else if (args.ksplit == 1) {
+        const int* meta = nullptr;
+        if constexpr (EPI == EPI_HEADS) {
+          stage_token_meta(args, n_tile * BN, BN, row, tmeta);
+          meta = tmeta;
+        }
         for (int c0 = 0; c0 < BN; c0 += 16) {
           tmem_ld16(tbase + c0, v0);
           if constexpr (DUAL) tmem_ld16(tbase + BN + c0, v1);
-          epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red);
+          epi_chunk<EPI, (BN > 16)>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red, 16, nullptr,
+                                    meta ? meta + 4 * c0 : nullptr);
         }
         tc_fence_before();
         mbar_arrive(&tempty[acc]);

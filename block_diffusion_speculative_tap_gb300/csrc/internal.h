@@ -122,6 +122,22 @@ int launch_rmsnorm_rows(__nv_bfloat16* out, const float* x, const __nv_bfloat16*
 // (stream, start, rows) per segment, on the host.
 int launch_prep_rows(int* row_stream, int* row_pos, int* row_end, int* lens, int nseg, int rows,
                      const int* seg_info_host_packed, cudaStream_t st);
+// Segments of a wide K/V-injection pass for kv_rows: segment s covers heads
+// [head0[s], head0[s+1]) of the pass and columns [col0[s], ...) of the raw
+// projection rows; gain null for V.
+struct KvSegs {
+  int n;
+  int head0[kMaxASeg + 1];
+  int64_t col0[kMaxASeg];
+  int heads[kMaxASeg];
+  int cap[kMaxASeg];
+  int window[kMaxASeg];
+  const __nv_bfloat16* gain[kMaxASeg];
+  __nv_bfloat16* dst[kMaxASeg];
+};
+// k_norm + RoPE + cache scatter of raw K/V projections y [rows][ld] fp32.
+int launch_kv_rows(const float* y, int64_t ld, const KvSegs& segs, const int* row_stream, const int* row_pos,
+                   const int* row_end, const float2* rope, int d, float eps, int rows, cudaStream_t st);
 int launch_hidden_norm(__nv_bfloat16* ring, __nv_bfloat16* fused_tmp, const float* y, const float* ss,
                        const __nv_bfloat16* g, const int* row_stream, const int* row_pos, int rows, int H, int R,
                        float eps, cudaStream_t st);

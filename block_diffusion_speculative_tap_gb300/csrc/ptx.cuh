@@ -190,6 +190,16 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 // kernel of the chain) writes. pdl_trigger() lets the successor launch once
 // every CTA of this grid has issued it. Both are no-ops without the launch
 // attribute.
+// Per-head RMSNorm and rotate-half RoPE with every rounding spelled out, so
+// the GEMM epilogue and the standalone K/V kernel give identical bits.
+__device__ __forceinline__ float head_norm_scale(float sumsq, float inv_d, float eps) {
+  return rsqrtf(__fmaf_rn(sumsq, inv_d, eps));
+}
+__device__ __forceinline__ float head_norm_apply(float v, float rs, float g) { return __fmul_rn(__fmul_rn(v, rs), g); }
+__device__ __forceinline__ float rope_rotate(float y, float yp, float2 cs, bool low) {
+  return low ? __fmaf_rn(y, cs.x, -__fmul_rn(yp, cs.y)) : __fmaf_rn(y, cs.x, __fmul_rn(yp, cs.y));
+}
+
 // Hint: bring the 128-byte line holding p into L2.
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));

@@ -169,6 +169,81 @@ __global__ void __launch_bounds__(128) hidden_norm_kernel(__nv_bfloat16* __restr
   *reinterpret_cast<uint4*>(fused_tmp + static_cast<int64_t>(r) * H + i) = o;
 }
 
+// K/V injection of wide fills, second half: the GEMM left the raw
+// projections y [rows][ld] (fp32, all segments side by side); one warp per
+// (row, head) applies k_norm (K segments: per-head RMSNorm over d, gain) and
+// rotate-half RoPE at the row's position, and stores bf16 to the head's cache
+// slot. Lane l holds features q*32 + l, q < d/32; the sum of squares of a
+// head is a xor tree per q and then the q's in order, the same arithmetic
+// as the fused epilogue, so both give the same bits.
+__global__ void __launch_bounds__(256) kv_rows_kernel(const float* __restrict__ y, int64_t ld, const KvSegs segs,
+                                                      const int* __restrict__ row_stream,
+                                                      const int* __restrict__ row_pos,
+                                                      const int* __restrict__ row_end,
+                                                      const float2* __restrict__ rope, int d, float eps, int rows) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x;
+  const int hh = blockIdx.y * 8 + (threadIdx.x >> 5);  // head over all segments
+  if (r >= rows || hh >= segs.head0[segs.n]) return;
+  int s = 0;
+  while (s + 1 < segs.n && hh >= segs.head0[s + 1]) ++s;
+  const int head = hh - segs.head0[s];
+  const int pos = row_pos[r];
+  const int window = segs.window[s];
+  if (window > 0 && pos < row_end[r] - window) return;  // a later row of the segment owns this ring slot
+  const int nq = d >> 5;
+  const float* src = y + static_cast<int64_t>(r) * ld + segs.col0[s] + static_cast<int64_t>(head) * d;
+  float v[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) v[q] = q < nq ? src[q * 32 + lane] : 0.f;
+  if (segs.gain[s] != nullptr) {
+    float tot = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (q < nq) {
+        float t = v[q] * v[q];
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+        tot = q == 0 ? t : tot + t;
+      }
+    }
+    const float inv_d = 1.0f / static_cast<float>(d);  // d is a power of two: exact
+    const float rs = head_norm_scale(tot, inv_d, eps);
+    const int half = d >> 1;
+    float yv[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (q < nq) {
+        const int dim = q * 32 + lane;
+        yv[q] = head_norm_apply(v[q], rs, __bfloat162float(segs.gain[s][dim]));
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (q < nq) {
+        const int dim = q * 32 + lane;
+        const int fi = dim < half ? dim : dim - half;
+        // the partner feature dim +- d/2: another q of this lane, or lane ^ 16 when d = 32
+        float yp;
+        if (nq == 1)
+          yp = __shfl_xor_sync(0xffffffffu, yv[0], 16);
+        else
+          yp = yv[q ^ (nq >> 1)];
+        const float2 cs = rope[static_cast<int64_t>(pos) * half + fi];
+        v[q] = rope_rotate(yv[q], yp, cs, dim < half);
+      }
+    }
+  }
+  const int slot = window > 0 ? pos % window : pos;
+  __nv_bfloat16* dst =
+      segs.dst[s] + ((static_cast<int64_t>(row_stream[r]) * segs.heads[s] + head) * segs.cap[s] + slot) * d;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (q < nq) dst[q * 32 + lane] = __float2bfloat16_rn(v[q]);
+}
+
 struct SegTable {
   int n;
   int stream[256];
@@ -222,6 +297,18 @@ int launch_rmsnorm_rows(__nv_bfloat16* out, const float* x, const __nv_bfloat16*
   const dim3 grid((H + kNormThreads * 8 - 1) / (kNormThreads * 8), rows);
   const cudaError_t e = launch_pdl(rmsnorm_rows_kernel, grid, dim3(kNormThreads), 0, st, out, x, g, ss, ss_ld, H,
                                    1.0f / static_cast<float>(H), eps, mask_rows_only);
+  count_launch();
+  return cuda_status(e);
+}
+
+int launch_kv_rows(const float* y, int64_t ld, const KvSegs& segs, const int* row_stream, const int* row_pos,
+                   const int* row_end, const float2* rope, int d, float eps, int rows, cudaStream_t st) {
+  if (rows <= 0) return DFLASH_OK;
+  if (d != 32 && d != 64 && d != 128) return DFLASH_E_SHAPE;
+  const int heads = segs.head0[segs.n];
+  TraceScope ts(st, "kv_rows", static_cast<double>(rows) * heads * d * 6.0, 0.0);
+  const cudaError_t e = launch_pdl(kv_rows_kernel, dim3(rows, (heads + 7) / 8), dim3(256), 0, st, y, ld, segs,
+                                   row_stream, row_pos, row_end, rope, d, eps, rows);
   count_launch();
   return cuda_status(e);
 }
