@@ -86,6 +86,8 @@ __all__ = [
     "argmax_lowest",
     "greedy_verify",
     "softmax_t",
+    "draft_confidence",
+    "draft_stop",
     "inverse_cdf",
     "sample_rows",
     "sampling_verify",
@@ -410,6 +412,35 @@ def softmax_t(row, T):
     z = z - z.max()
     e = np.exp(z)
     return e / e.sum()
+
+
+def draft_confidence(logits, T):
+    """The drafter's confidence at each mask row: the top-1 probability of
+    softmax(row / T).
+
+    Strata pull request #3457, "Problem and result": `--spec-min-p` stops a
+    draft where the confidence falls below it. Reading (the v1 body has no
+    selector): a position's confidence is the largest entry of the drafter's
+    softmax at that position. logits: [rows, V]; returns float64 [rows].
+    """
+    return np.asarray([softmax_t(r, T).max() for r in np.asarray(logits, dtype=np.float64)])
+
+
+def draft_stop(conf, min_p):
+    """Drafted tokens to send to verification, per stream: the number of
+    leading positions whose confidence is at least min_p (the draft stops at
+    the first position below it; Strata #3457, "Problem and result").
+
+    conf: [S, 15]; returns int64 [S] in [0, 15].
+    """
+    conf = np.asarray(conf, dtype=np.float64).reshape(-1, BLOCK - 1)
+    out = []
+    for row in conf:
+        n = 0
+        while n < BLOCK - 1 and row[n] >= min_p:
+            n += 1
+        out.append(n)
+    return np.asarray(out, dtype=np.int64)
 
 
 def inverse_cdf(wts, u):

@@ -472,3 +472,41 @@ def test_refusals():
     assert O.validate_config(bad) == "causal"
     for name in SI.presets():
         assert O.validate_config(SI.presets()[name]["model"]) is None
+
+
+# ---------------------------------------------------------------- min-p stop
+def test_draft_confidence_closed_forms():
+    """Confidence = top-1 softmax probability (Strata #3457 "Problem and
+    result", reading in the oracle): equal logits give 1/V; one logit a over
+    V-1 logits b give 1 / (1 + (V-1) e^((b-a)/T)); two tied maxima split it."""
+    V = 1000
+    c = O.draft_confidence(np.zeros((1, V)), 1.0)
+    assert abs(c[0] - 1.0 / V) < 1e-15
+    V, a, b, T = 100, 2.0, 0.5, 0.7
+    row = np.full(V, b)
+    row[37] = a
+    want = 1.0 / (1.0 + (V - 1) * np.exp((b - a) / T))
+    got = O.draft_confidence(row[None, :], T)[0]
+    assert abs(got - want) < 1e-14 * want
+    row[80] = a  # two maxima
+    want2 = 1.0 / (2.0 + (V - 2) * np.exp((b - a) / T))
+    assert abs(O.draft_confidence(row[None, :], T)[0] - want2) < 1e-14 * want2
+    # a hotter softmax is less confident, a colder one more
+    rng = np.random.default_rng(3)
+    rows = rng.normal(size=(5, 50))
+    c1, c2, c3 = (O.draft_confidence(rows, t) for t in (0.5, 1.0, 2.0))
+    assert np.all(c1 > c2) and np.all(c2 > c3)
+
+
+def test_draft_stop_rule():
+    """The draft stops at the first position whose confidence is below min-p
+    (equality keeps drafting); the length is in [0, 15]."""
+    conf = np.full((4, 15), 0.9)
+    conf[1, 2] = 0.6
+    conf[1, 5] = 0.1  # after the stop: irrelevant
+    conf[2, 0] = 0.69
+    conf[3, :] = 0.7
+    conf[3, 14] = 0.2
+    assert O.draft_stop(conf, 0.7).tolist() == [15, 2, 0, 14]
+    assert O.draft_stop(conf, 0.0).tolist() == [15, 15, 15, 15]
+    assert O.draft_stop(conf, 1.0).tolist() == [0, 0, 0, 0]
