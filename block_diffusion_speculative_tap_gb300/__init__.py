@@ -11,6 +11,7 @@ from .drafter import (  # noqa: F401
     Drafter,
     State,
     config_validate,
+    draft_stop,
     fused_row_bytes,
     kind,
     launch_count,

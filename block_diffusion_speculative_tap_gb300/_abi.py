@@ -132,6 +132,7 @@ def _load():
     fn("dflash_draft_stages", C.c_int, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, vp, vp, sz, vp)
     fn("dflash_draft_head", C.c_int, vp, vp, C.c_int, vp, vp, vp, vp, C.c_int, vp, sz, vp)
     fn("dflash_topk", C.c_int, vp, C.c_int, C.c_int, C.c_int, C.c_float, vp, vp, vp, vp, vp)
+    fn("dflash_draft_stop", C.c_int, vp, C.c_int, C.c_int, C.c_float, C.c_float, vp, vp, vp)
     fn("dflash_verify_workspace_bytes", C.c_int, C.c_int, C.c_int, C.c_int, P(sz))
     fn("dflash_verify", C.c_int, C.c_int, C.c_int, C.c_int, vp, C.c_int, vp, vp, vp, C.c_float, vp, vp, vp, sz, vp)
     fn("dflash_verify_sample_noalloc", C.c_int, C.c_int, C.c_int, vp, C.c_int, vp, vp, vp, C.c_float, vp, vp, vp)
@@ -167,6 +168,7 @@ EXPORTED = [
     "dflash_draft_stages",
     "dflash_draft_head",
     "dflash_topk",
+    "dflash_draft_stop",
     "dflash_verify_workspace_bytes",
     "dflash_verify",
     "dflash_verify_sample_noalloc",

@@ -1069,6 +1069,16 @@ int dflash_topk(const void* logits, int rows, int vocab, int k, float temperatur
                      uniforms, ids, vals, sampled, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int dflash_draft_stop(const void* logits, int streams, int vocab, float temperature, float min_p, float* conf,
+                      int32_t* draft_len, dflash_stream_t stream) {
+  if (streams < 0 || vocab < 8 || vocab % 8) return DFLASH_E_INVALID_ARG;
+  if (streams == 0) return DFLASH_OK;
+  if (!logits || !conf || !draft_len || !aligned16(logits)) return DFLASH_E_INVALID_ARG;
+  if (!(temperature > 0.f) || !(min_p >= 0.f && min_p <= 1.f)) return DFLASH_E_INVALID_ARG;
+  return launch_draft_stop(static_cast<const __nv_bfloat16*>(logits), streams, vocab, temperature, min_p, conf,
+                           draft_len, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int dflash_verify_workspace_bytes(int mode, int streams, int vocab, size_t* bytes) {
   if (!bytes || streams < 0 || vocab < 8) return DFLASH_E_INVALID_ARG;
   if (mode == DFLASH_VERIFY_GREEDY) *bytes = 0;

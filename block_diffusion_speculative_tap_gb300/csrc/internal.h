@@ -174,6 +174,10 @@ size_t attn_partial_floats(int s_count, int nq, int nchunk, int d);
 // ---------------------------------------------------------------- selection (select.cu)
 // Row-wise top-k (k <= 8) from per-tile candidate lists written by a GEMM
 // epilogue (EpiArgs::cand_*): rows x tiles lists of k, each sorted.
+// Per row of [streams * 15, V] bf16 logits the top-1 softmax probability at
+// temperature T (conf), and per stream the leading rows with conf >= min_p.
+int launch_draft_stop(const __nv_bfloat16* logits, int streams, int V, float T, float min_p, float* conf, int* len,
+                      cudaStream_t st);
 int launch_topk_merge(const float* cand_v, const int* cand_i, int rows, int tiles, int k, int* ids, float* vals,
                       cudaStream_t st);
 int launch_topk(const __nv_bfloat16* logits, int rows, int V, int k, float T, const float* uniforms, int* ids,

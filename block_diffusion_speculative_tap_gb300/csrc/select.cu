@@ -724,6 +724,102 @@ __global__ void __launch_bounds__(kSelThreads) sample_verify_kernel(int V, const
 
 }  // namespace
 
+// ---------------------------------------------------------------- confidence and min-p stop
+// conf[r] = the largest entry of softmax(row r / T) = 1 / sum_j exp((x_j - max) / T):
+// one CTA a row, one pass; every thread keeps a running (max, sum) over its
+// 8-element groups, the pairs merge by a xor tree in each warp and then over
+// the warps in order (the element equal to the final max contributes 1).
+__device__ __forceinline__ void ms_merge(float& m, float& s, float m2, float s2, float invT) {
+  const float mm = fmaxf(m, m2);
+  const float a = m == -INFINITY ? 0.f : s * expf((m - mm) * invT);
+  const float b = m2 == -INFINITY ? 0.f : s2 * expf((m2 - mm) * invT);
+  m = mm;
+  s = a + b;
+}
+
+__global__ void __launch_bounds__(kSelThreads) conf_kernel(const __nv_bfloat16* __restrict__ logits, int V,
+                                                           float invT, float* __restrict__ conf) {
+  __shared__ float wm[kSelWarps], ws[kSelWarps];
+  pdl_trigger();
+  pdl_wait();
+  const int r = blockIdx.x;
+  const __nv_bfloat16* row = logits + static_cast<int64_t>(r) * V;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Slice sl = warp_slice(V, w);
+  float m = -INFINITY, sm = 0.f;
+  for (int g0 = sl.g0 + lane; g0 < sl.g1; g0 += 4 * 32) {
+    float x[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int g = g0 + u * 32;
+      if (g < sl.g1) {
+        load8(row, g, x[u]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[u][e] = -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float gm = x[u][0];
+#pragma unroll
+      for (int e = 1; e < 8; ++e) gm = fmaxf(gm, x[u][e]);
+      if (gm == -INFINITY) continue;
+      float gs = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) gs += expf((x[u][e] - gm) * invT);
+      ms_merge(m, sm, gm, gs, invT);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+    const float s2 = __shfl_xor_sync(0xffffffffu, sm, off);
+    ms_merge(m, sm, m2, s2, invT);
+  }
+  if (lane == 0) {
+    wm[w] = m;
+    ws[w] = sm;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float M = wm[0], S = ws[0];
+    for (int j = 1; j < kSelWarps; ++j) ms_merge(M, S, wm[j], ws[j], invT);
+    conf[r] = 1.f / S;
+  }
+}
+
+// len[s] = the number of leading rows of stream s (15 a stream) whose
+// confidence is at least min_p.
+__global__ void stop_len_kernel(const float* __restrict__ conf, int S, float min_p, int* __restrict__ len) {
+  pdl_trigger();
+  pdl_wait();
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= S) return;
+  int n = 0;
+  while (n < 15 && conf[s * 15 + n] >= min_p) ++n;
+  len[s] = n;
+}
+
+int launch_draft_stop(const __nv_bfloat16* logits, int streams, int V, float T, float min_p, float* conf, int* len,
+                      cudaStream_t st) {
+  if (streams <= 0) return DFLASH_OK;
+  {
+    TraceScope ts(st, "draft_stop.conf", static_cast<double>(streams) * 15 * V * 2, 0.0);
+    const cudaError_t e = launch_pdl(conf_kernel, dim3(streams * 15), dim3(kSelThreads), 0, st, logits, V, 1.0f / T, conf);
+    count_launch();
+    if (e != cudaSuccess) return DFLASH_E_CUDA;
+  }
+  {
+    TraceScope ts(st, "draft_stop.len", static_cast<double>(streams) * 15 * 4, 0.0);
+    const cudaError_t e =
+        launch_pdl(stop_len_kernel, dim3((streams + 127) / 128), dim3(128), 0, st, conf, streams, min_p, len);
+    count_launch();
+    if (e != cudaSuccess) return DFLASH_E_CUDA;
+  }
+  return DFLASH_OK;
+}
+
 int launch_topk_merge(const float* cand_v, const int* cand_i, int rows, int tiles, int k, int* ids, float* vals,
                       cudaStream_t st) {
   if (rows <= 0) return DFLASH_OK;

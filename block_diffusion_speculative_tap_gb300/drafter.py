@@ -354,6 +354,26 @@ def topk(logits, k, temperature=1.0, uniforms=None, ids=None, vals=None, sampled
     return ids, vals, sampled
 
 
+def draft_stop(logits, min_p, temperature=1.0, conf=None, lens=None):
+    """dflash_draft_stop on bf16 draft logits [S*15, V]: the per-row
+    confidence (top-1 softmax probability) and, per stream, the number of
+    leading drafted tokens whose confidence is at least min_p.
+    Returns (conf fp32 [S*15], lens int32 [S])."""
+    _need(logits, torch.bfloat16, "logits")
+    rows, V = logits.shape
+    if rows % 15:
+        raise ValueError("logits: 15 rows a stream")
+    S = rows // 15
+    dev = logits.device
+    conf = conf if conf is not None else torch.empty(rows, dtype=torch.float32, device=dev)
+    lens = lens if lens is not None else torch.empty(S, dtype=torch.int32, device=dev)
+    check(
+        lib.dflash_draft_stop(_ptr(logits), S, V, float(temperature), float(min_p), _ptr(conf), _ptr(lens), _stream()),
+        "dflash_draft_stop",
+    )
+    return conf, lens
+
+
 def _draft_ld(draft_ids):
     """Elements between consecutive draft positions: 1 for [S, 15], k for the
     top-1 column of a [S*15, k] top-k tensor."""

@@ -286,6 +286,22 @@ int dflash_draft_head(dflash_handle* h, dflash_state* st, int s_count, const flo
 int dflash_topk(const void* logits, int rows, int vocab, int k, float temperature, const float* uniforms,
                 int32_t* ids, float* vals, int32_t* sampled, dflash_stream_t stream);
 
+/* ---------------------------------------------------------------- min-p stop
+ * Where a draft stops [ST3457 "Problem and result": `--spec-min-p` stops a
+ * draft where the confidence falls below it]. Reading (the v1 body has no
+ * selector): the confidence of mask row i is the largest entry of
+ * softmax(logits_i / temperature), and a stream's draft keeps its leading
+ * rows whose confidence is at least min_p.
+ *   logits:    device bf16 [streams * 15, vocab] (rows of a stream
+ *              contiguous, as dflash_draft_block writes them), 16-byte
+ *              aligned, vocab a multiple of 8.
+ *   conf:      device fp32 [streams * 15] out.
+ *   draft_len: device int32 [streams] out, in [0, 15].
+ * temperature > 0, 0 <= min_p <= 1; otherwise DFLASH_E_INVALID_ARG and
+ * nothing is enqueued. No workspace; asynchronous on `stream`. */
+int dflash_draft_stop(const void* logits, int streams, int vocab, float temperature, float min_p, float* conf,
+                      int32_t* draft_len, dflash_stream_t stream);
+
 /* ---------------------------------------------------------------- verify
  * Target verification of S drafted blocks [EXPL 四; PROT "What is portable"].
  * draft_ids: device int32, d_{i+1} of stream s at draft_ids[(s*15 + i) * draft_ld]

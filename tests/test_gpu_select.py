@@ -181,3 +181,54 @@ def test_sampling_verify_distribution_is_target(D):
     p = torch.softmax(tl1.to(torch.bfloat16).double(), -1)[0].numpy()
     counts = np.bincount(first, minlength=V)
     assert chisquare(counts, p * n).pvalue > 1e-3
+
+
+
+# ---------------------------------------------------------------- min-p stop
+@pytest.mark.parametrize("S,V,T", [(1, 151936, 1.0), (3, 4096, 0.7), (2, 136, 2.0)])
+def test_draft_stop_vs_oracle(S, V, T):
+    """Confidence (top-1 softmax probability) within 1e-4 relative of the
+    oracle on the same bf16 logits; stop lengths exact, except where an
+    oracle confidence sits within that tolerance of min-p (counted)."""
+    import block_diffusion_speculative_tap_gb300 as D
+
+    g = torch.Generator().manual_seed(4100 + V)
+    # peaked rows so that confidences spread over (0, 1)
+    logits = torch.randn(S * 15, V, generator=g) * 2.0
+    hot = torch.randint(0, V, (S * 15,), generator=g)
+    lift = torch.rand(S * 15, generator=g) * 14.0
+    logits[torch.arange(S * 15), hot] += lift
+    logits = logits.to(torch.bfloat16)
+    conf_ref = O.draft_confidence(logits.float().numpy().astype(np.float64), T)
+    min_p = float(np.median(conf_ref))
+    conf, lens = D.draft_stop(logits.cuda(), min_p, temperature=T)
+    conf = conf.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(conf - conf_ref) <= 1e-4 * conf_ref), np.max(np.abs(conf - conf_ref) / conf_ref)
+    want = O.draft_stop(conf_ref.reshape(S, 15), min_p)
+    got = lens.cpu().numpy()
+    near = 0
+    for s in range(S):
+        row = conf_ref.reshape(S, 15)[s]
+        # the rule's decision at each inspected row must be clear of the tolerance
+        n_clear = True
+        for i in range(min(int(want[s]) + 1, 15)):
+            if abs(row[i] - min_p) <= 1e-4 * row[i]:
+                n_clear = False
+        if n_clear:
+            assert got[s] == want[s], (s, got[s], want[s])
+        else:
+            near += 1
+    assert near < S or S == 1
+
+
+def test_draft_stop_rejects_bad_arguments():
+    import block_diffusion_speculative_tap_gb300 as D
+
+    x = torch.zeros(15, 136, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(D.DFlashError):
+        D.draft_stop(x, 1.5)
+    with pytest.raises(D.DFlashError):
+        D.draft_stop(x, 0.5, temperature=0.0)
+    conf, lens = D.draft_stop(x, 0.5)
+    torch.cuda.synchronize()
+    assert abs(float(conf[0]) - 1.0 / 136) < 1e-6 and int(lens[0]) == 0
