@@ -191,7 +191,8 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 // every CTA of this grid has issued it. Both are no-ops without the launch
 // attribute.
 // Per-head RMSNorm and rotate-half RoPE with every rounding spelled out, so
-// the GEMM epilogue and the standalone K/V kernel give identical bits.
+// the GEMM epilogue and the standalone K/V kernel do the same arithmetic on
+// the projections they are given.
 __device__ __forceinline__ float head_norm_scale(float sumsq, float inv_d, float eps) {
   return rsqrtf(__fmaf_rn(sumsq, inv_d, eps));
 }

@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(128) hidden_norm_kernel(__nv_bfloat16* __restr
 // rotate-half RoPE at the row's position, and stores bf16 to the head's cache
 // slot. Lane l holds features q*32 + l, q < d/32; the sum of squares of a
 // head is a xor tree per q and then the q's in order, the same arithmetic
-// as the fused epilogue, so both give the same bits.
+// as the fused epilogue.
 __global__ void __launch_bounds__(256) kv_rows_kernel(const float* __restrict__ y, int64_t ld, const KvSegs segs,
                                                       const int* __restrict__ row_stream,
                                                       const int* __restrict__ row_pos,

@@ -217,3 +217,40 @@ def test_query_group_sizes(D, nq, nkv):
         ol, _ = ref.draft(s, int(anchors[s]))
         compare_draft(lg[s], idn[s], ol, 4)
     staged_vs_oracle(st, ref, m, anchors, 4)
+
+
+def test_wide_kv_rebuild_vs_oracle(D):
+    """K/V injection of passes wider than 1024 rows runs as raw projections
+    plus an elementwise k_norm / RoPE / scatter kernel. Truncating a stream
+    rebuilds its sliding caches from the fused ring in one such pass (1400
+    rows here); the restored slots must match the oracle, and the slots the
+    rebuild does not own must be untouched."""
+    m = small_model()
+    m.update(sliding_window=1500, n_layers=3, layer_kinds=[1, 1, 0])
+    w = SI.make_weights(m, 601, device="cuda")
+    dr = D.Drafter(m, w)
+    st = dr.new_state(1, 3072)
+    ref = O.OracleStreams(m, O.weights_to_f64(w), 1)
+    taps = SI.make_taps(m, 3000, 602, device="cuda")
+    for r0, r1 in [(0, 1000), (1000, 1600), (1600, 2600), (2600, 3000)]:
+        st.fuse_taps([t[r0:r1] for t in taps], [(0, r0, r1 - r0)])
+    ref.append(0, [f64(t[:1600]) for t in taps])
+    keep = []
+    for l in range(2):
+        K, V, _ = st.cache_view(l)
+        keep.append((K[0][:, 0:100].clone(), V[0][:, 0:100].clone()))  # positions 1500..1599
+    # positions 100..1499 were overwritten by 1600..2999; truncating back to
+    # 1600 rebuilds them from the ring in one 1400-row pass
+    st.truncate(0, 1600)
+    torch.cuda.synchronize()
+    pos = np.arange(100, 1500)
+    for l in range(2):
+        K, V, cap = st.cache_view(l)
+        assert cap == 1500
+        kg = K[0][:, pos % cap].permute(1, 0, 2).cpu().float().numpy()
+        vg = V[0][:, pos % cap].permute(1, 0, 2).cpu().float().numpy()
+        assert_close(kg, ref.k[0][l][pos], f"rebuilt K layer {l}")
+        assert_close(vg, ref.v[0][l][pos], f"rebuilt V layer {l}")
+        assert torch.equal(K[0][:, 0:100], keep[l][0]) and torch.equal(V[0][:, 0:100], keep[l][1])
+    rc, bits = st.status()
+    assert rc == 0 and bits == 0
