@@ -143,6 +143,112 @@ def gemm_traffic():
         return None
 
 
+# ---------------------------------------------------------------- other configs
+def measure_config(name, dev, pk, steps, dr=None):
+    """Supplementary measurements of the parity workloads (not the headline):
+    draft stream-blocks/s and its HBM roofline fraction, the LM head's
+    TFLOP/s, and verification time, at the workload's streams and contexts."""
+    import ctypes as C
+
+    import torch
+
+    import block_diffusion_speculative_tap_gb300 as D
+    import synthetic_inputs as SI
+    from block_diffusion_speculative_tap_gb300 import _abi as A
+
+    P = SI.preset(name)
+    m = P["model"]
+    ctx = P["context"]
+    S = len(ctx)
+    if dr is None:
+        w = SI.make_weights(m, P["seed"], device=dev)
+        dr = D.Drafter(m, w)
+    st = dr.new_state(S, P["ring"])
+    for s_ in range(S):  # one stream at a time keeps the tap planes small
+        taps = SI.make_taps(m, ctx[s_], P["seed"] + 1 + s_, device=dev)
+        st.fuse_taps(taps, [(s_, 0, ctx[s_])])
+        del taps
+    anchors = SI.anchor_ids(S, m["vocab"], m["mask_token"], P["seed"] + 2, device=dev)
+    V = m["vocab"]
+    logits = torch.empty(S * 15, V, dtype=torch.bfloat16, device=dev)
+    ids = torch.empty(S * 15, 8, dtype=torch.int32, device=dev)
+    vals = torch.empty(S * 15, 8, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def draft():
+        st.draft(anchors, k=8, logits=logits, ids=ids, vals=vals)
+
+    for _ in range(3):
+        draft()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        draft()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    A.lib.dflash_trace_enable(1)
+    draft()
+    torch.cuda.synchronize()
+    A.lib.dflash_trace_enable(0)
+    tot_b, lm_ms, lm_fl = 0.0, 0.0, 0.0
+    per = {}
+    for i in range(A.lib.dflash_trace_count()):
+        nm, t, b, fl = C.c_char_p(), C.c_float(), C.c_double(), C.c_double()
+        if A.lib.dflash_trace_get(i, C.byref(nm), C.byref(t), C.byref(b), C.byref(fl)) == 0:
+            tot_b += b.value
+            key = nm.value.decode()
+            per[key] = per.get(key, 0.0) + t.value
+            if key == "gemm.lm_head":
+                lm_ms += t.value
+                lm_fl += fl.value
+    out = {
+        "streams": S,
+        "context": [min(ctx), max(ctx)],
+        "draft_stream_blocks_per_s": S * 1e3 / ms,
+        "draft_ms": ms,
+        "draft_algorithmic_bytes": tot_b,
+        "draft_frac_of_hbm_peak": tot_b / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+        "lm_head_tflops": lm_fl / (lm_ms * 1e-3) / 1e12 if lm_ms else None,
+        "lm_head_frac_of_bf16_peak": (lm_fl / (lm_ms * 1e-3) / 1e12 / pk["bf16_tflops"]) if lm_ms else None,
+        "kernels_ms_traced": {k: round(v, 4) for k, v in sorted(per.items(), key=lambda kv: -kv[1])},
+    }
+    # verification of the drafted rows against seeded target logits
+    tl = SI.make_logits((S, 16, V), P["target_logit_std"], P["seed"] + 3, device=dev)
+    if P["verify"] == "greedy":
+        def ver():
+            D.verify_greedy(ids, tl)
+    else:
+        T = P.get("temperature", 1.0)
+        u = SI.make_uniforms((S, 16, 2), P["seed"] + 5, device=dev)
+        draft_ids = ids[:, 0].reshape(S, 15).contiguous()
+
+        def ver():
+            D.verify_sample(draft_ids, tl, logits.view(S, 15, V), u, T)
+    for _ in range(3):
+        ver()
+    torch.cuda.synchronize()
+    v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    v0.record(stream)
+    for _ in range(steps):
+        ver()
+    v1.record(stream)
+    torch.cuda.synchronize()
+    vms = v0.elapsed_time(v1) / steps
+    vbytes = S * 16 * V * 2 * (1 if P["verify"] == "greedy" else 2)
+    out["verify_mode"] = P["verify"]
+    out["verify_ms"] = vms
+    out["verify_rows_per_s"] = S * 16 * 1e3 / vms
+    out["verify_frac_of_hbm_peak"] = vbytes / (vms * 1e-3) / 1e9 / pk["hbm_gbs"]
+    rc, bits = st.status()
+    if rc != 0:
+        raise RuntimeError(f"{name}: device status {rc} bits {bits}")
+    del st, logits
+    torch.cuda.empty_cache()
+    return out
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args, rank, world):
     import torch
@@ -415,6 +521,18 @@ def run_ours(args, rank, world):
         "gpu_launches": int(launches),
         "clocks": clk,
     }
+    if world == 1 and not args.no_other_configs:
+        others = {}
+        for name in ("long32k", "serve32"):
+            others[name] = measure_config(name, dev, pk, 20, dr=dr)
+        del st
+        torch.cuda.empty_cache()
+        others["dflash2geom"] = measure_config("dflash2geom", dev, pk, 20)
+        out["other_configs"] = {
+            "note": "supplementary: the parity workloads measured at their own streams and contexts "
+            "(draft = block forward + LM head + top-8; verify = the workload's mode); not the headline",
+            **others,
+        }
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args, m, w, seed, C0)
     if world > 1:
@@ -541,6 +659,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true", help="skip the supplementary workloads")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))

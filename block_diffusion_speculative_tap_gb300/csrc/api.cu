@@ -114,9 +114,38 @@ constexpr int kDecodeRegimeN = 1024;  // up to this many tokens a GEMM uses the 
 
 int head_threads_ok(int d) { return d == 32 || d == 64 || d == 128; }
 
-int ksplit_for(const dflash_handle* h, int rows_m, int K, int N) {
-  if (N > kDecodeRegimeN) return 1;
-  return gemm_choose_ksplit(rows_m / kTileM, K / kTileK, h->num_sms);
+// Split-K of a GEMM plan (M, K, N and the dual flag set):
+//  * up to invariant_n tokens, the split is fixed by the weight's shape
+//    (cluster split-K), so a row's result does not depend on the batch it
+//    runs in: the drafter's GEMMs keep this up to kInvariantN tokens (four
+//    streams' blocks), the fill GEMMs (fc, K/V injection) up to
+//    kDecodeRegimeN rows, so a fill resumed after a truncate rebuilds the
+//    same cache;
+//  * up to kDecodeRegimeN tokens, throughput: no split when the tiles already
+//    cover half the SMs, else the smallest split reaching 3/4 of them
+//    (global partials, persistent CTAs, at least 8 reduction blocks a chunk);
+//  * above, no split.
+constexpr int kInvariantN = 64;
+
+void set_split(const dflash_handle* h, GemmPlan& p, int invariant_n = kInvariantN) {
+  p.no_cluster = false;
+  if (p.N > kDecodeRegimeN) {
+    p.ksplit = 1;
+    return;
+  }
+  const int m_tiles = p.M / kTileM, kb = p.K / kTileK;
+  if (p.N <= invariant_n) {
+    p.ksplit = gemm_choose_ksplit(m_tiles, kb, h->num_sms);
+    return;
+  }
+  const int BN = gemm_bn_for(p.N);
+  const int tiles = m_tiles * ((p.N + BN - 1) / BN);
+  int ks = 1;
+  if (2 * tiles < h->num_sms) {
+    while (ks < 4 && tiles * ks * 4 < 3 * h->num_sms && kb / (ks + 1) >= 8) ++ks;
+  }
+  p.ksplit = ks;
+  p.no_cluster = true;
 }
 
 int attn_chunk(int cap) { return cap <= 8192 ? 256 : 512; }
@@ -448,7 +477,7 @@ GemmPlan fc_plan(const dflash_handle* h, int rows) {
   p.M = c.hidden;
   p.N = rows;
   p.K = c.n_taps * c.hidden;
-  p.ksplit = ksplit_for(h, p.M, p.K, rows);
+  set_split(h, p, kDecodeRegimeN);
   p.epi = EPI_STORE_F32;
   p.epi_args.ldo = c.hidden;
   p.name = "gemm.fc";
@@ -481,7 +510,7 @@ GemmPlan kv_plan(const dflash_handle* h, const dflash_state* st, int rows, int l
   p.M = n * kvd;
   p.N = rows;
   p.K = c.hidden;
-  p.ksplit = ksplit_for(h, p.M, p.K, rows);
+  set_split(h, p, kDecodeRegimeN);
   p.epi = EPI_HEADS;
   p.epi_args.head_dim = c.head_dim;
   p.epi_args.eps = c.rms_eps;
@@ -730,7 +759,7 @@ void layer_plans(const dflash_handle* h, int l, int T, GemmPlan& qkv, GemmPlan& 
   qkv.M = qd + 2 * kvd;
   qkv.N = T;
   qkv.K = c.hidden;
-  qkv.ksplit = ksplit_for(h, qkv.M, qkv.K, T);
+  set_split(h, qkv);
   qkv.epi = EPI_HEADS;
   qkv.name = "gemm.qkv";
   o = GemmPlan();
@@ -742,7 +771,7 @@ void layer_plans(const dflash_handle* h, int l, int T, GemmPlan& qkv, GemmPlan& 
   o.M = c.hidden;
   o.N = T;
   o.K = qd;
-  o.ksplit = ksplit_for(h, o.M, o.K, T);
+  set_split(h, o);
   o.epi = EPI_RESID;
   o.name = "gemm.o";
   gu = GemmPlan();
@@ -755,7 +784,7 @@ void layer_plans(const dflash_handle* h, int l, int T, GemmPlan& qkv, GemmPlan& 
   gu.M = c.ffn;
   gu.N = T;
   gu.K = c.hidden;
-  gu.ksplit = ksplit_for(h, gu.M, gu.K, T);
+  set_split(h, gu);
   gu.epi = EPI_SWIGLU;
   gu.name = "gemm.gate_up";
   dn = GemmPlan();
@@ -767,7 +796,7 @@ void layer_plans(const dflash_handle* h, int l, int T, GemmPlan& qkv, GemmPlan& 
   dn.M = c.hidden;
   dn.N = T;
   dn.K = c.ffn;
-  dn.ksplit = ksplit_for(h, dn.M, dn.K, T);
+  set_split(h, dn);
   dn.epi = EPI_RESID;
   dn.name = "gemm.down";
 }
@@ -783,7 +812,7 @@ GemmPlan lm_plan(const dflash_handle* h, int rows) {
   p.M = c.vocab;
   p.N = rows;
   p.K = c.hidden;
-  p.ksplit = ksplit_for(h, p.M, p.K, rows);
+  set_split(h, p);
   p.epi = EPI_STORE_BF16;
   p.epi_args.ldo = c.vocab;
   p.name = "gemm.lm_head";
@@ -971,9 +1000,12 @@ int run_head(dflash_handle* h, int* status, int s_count, const float* X, const D
   lp.b_ptr[0] = w.hbuf;
   lp.ldb = c.hidden;
   lp.epi_args.out = logits;
-  // top-k up to 8: the LM head's epilogue ranks each 128-id tile, a small
-  // kernel merges the tiles' lists
-  const bool fused_topk = topk_ids != nullptr && k <= 8;
+  // top-k up to 8 of a single stream's 15 rows: the LM head's epilogue ranks
+  // each 128-id tile (hidden under its weight stream), a small kernel merges
+  // the tiles' lists. Wider heads are compute-bound and their epilogues would
+  // rank 16 column chunks a tile: there a vocabulary scan after the GEMM is
+  // cheaper.
+  const bool fused_topk = topk_ids != nullptr && k <= 8 && gemm_bn_for(rows) == 16;
   if (fused_topk) {
     lp.epi_args.cand_k = k;
     lp.epi_args.cand_v = w.cand_v;

@@ -471,7 +471,11 @@ int splits_for(int G, Split* out) {
   switch (G) {
     case 1: add(attn_cluster_kernel<1, 1>, 1); break;
     case 2: add(attn_cluster_kernel<1, 2>, 1); break;
-    case 4: add(attn_cluster_kernel<1, 4>, 1); add(attn_cluster_kernel<2, 2>, 2); break;
+    case 4:
+      add(attn_cluster_kernel<1, 4>, 1);
+      add(attn_cluster_kernel<2, 2>, 2);
+      add(attn_cluster_kernel<4, 1>, 4);
+      break;
     case 5: add(attn_cluster_kernel<1, 5>, 1); add(attn_cluster_kernel<5, 1>, 5); break;
     case 8: add(attn_cluster_kernel<1, 8>, 1); add(attn_cluster_kernel<2, 4>, 2); add(attn_cluster_kernel<4, 2>, 4); break;
     default: break;
@@ -533,8 +537,10 @@ int launch_attention_cluster(const AttnArgs& a, const CUtensorMap& kmap, const C
   int rc = encode_map(&P.kbmap, a.Kb, 2, dims, strides, box);
   if (!rc) rc = encode_map(&P.vbmap, a.Vb, 2, dims, strides, box);
   if (rc) return rc;
-  // the most parallel split whose clusters are all resident at once; the
-  // split only regroups query heads, so every split gives the same results
+  // the most parallel split whose clusters are all resident at once, else
+  // (many streams: several waves anyway) the least split one, which reads
+  // each K/V tile once for all the kv head's query heads; the split only
+  // regroups query heads, so every split gives the same results
   const int G = a.nq / a.nkv;
   Split sp[4];
   const int ns = splits_for(G, sp);

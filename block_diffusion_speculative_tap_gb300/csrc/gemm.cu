@@ -219,16 +219,22 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
   const int m = m_tile * kTileM + row;
   if constexpr (EPI == EPI_RESID) {
     // X += v, and the tile's per-column sums of squares of the new X
-    float ss[16];
+    // all 16 loads are issued before the first store: interleaved, a store
+    // to X could alias the next load, and the loads would run one at a time
+    float ss[16], xo[16];
     float* X = static_cast<float*>(a.epi.out);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int t = n0 + j;
+      xo[j] = (j < nvalid && t < a.N && m < a.M) ? X[static_cast<int64_t>(t) * a.epi.ldo + m] : 0.f;
+    }
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int t = n0 + j;
       ss[j] = 0.f;
       if (j < nvalid && t < a.N && m < a.M) {
-        const int64_t o = static_cast<int64_t>(t) * a.epi.ldo + m;
-        const float xn = X[o] + v0[j];
-        X[o] = xn;
+        const float xn = xo[j] + v0[j];
+        X[static_cast<int64_t>(t) * a.epi.ldo + m] = xn;
         ss[j] = xn * xn;
       }
     }
@@ -699,13 +705,31 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
               v0[j] = 0.f;
               v1[j] = 0.f;
             }
-            for (int k2 = 0; k2 < args.ksplit; ++k2) {
-              const int u2 = (m_tile * args.ksplit + k2) * args.n_tiles + n_tile;
-              const float* s2 = args.partial + static_cast<size_t>(u2) * (Tr::kAcc * BN * kTileM);
+            // chunk order; the loads of two chunks are issued before their adds
+            for (int k2 = 0; k2 < args.ksplit; k2 += 2) {
+              const bool two = k2 + 1 < args.ksplit;
+              const float* sa =
+                  args.partial + static_cast<size_t>((m_tile * args.ksplit + k2) * args.n_tiles + n_tile) *
+                                     (Tr::kAcc * BN * kTileM);
+              const float* sb = two ? sa + static_cast<size_t>(args.n_tiles) * (Tr::kAcc * BN * kTileM) : sa;
+              float a0[16], b0[16], a1[16], b1[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
-                v0[j] += __ldcg(&s2[(c0 + j) * kTileM + row]);
-                if constexpr (DUAL) v1[j] += __ldcg(&s2[(BN + c0 + j) * kTileM + row]);
+                a0[j] = __ldcg(&sa[(c0 + j) * kTileM + row]);
+                b0[j] = two ? __ldcg(&sb[(c0 + j) * kTileM + row]) : 0.f;
+                if constexpr (DUAL) {
+                  a1[j] = __ldcg(&sa[(BN + c0 + j) * kTileM + row]);
+                  b1[j] = two ? __ldcg(&sb[(BN + c0 + j) * kTileM + row]) : 0.f;
+                }
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                v0[j] += a0[j];
+                if (two) v0[j] += b0[j];
+                if constexpr (DUAL) {
+                  v1[j] += a1[j];
+                  if (two) v1[j] += b1[j];
+                }
               }
             }
             epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red);
@@ -847,7 +871,7 @@ int launch_inst(const GemmArgs& a, int num_sms, cudaStream_t st) {
 template <int BN, bool DUAL, int STAGES, int MINB, int EPI>
 int launch_mode(const GemmArgs& a, int num_sms, cudaStream_t st) {
   using Tr = GemmTraits<BN, DUAL, STAGES, EPI>;
-  if (a.ksplit > 1 && a.ksplit <= kMaxClusterSplit) {
+  if (a.ksplit > 1 && a.ksplit <= kMaxClusterSplit && !a.no_cluster) {
     if constexpr (Tr::kClusterFits) return launch_inst<BN, DUAL, STAGES, EPI, MINB, true>(a, num_sms, st);
   }
   return launch_inst<BN, DUAL, STAGES, EPI, MINB, false>(a, num_sms, st);
@@ -932,6 +956,7 @@ static void fill_args(const GemmPlan& p, GemmArgs& a, int BN) {
   a.b_plane_kb = p.Kp / kTileK;
   a.ksplit = p.ksplit;
   a.units = a.m_tiles * a.n_tiles * a.ksplit;
+  a.no_cluster = p.no_cluster;
   a.epi = p.epi_args;
 }
 

@@ -68,6 +68,7 @@ struct GemmArgs {
   int b_plane_kb;                 // 64-wide reduction blocks per B plane
   int M, N, K;
   int m_tiles, n_tiles, kb_total, ksplit, units;
+  bool no_cluster;
   float* partial;                 // split-K partial tiles, [units][acc][BN][128]
   int* counters;                  // [m_tiles * n_tiles], zero before launch
   int* err;                       // device status word
@@ -88,6 +89,7 @@ struct GemmPlan {
   int Kp = 0;       // reduction length of one B plane
   int M = 0, N = 0, K = 0;
   int ksplit = 1;
+  bool no_cluster = false;  // split-K through global partials even when a cluster would fit
   int epi = EPI_STORE_F32;
   EpiArgs epi_args{};
   const char* name = "gemm";  // trace label
