@@ -2,8 +2,8 @@
 // (stream, kv head).
 //
 // The visible context keys of a (stream, kv head) are split evenly over the
-// kClusterCtas CTAs of a cluster; the last CTA also takes the block's own 16
-// rows. When the query heads of a kv head are an even number, two clusters
+// CS CTAs of a cluster (8; 4 or 2 when many streams already fill the GPU);
+// the last CTA also takes the block's own 16 rows. When the query heads of a kv head are an even number, two clusters
 // share the kv head, each taking half of its query heads (K/V tiles are read
 // by both, the second read mostly from L2), so twice as many SMs stream.
 // Inside a CTA one producer thread streams 64-key tiles of K and V from the
@@ -13,9 +13,9 @@
 // tensor cores (mma.sync m16n8k16, P in bf16) with an online softmax. The two parities of a head merge in shared memory, then the CTAs
 // of the cluster reduce-scatter their partial (max, sum, output) through
 // distributed shared memory, in rank order, and write the bf16 attention
-// output: no partials in global memory and no second kernel. The split
-// depends only on the stream's visible length, so a stream's result does
-// not depend on the batch.
+// output: no partials in global memory and no second kernel. Up to four
+// streams a launch the split is always 8 ways and depends only on the
+// stream's visible length, so a stream's result does not depend on the batch.
 #include <mutex>
 #include <utility>
 #include <vector>
@@ -31,7 +31,7 @@ constexpr int kD = 128;
 constexpr int kKeys = 64;             // keys per context tile
 constexpr int kBlockKeys = 16;        // the block's own keys
 constexpr int kStages = 3;
-constexpr int kClusterCtas = 8;
+constexpr int kClusterCtas = 8;  // CTAs a cluster up to four streams a launch
 constexpr int kSubBytes = kKeys * 128;   // 64 rows x 64 dims (128 B) per swizzled sub-tile
 constexpr int kTileBytes = 4 * kSubBytes;  // K lo, K hi, V lo, V hi = 32 KiB
 constexpr int kBlockSubBytes = kBlockKeys * 128;
@@ -222,8 +222,8 @@ struct ClusterAttnArgs {
 };
 
 // G: query heads handled by this CTA (of the kv head's group); HS: CTAs
-// (clusters) sharing a kv head.
-template <int G, int HS>
+// (clusters) sharing a kv head; CS: CTAs a cluster, splitting the keys.
+template <int G, int HS, int CS>
 __global__ void __launch_bounds__(32 * (2 * G + 1), G <= 2 ? 2 : 1) attn_cluster_kernel(const __grid_constant__ ClusterAttnArgs P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -257,10 +257,10 @@ __global__ void __launch_bounds__(32 * (2 * G + 1), G <= 2 ? 2 : 1) attn_cluster
   const int s = a.s_begin + si;
   const int C = a.lens[s];
   const int nvis = a.window > 0 ? min(C, a.window) : C;
-  const int k0 = static_cast<int>(static_cast<long long>(nvis) * rank / kClusterCtas);
-  const int k1 = static_cast<int>(static_cast<long long>(nvis) * (rank + 1) / kClusterCtas);
+  const int k0 = static_cast<int>(static_cast<long long>(nvis) * rank / CS);
+  const int k1 = static_cast<int>(static_cast<long long>(nvis) * (rank + 1) / CS);
   const int nt = (k1 - k0 + kKeys - 1) / kKeys;
-  const bool has_block = rank == kClusterCtas - 1;
+  const bool has_block = rank == CS - 1;
   const int slab = s * a.nkv + kvh;
   int* err = a.err;
 
@@ -387,28 +387,28 @@ __global__ void __launch_bounds__(32 * (2 * G + 1), G <= 2 ? 2 : 1) attn_cluster
   // reduce-scatter: this rank owns (head, row) vectors [v0, v1) of the G*16
   {
     const int nvec = G * 16;
-    const int v0 = static_cast<int>(rank) * nvec / kClusterCtas;
-    const int v1 = (static_cast<int>(rank) + 1) * nvec / kClusterCtas;
+    const int v0 = static_cast<int>(rank) * nvec / CS;
+    const int v1 = (static_cast<int>(rank) + 1) * nvec / CS;
     const uint32_t pbase = smem_u32(part), mlbase = smem_u32(ml);
     for (int idx = threadIdx.x; idx < (v1 - v0) * 32; idx += blockDim.x) {
       const int vec = v0 + idx / 32;
       const int d4 = (idx & 31) * 4;
       // every rank's (max, sum, partial) loaded before any is used
-      float mr[kClusterCtas], lr[kClusterCtas];
-      float4 pr[kClusterCtas];
+      float mr[CS], lr[CS];
+      float4 pr[CS];
 #pragma unroll
-      for (int r2 = 0; r2 < kClusterCtas; ++r2) {
+      for (int r2 = 0; r2 < CS; ++r2) {
         mr[r2] = cld(cmap(mlbase, r2) + vec * 8);
         lr[r2] = cld(cmap(mlbase, r2) + vec * 8 + 4);
         pr[r2] = cld4(cmap(pbase, r2) + (vec * kPartLd + d4) * 4);
       }
       float M = -INFINITY;
 #pragma unroll
-      for (int r2 = 0; r2 < kClusterCtas; ++r2) M = fmaxf(M, mr[r2]);
+      for (int r2 = 0; r2 < CS; ++r2) M = fmaxf(M, mr[r2]);
       float den = 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int r2 = 0; r2 < kClusterCtas; ++r2) {
+      for (int r2 = 0; r2 < CS; ++r2) {
         const float w = M == -INFINITY ? 0.f : exp2f(mr[r2] - M);
         den += w * lr[r2];
         acc.x += w * pr[r2].x;
@@ -457,27 +457,44 @@ bool attention_cluster_supported(const AttnArgs& a) {
 }
 
 namespace {
-// One way to cut a kv head's G query heads over HS clusters of GH heads each.
+// One way to cut a kv head's G query heads over HS clusters of GH heads
+// each, with CS CTAs a cluster.
 struct Split {
   void (*kern)(ClusterAttnArgs);
-  int GH, HS;
+  int GH, HS, CS;
 };
 
-// The splits of a group of G, most parallel first.
+// The 8-way splits of a group of G, most parallel first.
 int splits_for(int G, Split* out) {
   using K = void (*)(ClusterAttnArgs);
   int n = 0;
-  auto add = [&](K k, int gh) { out[n++] = Split{k, gh, G / gh}; };
+  auto add = [&](K k, int gh) { out[n++] = Split{k, gh, G / gh, kClusterCtas}; };
   switch (G) {
-    case 1: add(attn_cluster_kernel<1, 1>, 1); break;
-    case 2: add(attn_cluster_kernel<1, 2>, 1); break;
-    case 4:
-      add(attn_cluster_kernel<1, 4>, 1);
-      add(attn_cluster_kernel<2, 2>, 2);
-      add(attn_cluster_kernel<4, 1>, 4);
-      break;
-    case 5: add(attn_cluster_kernel<1, 5>, 1); add(attn_cluster_kernel<5, 1>, 5); break;
-    case 8: add(attn_cluster_kernel<1, 8>, 1); add(attn_cluster_kernel<2, 4>, 2); add(attn_cluster_kernel<4, 2>, 4); break;
+    case 1: add(attn_cluster_kernel<1, 1, 8>, 1); break;
+    case 2: add(attn_cluster_kernel<1, 2, 8>, 1); break;
+    case 4: add(attn_cluster_kernel<1, 4, 8>, 1); add(attn_cluster_kernel<2, 2, 8>, 2); break;
+    case 5: add(attn_cluster_kernel<1, 5, 8>, 1); add(attn_cluster_kernel<5, 1, 8>, 5); break;
+    case 8: add(attn_cluster_kernel<1, 8, 8>, 1); add(attn_cluster_kernel<2, 4, 8>, 2); add(attn_cluster_kernel<4, 2, 8>, 4); break;
+    default: break;
+  }
+  return n;
+}
+
+// Many streams: the least split grouping with 2, 4 or 8 CTAs a cluster, in
+// that order.
+int wide_splits_for(int G, Split* out) {
+  int n = 0;
+  auto add3 = [&](int gh, auto k2, auto k4, auto k8) {
+    out[n++] = Split{k2, gh, G / gh, 2};
+    out[n++] = Split{k4, gh, G / gh, 4};
+    out[n++] = Split{k8, gh, G / gh, 8};
+  };
+  switch (G) {
+    case 1: add3(1, attn_cluster_kernel<1, 1, 2>, attn_cluster_kernel<1, 1, 4>, attn_cluster_kernel<1, 1, 8>); break;
+    case 2: add3(1, attn_cluster_kernel<1, 2, 2>, attn_cluster_kernel<1, 2, 4>, attn_cluster_kernel<1, 2, 8>); break;
+    case 4: add3(2, attn_cluster_kernel<2, 2, 2>, attn_cluster_kernel<2, 2, 4>, attn_cluster_kernel<2, 2, 8>); break;
+    case 5: add3(5, attn_cluster_kernel<5, 1, 2>, attn_cluster_kernel<5, 1, 4>, attn_cluster_kernel<5, 1, 8>); break;
+    case 8: add3(4, attn_cluster_kernel<4, 2, 2>, attn_cluster_kernel<4, 2, 4>, attn_cluster_kernel<4, 2, 8>); break;
     default: break;
   }
   return n;
@@ -485,9 +502,9 @@ int splits_for(int G, Split* out) {
 
 constexpr int kSmemLaunch = ClusterAttnSmem::kBytes + 1024;
 
-// Clusters of this kernel that can be resident at once on this device
-// (queried once per kernel; 0 if the query fails).
-int resident_clusters(void (*kern)(ClusterAttnArgs), int threads) {
+// Clusters (of cs CTAs) of this kernel that can be resident at once on this
+// device (queried once per kernel; 0 if the query fails).
+int resident_clusters(void (*kern)(ClusterAttnArgs), int threads, int cs) {
   static std::mutex mu;
   static std::vector<std::pair<void (*)(ClusterAttnArgs), int>> memo;
   std::lock_guard<std::mutex> lk(mu);
@@ -498,11 +515,11 @@ int resident_clusters(void (*kern)(ClusterAttnArgs), int threads) {
       cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess) {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kClusterCtas;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(kClusterCtas, 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(cs), 1, 1);
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = kSmemLaunch;
     cfg.attrs = attr;
@@ -537,36 +554,50 @@ int launch_attention_cluster(const AttnArgs& a, const CUtensorMap& kmap, const C
   int rc = encode_map(&P.kbmap, a.Kb, 2, dims, strides, box);
   if (!rc) rc = encode_map(&P.vbmap, a.Vb, 2, dims, strides, box);
   if (rc) return rc;
-  // the most parallel split whose clusters are all resident at once, else
-  // (many streams: several waves anyway) the least split one, which reads
-  // each K/V tile once for all the kv head's query heads; the split only
-  // regroups query heads, so every split gives the same results
+  // Up to four streams: the most parallel 8-way split whose clusters are all
+  // resident at once, else the least parallel one; grouping query heads
+  // differently gives the same results. More streams: several waves anyway,
+  // so the fewest CTAs a cluster that still leave two waves of CTAs (each
+  // CTA then carries more keys over its fixed start and reduce costs).
   const int G = a.nq / a.nkv;
   Split sp[4];
-  const int ns = splits_for(G, sp);
+  int ns = splits_for(G, sp);
   if (ns == 0) return DFLASH_E_SHAPE;
   int pick = ns - 1;
-  for (int i = 0; i < ns; ++i) {
-    const int cap = resident_clusters(sp[i].kern, 32 * (2 * sp[i].GH + 1));
-    if (cap > 0 && a.nkv * sp[i].HS * s_count <= cap) {
-      pick = i;
-      break;
+  if (s_count <= 4) {
+    for (int i = 0; i < ns; ++i) {
+      const int cap = resident_clusters(sp[i].kern, 32 * (2 * sp[i].GH + 1), sp[i].CS);
+      if (cap > 0 && a.nkv * sp[i].HS * s_count <= cap) {
+        pick = i;
+        break;
+      }
+    }
+  } else {
+    ns = wide_splits_for(G, sp);
+    if (ns == 0) return DFLASH_E_SHAPE;
+    pick = ns - 1;
+    for (int i = 0; i < ns; ++i) {
+      const int resident_ctas = resident_clusters(sp[i].kern, 32 * (2 * sp[i].GH + 1), sp[i].CS) * sp[i].CS;
+      if (resident_ctas > 0 && a.nkv * sp[i].HS * s_count * sp[i].CS >= 2 * resident_ctas) {
+        pick = i;
+        break;
+      }
     }
   }
   void (*kern)(ClusterAttnArgs) = sp[pick].kern;
-  const int HS = sp[pick].HS, GH = sp[pick].GH;
+  const int HS = sp[pick].HS, GH = sp[pick].GH, CS = sp[pick].CS;
   const int threads = 32 * (2 * GH + 1);
-  if (resident_clusters(kern, threads) == 0) return DFLASH_E_CUDA;  // also sets the smem attributes
+  if (resident_clusters(kern, threads, CS) == 0) return DFLASH_E_CUDA;  // also sets the smem attributes
   const int smem = kSmemLaunch;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kClusterCtas;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(CS);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(kClusterCtas, a.nkv * HS, s_count);
+  cfg.gridDim = dim3(static_cast<unsigned>(CS), a.nkv * HS, s_count);
   cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;

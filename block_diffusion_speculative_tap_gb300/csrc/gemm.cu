@@ -19,11 +19,13 @@
 // one work unit overlaps the MMAs of the next. CTAs are persistent and walk
 // the work units round-robin.
 //
-// Split-K: each weight matrix's reduction is cut into a fixed number of
-// chunks (chosen from its shape only, never from N). A chunk writes its fp32
-// partial tile; the last chunk to finish a tile (atomic counter) adds all
-// partials in chunk order and runs the epilogue. Results are therefore
-// identical whatever the batch composition.
+// Split-K: the reduction is cut into ksplit chunks. Either the chunks of a
+// tile form a thread-block cluster and reduce through distributed shared
+// memory, or each chunk writes its fp32 partial tile to global memory and the
+// last chunk to finish a tile (atomic counter) adds all partials in chunk
+// order and runs the epilogue. The host fixes ksplit from the weight's shape
+// alone for small batches, so a token's result does not depend on the batch
+// it runs in; wider batches take a split chosen for throughput.
 #include <stdio.h>
 
 #include <algorithm>
@@ -209,13 +211,10 @@ __device__ __forceinline__ void stage_token_meta(const GemmArgs& a, int t0, int 
   named_bar_sync(1, 128);
 }
 
-// HOIST (wide tiles, whose kernels have the registers): the heads epilogue
-// issues its RoPE and gain loads before the reductions that precede their use.
-template <int EPI, bool HOIST = false>
+template <int EPI>
 __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0, int row, int q, int lane,
                                           const float (&v0)[16], const float (&v1)[16], float* xch, float* red,
-                                          int nvalid = 16, const HeadPre* pre = nullptr,
-                                          const int* tmeta = nullptr) {
+                                          int nvalid = 16, const HeadPre* pre = nullptr) {
   const int m = m_tile * kTileM + row;
   if constexpr (EPI == EPI_RESID) {
     // X += v, and the tile's per-column sums of squares of the new X
@@ -334,11 +333,6 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
           pos[j] = pre->pos[j];
           strm[j] = pre->strm[j];
         }
-      } else if (tmeta != nullptr) {
-        if (j < nvalid && t < a.N) {
-          pos[j] = tmeta[4 * j];
-          strm[j] = tmeta[4 * j + 1];
-        }
       } else if (j < nvalid && t < a.N) {
         if (a.epi.pos_mode == 0) {
           strm[j] = a.epi.s_begin + t / 16;
@@ -351,20 +345,6 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
     }
     float y[16];
     const int fi = dim < half ? dim : dim - half;
-    // RoPE values and the norm gain, issued before the reductions they wait for
-    float2 csv[HOIST ? 16 : 1];
-    float gval = 1.f;
-    if constexpr (HOIST) {
-      if (sg.kind != HEAD_V) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int t = n0 + j;
-          csv[j] = (j < nvalid && t < a.N) ? a.epi.rope[static_cast<int64_t>(pos[j]) * half + fi]
-                                           : make_float2(1.f, 0.f);
-        }
-        gval = __bfloat162float(sg.gain[dim]);
-      }
-    }
     if (sg.kind != HEAD_V) {
       // per-head sums of squares: warp partials (transpose reduction), then
       // the head's warps in order
@@ -379,7 +359,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
       const int q0 = (q / wph) * wph;
       // d is a power of two, so * (1/d) is exactly / d
       const float inv_d = 1.0f / static_cast<float>(d);
-      const float g = HOIST ? gval : (pre != nullptr ? pre->g : __bfloat162float(sg.gain[dim]));
+      const float g = pre != nullptr ? pre->g : __bfloat162float(sg.gain[dim]);
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         float s = red[q0 * 16 + j];
@@ -394,12 +374,8 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const float yp = xch[prow * 17 + j];
-        float2 cs;
-        if constexpr (HOIST)
-          cs = csv[j];
-        else
-          cs = pre != nullptr ? (j < kPre ? pre->cs[j] : make_float2(1.f, 0.f))
-                              : a.epi.rope[static_cast<int64_t>(pos[j]) * half + fi];
+        const float2 cs = pre != nullptr ? (j < kPre ? pre->cs[j] : make_float2(1.f, 0.f))
+                                         : a.epi.rope[static_cast<int64_t>(pos[j]) * half + fi];
         y[j] = rope_rotate(y[j], yp, cs, dim < half);
       }
       named_bar_sync(1, 128);  // xch / red reusable by the next chunk
@@ -416,12 +392,107 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
         o = static_cast<int64_t>(t) * (sg.heads * d) + f;
       } else {
         // a later row of the same segment owns this ring slot
-        const int rend = tmeta != nullptr ? tmeta[4 * j + 2] : a.epi.row_end[t];
+        const int rend = a.epi.row_end[t];
         if (sg.window > 0 && pos[j] < rend - sg.window) continue;
         const int slot = sg.window > 0 ? (pos[j] % sg.window) : pos[j];
         o = ((static_cast<int64_t>(strm[j]) * sg.heads + head) * sg.cap + slot) * d + dim;
       }
       sg.dst[o] = __float2bfloat16_rn(y[j]);
+    }
+  }
+}
+
+// Heads epilogue of one chunk of 16 columns, a warp per column: the chunk's
+// fp32 accumulators pass through shared memory (xch[j][129]), then warp w
+// takes columns w, w + 4, w + 8, w + 12 with lane l holding the tile's
+// features l + 32 i (i = 0..3), so a head's sum of squares and the RoPE
+// partner (feature -+ d/2) are inside one warp: the partner is slice i ^ 2
+// (d = 128), i ^ 1 (d = 64) or lane l ^ 16 (d = 32). Each slice's sum is the
+// xor butterfly over offsets 16, 8, 4, 2, 1 (the tree of warp_sum16) and the
+// slices of a head add in feature order, as the row-per-thread epilogue adds
+// its warps, so both give the same bits. tmeta holds the chunk's token
+// metadata (stage_token_meta).
+__device__ __forceinline__ void heads_cols(const GemmArgs& a, int m_tile, int n0, int row, int q, int lane,
+                                           const float (&v0)[16], float* xch, const int* tmeta) {
+  const int sidx = seg_of_tile(a, m_tile);
+  const HeadSeg& sg = a.epi.seg[sidx];
+  const int d = a.epi.head_dim;
+  const int half = d >> 1;
+  const int fbase = (m_tile - a.a_seg_tile[sidx]) * kTileM;  // the tile's first feature in the projection
+  const bool rot = sg.kind != HEAD_V;
+  int dim[4], fi[4];
+  float g[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    dim[i] = (lane + 32 * i) & (d - 1);  // d divides the tile's 128 rows
+    fi[i] = dim[i] < half ? dim[i] : dim[i] - half;
+    g[i] = rot ? __bfloat162float(sg.gain[dim[i]]) : 1.f;
+  }
+  // the RoPE values of this warp's four columns, in flight across the barriers
+  float2 cs[4][4];
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    const int pos = tmeta[4 * (q + 4 * jj)];  // 0 past the end of the tile's tokens
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      cs[jj][i] = rot ? a.epi.rope[static_cast<int64_t>(pos) * half + fi[i]] : make_float2(1.f, 0.f);
+  }
+  named_bar_sync(1, 128);  // the previous chunk's columns are done with xch
+#pragma unroll
+  for (int j = 0; j < 16; ++j) xch[j * (kTileM + 1) + row] = v0[j];
+  named_bar_sync(1, 128);
+  const float inv_d = 1.0f / static_cast<float>(d);  // d is a power of two: exact
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    const int j = q + 4 * jj;
+    const int t = n0 + j;
+    if (t >= a.N) break;
+    const int pos = tmeta[4 * j], strm = tmeta[4 * j + 1];
+    float y[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) y[i] = xch[j * (kTileM + 1) + lane + 32 * i];
+    if (rot) {
+      float s[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        s[i] = y[i] * y[i];
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) s[i] += __shfl_xor_sync(0xffffffffu, s[i], off);
+      }
+      float hs[4];
+      if (d == 128) {
+        const float s4 = ((s[0] + s[1]) + s[2]) + s[3];
+        hs[0] = hs[1] = hs[2] = hs[3] = s4;
+      } else if (d == 64) {
+        hs[0] = hs[1] = s[0] + s[1];
+        hs[2] = hs[3] = s[2] + s[3];
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) hs[i] = s[i];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) y[i] = head_norm_apply(y[i], head_norm_scale(hs[i], inv_d, a.epi.eps), g[i]);
+      float yp[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        yp[i] = d == 128 ? y[i ^ 2] : d == 64 ? y[i ^ 1] : __shfl_xor_sync(0xffffffffu, y[i], 16);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) y[i] = rope_rotate(y[i], yp[i], cs[jj][i], dim[i] < half);
+    }
+    if (a.epi.pos_mode == 0) {
+      __nv_bfloat16* dst = sg.dst + static_cast<int64_t>(t) * (sg.heads * d) + fbase + lane;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dst[32 * i] = __float2bfloat16_rn(y[i]);
+    } else {
+      // a later row of the same segment owns this ring slot
+      if (sg.window > 0 && pos < tmeta[4 * j + 2] - sg.window) continue;
+      const int slot = sg.window > 0 ? (pos % sg.window) : pos;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int head = (fbase + lane + 32 * i) / d;
+        sg.dst[((static_cast<int64_t>(strm) * sg.heads + head) * sg.cap + slot) * d + dim[i]] =
+            __float2bfloat16_rn(y[i]);
+      }
     }
   }
 }
@@ -662,16 +733,14 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
         mbar_arrive(&tempty[acc]);
         clu_tile = u;  // reduced after the cluster barrier below
       } else if (args.ksplit == 1) {
-        const int* meta = nullptr;
-        if constexpr (EPI == EPI_HEADS) {
-          stage_token_meta(args, n_tile * BN, BN, row, tmeta);
-          meta = tmeta;
-        }
+        if constexpr (EPI == EPI_HEADS) stage_token_meta(args, n_tile * BN, BN, row, tmeta);
         for (int c0 = 0; c0 < BN; c0 += 16) {
           tmem_ld16(tbase + c0, v0);
           if constexpr (DUAL) tmem_ld16(tbase + BN + c0, v1);
-          epi_chunk<EPI, (BN > 16)>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red, 16, nullptr,
-                                    meta ? meta + 4 * c0 : nullptr);
+          if constexpr (EPI == EPI_HEADS)
+            heads_cols(args, m_tile, n_tile * BN + c0, row, q, lane, v0, xch, tmeta + 4 * c0);
+          else
+            epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red);
         }
         tc_fence_before();
         mbar_arrive(&tempty[acc]);
@@ -699,6 +768,7 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
         const bool last = *last_word != 0;
         if (last) {
           __threadfence();
+          if constexpr (EPI == EPI_HEADS) stage_token_meta(args, n_tile * BN, BN, row, tmeta);
           for (int c0 = 0; c0 < BN; c0 += 16) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -732,7 +802,10 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
                 }
               }
             }
-            epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red);
+            if constexpr (EPI == EPI_HEADS)
+              heads_cols(args, m_tile, n_tile * BN + c0, row, q, lane, v0, xch, tmeta + 4 * c0);
+            else
+              epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red);
           }
         }
       }
