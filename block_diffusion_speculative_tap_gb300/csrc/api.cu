@@ -121,14 +121,18 @@ int head_threads_ok(int d) { return d == 32 || d == 64 || d == 128; }
 //    streams' blocks), the fill GEMMs (fc, K/V injection) up to
 //    kDecodeRegimeN rows, so a fill resumed after a truncate rebuilds the
 //    same cache;
-//  * up to kDecodeRegimeN tokens, throughput: no split when the tiles already
-//    cover half the SMs, else the smallest split reaching 3/4 of them
+//  * up to kDecodeRegimeN tokens, throughput: 128-token tiles unless the
+//    weight alone gives two waves of 256-token tiles (a wide tile's epilogue
+//    costs about as much as its MMAs, and two accumulators in tensor memory
+//    let a CTA's next tile run under it), no split when the tiles
+//    already cover half the SMs, else the smallest split reaching 3/4 of them
 //    (global partials, persistent CTAs, at least 8 reduction blocks a chunk);
 //  * above, no split.
 constexpr int kInvariantN = 64;
 
 void set_split(const dflash_handle* h, GemmPlan& p, int invariant_n = kInvariantN) {
   p.no_cluster = false;
+  p.bn = 0;
   if (p.N > kDecodeRegimeN) {
     p.ksplit = 1;
     return;
@@ -138,7 +142,9 @@ void set_split(const dflash_handle* h, GemmPlan& p, int invariant_n = kInvariant
     p.ksplit = gemm_choose_ksplit(m_tiles, kb, h->num_sms);
     return;
   }
-  const int BN = gemm_bn_for(p.N);
+  // wide weights (the LM head) have tiles for many waves at 256 columns
+  if (m_tiles * ((p.N + 255) / 256) < 2 * h->num_sms) p.bn = 128;
+  const int BN = plan_bn(p);
   const int tiles = m_tiles * ((p.N + BN - 1) / BN);
   int ks = 1;
   if (2 * tiles < h->num_sms) {
@@ -1005,7 +1011,7 @@ int run_head(dflash_handle* h, int* status, int s_count, const float* X, const D
   // the tiles' lists. Wider heads are compute-bound and their epilogues would
   // rank 16 column chunks a tile: there a vocabulary scan after the GEMM is
   // cheaper.
-  const bool fused_topk = topk_ids != nullptr && k <= 8 && gemm_bn_for(rows) == 16;
+  const bool fused_topk = topk_ids != nullptr && k <= 8 && plan_bn(lp) == 16;
   if (fused_topk) {
     lp.epi_args.cand_k = k;
     lp.epi_args.cand_v = w.cand_v;

@@ -211,10 +211,23 @@ __device__ __forceinline__ void stage_token_meta(const GemmArgs& a, int t0, int 
   named_bar_sync(1, 128);
 }
 
+// The residual rows X[n0 .. n0+15][m] a residual epilogue chunk adds to.
+__device__ __forceinline__ void resid_load(const GemmArgs& a, int m, int n0, int nvalid, float (&xo)[16]) {
+  const float* X = static_cast<const float*>(a.epi.out);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int t = n0 + j;
+    xo[j] = (j < nvalid && t < a.N && m < a.M) ? X[static_cast<int64_t>(t) * a.epi.ldo + m] : 0.f;
+  }
+}
+
+// xpre (residual epilogue): the chunk's X values, loaded earlier by the
+// caller (so a wide tile's next chunk loads while this one computes).
 template <int EPI>
 __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0, int row, int q, int lane,
                                           const float (&v0)[16], const float (&v1)[16], float* xch, float* red,
-                                          int nvalid = 16, const HeadPre* pre = nullptr) {
+                                          int nvalid = 16, const HeadPre* pre = nullptr,
+                                          const float (*xpre)[16] = nullptr) {
   const int m = m_tile * kTileM + row;
   if constexpr (EPI == EPI_RESID) {
     // X += v, and the tile's per-column sums of squares of the new X
@@ -222,10 +235,11 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
     // to X could alias the next load, and the loads would run one at a time
     float ss[16], xo[16];
     float* X = static_cast<float*>(a.epi.out);
+    if (xpre != nullptr) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int t = n0 + j;
-      xo[j] = (j < nvalid && t < a.N && m < a.M) ? X[static_cast<int64_t>(t) * a.epi.ldo + m] : 0.f;
+      for (int j = 0; j < 16; ++j) xo[j] = (*xpre)[j];
+    } else {
+      resid_load(a, m, n0, nvalid, xo);
     }
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -442,56 +456,69 @@ __device__ __forceinline__ void heads_cols(const GemmArgs& a, int m_tile, int n0
   for (int j = 0; j < 16; ++j) xch[j * (kTileM + 1) + row] = v0[j];
   named_bar_sync(1, 128);
   const float inv_d = 1.0f / static_cast<float>(d);  // d is a power of two: exact
+  // the four columns go through each step together (independent chains)
+  float y[4][4];
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) y[jj][i] = xch[(q + 4 * jj) * (kTileM + 1) + lane + 32 * i];
+  if (rot) {
+    float sq[4][4];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sq[jj][i] = y[jj][i] * y[jj][i];
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sq[jj][i] += __shfl_xor_sync(0xffffffffu, sq[jj][i], off);
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      float hs[4];
+      if (d == 128) {
+        const float s4 = ((sq[jj][0] + sq[jj][1]) + sq[jj][2]) + sq[jj][3];
+        hs[0] = hs[1] = hs[2] = hs[3] = s4;
+      } else if (d == 64) {
+        hs[0] = hs[1] = sq[jj][0] + sq[jj][1];
+        hs[2] = hs[3] = sq[jj][2] + sq[jj][3];
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) hs[i] = sq[jj][i];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) y[jj][i] = head_norm_apply(y[jj][i], head_norm_scale(hs[i], inv_d, a.epi.eps), g[i]);
+    }
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      float yp[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        yp[i] = d == 128 ? y[jj][i ^ 2] : d == 64 ? y[jj][i ^ 1] : __shfl_xor_sync(0xffffffffu, y[jj][i], 16);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) y[jj][i] = rope_rotate(y[jj][i], yp[i], cs[jj][i], dim[i] < half);
+    }
+  }
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) {
     const int j = q + 4 * jj;
     const int t = n0 + j;
     if (t >= a.N) break;
-    const int pos = tmeta[4 * j], strm = tmeta[4 * j + 1];
-    float y[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) y[i] = xch[j * (kTileM + 1) + lane + 32 * i];
-    if (rot) {
-      float s[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        s[i] = y[i] * y[i];
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) s[i] += __shfl_xor_sync(0xffffffffu, s[i], off);
-      }
-      float hs[4];
-      if (d == 128) {
-        const float s4 = ((s[0] + s[1]) + s[2]) + s[3];
-        hs[0] = hs[1] = hs[2] = hs[3] = s4;
-      } else if (d == 64) {
-        hs[0] = hs[1] = s[0] + s[1];
-        hs[2] = hs[3] = s[2] + s[3];
-      } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) hs[i] = s[i];
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) y[i] = head_norm_apply(y[i], head_norm_scale(hs[i], inv_d, a.epi.eps), g[i]);
-      float yp[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        yp[i] = d == 128 ? y[i ^ 2] : d == 64 ? y[i ^ 1] : __shfl_xor_sync(0xffffffffu, y[i], 16);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) y[i] = rope_rotate(y[i], yp[i], cs[jj][i], dim[i] < half);
-    }
     if (a.epi.pos_mode == 0) {
       __nv_bfloat16* dst = sg.dst + static_cast<int64_t>(t) * (sg.heads * d) + fbase + lane;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) dst[32 * i] = __float2bfloat16_rn(y[i]);
+      for (int i = 0; i < 4; ++i) dst[32 * i] = __float2bfloat16_rn(y[jj][i]);
     } else {
       // a later row of the same segment owns this ring slot
+      const int pos = tmeta[4 * j], strm = tmeta[4 * j + 1];
       if (sg.window > 0 && pos < tmeta[4 * j + 2] - sg.window) continue;
       const int slot = sg.window > 0 ? (pos % sg.window) : pos;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int head = (fbase + lane + 32 * i) / d;
         sg.dst[((static_cast<int64_t>(strm) * sg.heads + head) * sg.cap + slot) * d + dim[i]] =
-            __float2bfloat16_rn(y[i]);
+            __float2bfloat16_rn(y[jj][i]);
       }
     }
   }
@@ -734,13 +761,23 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
         clu_tile = u;  // reduced after the cluster barrier below
       } else if (args.ksplit == 1) {
         if constexpr (EPI == EPI_HEADS) stage_token_meta(args, n_tile * BN, BN, row, tmeta);
+        const int m = m_tile * kTileM + row;
+        float xn[16];  // residual: the next chunk's X, loaded a chunk ahead
+        if constexpr (EPI == EPI_RESID) resid_load(args, m, n_tile * BN, 16, xn);
         for (int c0 = 0; c0 < BN; c0 += 16) {
           tmem_ld16(tbase + c0, v0);
           if constexpr (DUAL) tmem_ld16(tbase + BN + c0, v1);
-          if constexpr (EPI == EPI_HEADS)
+          if constexpr (EPI == EPI_HEADS) {
             heads_cols(args, m_tile, n_tile * BN + c0, row, q, lane, v0, xch, tmeta + 4 * c0);
-          else
+          } else if constexpr (EPI == EPI_RESID) {
+            float xc[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) xc[j] = xn[j];
+            if (c0 + 16 < BN) resid_load(args, m, n_tile * BN + c0 + 16, 16, xn);
+            epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red, 16, nullptr, &xc);
+          } else {
             epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red);
+          }
         }
         tc_fence_before();
         mbar_arrive(&tempty[acc]);
@@ -769,6 +806,9 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
         if (last) {
           __threadfence();
           if constexpr (EPI == EPI_HEADS) stage_token_meta(args, n_tile * BN, BN, row, tmeta);
+          const int m = m_tile * kTileM + row;
+          float xn[16];  // residual: the next chunk's X, loaded a chunk ahead
+          if constexpr (EPI == EPI_RESID) resid_load(args, m, n_tile * BN, 16, xn);
           for (int c0 = 0; c0 < BN; c0 += 16) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -802,10 +842,17 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
                 }
               }
             }
-            if constexpr (EPI == EPI_HEADS)
+            if constexpr (EPI == EPI_HEADS) {
               heads_cols(args, m_tile, n_tile * BN + c0, row, q, lane, v0, xch, tmeta + 4 * c0);
-            else
+            } else if constexpr (EPI == EPI_RESID) {
+              float xc[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) xc[j] = xn[j];
+              if (c0 + 16 < BN) resid_load(args, m, n_tile * BN + c0 + 16, 16, xn);
+              epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red, 16, nullptr, &xc);
+            } else {
               epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red);
+            }
           }
         }
       }
@@ -1035,21 +1082,21 @@ static void fill_args(const GemmPlan& p, GemmArgs& a, int BN) {
 
 size_t gemm_partial_bytes(const GemmPlan& p) {
   if (p.ksplit <= 1) return 0;
-  const int BN = gemm_bn_for(p.N);
+  const int BN = plan_bn(p);
   const size_t units = static_cast<size_t>(p.M / kTileM) * ((p.N + BN - 1) / BN) * p.ksplit;
   return units * (p.a2_map ? 2 : 1) * BN * kTileM * sizeof(float);
 }
 
 size_t gemm_counter_count(const GemmPlan& p) {
-  const int BN = gemm_bn_for(p.N);
+  const int BN = plan_bn(p);
   return static_cast<size_t>(p.M / kTileM) * ((p.N + BN - 1) / BN);
 }
 
 int gemm_launch(const GemmPlan& p, float* partial, int* counters, int* err, int num_sms, cudaStream_t st) {
   if (p.M % kTileM || p.K % kTileK || p.Kp % kTileK || p.N <= 0 || p.n_aseg < 1 || p.n_aseg > kMaxASeg ||
-      p.n_b < 1 || p.n_b > kMaxBPlane || p.Kp * p.n_b != p.K)
+      p.n_b < 1 || p.n_b > kMaxBPlane || p.Kp * p.n_b != p.K || (p.bn != 0 && p.bn != 16 && p.bn != 128 && p.bn != 256))
     return DFLASH_E_SHAPE;
-  const int BN = gemm_bn_for(p.N);
+  const int BN = plan_bn(p);
   static thread_local GemmArgs a;  // ~4 KiB: kept off the stack
   memset(&a, 0, sizeof(a));
   fill_args(p, a, BN);

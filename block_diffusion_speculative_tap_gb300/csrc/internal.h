@@ -89,6 +89,7 @@ struct GemmPlan {
   int Kp = 0;       // reduction length of one B plane
   int M = 0, N = 0, K = 0;
   int ksplit = 1;
+  int bn = 0;               // token tile width (16, 128 or 256); 0: gemm_bn_for(N)
   bool no_cluster = false;  // split-K through global partials even when a cluster would fit
   int epi = EPI_STORE_F32;
   EpiArgs epi_args{};
@@ -99,6 +100,8 @@ struct GemmPlan {
 size_t gemm_partial_bytes(const GemmPlan& p);
 size_t gemm_counter_count(const GemmPlan& p);
 int gemm_bn_for(int N);
+// The token tile width a plan launches with.
+inline int plan_bn(const GemmPlan& p) { return p.bn ? p.bn : gemm_bn_for(p.N); }
 // Fixed split of the reduction for a weight matrix (independent of N).
 int gemm_choose_ksplit(int m_tiles, int kb_total, int num_sms);
 // Encode the TMA map of a K-contiguous bf16 matrix [rows, cols] (row stride ld

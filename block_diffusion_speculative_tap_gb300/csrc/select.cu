@@ -207,8 +207,15 @@ __device__ float range_topk(const __nv_bfloat16* row, int g_begin, int g_end, in
   const int wg1 = g_begin + static_cast<int>(static_cast<long long>(ng) * (w + 1) / kSelWarps);
   TopList<KM> tl;
   tl.init();
-  // four 16-byte loads in flight before any is ranked
-  for (int g0 = wg0 + lane; g0 < wg1; g0 += 4 * 32) {
+  // A lane's KM-th best is a lower bound of the warp's KM-th best, so a value
+  // strictly below the largest of them over the warp cannot be in the top KM:
+  // skipping those keeps most lanes off the insertion path (a warp runs it
+  // when any lane does).
+  float floor_v = -INFINITY;
+  // four 16-byte loads in flight before any is ranked; the trip count is
+  // the warp's (every lane reaches the shuffles)
+  for (int base = wg0; base < wg1; base += 4 * 32) {
+    const int g0 = base + lane;
     float x[4][8];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -225,9 +232,14 @@ __device__ float range_topk(const __nv_bfloat16* row, int g_begin, int g_end, in
       const int g = g0 + u * 32;
       if (g < wg1) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) tl.push(x[u][e], g * 8 + e);
+        for (int e = 0; e < 8; ++e)
+          if (!(x[u][e] < floor_v)) tl.push(x[u][e], g * 8 + e);
       }
     }
+    float f = tl.v[KM - 1];
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) f = fmaxf(f, __shfl_xor_sync(0xffffffffu, f, off));
+    floor_v = f;
   }
   if (k >= 1 && k <= KM && KM <= 16) {
     __shared__ float wv[kSelWarps * KM];
@@ -583,6 +595,9 @@ __device__ int weights_draw(const Weights& W, int V, float thr, const float* sw,
   return r;
 }
 
+// One CTA a row: the top-k (k <= KM) of the row and, with uniforms, one
+// inverse-CDF draw from softmax(row / T).
+template <int KM>
 __global__ void __launch_bounds__(kSelThreads) topk_kernel(const __nv_bfloat16* __restrict__ logits, int V, int k,
                                                            float invT, const float* __restrict__ uniforms,
                                                            int* __restrict__ ids, float* __restrict__ vals,
@@ -597,11 +612,11 @@ __global__ void __launch_bounds__(kSelThreads) topk_kernel(const __nv_bfloat16* 
   __shared__ float sval[kKMax];
   const int r = blockIdx.x;
   const __nv_bfloat16* row = logits + static_cast<int64_t>(r) * V;
-  const float mx = k <= 8 ? row_topk<8>(row, V, k, sid, sval, sv, si) : row_topk<kKMax>(row, V, k, sid, sval, sv, si);
+  const float mx = row_topk<KM>(row, V, k, sid, sval, sv, si);
   __syncthreads();
   if (threadIdx.x < k) {
     ids[static_cast<int64_t>(r) * k + threadIdx.x] = sid[threadIdx.x];
-    vals[static_cast<int64_t>(r) * k + threadIdx.x] = sval[threadIdx.x];
+    if (vals) vals[static_cast<int64_t>(r) * k + threadIdx.x] = sval[threadIdx.x];
   }
   if (uniforms != nullptr) {
     Weights W{row, nullptr, mx, 1.f, 0.f, 1.f, invT, 0};
@@ -843,17 +858,34 @@ int launch_topk_merge(const float* cand_v, const int* cand_i, int rows, int tile
   return cuda_status(e);
 }
 
+// Plain top-k scans: up to kClusterRows rows a row is split over a cluster of
+// kSlices CTAs (few rows: fill the GPU); more rows already fill it, and one
+// CTA a row avoids the cluster's fixed ranking and merge cost per slice. The
+// ranking is exact with ties to the lower id, so both give the same result.
+constexpr int kClusterRows = 64;
+
+template <int KM>
+cudaError_t launch_topk_scan(const __nv_bfloat16* logits, int rows, int V, int k, int* ids, float* vals,
+                             cudaStream_t st) {
+  if (rows <= kClusterRows) return launch_topk_cluster<KM>(logits, rows, V, k, ids, vals, st);
+  return launch_pdl(topk_kernel<KM>, dim3(rows), dim3(kSelThreads), 0, st, logits, V, k, 1.0f, nullptr, ids, vals,
+                    nullptr);
+}
+
 int launch_topk(const __nv_bfloat16* logits, int rows, int V, int k, float T, const float* uniforms, int* ids,
                 float* vals, int* sampled, cudaStream_t st) {
   if (rows <= 0) return DFLASH_OK;
   TraceScope ts(st, "topk", static_cast<double>(rows) * V * 2, 0.0);
   cudaError_t e;
   if (uniforms == nullptr && k >= 1) {
-    e = k <= 8 ? launch_topk_cluster<8>(logits, rows, V, k, ids, vals, st)
-               : launch_topk_cluster<kKMax>(logits, rows, V, k, ids, vals, st);
-  } else {
-    e = launch_pdl(topk_kernel, dim3(rows), dim3(kSelThreads), 0, st, logits, V, k, 1.0f / T, uniforms, ids, vals,
+    e = k <= 8 ? launch_topk_scan<8>(logits, rows, V, k, ids, vals, st)
+               : launch_topk_scan<kKMax>(logits, rows, V, k, ids, vals, st);
+  } else if (k <= 8) {
+    e = launch_pdl(topk_kernel<8>, dim3(rows), dim3(kSelThreads), 0, st, logits, V, k, 1.0f / T, uniforms, ids, vals,
                    sampled);
+  } else {
+    e = launch_pdl(topk_kernel<kKMax>, dim3(rows), dim3(kSelThreads), 0, st, logits, V, k, 1.0f / T, uniforms, ids,
+                   vals, sampled);
   }
   count_launch();
   return cuda_status(e);
@@ -863,7 +895,7 @@ int launch_verify_greedy(int S, int V, const int* draft, int dld, const __nv_bfl
                          cudaStream_t st) {
   {
     TraceScope ts(st, "verify.argmax", static_cast<double>(S) * 16 * V * 2, 0.0);
-    const cudaError_t e = launch_topk_cluster<1>(tl, S * 16, V, 1, out, nullptr, st);
+    const cudaError_t e = launch_topk_scan<1>(tl, S * 16, V, 1, out, nullptr, st);
     count_launch();
     if (e != cudaSuccess) return DFLASH_E_CUDA;
   }

@@ -40,9 +40,9 @@ def _tie_heavy(rows, V, seed):
     return x.to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("V,k", [(4096, 4), (151936, 8), (5000, 16), (136, 3)])
-def test_topk_matches_oracle(D, V, k):
-    rows = 37
+@pytest.mark.parametrize("rows", [37, 130])  # a cluster a row / a CTA a row
+@pytest.mark.parametrize("V,k", [(4096, 4), (151936, 8), (5000, 16), (136, 3), (151936, 1)])
+def test_topk_matches_oracle(D, V, k, rows):
     lg = SI.make_logits((rows, V), 1.0, seed=V + k)
     lg[5:9] = _tie_heavy(4, V, 3)  # rows full of exact ties
     ids, vals, _ = D.topk(lg.cuda(), k)
