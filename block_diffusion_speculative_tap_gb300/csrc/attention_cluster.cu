@@ -135,16 +135,25 @@ __device__ __forceinline__ void attend_tile(AttnState& S, const uint32_t (&qa)[k
   constexpr int kN = NK / 8;  // 8-key score tiles
   float sacc[kN][4];
 #pragma unroll
-  for (int n = 0; n < kN; ++n) {
-    sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
-    const int key = n * 8 + (lane & 7);
+  for (int n = 0; n < kN; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
+  // Each score tile accumulates its 8 k16 steps in order; the MMAs issue
+  // over groups of up to four score tiles, so consecutive MMAs are
+  // independent (a tile's own chain would wait out each MMA's latency).
+  constexpr int kGrp = kN < 4 ? kN : 4;
+#pragma unroll
+  for (int n0 = 0; n0 < kN; n0 += kGrp) {
 #pragma unroll
     for (int kp = 0; kp < kD / 32; ++kp) {
-      // four 8x8 matrices: dims [32kp, 32kp + 32) of keys n*8 .. n*8+7
-      uint32_t kb[4];
-      ldsm_x4(kb, t + static_cast<uint32_t>((kp >> 1) * kSub) + swz(key, 4 * (kp & 1) + (lane >> 3)));
-      mma16816(sacc[n], qa[2 * kp], kb[0], kb[1]);
-      mma16816(sacc[n], qa[2 * kp + 1], kb[2], kb[3]);
+      // four 8x8 matrices a tile: dims [32kp, 32kp + 32) of keys n*8 .. n*8+7
+      uint32_t kb[kGrp][4];
+#pragma unroll
+      for (int g = 0; g < kGrp; ++g)
+        ldsm_x4(kb[g], t + static_cast<uint32_t>((kp >> 1) * kSub) +
+                           swz((n0 + g) * 8 + (lane & 7), 4 * (kp & 1) + (lane >> 3)));
+#pragma unroll
+      for (int g = 0; g < kGrp; ++g) mma16816(sacc[n0 + g], qa[2 * kp], kb[g][0], kb[g][1]);
+#pragma unroll
+      for (int g = 0; g < kGrp; ++g) mma16816(sacc[n0 + g], qa[2 * kp + 1], kb[g][2], kb[g][3]);
     }
   }
   float tmax[2] = {-INFINITY, -INFINITY};
