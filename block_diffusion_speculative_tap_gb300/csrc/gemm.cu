@@ -144,46 +144,61 @@ __device__ __forceinline__ void publish_ss(const GemmArgs& a, const float (&sq)[
   named_bar_sync(1, 128);  // red reusable by the next chunk
 }
 
-// Heads-epilogue operands of one thread's columns, loaded while the main
-// loop runs (batch-1 cluster launches: one tile a CTA, at most kPre columns
-// a rank): positions, streams, the RoPE (cos, sin) of the thread's feature at
-// each position, and the feature's norm gain.
-constexpr int kPre = 8;
-struct HeadPre {
-  int pos[kPre];
-  int strm[kPre];
-  float2 cs[kPre];
-  float g;
+// Heads-epilogue operands of one warp's columns of a 16-column chunk
+// (columns q, q + 4, q + 8, q + 12 of warp q; lane l holds features l + 32i):
+// each column's position, stream and segment end, the RoPE (cos, sin) of the
+// lane's four features at that position, and the four features' norm gains.
+// Cluster launches load them while the MMAs run (under a full-rate weight
+// stream they would miss L2 after it).
+struct ColOps {
+  int pos[4], strm[4], rend[4];
+  float2 cs[4][4];
+  float g[4];
 };
 
-__device__ __forceinline__ void head_pre_load(const GemmArgs& a, int m_tile, int n0, int nvalid, int row,
-                                              HeadPre& pre) {
+// tmeta: the chunk's token metadata staged in shared memory
+// (stage_token_meta), or nullptr to read it from the epilogue arguments.
+// Columns at or past nvalid (or N) get position 0: their values are never
+// stored.
+__device__ __forceinline__ void col_ops_load(const GemmArgs& a, int m_tile, int n0, int nvalid, int q, int lane,
+                                             const int* tmeta, ColOps& o) {
   const int sidx = seg_of_tile(a, m_tile);
   const HeadSeg& sg = a.epi.seg[sidx];
   const int d = a.epi.head_dim;
-  const int f = (m_tile - a.a_seg_tile[sidx]) * kTileM + row;
-  const int dim = f % d;
   const int half = d >> 1;
-  const int fi = dim < half ? dim : dim - half;
   const bool rot = sg.kind != HEAD_V;
 #pragma unroll
-  for (int j = 0; j < kPre; ++j) {
+  for (int jj = 0; jj < 4; ++jj) {
+    const int j = q + 4 * jj;
     const int t = n0 + j;
-    int p = 0, sm = 0;
+    int p = 0, sm = 0, e = 0;
     if (j < nvalid && t < a.N) {
-      if (a.epi.pos_mode == 0) {
+      if (tmeta != nullptr) {
+        p = tmeta[4 * j];
+        sm = tmeta[4 * j + 1];
+        e = tmeta[4 * j + 2];
+      } else if (a.epi.pos_mode == 0) {
         sm = a.epi.s_begin + t / 16;
         p = a.epi.lens[sm] + (t & 15);
       } else {
         sm = a.epi.row_stream[t];
         p = a.epi.row_pos[t];
+        e = a.epi.row_end[t];
       }
     }
-    pre.pos[j] = p;
-    pre.strm[j] = sm;
-    pre.cs[j] = rot && j < nvalid && t < a.N ? a.epi.rope[static_cast<int64_t>(p) * half + fi] : make_float2(1.f, 0.f);
+    o.pos[jj] = p;
+    o.strm[jj] = sm;
+    o.rend[jj] = e;
   }
-  pre.g = rot ? __bfloat162float(sg.gain[dim]) : 1.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int dim = (lane + 32 * i) & (d - 1);  // d divides the tile's 128 rows
+    const int fi = dim < half ? dim : dim - half;
+    o.g[i] = rot ? __bfloat162float(sg.gain[dim]) : 1.f;
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj)
+      o.cs[jj][i] = rot ? a.epi.rope[static_cast<int64_t>(o.pos[jj]) * half + fi] : make_float2(1.f, 0.f);
+  }
 }
 
 // Heads epilogue of a whole tile (row-table mode or block mode): the
@@ -226,8 +241,7 @@ __device__ __forceinline__ void resid_load(const GemmArgs& a, int m, int n0, int
 template <int EPI>
 __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0, int row, int q, int lane,
                                           const float (&v0)[16], const float (&v1)[16], float* xch, float* red,
-                                          int nvalid = 16, const HeadPre* pre = nullptr,
-                                          const float (*xpre)[16] = nullptr) {
+                                          int nvalid = 16, const float (*xpre)[16] = nullptr) {
   const int m = m_tile * kTileM + row;
   if constexpr (EPI == EPI_RESID) {
     // X += v, and the tile's per-column sums of squares of the new X
@@ -326,131 +340,26 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
       const int64_t o = static_cast<int64_t>(t) * a.epi.ldo + m;
       static_cast<__nv_bfloat16*>(a.epi.out)[o] = __float2bfloat16_rn(silu_f(v0[j]) * v1[j]);
     }
-  } else {
-    // heads: per-head RMSNorm over d (q_norm / k_norm), rotate-half RoPE, bf16
-    const int sidx = seg_of_tile(a, m_tile);
-    const HeadSeg& sg = a.epi.seg[sidx];
-    const int d = a.epi.head_dim;
-    const int f = (m_tile - a.a_seg_tile[sidx]) * kTileM + row;  // feature inside the projection
-    const int head = f / d;
-    const int dim = f - head * d;
-    const int half = d >> 1;
-    int pos[16];
-    int strm[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int t = n0 + j;
-      pos[j] = 0;
-      strm[j] = 0;
-      if (pre != nullptr) {
-        if (j < kPre) {
-          pos[j] = pre->pos[j];
-          strm[j] = pre->strm[j];
-        }
-      } else if (j < nvalid && t < a.N) {
-        if (a.epi.pos_mode == 0) {
-          strm[j] = a.epi.s_begin + t / 16;
-          pos[j] = a.epi.lens[strm[j]] + (t & 15);
-        } else {
-          strm[j] = a.epi.row_stream[t];
-          pos[j] = a.epi.row_pos[t];
-        }
-      }
-    }
-    float y[16];
-    const int fi = dim < half ? dim : dim - half;
-    if (sg.kind != HEAD_V) {
-      // per-head sums of squares: warp partials (transpose reduction), then
-      // the head's warps in order
-      float sq[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) sq[j] = v0[j] * v0[j];
-      int jj;
-      const float w = warp_sum16(sq, lane, jj);
-      if ((lane & 1) == 0) red[q * 16 + jj] = w;
-      named_bar_sync(1, 128);
-      const int wph = d >> 5;  // warps per head (1, 2 or 4)
-      const int q0 = (q / wph) * wph;
-      // d is a power of two, so * (1/d) is exactly / d
-      const float inv_d = 1.0f / static_cast<float>(d);
-      const float g = pre != nullptr ? pre->g : __bfloat162float(sg.gain[dim]);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        float s = red[q0 * 16 + j];
-        for (int qq = 1; qq < wph; ++qq) s += red[(q0 + qq) * 16 + j];
-        y[j] = head_norm_apply(v0[j], head_norm_scale(s, inv_d, a.epi.eps), g);
-      }
-      // partner value (dim +- d/2) via shared memory
-#pragma unroll
-      for (int j = 0; j < 16; ++j) xch[row * 17 + j] = y[j];
-      named_bar_sync(1, 128);
-      const int prow = dim < half ? row + half : row - half;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float yp = xch[prow * 17 + j];
-        const float2 cs = pre != nullptr ? (j < kPre ? pre->cs[j] : make_float2(1.f, 0.f))
-                                         : a.epi.rope[static_cast<int64_t>(pos[j]) * half + fi];
-        y[j] = rope_rotate(y[j], yp, cs, dim < half);
-      }
-      named_bar_sync(1, 128);  // xch / red reusable by the next chunk
-    } else {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) y[j] = v0[j];
-    }
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int t = n0 + j;
-      if (j >= nvalid || t >= a.N) break;
-      int64_t o;
-      if (a.epi.pos_mode == 0) {
-        o = static_cast<int64_t>(t) * (sg.heads * d) + f;
-      } else {
-        // a later row of the same segment owns this ring slot
-        const int rend = a.epi.row_end[t];
-        if (sg.window > 0 && pos[j] < rend - sg.window) continue;
-        const int slot = sg.window > 0 ? (pos[j] % sg.window) : pos[j];
-        o = ((static_cast<int64_t>(strm[j]) * sg.heads + head) * sg.cap + slot) * d + dim;
-      }
-      sg.dst[o] = __float2bfloat16_rn(y[j]);
-    }
   }
 }
 
-// Heads epilogue of one chunk of 16 columns, a warp per column: the chunk's
-// fp32 accumulators pass through shared memory (xch[j][129]), then warp w
-// takes columns w, w + 4, w + 8, w + 12 with lane l holding the tile's
-// features l + 32 i (i = 0..3), so a head's sum of squares and the RoPE
-// partner (feature -+ d/2) are inside one warp: the partner is slice i ^ 2
-// (d = 128), i ^ 1 (d = 64) or lane l ^ 16 (d = 32). Each slice's sum is the
-// xor butterfly over offsets 16, 8, 4, 2, 1 (the tree of warp_sum16) and the
-// slices of a head add in feature order, as the row-per-thread epilogue adds
-// its warps, so both give the same bits. tmeta holds the chunk's token
-// metadata (stage_token_meta).
+// Heads epilogue (per-head RMSNorm over d with q_norm / k_norm gains,
+// rotate-half RoPE, bf16 out) of one chunk of up to 16 columns, a warp per
+// column: the chunk's fp32 accumulators pass through shared memory
+// (xch[j][129]), then warp w takes columns w, w + 4, w + 8, w + 12 with lane l
+// holding the tile's features l + 32 i (i = 0..3), so a head's sum of squares
+// and the RoPE partner (feature -+ d/2) are inside one warp: the partner is
+// slice i ^ 2 (d = 128), i ^ 1 (d = 64) or lane l ^ 16 (d = 32). Each slice's
+// sum is the xor butterfly over offsets 16, 8, 4, 2, 1 and the slices of a
+// head add in feature order. Columns at or past nvalid are not stored.
 __device__ __forceinline__ void heads_cols(const GemmArgs& a, int m_tile, int n0, int row, int q, int lane,
-                                           const float (&v0)[16], float* xch, const int* tmeta) {
+                                           const float (&v0)[16], float* xch, int nvalid, const ColOps& o) {
   const int sidx = seg_of_tile(a, m_tile);
   const HeadSeg& sg = a.epi.seg[sidx];
   const int d = a.epi.head_dim;
   const int half = d >> 1;
   const int fbase = (m_tile - a.a_seg_tile[sidx]) * kTileM;  // the tile's first feature in the projection
   const bool rot = sg.kind != HEAD_V;
-  int dim[4], fi[4];
-  float g[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    dim[i] = (lane + 32 * i) & (d - 1);  // d divides the tile's 128 rows
-    fi[i] = dim[i] < half ? dim[i] : dim[i] - half;
-    g[i] = rot ? __bfloat162float(sg.gain[dim[i]]) : 1.f;
-  }
-  // the RoPE values of this warp's four columns, in flight across the barriers
-  float2 cs[4][4];
-#pragma unroll
-  for (int jj = 0; jj < 4; ++jj) {
-    const int pos = tmeta[4 * (q + 4 * jj)];  // 0 past the end of the tile's tokens
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      cs[jj][i] = rot ? a.epi.rope[static_cast<int64_t>(pos) * half + fi[i]] : make_float2(1.f, 0.f);
-  }
   named_bar_sync(1, 128);  // the previous chunk's columns are done with xch
 #pragma unroll
   for (int j = 0; j < 16; ++j) xch[j * (kTileM + 1) + row] = v0[j];
@@ -488,7 +397,8 @@ __device__ __forceinline__ void heads_cols(const GemmArgs& a, int m_tile, int n0
         for (int i = 0; i < 4; ++i) hs[i] = sq[jj][i];
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) y[jj][i] = head_norm_apply(y[jj][i], head_norm_scale(hs[i], inv_d, a.epi.eps), g[i]);
+      for (int i = 0; i < 4; ++i)
+        y[jj][i] = head_norm_apply(y[jj][i], head_norm_scale(hs[i], inv_d, a.epi.eps), o.g[i]);
     }
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
@@ -497,27 +407,30 @@ __device__ __forceinline__ void heads_cols(const GemmArgs& a, int m_tile, int n0
       for (int i = 0; i < 4; ++i)
         yp[i] = d == 128 ? y[jj][i ^ 2] : d == 64 ? y[jj][i ^ 1] : __shfl_xor_sync(0xffffffffu, y[jj][i], 16);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) y[jj][i] = rope_rotate(y[jj][i], yp[i], cs[jj][i], dim[i] < half);
+      for (int i = 0; i < 4; ++i) {
+        const int dim = (lane + 32 * i) & (d - 1);
+        y[jj][i] = rope_rotate(y[jj][i], yp[i], o.cs[jj][i], dim < half);
+      }
     }
   }
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) {
     const int j = q + 4 * jj;
     const int t = n0 + j;
-    if (t >= a.N) break;
+    if (j >= nvalid || t >= a.N) break;
     if (a.epi.pos_mode == 0) {
       __nv_bfloat16* dst = sg.dst + static_cast<int64_t>(t) * (sg.heads * d) + fbase + lane;
 #pragma unroll
       for (int i = 0; i < 4; ++i) dst[32 * i] = __float2bfloat16_rn(y[jj][i]);
     } else {
       // a later row of the same segment owns this ring slot
-      const int pos = tmeta[4 * j], strm = tmeta[4 * j + 1];
-      if (sg.window > 0 && pos < tmeta[4 * j + 2] - sg.window) continue;
+      const int pos = o.pos[jj];
+      if (sg.window > 0 && pos < o.rend[jj] - sg.window) continue;
       const int slot = sg.window > 0 ? (pos % sg.window) : pos;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int head = (fbase + lane + 32 * i) / d;
-        sg.dst[((static_cast<int64_t>(strm) * sg.heads + head) * sg.cap + slot) * d + dim[i]] =
+        const int f = fbase + lane + 32 * i;
+        sg.dst[((static_cast<int64_t>(o.strm[jj]) * sg.heads + f / d) * sg.cap + slot) * d + (f & (d - 1))] =
             __float2bfloat16_rn(y[jj][i]);
       }
     }
@@ -546,7 +459,7 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   int clu_tile = -1;  // cluster split-K: this CTA's unit, once its partial is parked
-  HeadPre hpre;       // heads epilogue operands, preloaded (cluster launches)
+  ColOps cpre;        // heads epilogue operands, preloaded (cluster launches)
   bool have_pre = false;
 
   if (threadIdx.x == 0) {
@@ -708,14 +621,14 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
     for (int u = blockIdx.x; u < args.units; u += gridDim.x) {
       int m_tile, kc, n_tile;
       decode_unit<CLU>(args, u, m_tile, kc, n_tile);
-      if constexpr (EPI == EPI_HEADS && CLU && BN == 16) {
-        // the epilogue's gain, positions and RoPE values, loaded while the
+      if constexpr (EPI == EPI_HEADS && CLU) {
+        // the epilogue's gains, positions and RoPE values, loaded while the
         // MMAs run (under a full-rate weight stream they miss L2)
         const int ks = args.ksplit;
         const int rk = static_cast<int>(gemm_cluster_rank());
         const int cb = rk * BN / ks, ce = (rk + 1) * BN / ks;
-        if (ce - cb <= kPre) {
-          head_pre_load(args, m_tile, n_tile * BN + cb, ce - cb, row, hpre);
+        if (ce - cb <= 16) {
+          col_ops_load(args, m_tile, n_tile * BN + cb, ce - cb, q, lane, nullptr, cpre);
           have_pre = true;
         }
       } else if constexpr (EPI == EPI_HEADS) {
@@ -768,13 +681,15 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
           tmem_ld16(tbase + c0, v0);
           if constexpr (DUAL) tmem_ld16(tbase + BN + c0, v1);
           if constexpr (EPI == EPI_HEADS) {
-            heads_cols(args, m_tile, n_tile * BN + c0, row, q, lane, v0, xch, tmeta + 4 * c0);
+            ColOps o;
+            col_ops_load(args, m_tile, n_tile * BN + c0, 16, q, lane, tmeta + 4 * c0, o);
+            heads_cols(args, m_tile, n_tile * BN + c0, row, q, lane, v0, xch, 16, o);
           } else if constexpr (EPI == EPI_RESID) {
             float xc[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) xc[j] = xn[j];
             if (c0 + 16 < BN) resid_load(args, m, n_tile * BN + c0 + 16, 16, xn);
-            epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red, 16, nullptr, &xc);
+            epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red, 16, &xc);
           } else {
             epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red);
           }
@@ -843,13 +758,15 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
               }
             }
             if constexpr (EPI == EPI_HEADS) {
-              heads_cols(args, m_tile, n_tile * BN + c0, row, q, lane, v0, xch, tmeta + 4 * c0);
+              ColOps o;
+              col_ops_load(args, m_tile, n_tile * BN + c0, 16, q, lane, tmeta + 4 * c0, o);
+              heads_cols(args, m_tile, n_tile * BN + c0, row, q, lane, v0, xch, 16, o);
             } else if constexpr (EPI == EPI_RESID) {
               float xc[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) xc[j] = xn[j];
               if (c0 + 16 < BN) resid_load(args, m, n_tile * BN + c0 + 16, 16, xn);
-              epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red, 16, nullptr, &xc);
+              epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red, 16, &xc);
             } else {
               epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red);
             }
@@ -914,8 +831,17 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
             }
           }
         }
-        epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red, nv,
-                       have_pre ? &hpre : nullptr);
+        if constexpr (EPI == EPI_HEADS) {
+          if (have_pre) {
+            heads_cols(args, m_tile, n_tile * BN + c0, row, q, lane, v0, xch, nv, cpre);
+          } else {
+            ColOps o;
+            col_ops_load(args, m_tile, n_tile * BN + c0, nv, q, lane, nullptr, o);
+            heads_cols(args, m_tile, n_tile * BN + c0, row, q, lane, v0, xch, nv, o);
+          }
+        } else {
+          epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red, nv);
+        }
       }
     }
     __syncwarp();
