@@ -68,6 +68,10 @@ __device__ __forceinline__ uint32_t gemm_cluster_rank() {
 __device__ __forceinline__ void gemm_cluster_sync() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
+// The two halves of a cluster barrier: a thread arrives once its reads of
+// other CTAs' shared memory are done and waits before its CTA exits.
+__device__ __forceinline__ void gemm_cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void gemm_cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 __device__ __forceinline__ uint32_t gemm_mapa(uint32_t saddr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
@@ -787,6 +791,7 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
     // every rank has read them
     __syncwarp();
     gemm_cluster_sync();
+    bool arrived = false;
     if (warp >= 2 && named_bar_or(1, 128, clu_tile < 0 ? 1 : 0) == 0) {
       int m_tile, kc, n_tile;
       decode_unit<CLU>(args, clu_tile, m_tile, kc, n_tile);
@@ -804,32 +809,60 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
           v0[j] = 0.f;
           v1[j] = 0.f;
         }
-        // rank order; the loads of two ranks are issued before their adds
-        for (int r2 = 0; r2 < ks; r2 += 2) {
-          const bool two = r2 + 1 < ks;
-          const uint32_t ra = gemm_mapa(pbase, static_cast<uint32_t>(r2));
-          const uint32_t rb = gemm_mapa(pbase, static_cast<uint32_t>(two ? r2 + 1 : r2));
-          float a0[16], b0[16], a1[16], b1[16];
+        if (!DUAL && nv <= 4) {
+          // few columns a rank (batch-1 tiles): four ranks' loads in flight at once
+          for (int r0 = 0; r0 < ks; r0 += 4) {
+            float buf[4][4];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const uint32_t o0 = static_cast<uint32_t>(((c0 + j) * kTileM + row) * 4);
-            const uint32_t o1 = static_cast<uint32_t>(((BN + c0 + j) * kTileM + row) * 4);
-            a0[j] = j < nv ? gemm_ld_dsmem(ra + o0) : 0.f;
-            b0[j] = (j < nv && two) ? gemm_ld_dsmem(rb + o0) : 0.f;
-            if constexpr (DUAL) {
-              a1[j] = j < nv ? gemm_ld_dsmem(ra + o1) : 0.f;
-              b1[j] = (j < nv && two) ? gemm_ld_dsmem(rb + o1) : 0.f;
+            for (int r = 0; r < 4; ++r) {
+              const uint32_t ra = gemm_mapa(pbase, static_cast<uint32_t>(r0 + r < ks ? r0 + r : r0));
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                buf[r][j] = (r0 + r < ks && j < nv)
+                                ? gemm_ld_dsmem(ra + static_cast<uint32_t>(((c0 + j) * kTileM + row) * 4))
+                                : 0.f;
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              if (r0 + r < ks) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) v0[j] += buf[r][j];
+              }
             }
           }
+        } else {
+          // rank order; the loads of two ranks are issued before their adds
+          for (int r2 = 0; r2 < ks; r2 += 2) {
+            const bool two = r2 + 1 < ks;
+            const uint32_t ra = gemm_mapa(pbase, static_cast<uint32_t>(r2));
+            const uint32_t rb = gemm_mapa(pbase, static_cast<uint32_t>(two ? r2 + 1 : r2));
+            float a0[16], b0[16], a1[16], b1[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            v0[j] += a0[j];
-            if (two) v0[j] += b0[j];
-            if constexpr (DUAL) {
-              v1[j] += a1[j];
-              if (two) v1[j] += b1[j];
+            for (int j = 0; j < 16; ++j) {
+              const uint32_t o0 = static_cast<uint32_t>(((c0 + j) * kTileM + row) * 4);
+              const uint32_t o1 = static_cast<uint32_t>(((BN + c0 + j) * kTileM + row) * 4);
+              a0[j] = j < nv ? gemm_ld_dsmem(ra + o0) : 0.f;
+              b0[j] = (j < nv && two) ? gemm_ld_dsmem(rb + o0) : 0.f;
+              if constexpr (DUAL) {
+                a1[j] = j < nv ? gemm_ld_dsmem(ra + o1) : 0.f;
+                b1[j] = (j < nv && two) ? gemm_ld_dsmem(rb + o1) : 0.f;
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              v0[j] += a0[j];
+              if (two) v0[j] += b0[j];
+              if constexpr (DUAL) {
+                v1[j] += a1[j];
+                if (two) v1[j] += b1[j];
+              }
             }
           }
+        }
+        if (c0 + 16 >= ce) {
+          // the last remote reads are in registers: the other ranks may go
+          gemm_cluster_arrive();
+          arrived = true;
         }
         if constexpr (EPI == EPI_HEADS) {
           if (have_pre) {
@@ -844,8 +877,8 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
         }
       }
     }
-    __syncwarp();
-    gemm_cluster_sync();
+    if (!arrived) gemm_cluster_arrive();
+    gemm_cluster_wait();  // the partials stay alive until every rank has read them
   }
 
   tc_fence_before();
