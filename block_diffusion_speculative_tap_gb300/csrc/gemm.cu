@@ -464,6 +464,7 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
   const int lane = threadIdx.x & 31;
   int clu_tile = -1;  // cluster split-K: this CTA's unit, once its partial is parked
   ColOps cpre;        // heads epilogue operands, preloaded (cluster launches)
+  float xpre[16];     // residual epilogue: this rank's X values, preloaded (cluster launches)
   bool have_pre = false;
 
   if (threadIdx.x == 0) {
@@ -633,6 +634,15 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
         const int cb = rk * BN / ks, ce = (rk + 1) * BN / ks;
         if (ce - cb <= 16) {
           col_ops_load(args, m_tile, n_tile * BN + cb, ce - cb, q, lane, nullptr, cpre);
+          have_pre = true;
+        }
+      } else if constexpr (EPI == EPI_RESID && CLU) {
+        // the residual this rank adds to (final: the epilogue is past its PDL wait)
+        const int ks = args.ksplit;
+        const int rk = static_cast<int>(gemm_cluster_rank());
+        const int cb = rk * BN / ks, ce = (rk + 1) * BN / ks;
+        if (ce - cb <= 16) {
+          resid_load(args, m_tile * kTileM + row, n_tile * BN + cb, ce - cb, xpre);
           have_pre = true;
         }
       } else if constexpr (EPI == EPI_HEADS) {
@@ -810,11 +820,13 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
           v1[j] = 0.f;
         }
         if (!DUAL && nv <= 4) {
-          // few columns a rank (batch-1 tiles): four ranks' loads in flight at once
-          for (int r0 = 0; r0 < ks; r0 += 4) {
-            float buf[4][4];
+          // few columns a rank (batch-1 tiles): several ranks' loads in flight
+          // at once (four beside the heads epilogue's preloaded operands)
+          constexpr int kR = EPI == EPI_HEADS ? 4 : kMaxClusterSplit;
+          for (int r0 = 0; r0 < ks; r0 += kR) {
+            float buf[kR][4];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
+            for (int r = 0; r < kR; ++r) {
               const uint32_t ra = gemm_mapa(pbase, static_cast<uint32_t>(r0 + r < ks ? r0 + r : r0));
 #pragma unroll
               for (int j = 0; j < 4; ++j)
@@ -823,7 +835,7 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
                                 : 0.f;
             }
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
+            for (int r = 0; r < kR; ++r) {
               if (r0 + r < ks) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) v0[j] += buf[r][j];
@@ -872,6 +884,9 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
             col_ops_load(args, m_tile, n_tile * BN + c0, nv, q, lane, nullptr, o);
             heads_cols(args, m_tile, n_tile * BN + c0, row, q, lane, v0, xch, nv, o);
           }
+        } else if constexpr (EPI == EPI_RESID) {
+          epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red, nv,
+                         have_pre ? &xpre : nullptr);
         } else {
           epi_chunk<EPI>(args, m_tile, n_tile * BN + c0, row, q, lane, v0, v1, xch, red, nv);
         }
