@@ -154,3 +154,42 @@ def staged_parity(st, ref, rs, m, s, anchor, k):
     return ol
 
 
+
+
+def staged_parity_all(st, ref, m, anchors, k):
+    """Stage-isolated parity of all streams in one call per stage (the launch
+    shapes of a multi-stream draft): every stream's caches get the oracle's
+    K/V, each half layer and the head run on the oracle's inputs of all
+    streams at once, and every output must meet the tolerance."""
+    S = anchors.numel()
+    ols, Xss = [], []
+    for s in range(S):
+        ol, Xs = ref.draft(s, int(anchors[s]), keep_residuals=True)
+        ols.append(ol)
+        Xss.append(Xs)
+        C = ref.length(s)
+        assert st.length(s) == C
+        for l in range(m["n_layers"]):
+            K, V, cap = st.cache_view(l)
+            if m["layer_kinds"][l] == SI.SLIDING:
+                pos = np.arange(max(0, C - cap), C)
+                slots = torch.from_numpy(pos % cap)
+            else:
+                pos = np.arange(C)
+                slots = torch.from_numpy(pos)
+            K[s][:, slots.cuda()] = torch.from_numpy(ref.k[s][l][pos].transpose(1, 0, 2).copy()).to(torch.bfloat16).cuda()
+            V[s][:, slots.cuda()] = torch.from_numpy(ref.v[s][l][pos].transpose(1, 0, 2).copy()).to(torch.bfloat16).cuda()
+    for g in range(2 * m["n_layers"]):
+        X = torch.from_numpy(np.concatenate([Xs[g] for Xs in Xss]).astype(np.float32)).cuda()
+        st.draft_stages(X, g, g + 1, s_begin=0)
+        part = "attention" if g % 2 == 0 else "mlp"
+        rep = assert_close(X.cpu().numpy(), np.concatenate([Xs[g + 1] for Xs in Xss]), f"layer {g // 2} {part} residual")
+        print(f"stage layer {g // 2} {part} ({S} streams): {rep}")
+    X = torch.from_numpy(np.concatenate([Xs[-1] for Xs in Xss]).astype(np.float32)).cuda()
+    logits, ids, vals = st.draft_head(X, k=k)
+    ol = np.concatenate(ols)
+    rep = assert_close(logits.cpu().float().numpy(), ol, "head logits")
+    print(f"stage head ({S} streams): {rep}")
+    check_topk_consistent(logits, ids, vals)
+    checked, near, bad = topk_ids_match(ids.cpu().numpy(), ol, k, 2 * (ATOL + RTOL * np.abs(ol).max()))
+    assert bad == 0, (checked, near, bad)

@@ -11,12 +11,15 @@ import oracle as O
 import synthetic_inputs as SI
 from parity_util import (
     ATOL,
+    E2E_MEAN,
     RTOL,
     assert_close,
     check_topk_consistent,
     compare_draft,
     f64,
     staged_parity,
+    staged_parity_all,
+    tol_report,
     topk_ids_match,
 )
 
@@ -254,3 +257,46 @@ def test_wide_kv_rebuild_vs_oracle(D):
         assert torch.equal(K[0][:, 0:100], keep[l][0]) and torch.equal(V[0][:, 0:100], keep[l][1])
     rc, bits = st.status()
     assert rc == 0 and bits == 0
+
+
+def test_wide_round_throughput_paths(D):
+    """More than four streams a draft: the throughput GEMM configuration
+    (128-token tiles, global split-K with the last-arriver epilogues) and
+    attention clusters of fewer than eight CTAs, against the oracle."""
+    m = dict(
+        variant=1, hidden=2048, n_taps=4, tap_layers=[2, 9, 17, 25], target_layers=32, n_layers=2,
+        n_q_heads=16, n_kv_heads=8, head_dim=128, ffn=5632, vocab=8192, block=16, mask_token=8191,
+        causal=0, sliding_window=96, layer_kinds=[1, 0], rope_theta=1.0e6, rms_eps=1.0e-6,
+    )
+    w = SI.make_weights(m, 91, device="cuda")
+    dr = D.Drafter(m, w)
+    S = 24
+    g = torch.Generator().manual_seed(92)
+    ctx = torch.randint(1, 200, (S,), generator=g).tolist()
+    st = dr.new_state(S, 256)
+    ref = O.OracleStreams(m, O.weights_to_f64(w), S)
+    taps = SI.make_taps(m, sum(ctx), 93, device="cuda")
+    segs, r0 = [], 0
+    for s, c in enumerate(ctx):
+        segs.append((s, 0, c))
+        ref.append(s, [f64(t[r0 : r0 + c]) for t in taps])
+        r0 += c
+    st.fuse_taps(taps, segs)
+    for s in (0, S - 1):
+        check_state_vs_oracle(st, ref, m, s, ctx[s])
+    anchors = SI.anchor_ids(S, m["vocab"], m["mask_token"], 94)
+    # end to end: the mean (at hidden 2048 a few of the 122880 logits of a
+    # stream land just past the element-wise bound: bf16 flips between the
+    # layers, as for the six-layer drafters; this drafter's logits are too
+    # flat for the end-to-end id margin, the staged check below ranks them)
+    logits, ids, vals = st.draft(anchors.cuda(), k=8)
+    rc, bits = st.status()
+    assert rc == 0 and bits == 0, (rc, bits)
+    check_topk_consistent(logits, ids, vals)
+    lg = logits.cpu().float().numpy().reshape(S, 15, -1)
+    for s in range(S):
+        ol, _ = ref.draft(s, int(anchors[s]))
+        rep = tol_report(lg[s], ol)
+        assert rep["mean_abs"] < E2E_MEAN, (s, rep)
+    # stage by stage, all 24 streams a launch: every element within the tolerance
+    staged_parity_all(st, ref, m, anchors, 8)
