@@ -650,6 +650,34 @@ def run_reference(args):
     }
 
 
+def profile_workload(name):
+    """A small workload for an ncu capture of one kernel (no timing, no JSON
+    line): 'attention32' drafts 32 streams x 2048 context rows through a
+    two-layer 9B-shaped drafter (both layers sliding) three times, so the
+    many-stream attention launch is captured at a few GB of device memory."""
+    import torch
+
+    import block_diffusion_speculative_tap_gb300 as D
+    import synthetic_inputs as SI
+
+    if name != "attention32":
+        raise SystemExit(f"unknown profile workload {name}")
+    torch.cuda.set_device(0)
+    m = SI.shrink(SI.preset("9b")["model"], n_layers=2, layer_kinds=[SI.SLIDING] * 2)
+    S, C = 32, 2048
+    dr = D.Drafter(m, SI.make_weights(m, 5, device="cuda"))
+    st = dr.new_state(S, C + 1024)
+    for s in range(S):
+        st.fuse_taps(SI.make_taps(m, C, 100 + s, device="cuda"), [(s, 0, C)])
+    anchors = SI.anchor_ids(S, m["vocab"], m["mask_token"], 7, device="cuda")
+    for _ in range(3):
+        st.draft(anchors, k=8)
+    torch.cuda.synchronize()
+    rc, bits = st.status()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} bits {bits}")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -660,7 +688,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-configs", action="store_true", help="skip the supplementary workloads")
+    ap.add_argument("--profile-workload", default=None, help="run a small workload for ncu (attention32) and exit")
     args = ap.parse_args()
+    if args.profile_workload:
+        profile_workload(args.profile_workload)
+        return 0
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     if args.warmup < 3:

@@ -48,73 +48,6 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
-// Local sorted top list of one thread; elements arrive in ascending id order,
-// so a strict comparison keeps the lower id ahead on ties.
-template <int KM>
-struct TopList {
-  float v[KM];
-  int i[KM];
-  __device__ __forceinline__ void init() {
-#pragma unroll
-    for (int j = 0; j < KM; ++j) {
-      v[j] = -INFINITY;
-      i[j] = INT_MAX;
-    }
-  }
-  __device__ __forceinline__ void push(float x, int id) {
-    if (!(x > v[KM - 1])) return;
-    v[KM - 1] = x;
-    i[KM - 1] = id;
-#pragma unroll
-    for (int j = KM - 1; j > 0; --j) {
-      if (v[j] > v[j - 1]) {
-        const float tv = v[j];
-        v[j] = v[j - 1];
-        v[j - 1] = tv;
-        const int ti = i[j];
-        i[j] = i[j - 1];
-        i[j - 1] = ti;
-      }
-    }
-  }
-  __device__ __forceinline__ void pop() {
-#pragma unroll
-    for (int j = 0; j < KM - 1; ++j) {
-      v[j] = v[j + 1];
-      i[j] = i[j + 1];
-    }
-    v[KM - 1] = -INFINITY;
-    i[KM - 1] = INT_MAX;
-  }
-};
-
-// Block-wide best of every thread's (v, i); all threads receive it.
-__device__ __forceinline__ void block_best(float v, int i, float* sv, int* si, float& bv, int& bi) {
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, off);
-    const int oi = __shfl_xor_sync(0xffffffffu, i, off);
-    if (better(ov, oi, v, i)) {
-      v = ov;
-      i = oi;
-    }
-  }
-  const int w = threadIdx.x >> 5;
-  if ((threadIdx.x & 31) == 0) {
-    sv[w] = v;
-    si[w] = i;
-  }
-  __syncthreads();
-  bv = sv[0];
-  bi = si[0];
-  for (int j = 1; j < kSelWarps; ++j)
-    if (better(sv[j], si[j], bv, bi)) {
-      bv = sv[j];
-      bi = si[j];
-    }
-  __syncthreads();
-}
-
 // Inserts (x, xi) into a thread's sorted list (larger value, then lower id).
 template <int KM>
 __device__ __forceinline__ void list_insert(float (&v)[KM], int (&id)[KM], float x, int xi) {
@@ -194,26 +127,54 @@ __device__ float block_topk(float (&v)[KM], int (&id)[KM], int k, int* ids, floa
   return smx;
 }
 
-// Top-k (k <= KM) of the 8-element groups [g_begin, g_end) of a row into
-// (ids, vals) (thread 0 writes them); also returns the range maximum. The
-// 16 warps split the range into contiguous pieces, lanes interleave inside.
+// A warp's running top KM (KM <= 32) of (value, id) pairs, sorted (larger
+// value, then lower id): lane j < KM holds the j-th best. A candidate enters
+// at the rank counted by a ballot of the better entries, and the entries
+// after it move down one lane.
 template <int KM>
-__device__ float range_topk(const __nv_bfloat16* row, int g_begin, int g_end, int k, int* ids, float* vals,
-                            float* sv, int* si) {
+struct WarpTop {
+  float v = -INFINITY;
+  int i = INT_MAX;
+  __device__ __forceinline__ void insert(float x, int xi, int lane) {
+    const unsigned m = __ballot_sync(0xffffffffu, lane < KM && better(v, i, x, xi));
+    const int pos = __popc(m);  // the better entries are a prefix
+    if (pos >= KM) return;      // warp-uniform
+    const float pv = __shfl_up_sync(0xffffffffu, v, 1);
+    const int pi = __shfl_up_sync(0xffffffffu, i, 1);
+    if (lane > pos && lane < KM) {
+      v = pv;
+      i = pi;
+    }
+    if (lane == pos) {
+      v = x;
+      i = xi;
+    }
+  }
+};
+
+// Top-k (k <= KM <= 16) of the 8-element groups [g_begin, g_end) of a row
+// into (ids, vals) (thread 0 writes them); returns the range maximum to every
+// thread. The 16 warps split the range into contiguous pieces, lanes
+// interleave inside; each warp keeps its exact running top KM across its
+// lanes, and a lane's value competes only when it beats the warp's current
+// KM-th entry, so after the first few hundred values almost no value leaves
+// the load-compare path. Warp 0 merges the 16 warp lists (lane w walks warp
+// w's list).
+template <int KM>
+__device__ float range_topk(const __nv_bfloat16* row, int g_begin, int g_end, int k, int* ids, float* vals) {
+  static_assert(KM >= 1 && KM <= 16, "warp lists hold at most 16 entries");
   const int w = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int ng = g_end - g_begin;
   const int wg0 = g_begin + static_cast<int>(static_cast<long long>(ng) * w / kSelWarps);
   const int wg1 = g_begin + static_cast<int>(static_cast<long long>(ng) * (w + 1) / kSelWarps);
-  TopList<KM> tl;
-  tl.init();
-  // A lane's KM-th best is a lower bound of the warp's KM-th best, so a value
-  // strictly below the largest of them over the warp cannot be in the top KM:
-  // skipping those keeps most lanes off the insertion path (a warp runs it
-  // when any lane does).
-  float floor_v = -INFINITY;
+  WarpTop<KM> wt;
+  float fv = -INFINITY;  // the warp's KM-th entry (lane KM - 1), broadcast
+  int fi = INT_MAX;
+  float lv = -INFINITY;  // KM == 1: the lane's own running best
+  int li = INT_MAX;
   // four 16-byte loads in flight before any is ranked; the trip count is
-  // the warp's (every lane reaches the shuffles)
+  // the warp's (every lane reaches the ballots)
   for (int base = wg0; base < wg1; base += 4 * 32) {
     const int g0 = base + lane;
     float x[4][8];
@@ -227,44 +188,76 @@ __device__ float range_topk(const __nv_bfloat16* row, int g_begin, int g_end, in
         for (int e = 0; e < 8; ++e) x[u][e] = -INFINITY;
       }
     }
+    if constexpr (KM == 1) {
+      // arg-max: a compare-select a value, one warp reduction at the end
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int g = g0 + u * 32;
-      if (g < wg1) {
+      for (int u = 0; u < 4; ++u)
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if (!(x[u][e] < floor_v)) tl.push(x[u][e], g * 8 + e);
+        for (int e = 0; e < 8; ++e) {
+          const int id = (g0 + u * 32) * 8 + e;
+          if (g0 + u * 32 < wg1 && better(x[u][e], id, lv, li)) {
+            lv = x[u][e];
+            li = id;
+          }
+        }
+    } else {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int id = (g0 + u * 32) * 8 + e;
+          unsigned cand = __ballot_sync(0xffffffffu, g0 + u * 32 < wg1 && better(x[u][e], id, fv, fi));
+          while (cand) {
+            const int src = __ffs(cand) - 1;
+            cand &= cand - 1;
+            const float cv = __shfl_sync(0xffffffffu, x[u][e], src);
+            const int ci = __shfl_sync(0xffffffffu, id, src);
+            if (better(cv, ci, fv, fi)) {  // the floor may have risen since the ballot
+              wt.insert(cv, ci, lane);
+              fv = __shfl_sync(0xffffffffu, wt.v, KM - 1);
+              fi = __shfl_sync(0xffffffffu, wt.i, KM - 1);
+            }
+          }
+        }
       }
     }
-    float f = tl.v[KM - 1];
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) f = fmaxf(f, __shfl_xor_sync(0xffffffffu, f, off));
-    floor_v = f;
   }
-  if (k >= 1 && k <= KM && KM <= 16) {
-    __shared__ float wv[kSelWarps * KM];
-    __shared__ int wi[kSelWarps * KM];
-    return block_topk<KM>(tl.v, tl.i, k, ids, vals, wv, wi);
+  if constexpr (KM == 1) {
+    warp_best(lv, li);
+    wt.v = lv;
+    wt.i = li;
   }
-  float mx = -INFINITY;
-  const int rounds = k < 1 ? 1 : k;
-  for (int r = 0; r < rounds; ++r) {
-    float bv;
-    int bi;
-    block_best(tl.v[0], tl.i[0], sv, si, bv, bi);
-    if (r == 0) mx = bv;
-    if (tl.i[0] == bi) tl.pop();
-    if (threadIdx.x == 0 && r < k) {
-      ids[r] = bi;
-      vals[r] = bv;
+  __shared__ float wv[kSelWarps * KM];
+  __shared__ int wi[kSelWarps * KM];
+  __shared__ float smx;
+  if (lane < KM) {
+    wv[w * KM + lane] = wt.v;
+    wi[w * KM + lane] = wt.i;
+  }
+  __syncthreads();
+  if (w == 0) {
+    int pos = 0;
+    const int rounds = k < 1 ? 1 : k;
+    for (int r = 0; r < rounds; ++r) {
+      float bv = lane < kSelWarps && pos < KM ? wv[lane * KM + pos] : -INFINITY;
+      int bi = lane < kSelWarps && pos < KM ? wi[lane * KM + pos] : INT_MAX;
+      const int mine = bi;
+      warp_best(bv, bi);
+      if (r == 0 && lane == 0) smx = bv;
+      if (mine == bi && lane < kSelWarps) ++pos;
+      if (lane == 0 && r < k) {
+        ids[r] = bi;
+        if (vals) vals[r] = bv;
+      }
     }
   }
-  return mx;
+  __syncthreads();
+  return smx;
 }
 
 template <int KM>
-__device__ float row_topk(const __nv_bfloat16* row, int V, int k, int* ids, float* vals, float* sv, int* si) {
-  return range_topk<KM>(row, 0, V >> 3, k, ids, vals, sv, si);
+__device__ float row_topk(const __nv_bfloat16* row, int V, int k, int* ids, float* vals) {
+  return range_topk<KM>(row, 0, V >> 3, k, ids, vals);
 }
 
 // ---------------------------------------------------------------- cluster top-k
@@ -304,8 +297,6 @@ template <int KM>
 __global__ void __launch_bounds__(kSelThreads) topk_cluster_kernel(const __nv_bfloat16* __restrict__ logits, int V,
                                                                    int k, int* __restrict__ ids,
                                                                    float* __restrict__ vals) {
-  __shared__ float sv[kSelWarps];
-  __shared__ int si[kSelWarps];
   __shared__ int cid[kKMax];
   __shared__ float cval[kKMax];
   pdl_trigger();
@@ -315,7 +306,7 @@ __global__ void __launch_bounds__(kSelThreads) topk_cluster_kernel(const __nv_bf
   const int ng = V >> 3;
   const int g0 = static_cast<int>(static_cast<long long>(ng) * rank / kSlices);
   const int g1 = static_cast<int>(static_cast<long long>(ng) * (rank + 1) / kSlices);
-  range_topk<KM>(logits + static_cast<int64_t>(row) * V, g0, g1, k, cid, cval, sv, si);
+  range_topk<KM>(logits + static_cast<int64_t>(row) * V, g0, g1, k, cid, cval);
   __syncthreads();
   cluster_sync_all();
   if (rank == 0) {
@@ -604,15 +595,13 @@ __global__ void __launch_bounds__(kSelThreads) topk_kernel(const __nv_bfloat16* 
                                                            int* __restrict__ sampled) {
   pdl_trigger();
   pdl_wait();
-  __shared__ float sv[kSelWarps];
-  __shared__ int si[kSelWarps];
   __shared__ float sw[kSelWarps];
   __shared__ int sres[1];
   __shared__ int sid[kKMax];
   __shared__ float sval[kKMax];
   const int r = blockIdx.x;
   const __nv_bfloat16* row = logits + static_cast<int64_t>(r) * V;
-  const float mx = row_topk<KM>(row, V, k, sid, sval, sv, si);
+  const float mx = row_topk<KM>(row, V, k, sid, sval);
   __syncthreads();
   if (threadIdx.x < k) {
     ids[static_cast<int64_t>(r) * k + threadIdx.x] = sid[threadIdx.x];
@@ -659,8 +648,6 @@ __global__ void __launch_bounds__(kSelThreads) softmax_stats_kernel(const __nv_b
                                                                     float invT, float* __restrict__ stats) {
   pdl_trigger();
   pdl_wait();
-  __shared__ float sv[kSelWarps];
-  __shared__ int si[kSelWarps];
   __shared__ float sw[kSelWarps];
   __shared__ int sid[1];
   __shared__ float sval[1];
@@ -668,7 +655,7 @@ __global__ void __launch_bounds__(kSelThreads) softmax_stats_kernel(const __nv_b
   const int s = blockIdx.y;
   const __nv_bfloat16* row =
       r < 16 ? tl + (static_cast<int64_t>(s) * 16 + r) * V : dl + (static_cast<int64_t>(s) * 15 + (r - 16)) * V;
-  const float mx = row_topk<1>(row, V, 1, sid, sval, sv, si);
+  const float mx = row_topk<1>(row, V, 1, sid, sval);
   Weights W{row, nullptr, mx, 1.f, 0.f, 1.f, invT, 0};
   const float tot = weights_total(W, V, sw);
   if (threadIdx.x == 0) {
