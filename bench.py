@@ -276,7 +276,10 @@ def run_ours(args, rank, world):
     ctx = SI.make_taps(m, C0, seed + 1, device=dev)
     st.fuse_taps(ctx, [(0, 0, C0)])
     del ctx
-    step_taps = SI.make_taps(m, 16, seed + 2, device=dev)
+    # a round's 16 tap rows of every tap layer in one buffer [n_taps, 16, H]
+    # (one host-to-device copy a round end to end); the planes are its slices
+    taps_buf = torch.stack(SI.make_taps(m, 16, seed + 2, device=dev)).contiguous()
+    step_taps = [taps_buf[i] for i in range(taps_buf.shape[0])]
     anchor = SI.anchor_ids(1, m["vocab"], m["mask_token"], seed + 3, device=dev)
     tl = SI.make_logits((1, 16, m["vocab"]), 1.0, seed + 4, device=dev)
     logits = torch.empty(15, m["vocab"], dtype=torch.bfloat16, device=dev)
@@ -419,22 +422,33 @@ def run_ours(args, rank, world):
     del st2, fill_taps
 
     # ---- e2e: host buffers, copies inside the timed region, one readback a step
-    h_taps = [t.cpu().pin_memory() for t in step_taps]
+    h_taps = taps_buf.cpu().pin_memory()
     h_anchor = anchor.cpu().pin_memory()
     h_tl = tl.cpu().pin_memory()
     h_acc = torch.empty(1, dtype=torch.int32).pin_memory()
     h_toks = torch.empty(1, 16, dtype=torch.int32).pin_memory()
     h_ids = torch.empty(15, 8, dtype=torch.int32).pin_memory()
-    h2d = sum(t.numel() * 2 for t in h_taps) + 4 + h_tl.numel() * 2
+    h2d = h_taps.numel() * 2 + 4 + h_tl.numel() * 2
+    # the target logits (the bulk of the bytes; needed only by verification)
+    # travel on a side stream, queued behind the tap copy, under the draft
+    side = torch.cuda.Stream(device=dev)
+    e_go, e_tl = torch.cuda.Event(), torch.cuda.Event()
     d2h = 4 + 64 + 15 * 8 * 4
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(args.e2e_steps):
-        for d_, h_ in zip(step_taps, h_taps):
-            d_.copy_(h_, non_blocking=True)
+        taps_buf.copy_(h_taps, non_blocking=True)
         anchor.copy_(h_anchor, non_blocking=True)
-        tl.copy_(h_tl, non_blocking=True)
-        step()
+        e_go.record(stream)
+        with torch.cuda.stream(side):
+            side.wait_event(e_go)
+            tl.copy_(h_tl, non_blocking=True)
+            e_tl.record(side)
+        C = st.length(0)
+        st.fuse_taps(step_taps, [(0, C, 16)])
+        st.draft(anchor, k=8, logits=logits, ids=ids, vals=vals)
+        stream.wait_event(e_tl)
+        D.verify_greedy(ids, tl, accept=acc, tokens=toks)
         h_acc.copy_(acc, non_blocking=True)
         h_toks.copy_(toks, non_blocking=True)
         h_ids.copy_(ids, non_blocking=True)

@@ -162,6 +162,11 @@ class State:
         self.st = st
         self.ws_fuse = _Workspace(drafter.device)
         self.ws_draft = _Workspace(drafter.device)
+        # argument marshalling kept between calls: workspace sizes by shape,
+        # and the pointer array of the last validated list of tap planes
+        self._ws_bytes = {}
+        self._planes = None
+        self._planes_arr = None
 
     def __del__(self):
         try:
@@ -212,17 +217,33 @@ class State:
         """planes: N bf16 CUDA tensors [rows, H] (same row stride);
         segments: list of (stream, start, rows)."""
         m = self.drafter.model
-        if len(planes) != m["n_taps"]:
-            raise ValueError("one plane per tap")
-        stride = planes[0].stride(0)
-        for p in planes:
-            if p.dtype != torch.bfloat16 or p.device.type != "cuda" or p.stride(1) != 1 or p.stride(0) != stride:
-                raise ValueError("planes: bf16 CUDA [rows, H] with a common row stride")
+        cached = self._planes
+        if (
+            cached is not None
+            and len(planes) == len(cached[0])
+            and all(p is q for p, q in zip(planes, cached[0]))
+            and [p.data_ptr() for p in planes] == cached[1]
+        ):
+            # the same tensors as the last call (a capture buffer reused every round)
+            arr, stride = self._planes_arr
+        else:
+            if len(planes) != m["n_taps"]:
+                raise ValueError("one plane per tap")
+            stride = planes[0].stride(0)
+            for p in planes:
+                if p.dtype != torch.bfloat16 or p.device.type != "cuda" or p.stride(1) != 1 or p.stride(0) != stride:
+                    raise ValueError("planes: bf16 CUDA [rows, H] with a common row stride")
+            arr = (C.c_void_p * len(planes))(*[p.data_ptr() for p in planes])
+            self._planes = (list(planes), [p.data_ptr() for p in planes])
+            self._planes_arr = (arr, stride)
         rows = sum(r for _, _, r in segments)
-        nb = C.c_size_t()
-        check(lib.dflash_fuse_workspace_bytes(self.drafter.handle, rows, C.byref(nb)), "fuse_workspace_bytes")
-        ws = self.ws_fuse.get(nb.value)
-        arr = (C.c_void_p * len(planes))(*[p.data_ptr() for p in planes])
+        key = ("fuse", rows)
+        nbytes = self._ws_bytes.get(key)
+        if nbytes is None:
+            nb = C.c_size_t()
+            check(lib.dflash_fuse_workspace_bytes(self.drafter.handle, rows, C.byref(nb)), "fuse_workspace_bytes")
+            nbytes = self._ws_bytes[key] = nb.value
+        ws = self.ws_fuse.get(nbytes)
         n = len(segments)
         ss = (C.c_int32 * n)(*[s for s, _, _ in segments])
         st = (C.c_int64 * n)(*[b for _, b, _ in segments])
@@ -268,7 +289,11 @@ class State:
                 ids = torch.empty(S * 15, k, dtype=torch.int32, device=dev)
             if vals is None:
                 vals = torch.empty(S * 15, k, dtype=torch.float32, device=dev)
-        ws = self.ws_draft.get(self.draft_workspace_bytes(S, logits is None))
+        key = ("draft", S, logits is None)
+        nbytes = self._ws_bytes.get(key)
+        if nbytes is None:
+            nbytes = self._ws_bytes[key] = self.draft_workspace_bytes(S, logits is None)
+        ws = self.ws_draft.get(nbytes)
         check(
             lib.dflash_draft_block(
                 self.drafter.handle,
