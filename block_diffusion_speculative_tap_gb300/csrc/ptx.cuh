@@ -1,8 +1,9 @@
 // Inline-PTX building blocks for sm_103a: mbarriers, TMA tile loads and the
 // fifth-generation tensor-core path (tcgen05: TMEM allocation, MMA with fp32
 // accumulators in tensor memory, commit to an mbarrier, loads back to
-// registers). Every wait is bounded by the global timer so that no kernel can
-// spin forever: on expiry it reports through an error word and returns false.
+// registers). Every wait is bounded by the SM's cycle counter so that no
+// kernel can spin forever: on expiry it reports through an error word and
+// returns false.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -10,17 +11,14 @@
 
 namespace dfl {
 
-// A wait that has not completed after this many nanoseconds is abandoned.
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+// A wait that has not completed after this many SM cycles is abandoned
+// (about 1.5 s at the 2.07 GHz maximum clock, longer at lower clocks). The
+// cycle counter only moves forward; the global timer follows system time,
+// which the driver may adjust, so it is not used to bound waits.
+constexpr long long kWaitLimitCycles = 3000000000ll;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
 }
 
 // ---------------------------------------------------------------- mbarrier
@@ -54,18 +52,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase of the given parity. Gives up after kWaitLimitNs, sets
+// Wait for the phase of the given parity. Gives up after kWaitLimitCycles, sets
 // `flag` in *err and returns false. A shared abort word lets the other roles
 // of the CTA stop waiting as soon as one of them gave up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int flag,
                                           volatile int* abort_word) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
+  const long long c0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0u) {
       if (abort_word != nullptr && *abort_word) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
+      if (clock64() - c0 > kWaitLimitCycles) {
         if (err) atomicOr(err, flag);
         if (abort_word != nullptr) *abort_word = 1;
         return false;

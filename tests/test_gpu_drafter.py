@@ -300,3 +300,29 @@ def test_wide_round_throughput_paths(D):
         assert rep["mean_abs"] < E2E_MEAN, (s, rep)
     # stage by stage, all 24 streams a launch: every element within the tolerance
     staged_parity_all(st, ref, m, anchors, 8)
+
+
+def test_fuse_reused_plane_list(D):
+    """The binding reuses a validated list of tap planes between calls: new
+    data written into the same buffers, and a list whose element was
+    replaced, must both reach the fill."""
+    P = SI.preset("tiny")
+    m = P["model"]
+    w = SI.make_weights(m, 31, device="cuda")
+    dr = D.Drafter(m, w)
+    st = dr.new_state(1, 64)
+    ref = O.OracleStreams(m, O.weights_to_f64(w), 1)
+    rounds = [SI.make_taps(m, 16, 40 + r, device="cuda") for r in range(3)]
+    buf = torch.stack(rounds[0]).contiguous()
+    planes = [buf[i] for i in range(buf.shape[0])]
+    st.fuse_taps(planes, [(0, 0, 16)])  # first call: validated and kept
+    ref.append(0, [f64(t) for t in rounds[0]])
+    buf.copy_(torch.stack(rounds[1]))  # same tensors, new rows
+    st.fuse_taps(planes, [(0, 16, 16)])
+    ref.append(0, [f64(t) for t in rounds[1]])
+    buf.copy_(torch.stack(rounds[2]))
+    other = rounds[0][2].clone()  # one plane replaced by another tensor
+    planes[2] = other
+    st.fuse_taps(planes, [(0, 32, 16)])
+    ref.append(0, [f64(planes[i]) for i in range(len(planes))])
+    check_state_vs_oracle(st, ref, m, 0, 48)
