@@ -261,7 +261,12 @@ __global__ void __launch_bounds__(32 * (2 * G + 1), G <= 2 ? 2 : 1) attn_cluster
   }
   __syncthreads();
   pdl_trigger();
-  pdl_wait();
+  // The context K/V tiles and the stream lengths come from earlier fills,
+  // which every draft call's stream-ordered workspace reset completes before
+  // its first kernel: the producer loads the first stages before the PDL
+  // wait. Q and the block's own K/V come from the Q/K/V GEMM, after it.
+  const bool producer = warp == 2 * G && lane == 0;
+  if (!producer) pdl_wait();
 
   const int s = a.s_begin + si;
   const int C = a.lens[s];
@@ -275,6 +280,17 @@ __global__ void __launch_bounds__(32 * (2 * G + 1), G <= 2 ? 2 : 1) attn_cluster
 
   if (warp == ncons) {
     if (lane == 0) {
+      const int npre = nt < kStages ? nt : kStages;
+      for (int t = 0; t < npre; ++t) {  // fresh stages: nothing to wait for
+        mbar_arrive_expect_tx(&full[t], kTileBytes);
+        const uint32_t d = sbase + ClusterAttnSmem::kStageOff + t * kTileBytes;
+        const int row = k0 + t * kKeys;
+        tma3d(d, &P.kmap, &full[t], 0, row, slab);
+        tma3d(d + kSubBytes, &P.kmap, &full[t], 64, row, slab);
+        tma3d(d + 2 * kSubBytes, &P.vmap, &full[t], 0, row, slab);
+        tma3d(d + 3 * kSubBytes, &P.vmap, &full[t], 64, row, slab);
+      }
+      pdl_wait();
       if (has_block) {
         mbar_arrive_expect_tx(blkbar, 4 * kBlockSubBytes);
         const uint32_t b = sbase + ClusterAttnSmem::kBlockOff;
@@ -283,7 +299,7 @@ __global__ void __launch_bounds__(32 * (2 * G + 1), G <= 2 ? 2 : 1) attn_cluster
         tma2d(b + 2 * kBlockSubBytes, &P.vbmap, blkbar, kvh * kD, 16 * si);
         tma2d(b + 3 * kBlockSubBytes, &P.vbmap, blkbar, kvh * kD + 64, 16 * si);
       }
-      for (int t = 0; t < nt; ++t) {
+      for (int t = npre; t < nt; ++t) {
         const int st = t % kStages;
         if (!mbar_wait(&empty[st], ((t / kStages) & 1) ^ 1u, err, DFLASH_STATUS_TIMEOUT, nullptr)) break;
         mbar_arrive_expect_tx(&full[st], kTileBytes);
