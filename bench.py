@@ -437,15 +437,16 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(args.e2e_steps):
+        # the fill goes first, so the GPU starts while the host queues the rest
         taps_buf.copy_(h_taps, non_blocking=True)
-        anchor.copy_(h_anchor, non_blocking=True)
         e_go.record(stream)
+        C = st.length(0)
+        st.fuse_taps(step_taps, [(0, C, 16)])
         with torch.cuda.stream(side):
             side.wait_event(e_go)
             tl.copy_(h_tl, non_blocking=True)
             e_tl.record(side)
-        C = st.length(0)
-        st.fuse_taps(step_taps, [(0, C, 16)])
+        anchor.copy_(h_anchor, non_blocking=True)
         st.draft(anchor, k=8, logits=logits, ids=ids, vals=vals)
         stream.wait_event(e_tl)
         D.verify_greedy(ids, tl, accept=acc, tokens=toks)
