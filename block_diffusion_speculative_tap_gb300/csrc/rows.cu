@@ -1,31 +1,18 @@
 // Row-wise kernels of the hot path: block embedding, RMSNorm of the fp32
 // residual into bf16 GEMM operands, the hidden_norm that turns fc's output
-// into fused ring rows, and the bookkeeping of appended rows.
+// into fused ring rows, the K/V rows of wide fills, and the bookkeeping of
+// appended rows.
 //
-// Each row is reduced by one CTA in a fixed order (per-thread strided sums,
-// then a warp tree, then the warps in order), so results do not depend on
-// which other rows share the launch.
+// A row's sum of squares arrives as per-128-feature parts (published by the
+// kernel that wrote the row, or by row_sumsq) and is summed in part order, so
+// the norms are elementwise and a row's result does not depend on which other
+// rows share the launch.
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace dfl {
 
 namespace {
-
-constexpr int kRowThreads = 256;
-
-__device__ __forceinline__ float block_sum(float v, float* red) {
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  const int w = threadIdx.x >> 5;
-  if ((threadIdx.x & 31) == 0) red[w] = v;
-  __syncthreads();
-  float t = 0.f;
-  const int nw = blockDim.x >> 5;
-  for (int i = 0; i < nw; ++i) t += red[i];
-  __syncthreads();
-  return t;
-}
 
 // Per-128-feature sums of squares of one row, ss[p * ss_ld + t], for an
 // input norm fused into the GEMM that reads the row next (lane sums of four
@@ -113,15 +100,22 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_rows_kernel(__nv_bfloat1
                                                                     const float* __restrict__ ss, int ss_ld, int H,
                                                                     float inv_h, float eps, int mask_rows_only) {
   pdl_trigger();
-  pdl_wait();
   const int r = blockIdx.y;
   const int src = mask_rows_only ? (r / 15) * 16 + 1 + (r % 15) : r;
   const int i = (blockIdx.x * kNormThreads + threadIdx.x) * 8;  // first feature
+  const bool live = i < H;
+  // the gain is a weight: loaded before the wait; the row's values are
+  // loaded before its sum of squares is reduced (no round trip in between)
+  const uint4 gr = live ? *reinterpret_cast<const uint4*>(g + i) : make_uint4(0, 0, 0, 0);
+  pdl_wait();
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+  if (live) {
+    const float4* xr = reinterpret_cast<const float4*>(x + static_cast<int64_t>(src) * H + i);
+    a = __ldcg(xr);
+    b = __ldcg(xr + 1);
+  }
   const float rstd = parts_rstd(ss, ss_ld, src, H, inv_h, eps);
-  if (i >= H) return;
-  const float4* xr = reinterpret_cast<const float4*>(x + static_cast<int64_t>(src) * H + i);
-  const float4 a = xr[0], b = xr[1];
-  const uint4 gr = *reinterpret_cast<const uint4*>(g + i);
+  if (!live) return;
   const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gr);
   const float xs[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
   uint4 o;
@@ -149,12 +143,18 @@ __global__ void __launch_bounds__(128) hidden_norm_kernel(__nv_bfloat16* __restr
   pdl_trigger();
   pdl_wait();
   const int r = blockIdx.y;
-  const float rstd = parts_rstd(ss, rows, r, H, inv_h, eps);
   const int i = (blockIdx.x * 128 + threadIdx.x) * 8;
-  if (i >= H) return;
-  const float4* yr = reinterpret_cast<const float4*>(y + static_cast<int64_t>(r) * H + i);
-  const float4 a = yr[0], b = yr[1];
-  const uint4 gr = *reinterpret_cast<const uint4*>(g + i);
+  const bool live = i < H;
+  // the row's values are loaded before its sum of squares is reduced
+  const uint4 gr = live ? *reinterpret_cast<const uint4*>(g + i) : make_uint4(0, 0, 0, 0);
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+  if (live) {
+    const float4* yr = reinterpret_cast<const float4*>(y + static_cast<int64_t>(r) * H + i);
+    a = __ldcg(yr);
+    b = __ldcg(yr + 1);
+  }
+  const float rstd = parts_rstd(ss, rows, r, H, inv_h, eps);
+  if (!live) return;
   const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gr);
   const float xs[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
   uint4 o;
