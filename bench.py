@@ -669,15 +669,31 @@ def profile_workload(name):
     """A small workload for an ncu capture of one kernel (no timing, no JSON
     line): 'attention32' drafts 32 streams x 2048 context rows through a
     two-layer 9B-shaped drafter (both layers sliding) three times, so the
-    many-stream attention launch is captured at a few GB of device memory."""
+    many-stream attention launch is captured at a few GB of device memory;
+    'fill4096' runs a 4096-row prompt fill of the 9B-shaped drafter three
+    times (fc GEMM, hidden_norm, K/V injection)."""
     import torch
 
     import block_diffusion_speculative_tap_gb300 as D
     import synthetic_inputs as SI
 
+    torch.cuda.set_device(0)
+    if name == "fill4096":
+        # a 4096-row prompt fill of the 9B-shaped drafter, three times
+        m = SI.preset("9b")["model"]
+        dr = D.Drafter(m, SI.make_weights(m, 5, device="cuda"))
+        st = dr.new_state(1, 4096)
+        taps = SI.make_taps(m, 4096, 6, device="cuda")
+        for _ in range(3):
+            st.fuse_taps(taps, [(0, 0, 4096)])
+            st.truncate(0, 0)
+        torch.cuda.synchronize()
+        rc, bits = st.status()
+        if rc != 0:
+            raise RuntimeError(f"device status {rc} bits {bits}")
+        return
     if name != "attention32":
         raise SystemExit(f"unknown profile workload {name}")
-    torch.cuda.set_device(0)
     m = SI.shrink(SI.preset("9b")["model"], n_layers=2, layer_kinds=[SI.SLIDING] * 2)
     S, C = 32, 2048
     dr = D.Drafter(m, SI.make_weights(m, 5, device="cuda"))
@@ -703,7 +719,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-configs", action="store_true", help="skip the supplementary workloads")
-    ap.add_argument("--profile-workload", default=None, help="run a small workload for ncu (attention32) and exit")
+    ap.add_argument("--profile-workload", default=None, help="run a small workload for ncu (attention32, fill4096) and exit")
     args = ap.parse_args()
     if args.profile_workload:
         profile_workload(args.profile_workload)
