@@ -527,11 +527,62 @@ GemmPlan kv_plan(const dflash_handle* h, const dflash_state* st, int rows, int l
 
 int layers_per_kv_pass() { return kMaxASeg / 2; }
 
+// A wide fill's fc GEMM whose tiles leave the last wave at most half full
+// runs as two launches: the row tiles that fill whole waves, then the rest
+// with their reduction split so that they still cover the SMs (4096 rows of
+// the 9B shape: 3 waves + a half-filled fourth -> 3 waves + one of half-K
+// units: 0.78 -> 0.71 ms). (On the K/V projections, whose last wave holds 16
+// of 1536 tiles, the extra launch cost more than it saved.) Returns the
+// first row tile of the tail (0: no split) and its split.
+int tail_split(const dflash_handle* h, const GemmPlan& p, int& ks_tail) {
+  ks_tail = 1;
+  if (p.N <= kDecodeRegimeN || p.ksplit != 1) return 0;
+  const int m_tiles = p.M / kTileM, BN = plan_bn(p), sms = h->num_sms;
+  const int n_tiles = (p.N + BN - 1) / BN;
+  const int tiles = m_tiles * n_tiles, full = tiles / sms, rem = tiles - full * sms;
+  if (full < 1 || rem == 0 || 2 * rem > sms) return 0;
+  const int msplit = full * sms / n_tiles;
+  if (msplit <= 0 || msplit >= m_tiles) return 0;
+  const int kb = p.K / kTileK;
+  int ks = std::min(4, sms / ((m_tiles - msplit) * n_tiles));
+  while (ks > 1 && kb / ks < 8) --ks;
+  if (ks < 2) return 0;
+  ks_tail = ks;
+  return msplit;
+}
+
+// Launches p (a wide fill's fc GEMM), as two launches when tail_split says so;
+// advances the counter cursor past what they used.
+int launch_wide(const dflash_handle* h, GemmPlan p, float* partial, int*& counters, int* status, cudaStream_t s) {
+  int ks_tail = 1;
+  const int msplit = tail_split(h, p, ks_tail);
+  GemmPlan tail = p;
+  if (msplit > 0) {
+    p.M = msplit * kTileM;
+    tail.m_tile0 = msplit;
+    tail.M -= msplit * kTileM;
+    tail.ksplit = ks_tail;
+    tail.no_cluster = true;
+  }
+  int rc = gemm_launch(p, partial, counters, status, h->num_sms, s);
+  if (rc) return rc;
+  counters += gemm_counter_count(p);
+  if (msplit > 0) {
+    rc = gemm_launch(tail, partial, counters, status, h->num_sms, s);
+    if (rc) return rc;
+    counters += gemm_counter_count(tail);
+  }
+  return DFLASH_OK;
+}
+
 size_t fuse_ws_layout(const dflash_handle* h, int rows, void* base, FuseWs* ws) {
   const dflash_config& c = h->cfg;
   const int pass = std::min(std::max(rows, 1), kFusePass);
   size_t counters = gemm_counter_count(fc_plan(h, pass));
   size_t partial = gemm_partial_bytes(fc_plan(h, pass));
+  // a split fc tail: at most one wave of units of at most 256 columns
+  if (pass > kDecodeRegimeN)
+    partial = std::max(partial, static_cast<size_t>(h->num_sms) * 256 * kTileM * sizeof(float));
   for (int l0 = 0; l0 < c.n_layers; l0 += layers_per_kv_pass()) {
     const GemmPlan kp = kv_plan(h, nullptr, pass, l0, std::min(c.n_layers, l0 + layers_per_kv_pass()), false);
     counters += gemm_counter_count(kp);
@@ -660,9 +711,8 @@ int dflash_fuse_taps(dflash_handle* h, dflash_state* st, const void* const* plan
     fp.epi_args.out = w.y;
     fp.epi_args.ss_out = w.ss;
     fp.epi_args.ss_ld = n;
-    rc = gemm_launch(fp, w.partial, counters, st->status, h->num_sms, s);
+    rc = launch_wide(h, fp, w.partial, counters, st->status, s);
     if (rc) return rc;
-    counters += gemm_counter_count(fp);
     rc = launch_hidden_norm(st->ring, w.fused, w.y, w.ss, h->hidden_norm, w.row_stream + r0, w.row_pos + r0, n,
                             c.hidden, st->R, c.rms_eps, s);
     if (rc) return rc;

@@ -101,6 +101,7 @@ __device__ __forceinline__ void decode_unit(const GemmArgs& a, int u, int& m_til
     kc = r % a.ksplit;
     m_tile = r / a.ksplit;
   }
+  m_tile += a.m_tile0;  // the weight's tile index
 }
 
 __device__ __forceinline__ int seg_of_tile(const GemmArgs& a, int m_tile) {
@@ -727,7 +728,7 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
         __threadfence();
         named_bar_sync(1, 128);
         if (epi_leader) {
-          const int old = atomicAdd(&args.counters[m_tile * args.n_tiles + n_tile], 1);
+          const int old = atomicAdd(&args.counters[(m_tile - args.m_tile0) * args.n_tiles + n_tile], 1);
           *last_word = (old == args.ksplit - 1) ? 1 : 0;
         }
         named_bar_sync(1, 128);
@@ -748,7 +749,7 @@ __global__ void __launch_bounds__(kGemmThreads, MINB) gemm_kernel(const __grid_c
             for (int k2 = 0; k2 < args.ksplit; k2 += 2) {
               const bool two = k2 + 1 < args.ksplit;
               const float* sa =
-                  args.partial + static_cast<size_t>((m_tile * args.ksplit + k2) * args.n_tiles + n_tile) *
+                  args.partial + static_cast<size_t>(((m_tile - args.m_tile0) * args.ksplit + k2) * args.n_tiles + n_tile) *
                                      (Tr::kAcc * BN * kTileM);
               const float* sb = two ? sa + static_cast<size_t>(args.n_tiles) * (Tr::kAcc * BN * kTileM) : sa;
               float a0[16], b0[16], a1[16], b1[16];
@@ -1041,7 +1042,8 @@ static void fill_args(const GemmPlan& p, GemmArgs& a, int BN) {
     a.a_seg_tile[i + 1] = a.a_seg_tile[i] + p.a_rows[i] / kTileM;
   }
   if (p.a2_map) a.a2_map = *p.a2_map;
-  a.M = p.M;
+  a.m_tile0 = p.m_tile0;
+  a.M = p.m_tile0 * kTileM + p.M;  // the end row: epilogue row indices are the weight's
   a.N = p.N;
   a.K = p.K;
   a.m_tiles = p.M / kTileM;

@@ -68,6 +68,7 @@ struct GemmArgs {
   int b_plane_kb;                 // 64-wide reduction blocks per B plane
   int M, N, K;
   int m_tiles, n_tiles, kb_total, ksplit, units;
+  int m_tile0;  // the launch covers weight rows [m_tile0 * 128, M); m_tiles of them
   bool no_cluster;
   float* partial;                 // split-K partial tiles, [units][acc][BN][128]
   int* counters;                  // [m_tiles * n_tiles], zero before launch
@@ -90,6 +91,7 @@ struct GemmPlan {
   int M = 0, N = 0, K = 0;
   int ksplit = 1;
   int bn = 0;               // token tile width (16, 128 or 256); 0: gemm_bn_for(N)
+  int m_tile0 = 0;          // first 128-row tile of the weight this launch covers (M rows from there)
   bool no_cluster = false;  // split-K through global partials even when a cluster would fit
   int epi = EPI_STORE_F32;
   EpiArgs epi_args{};
