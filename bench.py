@@ -250,6 +250,18 @@ def measure_config(name, dev, pk, steps, dr=None):
 
 
 # ---------------------------------------------------------------- our arm
+def max_over_ranks(value, world, device):
+    """The largest of every rank's value (the slowest replica's time), as
+    every rank sees it; the value itself on a single rank."""
+    if world <= 1:
+        return value
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_ours(args, rank, world):
     import torch
 
@@ -347,11 +359,7 @@ def run_ours(args, rank, world):
         e[1] += t
         e[2] += b
         e[3] += fl
-    ms_max = ms
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(tt.item())
+    ms_max = max_over_ranks(ms, world, dev)
 
     # ---- the draft alone (block forward + LM head + top-8) at the current
     # context: blocks/s and its fraction of the weight-streaming roofline
