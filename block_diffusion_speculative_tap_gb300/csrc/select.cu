@@ -203,6 +203,12 @@ __device__ float range_topk(const __nv_bfloat16* row, int g_begin, int g_end, in
     } else {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
+        // a group of 8 whose largest value is below the floor holds no
+        // candidate (ties at the floor go on to the exact test)
+        float gm = x[u][0];
+#pragma unroll
+        for (int e = 1; e < 8; ++e) gm = fmaxf(gm, x[u][e]);
+        if (__ballot_sync(0xffffffffu, g0 + u * 32 < wg1 && !(gm < fv)) == 0u) continue;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int id = (g0 + u * 32) * 8 + e;
