@@ -189,17 +189,24 @@ __device__ float range_topk(const __nv_bfloat16* row, int g_begin, int g_end, in
       }
     }
     if constexpr (KM == 1) {
-      // arg-max: a compare-select a value, one warp reduction at the end
+      // arg-max, one warp reduction at the end: a lane's groups arrive in
+      // ascending id order, so a group replaces the lane's best only with a
+      // strictly larger maximum, taken at its first (lowest) position; an
+      // empty lane (li == INT_MAX) also takes a group that only ties
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < 4; ++u) {
+        float gm = x[u][0];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int id = (g0 + u * 32) * 8 + e;
-          if (g0 + u * 32 < wg1 && better(x[u][e], id, lv, li)) {
-            lv = x[u][e];
-            li = id;
-          }
+        for (int e = 1; e < 8; ++e) gm = fmaxf(gm, x[u][e]);
+        if (g0 + u * 32 < wg1 && (gm > lv || (gm == lv && li == INT_MAX))) {
+          int first = 7;
+#pragma unroll
+          for (int e = 6; e >= 0; --e)
+            if (x[u][e] == gm) first = e;
+          lv = gm;
+          li = (g0 + u * 32) * 8 + first;
         }
+      }
     } else {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
