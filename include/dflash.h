@@ -231,7 +231,10 @@ int dflash_device_status(dflash_state* st, dflash_stream_t stream, int32_t* out)
  * also gets K = bf16(RoPE(k_norm(fused * k_proj_l^T), pos)) and V =
  * bf16(fused * v_proj_l^T) in its cache ("k and v only"), and the stream
  * lengths advance. Without it only the ring is written and lengths stay
- * (fusion-only timing). ws: >= dflash_fuse_workspace_bytes(h, rows). */
+ * (fusion-only timing). Up to 1024 rows a call, a row's fused values and
+ * K/V do not depend on which other rows share the call (a fill resumed after
+ * dflash_state_truncate rebuilds the same cache). ws: >=
+ * dflash_fuse_workspace_bytes(h, rows). */
 int dflash_fuse_workspace_bytes(const dflash_handle* h, int rows, size_t* bytes);
 int dflash_fuse_taps(dflash_handle* h, dflash_state* st, const void* const* planes, int64_t plane_row_stride,
                      int nseg, const int32_t* seg_stream, const int64_t* seg_start, const int32_t* seg_rows,
@@ -250,6 +253,12 @@ int dflash_fuse_taps(dflash_handle* h, dflash_state* st, const void* const* plan
  * [s_count*15, V] or NULL (then the logits live in ws). topk_ids (int32) and
  * topk_vals (fp32, the bf16 logit values): device [s_count*15, k], k in
  * 1..16, descending, ties to the lower id; either may be NULL to skip top-k.
+ * Batch invariance [TF1851 "Exactness": concurrent equals solo]: with
+ * s_count <= 4 a stream's logits and ids are bit-identical whichever streams
+ * share the call (the reductions' split depends only on the weights' shapes
+ * and the stream's own length); with more streams the GEMM split and the
+ * attention split are chosen for throughput and the fp32 summation order,
+ * hence the last bits, depend on s_count.
  * ws: >= dflash_draft_workspace_bytes(h, st, s_count, logits_out == NULL). */
 int dflash_draft_workspace_bytes(const dflash_handle* h, const dflash_state* st, int s_count, int need_logits,
                                  size_t* bytes);
