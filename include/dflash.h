@@ -229,7 +229,7 @@ int dflash_device_status(dflash_state* st, dflash_stream_t stream, int32_t* out)
  * For every row: y = concat(planes) * fc^T; fused = bf16(RMSNorm(y) *
  * hidden_norm) written to the ring. With DFLASH_FUSE_INJECT_KV, every layer l
  * also gets K = bf16(RoPE(k_norm(fused * k_proj_l^T), pos)) and V =
- * bf16(fused * v_proj_l^T) in its cache ("k and v only"), and the stream
+ * bf16(fused * v_proj_l^T) in its cache (context rows feed K and V only), and the stream
  * lengths advance. Without it only the ring is written and lengths stay
  * (fusion-only timing). Up to 1024 rows a call, a row's fused values and
  * K/V do not depend on which other rows share the call (a fill resumed after

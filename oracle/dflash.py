@@ -10,7 +10,7 @@ Sources (cited by page title and section):
   body, eleven tensors a layer, fc, hidden_norm, norm, two residual adds, the
   fifteen mask rows, refusal of a causal draft), 3 (prompt-memory planner:
   18 x hidden x 2 bytes a prompt row for eight taps), 4 (fused ring rows of
-  8 KiB a token; context append "k and v only"; sliding layers attend their
+  8 KiB a token; context rows appended as K and V only; sliding layers attend their
   own window, the full layer the whole span); "Exactness", the Precision
   bullet (bf16 activations, fp32 sums).
 * Strata pull request #3457, "Metal: opt-in --dflash DFlash2 drafter in place
@@ -183,7 +183,7 @@ def fuse_taps(planes, fc, hidden_norm, eps):
 
 
 def context_kv(fused, positions, layer, model):
-    """One drafter layer's K and V for fused context rows ("k and v only").
+    """One drafter layer's K and V for fused context rows (context rows feed K and V only).
 
     TensorFold #1851 item 4 and the explainer's section 三 (KV injection into
     every draft layer). Reading: no input norm on context rows (they already
@@ -281,7 +281,7 @@ def mlp_half(model, w, l, X):
 
 def draft_layer(model, w, l, X, ctx_k, ctx_v, C):
     """One drafter layer on the block's residual X [16, H] (qwen3 body:
-    TensorFold #1851 item 1, "two residual adds a layer")."""
+    TensorFold #1851 item 1: two residual adds per layer)."""
     return mlp_half(model, w, l, attention_half(model, w, l, X, ctx_k, ctx_v, C))
 
 
