@@ -295,10 +295,13 @@ def run_ours(args, rank, world):
     anchor = SI.anchor_ids(1, m["vocab"], m["mask_token"], seed + 3, device=dev)
     tl = SI.make_logits((1, 16, m["vocab"]), 1.0, seed + 4, device=dev)
     logits = torch.empty(15, m["vocab"], dtype=torch.bfloat16, device=dev)
-    ids = torch.empty(15, 8, dtype=torch.int32, device=dev)
+    # a round's int32 results in one buffer (one readback end to end):
+    # accept length [1], tokens [1, 16], top-8 draft ids [15, 8]
+    results = torch.empty(1 + 16 + 15 * 8, dtype=torch.int32, device=dev)
+    ids = results[17:].view(15, 8)
     vals = torch.empty(15, 8, dtype=torch.float32, device=dev)
-    acc = torch.empty(1, dtype=torch.int32, device=dev)
-    toks = torch.empty(1, 16, dtype=torch.int32, device=dev)
+    acc = results[0:1]
+    toks = results[1:17].view(1, 16)
     stream = torch.cuda.current_stream()
 
     def step():
@@ -433,15 +436,13 @@ def run_ours(args, rank, world):
     h_taps = taps_buf.cpu().pin_memory()
     h_anchor = anchor.cpu().pin_memory()
     h_tl = tl.cpu().pin_memory()
-    h_acc = torch.empty(1, dtype=torch.int32).pin_memory()
-    h_toks = torch.empty(1, 16, dtype=torch.int32).pin_memory()
-    h_ids = torch.empty(15, 8, dtype=torch.int32).pin_memory()
+    h_results = torch.empty(results.numel(), dtype=torch.int32).pin_memory()
     h2d = h_taps.numel() * 2 + 4 + h_tl.numel() * 2
     # the target logits (the bulk of the bytes; needed only by verification)
     # travel on a side stream, queued behind the tap copy, under the draft
     side = torch.cuda.Stream(device=dev)
     e_go, e_tl = torch.cuda.Event(), torch.cuda.Event()
-    d2h = 4 + 64 + 15 * 8 * 4
+    d2h = h_results.numel() * 4
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(args.e2e_steps):
@@ -458,9 +459,7 @@ def run_ours(args, rank, world):
         st.draft(anchor, k=8, logits=logits, ids=ids, vals=vals)
         stream.wait_event(e_tl)
         D.verify_greedy(ids, tl, accept=acc, tokens=toks)
-        h_acc.copy_(acc, non_blocking=True)
-        h_toks.copy_(toks, non_blocking=True)
-        h_ids.copy_(ids, non_blocking=True)
+        h_results.copy_(results, non_blocking=True)
         stream.synchronize()  # the next round's anchor depends on this round's result
     e2e_s = time.perf_counter() - t0
     rc, bits = st.status()
