@@ -54,6 +54,7 @@ def test_refusals_match_the_oracle(D):
         (dict(m, block=8), -5),
         (dict(m, n_kv_heads=5), -5),
         (dict(m, layer_kinds=[1] * 6, sliding_window=0), -5),
+        (dict(m, hidden=4224), -5),  # hidden != q heads x head dim
     ]
     for cfg, code in cases:
         assert D.config_validate(cfg) == code, cfg
@@ -93,3 +94,20 @@ def test_null_arguments_are_refused(A):
     nb = C.c_size_t()
     assert A.lib.dflash_verify_workspace_bytes(1, 4, 4096, C.byref(nb)) == 0 and nb.value == 4 * 31 * 2 * 4
     assert A.lib.dflash_verify_workspace_bytes(7, 4, 4096, C.byref(nb)) == -1
+
+
+def test_kernel_shape_limits_are_refused(D):
+    """Shapes the method allows but the kernels do not serve are refused
+    up front (DFLASH_E_SHAPE), never run: query groups over 8 heads a kv head,
+    head dims other than 32, 64, 128, widths and vocabularies off the 128-row
+    tile, a mask token outside the vocabulary."""
+    m = SI.presets()["9b"]["model"]
+    for cfg in (
+        dict(m, n_kv_heads=2),                            # 16 query heads a kv head
+        dict(m, n_q_heads=16, head_dim=256),              # head dim 256
+        dict(m, hidden=4096 + 64, n_q_heads=65, head_dim=64, n_kv_heads=13),  # width off the tile
+        dict(m, ffn=12288 + 64),
+        dict(m, vocab=151936 + 64, mask_token=151999),
+        dict(m, mask_token=151936),
+    ):
+        assert D.config_validate(cfg) == -5, cfg
