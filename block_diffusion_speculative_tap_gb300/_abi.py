@@ -123,6 +123,7 @@ def _load():
     fn("dflash_state_length", C.c_int, vp, C.c_int, P(i64))
     fn("dflash_state_truncate", C.c_int, vp, vp, C.c_int, i64, vp, sz, vp)
     fn("dflash_device_status", C.c_int, vp, vp, P(i32))
+    fn("dflash_state_wait_probe", C.c_int, vp, C.c_int64, vp)
     fn("dflash_state_ring", C.c_int, vp, P(vp))
     fn("dflash_state_cache", C.c_int, vp, C.c_int, P(vp), P(vp), P(C.c_int))
     fn("dflash_fuse_workspace_bytes", C.c_int, vp, C.c_int, P(sz))
@@ -159,6 +160,7 @@ EXPORTED = [
     "dflash_state_length",
     "dflash_state_truncate",
     "dflash_device_status",
+    "dflash_state_wait_probe",
     "dflash_state_ring",
     "dflash_state_cache",
     "dflash_fuse_workspace_bytes",

@@ -454,6 +454,11 @@ int dflash_device_status(dflash_state* st, dflash_stream_t stream, int32_t* out)
   return DFLASH_OK;
 }
 
+int dflash_state_wait_probe(dflash_state* st, int64_t cycles, dflash_stream_t stream) {
+  if (!st || cycles < 0 || cycles > 10000000000ll) return DFLASH_E_INVALID_ARG;
+  return launch_wait_probe(st->status, static_cast<long long>(cycles), reinterpret_cast<cudaStream_t>(stream));
+}
+
 // ---------------------------------------------------------------- fusion
 namespace {
 

@@ -118,6 +118,7 @@ int launch_embed(float* X, float* ss, const __nv_bfloat16* embed, const int* anc
                  int* err, cudaStream_t st);
 // The same sums of squares for rows of a caller-given X [rows, H].
 int launch_row_sumsq(float* ss, const float* X, int rows, int H, cudaStream_t st);
+int launch_wait_probe(int* err, long long cycles, cudaStream_t st);
 // out[r] = bf16(x[src] * rstd * g) with rstd = rsqrt(sum_p ss[p][src] / H +
 // eps) from the rows' published per-128-feature sums of squares (parts summed
 // in order); src = r, or the r-th mask row (block rows 1..15) when

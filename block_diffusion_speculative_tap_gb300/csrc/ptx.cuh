@@ -56,14 +56,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // `flag` in *err and returns false. A shared abort word lets the other roles
 // of the CTA stop waiting as soon as one of them gave up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int flag,
-                                          volatile int* abort_word) {
+                                          volatile int* abort_word, long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long c0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0u) {
       if (abort_word != nullptr && *abort_word) return false;
-      if (clock64() - c0 > kWaitLimitCycles) {
+      if (clock64() - c0 > limit) {
         if (err) atomicOr(err, flag);
         if (abort_word != nullptr) *abort_word = 1;
         return false;

@@ -272,7 +272,25 @@ __global__ void set_lens_kernel(int* __restrict__ lens, const SegTable tab) {
   if (i < tab.n) lens[tab.stream[i]] = tab.start[i] + tab.rows[i];
 }
 
+// A bounded wait on an mbarrier that nothing arrives at: it gives up after
+// `limit` cycles and sets the timeout bit of *err, as any expired wait of the
+// hot path does (the self-test of that mechanism).
+__global__ void wait_probe_kernel(int* err, long long limit) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    mbar_wait(&bar, 0, err, DFLASH_STATUS_TIMEOUT, nullptr, limit);
+  }
+}
+
 }  // namespace
+
+int launch_wait_probe(int* err, long long cycles, cudaStream_t st) {
+  wait_probe_kernel<<<1, 32, 0, st>>>(err, cycles);
+  count_launch();
+  return cuda_status(cudaGetLastError());
+}
 
 int launch_embed(float* X, float* ss, const __nv_bfloat16* embed, const int* anchors, int S, int H, int V, int mask,
                  int* err, cudaStream_t st) {

@@ -182,6 +182,11 @@ class State:
         check(lib.dflash_state_length(self.st, s, C.byref(v)), "dflash_state_length")
         return v.value
 
+    def wait_probe(self, cycles: int):
+        """Run the bounded-wait self-test (a wait nothing completes, given up
+        after `cycles` SM cycles); read the outcome with status()."""
+        check(lib.dflash_state_wait_probe(self.st, int(cycles), _stream()), "dflash_state_wait_probe")
+
     def status(self):
         """(rc, bits) of the device status word (synchronises the stream)."""
         v = C.c_int32()

@@ -216,6 +216,13 @@ int dflash_state_cache(const dflash_state* st, int layer, void** k, void** v, in
  * the corresponding bits were set, DFLASH_OK when clear. */
 int dflash_device_status(dflash_state* st, dflash_stream_t stream, int32_t* out);
 
+/* Self-test of the bounded waits: one kernel waits on an mbarrier that
+ * nothing arrives at, gives up after `cycles` SM cycles (0 .. 1e10; the hot
+ * path's waits use 3e9) and sets DFLASH_STATUS_TIMEOUT in the state's status
+ * word, exactly as an expired wait of the hot path does; the context stays
+ * usable. Read the result with dflash_device_status (E_TIMEOUT). */
+int dflash_state_wait_probe(dflash_state* st, int64_t cycles, dflash_stream_t stream);
+
 /* ---------------------------------------------------------------- fusion
  * Tap fusion and context append [TF1851 item 4; ST3457 "Approach": each
  * prompt chunk and committed window injects its rows' features].

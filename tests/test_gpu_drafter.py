@@ -326,3 +326,25 @@ def test_fuse_reused_plane_list(D):
     st.fuse_taps(planes, [(0, 32, 16)])
     ref.append(0, [f64(planes[i]) for i in range(len(planes))])
     check_state_vs_oracle(st, ref, m, 0, 48)
+
+
+def test_bounded_wait_expires_and_context_survives(D):
+    """Failure detection on the device: a wait that nothing completes gives up
+    after its cycle bound and sets the timeout bit of the status word (no
+    trap, no hang), and the next fill and draft run and match the oracle."""
+    P = SI.preset("tiny")
+    m = P["model"]
+    w = SI.make_weights(m, 51, device="cuda")
+    dr = D.Drafter(m, w)
+    st = dr.new_state(1, 256)
+    st.wait_probe(20_000_000)  # about 10 ms of SM cycles
+    rc, bits = st.status()
+    assert rc == -9 and bits & 2, (rc, bits)
+    rc, bits = st.status()  # the read cleared the word
+    assert rc == 0 and bits == 0
+    ref = O.OracleStreams(m, O.weights_to_f64(w), 1)
+    taps = SI.make_taps(m, 40, 52, device="cuda")
+    st.fuse_taps(taps, [(0, 0, 40)])
+    ref.append(0, [f64(t) for t in taps])
+    anchors = SI.anchor_ids(1, m["vocab"], m["mask_token"], 53)
+    draft_vs_oracle(D, st, ref, m, anchors, P["topk"])
