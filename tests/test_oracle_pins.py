@@ -510,3 +510,52 @@ def test_draft_stop_rule():
     assert O.draft_stop(conf, 0.7).tolist() == [15, 2, 0, 14]
     assert O.draft_stop(conf, 0.0).tolist() == [15, 15, 15, 15]
     assert O.draft_stop(conf, 1.0).tolist() == [0, 0, 0, 0]
+
+
+# ----------------------------------------------------------------------------
+# helpers of the layer: SiLU, arg-max, the context K/V
+
+
+def test_silu_closed_forms():
+    # silu(x) = x * sigmoid(x): zero at 0, sigmoid(1) and -sigmoid(-1) at +-1,
+    # silu(x) - silu(-x) = x, and x for large x
+    assert O.silu(np.float64(0.0)) == 0.0
+    assert abs(O.silu(np.float64(1.0)) - 0.7310585786300049) < 1e-15
+    assert abs(O.silu(np.float64(-1.0)) + 0.2689414213699951) < 1e-15
+    x = np.linspace(-20, 20, 81)
+    assert np.allclose(O.silu(x) - O.silu(-x), x, rtol=0, atol=1e-12)
+    assert abs(O.silu(np.float64(40.0)) - 40.0) < 1e-12
+
+
+def test_argmax_lowest_takes_the_first_of_ties():
+    assert O.argmax_lowest([1.0, 3.0, 3.0, 2.0]) == 1
+    assert O.argmax_lowest([5.0] * 7) == 0
+    assert O.argmax_lowest([-4.0, -1.0, -2.0, -1.0]) == 1
+    assert O.argmax_lowest([float("-inf"), 0.0]) == 1
+
+
+def test_context_kv_properties():
+    """K/V of context rows: V does not depend on the position; RoPE is a
+    rotation, so each key head keeps its length (k_norm with unit gain makes
+    that length sqrt(d) at every position), and a key pair's dot product
+    depends only on the distance between the two positions."""
+    m = _tiny_model()
+    w = _weights64(m, seed=11)
+    layer = dict(w["layers"][0])
+    d, nkv = m["head_dim"], m["n_kv_heads"]
+    layer["k_norm"] = np.ones(d)
+    rng = np.random.default_rng(3)
+    fused = O.round_bf16(rng.standard_normal((2, m["hidden"])))
+    rows = np.concatenate([fused, fused])  # the same two rows at two position pairs
+    k, v = O.context_kv(rows, [0, 5, 37, 42], layer, m)
+    assert np.array_equal(v[:2], v[2:])
+    # head lengths: sqrt(d) up to the bf16 rounding of the stored keys
+    assert np.allclose(np.linalg.norm(k, axis=-1), math.sqrt(d), rtol=2 ** -7, atol=0)
+    # relative positions: (0, 5) and (37, 42) are both 5 apart
+    dots_a = np.einsum("hd,hd->h", k[0], k[1])
+    dots_b = np.einsum("hd,hd->h", k[2], k[3])
+    assert np.allclose(dots_a, dots_b, rtol=0, atol=d * 2 ** -6)
+    # and a different distance gives different dots (the rotation is not the identity)
+    k2, _ = O.context_kv(rows[:2], [0, 9], layer, m)
+    assert not np.allclose(np.einsum("hd,hd->h", k2[0], k2[1]), dots_a, rtol=0, atol=d * 2 ** -6)
+    assert k.shape == (4, nkv, d)
