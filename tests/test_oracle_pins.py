@@ -559,3 +559,29 @@ def test_context_kv_properties():
     k2, _ = O.context_kv(rows[:2], [0, 9], layer, m)
     assert not np.allclose(np.einsum("hd,hd->h", k2[0], k2[1]), dots_a, rtol=0, atol=d * 2 ** -6)
     assert k.shape == (4, nkv, d)
+
+
+def test_layer_halves_add_to_the_residual():
+    """Each half of a layer adds its branch to the residual (two residual adds
+    a layer): with a zero output projection the half returns X unchanged, and
+    the added branch does not depend on X's scale (an RMSNorm input: X and 3X
+    give the same branch up to the bf16 rounding of the norm's output)."""
+    m = _tiny_model()
+    w = _weights64(m, seed=13)
+    rng = np.random.default_rng(5)
+    X = rng.standard_normal((O.BLOCK, m["hidden"]))
+    C = 9
+    nkv, d = m["n_kv_heads"], m["head_dim"]
+    ck = O.round_bf16(rng.standard_normal((C, nkv, d)))
+    cv = O.round_bf16(rng.standard_normal((C, nkv, d)))
+    wz = {**w, "layers": [dict(L) for L in w["layers"]]}
+    wz["layers"][0]["o_proj"] = np.zeros_like(w["layers"][0]["o_proj"])
+    wz["layers"][0]["down_proj"] = np.zeros_like(w["layers"][0]["down_proj"])
+    assert np.array_equal(O.attention_half(m, wz, 0, X, ck, cv, C), X)
+    assert np.array_equal(O.mlp_half(m, wz, 0, X), X)
+    a1 = O.attention_half(m, w, 0, X, ck, cv, C) - X
+    a3 = O.attention_half(m, w, 0, 3 * X, ck, cv, C) - 3 * X
+    assert np.allclose(a1, a3, rtol=0, atol=1e-6 + 2 ** -6 * np.abs(a1).max())
+    g1 = O.mlp_half(m, w, 0, X) - X
+    g3 = O.mlp_half(m, w, 0, 3 * X) - 3 * X
+    assert np.allclose(g1, g3, rtol=0, atol=1e-6 + 2 ** -6 * np.abs(g1).max())
