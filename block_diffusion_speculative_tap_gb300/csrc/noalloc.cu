@@ -17,8 +17,10 @@ namespace {
 
 // Statistics of up to kNoAllocMaxStreams streams: 31 rows (16 target, 15
 // draft) x (max, sum) floats each, 248 KiB. Every GPU that loads the library
-// holds this array until the process exits.
-constexpr int kNoAllocMaxStreams = 1024;
+// holds this array until the process exits. The limit is the one the header
+// documents, so the refusal below and the documented maximum cannot diverge.
+constexpr int kNoAllocMaxStreams = DFLASH_NOALLOC_MAX_STREAMS;
+static_assert(kNoAllocMaxStreams > 0, "the no-allocation stream limit must be positive");
 static __device__ __align__(256) float g_sample_scratch[kNoAllocMaxStreams * 31 * 2];
 
 constexpr int kMaxDevices = 64;

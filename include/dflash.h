@@ -353,8 +353,12 @@ int dflash_verify(int mode, int streams, int vocab, const int32_t* draft_ids, in
  * - At most DFLASH_NOALLOC_MAX_STREAMS streams; more returns
  *   DFLASH_E_WORKSPACE and enqueues nothing.
  * - The first call on a device looks up the array's device address (once per
- *   device, with that device current); make that first call before any
- *   stream capture.
+ *   device, with that device current). With lazy module loading (the CUDA
+ *   default) that lookup may load the library's device code on that device,
+ *   which allocates device memory for the module and may synchronise. So
+ *   make one warm-up call per device at initialisation, before the loop
+ *   that must not allocate and before any stream capture; later calls
+ *   allocate nothing and never synchronise.
  * - All calls share the array: calls that overlap on the GPU (issued on
  *   different streams or from several host threads with nothing ordering
  *   them) race on it. Nothing in it needs to start at zero; each call writes
