@@ -34,6 +34,15 @@ attention output, the SwiGLU product, the final normed rows and the logits.
 Everything in between (projection outputs before their norms, the residual
 stream, norm statistics, the softmax) stays float64.
 
+The same steps can also run with float32 arithmetic (``arithmetic(np.float32)``,
+weights from ``weights_as(w, np.float32)``): a plain implementation of the
+pages' precision (bf16 activations, fp32 sums; TensorFold #1851, "Exactness",
+the Precision bullet), with the rotary angles still formed in float64 as any
+careful implementation does. Its distance from the float64 run measures how
+far two correct fp32 implementations of this method may drift apart after
+several layers of bf16 rounding; the parity tests take their end-to-end
+envelope for deep drafters from it. The default is float64.
+
 Readings of points the pages leave open (each one is stated where used):
 RMSNorm epsilon 1e-6; rotate-half RoPE with theta from the config; context
 rows at absolute positions 0..C-1, the anchor at C and the mask rows at
@@ -53,6 +62,7 @@ acceptance, ties); the sampling rule's output distribution equal to p
 """
 from __future__ import annotations
 
+import contextlib
 import math
 
 import numpy as np
@@ -62,6 +72,8 @@ SLIDING = 1
 BLOCK = 16  # anchor + 15 mask rows (TensorFold #1851, item 1)
 
 __all__ = [
+    "arithmetic",
+    "weights_as",
     "BLOCK",
     "FULL",
     "SLIDING",
@@ -100,6 +112,37 @@ __all__ = [
 ]
 
 # ----------------------------------------------------------------------------
+# arithmetic precision
+
+_F = np.float64  # floating type of every sum, product and norm statistic below
+
+
+@contextlib.contextmanager
+def arithmetic(dtype):
+    """Run the drafter's arithmetic (fusion, context K/V, the block forward
+    and the head) in ``dtype`` (np.float64 or np.float32) inside the block.
+
+    The bf16 rounding points stay where they are; only the type of the sums
+    in between changes. Verification and sampling keep float64.
+    """
+    global _F
+    old = _F
+    _F = np.dtype(dtype).type
+    try:
+        yield
+    finally:
+        _F = old
+
+
+def weights_as(w, dtype):
+    """A copy of a weight dict (as from weights_to_f64) in another floating
+    type; bf16 weights are exact in float32 and float64."""
+    out = {k: np.asarray(v, dtype=dtype) for k, v in w.items() if k != "layers"}
+    out["layers"] = [{k: np.asarray(v, dtype=dtype) for k, v in lw.items()} for lw in w["layers"]]
+    return out
+
+
+# ----------------------------------------------------------------------------
 # number formats
 
 _BF16_OVERFLOW = 2.0 ** 128
@@ -113,7 +156,10 @@ def round_bf16(x):
     the spacing stays at the subnormal step 2^-133. Values that round to
     2^128 or beyond become infinities.
     """
-    x = np.asarray(x, dtype=np.float64)
+    x = np.asarray(x)
+    if x.dtype == np.float32:  # float32 arithmetic: round in float64, bf16 values are exact in float32
+        return round_bf16(x.astype(np.float64)).astype(np.float32)
+    x = x.astype(np.float64)
     _, e = np.frexp(x)
     q = np.maximum(e - 8, -133)
     r = np.ldexp(np.rint(np.ldexp(x, -q)), q)
@@ -143,7 +189,7 @@ def weights_to_f64(w):
 
 def rms_norm(x, g, eps):
     """RMSNorm over the last axis: x / sqrt(mean(x^2) + eps) * g."""
-    x = np.asarray(x, dtype=np.float64)
+    x = np.asarray(x, dtype=_F)
     ms = np.mean(x * x, axis=-1, keepdims=True)
     return x / np.sqrt(ms + eps) * g
 
@@ -154,12 +200,12 @@ def rope(x, pos, theta):
     Dimension i < d/2 pairs with i + d/2 and turns by the angle
     pos * theta^(-2i/d). ``pos`` broadcasts against x's leading axes.
     """
-    x = np.asarray(x, dtype=np.float64)
+    x = np.asarray(x, dtype=_F)
     d = x.shape[-1]
     half = d // 2
     inv = theta ** (-(np.arange(half, dtype=np.float64) * 2.0) / d)
     ang = np.asarray(pos, dtype=np.float64)[..., None] * inv
-    c, s = np.cos(ang), np.sin(ang)
+    c, s = np.cos(ang).astype(_F), np.sin(ang).astype(_F)
     x1, x2 = x[..., :half], x[..., half:]
     return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
 
@@ -177,8 +223,8 @@ def fuse_taps(planes, fc, hidden_norm, eps):
     several depths fused by a projection). planes: list of [rows, H];
     fc: [H, N*H]. Returns the bf16 fused rows as float64 [rows, H].
     """
-    x = np.concatenate([np.asarray(p, dtype=np.float64) for p in planes], axis=1)
-    y = x @ np.asarray(fc, dtype=np.float64).T
+    x = np.concatenate([np.asarray(p, dtype=_F) for p in planes], axis=1)
+    y = x @ np.asarray(fc, dtype=_F).T
     return round_bf16(rms_norm(y, hidden_norm, eps))
 
 
@@ -221,7 +267,7 @@ def block_attention(q, k, v):
     nq, d = q.shape[1], q.shape[2]
     nkv = k.shape[1]
     grp = nq // nkv
-    out = np.empty((q.shape[0], nq, d))
+    out = np.empty((q.shape[0], nq, d), dtype=_F)
     for h in range(nq):
         kk = k[:, h // grp, :]
         vv = v[:, h // grp, :]
@@ -238,7 +284,7 @@ def block_embed(model, w, anchor):
     (TensorFold #1851 item 1: the fifteen mask rows), float64 copies of the
     shared embedding rows."""
     tokens = [int(anchor)] + [model["mask_token"]] * (BLOCK - 1)
-    return w["embed"][tokens].astype(np.float64)
+    return w["embed"][tokens].astype(_F)
 
 
 def attention_half(model, w, l, X, ctx_k, ctx_v, C):
@@ -335,9 +381,9 @@ class OracleStreams:
         self.w = w
         L = model["n_layers"]
         nkv, d, H = model["n_kv_heads"], model["head_dim"], model["hidden"]
-        self.fused = [np.zeros((0, H)) for _ in range(streams)]
-        self.k = [[np.zeros((0, nkv, d)) for _ in range(L)] for _ in range(streams)]
-        self.v = [[np.zeros((0, nkv, d)) for _ in range(L)] for _ in range(streams)]
+        self.fused = [np.zeros((0, H), dtype=_F) for _ in range(streams)]
+        self.k = [[np.zeros((0, nkv, d), dtype=_F) for _ in range(L)] for _ in range(streams)]
+        self.v = [[np.zeros((0, nkv, d), dtype=_F) for _ in range(L)] for _ in range(streams)]
 
     def length(self, s):
         return self.fused[s].shape[0]

@@ -50,18 +50,24 @@ def gpu_weights(model, seed, device="cuda"):
 def topk_ids_match(gpu_ids, ref_logits, k, margin):
     """Compare GPU top-k ids with the oracle's ranking where it is clear.
 
-    A rank j is checked when the oracle's values at ranks j-1, j, j+1 are
-    more than `margin` apart from its own; otherwise it is a near-tie and is
-    only counted. Returns (checked, near_ties, mismatches)."""
+    ``margin`` is how far each GPU logit may be from the oracle's: a scalar,
+    or an array of ref_logits' shape holding each logit's own bound. The
+    entries at ranks j and j+1 can swap only if their oracle gap is at most
+    the sum of their two bounds; a rank that could swap with either
+    neighbour is a near-tie and is only counted. Returns (checked,
+    near_ties, mismatches)."""
+    ref_logits = np.asarray(ref_logits, dtype=np.float64)
+    bounds = np.broadcast_to(np.asarray(margin, dtype=np.float64) / 2.0, ref_logits.shape)
     checked = near = bad = 0
     for r in range(ref_logits.shape[0]):
         row = ref_logits[r]
         order = np.lexsort((np.arange(row.shape[0]), -row))[: k + 1]
         vals = row[order]
+        b = bounds[r][order]
         for j in range(k):
-            gap_prev = vals[j - 1] - vals[j] if j > 0 else np.inf
-            gap_next = vals[j] - vals[j + 1]
-            if min(gap_prev, gap_next) <= margin:
+            gap_prev = vals[j - 1] - vals[j] - (b[j - 1] + b[j]) if j > 0 else np.inf
+            gap_next = vals[j] - vals[j + 1] - (b[j] + b[j + 1])
+            if min(gap_prev, gap_next) <= 0.0:
                 near += 1
                 continue
             checked += 1
@@ -92,31 +98,111 @@ def check_topk_consistent(logits, ids, vals):
 
 
 # ---------------------------------------------------------------- deep drafters
-# End to end, several bf16-activation layers amplify fp32-sized differences:
-# the oracle's own arithmetic run in float32 lands at mean |d logit| 6.7e-3
-# (max ~5e-2) from float64 at the 9B shape, doubling about every layer
-# through bf16 rounding flips. The stated tolerance is therefore enforced
-# stage by stage: every residual add (half a layer) and the head are fed the
-# oracle's input and K/V, so errors cannot compound. End to end the mean
-# error must stay below the tolerance's absolute term and every clearly
-# separated candidate must agree.
-E2E_MEAN = 2e-2
-E2E_ID_MARGIN = 0.25
+# The drafter rounds its activations to bf16 between operators, and several
+# such layers amplify fp32-sized differences: two correct fp32
+# implementations of the method drift apart with depth, well past the stated
+# tolerance at six layers (tests/test_oracle_conditioning.py). So the
+# end-to-end envelope comes from the oracle alone: its own arithmetic run in
+# float32 (O.arithmetic) against its float64 run on the same inputs. Every
+# GPU logit must lie within the stated tolerance or within ENV_FACTOR times
+# the largest fp32-vs-fp64 difference of that draft, whichever is larger,
+# and the 99.9th percentile of the GPU's error (in units of the stated
+# tolerance) within ENV_FACTOR times the oracle's own. The factor covers the
+# kernels' one extra rounding the oracle's fp32 run does not make: the
+# attention probabilities enter the P.V product as bf16 (a matrix-product
+# input, as reading 1 has it), against a running maximum rather than the
+# row's final one. Measured, the GPU's end-to-end error is 1.3 to 2 times
+# the oracle's fp32 drift. Near-ties of the top-k ids are pairs whose oracle
+# gap is within the sum of their two bounds.
+ENV_FACTOR = 3.0
 
 
-def oracle_stream(m, w64, planes_host):
-    ref = O.OracleStreams(m, w64, 1)
+class OraclePair:
+    """The oracle's float64 streams (the reference) and the same streams
+    computed with float32 arithmetic (the envelope). Reads (fused, k, v,
+    length, draft) go to the float64 side."""
+
+    def __init__(self, m, w64, streams, w32=None):
+        self.m = m
+        self.r64 = O.OracleStreams(m, w64, streams)
+        self.w32 = O.weights_as(w64, np.float32) if w32 is None else w32
+        with O.arithmetic(np.float32):
+            self.r32 = O.OracleStreams(m, self.w32, streams)
+
+    @property
+    def fused(self):
+        return self.r64.fused
+
+    @property
+    def k(self):
+        return self.r64.k
+
+    @property
+    def v(self):
+        return self.r64.v
+
+    def length(self, s):
+        return self.r64.length(s)
+
+    def append(self, s, planes):
+        rows = self.r64.append(s, planes)
+        with O.arithmetic(np.float32):
+            self.r32.append(s, planes)
+        return rows
+
+    def truncate(self, s, new_len):
+        self.r64.truncate(s, new_len)
+        self.r32.truncate(s, new_len)
+
+    def draft(self, s, anchor, keep_residuals=False):
+        return self.r64.draft(s, anchor, keep_residuals)
+
+    def draft32(self, s, anchor):
+        with O.arithmetic(np.float32):
+            return self.r32.draft(s, anchor)[0].astype(np.float64)
+
+
+def oracle_stream(m, w64, planes_host, w32=None):
+    ref = OraclePair(m, w64, 1, w32)
     ref.append(0, planes_host)
     return ref
 
 
-def compare_draft(lg_gpu, ids_gpu, ol, k):
-    rep = tol_report(lg_gpu, ol)
+def envelope(o64, o32):
+    """Per-logit bound of a draft from the oracle alone: the stated
+    tolerance, or ENV_FACTOR x the largest fp32-vs-fp64 difference, whichever
+    is larger; and the oracle's own 99.9th-percentile error in units of the
+    stated tolerance."""
+    o64 = np.asarray(o64, dtype=np.float64)
+    e32 = np.abs(np.asarray(o32, dtype=np.float64) - o64)
+    tol = ATOL + RTOL * np.abs(o64)
+    bound = np.maximum(tol, ENV_FACTOR * e32.max())
+    return bound, float(np.quantile(e32 / tol, 0.999)), float(e32.max())
+
+
+def compare_draft(lg_gpu, ids_gpu, o64, o32, k, require_checked=True):
+    """End-to-end draft logits and top-k ids against the oracle, element by
+    element within the envelope (see above)."""
+    g = np.asarray(lg_gpu, dtype=np.float64)
+    o64 = np.asarray(o64, dtype=np.float64)
+    bound, q32, e32max = envelope(o64, o32)
+    err = np.abs(g - o64)
+    tol = ATOL + RTOL * np.abs(o64)
+    n_bad = int((err > bound).sum())
+    q_gpu = float(np.quantile(err / tol, 0.999))
+    rep = tol_report(g, o64)
+    rep.update(
+        envelope_max=float(bound.max()), oracle_fp32_max=e32max, oracle_fp32_p999_ratio=q32,
+        n_outside_envelope=n_bad, worst_vs_envelope=float((err / bound).max()),
+    )
     print(f"end-to-end draft logits: {rep}")
-    assert rep["mean_abs"] < E2E_MEAN, rep
-    checked, near, bad = topk_ids_match(ids_gpu, ol, k, E2E_ID_MARGIN)
+    assert n_bad == 0, rep
+    assert q_gpu <= max(1.0, ENV_FACTOR * q32), rep
+    checked, near, bad = topk_ids_match(ids_gpu, o64, k, 2.0 * bound)
     print(f"top-{k} ids: checked {checked}, near ties {near}, mismatches {bad}")
-    assert bad == 0 and checked > 0, (checked, near, bad)
+    assert bad == 0, (checked, near, bad)
+    if require_checked:
+        assert checked > 0, (checked, near, bad)
     return rep
 
 
@@ -152,7 +238,7 @@ def staged_parity(st, ref, rs, m, s, anchor, k):
     rep = assert_close(logits.cpu().float().numpy(), ol, "head logits")
     print(f"stage head: {rep}")
     check_topk_consistent(logits, ids, vals)
-    checked, near, bad = topk_ids_match(ids.cpu().numpy(), ol, k, 2 * (ATOL + RTOL * np.abs(ol).max()))
+    checked, near, bad = topk_ids_match(ids.cpu().numpy(), ol, k, 2 * (ATOL + RTOL * np.abs(ol)))
     assert bad == 0, (checked, near, bad)
     return ol
 
@@ -194,5 +280,5 @@ def staged_parity_all(st, ref, m, anchors, k):
     rep = assert_close(logits.cpu().float().numpy(), ol, "head logits")
     print(f"stage head ({S} streams): {rep}")
     check_topk_consistent(logits, ids, vals)
-    checked, near, bad = topk_ids_match(ids.cpu().numpy(), ol, k, 2 * (ATOL + RTOL * np.abs(ol).max()))
+    checked, near, bad = topk_ids_match(ids.cpu().numpy(), ol, k, 2 * (ATOL + RTOL * np.abs(ol)))
     assert bad == 0, (checked, near, bad)

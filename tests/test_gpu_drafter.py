@@ -11,15 +11,14 @@ import oracle as O
 import synthetic_inputs as SI
 from parity_util import (
     ATOL,
-    E2E_MEAN,
     RTOL,
+    OraclePair,
     assert_close,
     check_topk_consistent,
     compare_draft,
     f64,
     staged_parity,
     staged_parity_all,
-    tol_report,
     topk_ids_match,
 )
 
@@ -58,9 +57,10 @@ def check_state_vs_oracle(st, ref, m, s, upto):
 
 def draft_vs_oracle(D, st, ref, m, anchors, k):
     """Draft every stream and compare with the oracle: element-wise within
-    the tolerance for drafters of at most two layers; deeper drafters stage
-    by stage (within the tolerance) and end to end on the mean (see
-    parity_util)."""
+    the tolerance for drafters of at most two layers; deeper drafters end to
+    end within the envelope the oracle's own float32 run gives (ref is then
+    an OraclePair; see parity_util), and stage by stage within the
+    tolerance (staged_vs_oracle)."""
     S = anchors.numel()
     logits, ids, vals = st.draft(anchors.cuda(), k=k)
     torch.cuda.synchronize()
@@ -75,10 +75,10 @@ def draft_vs_oracle(D, st, ref, m, anchors, k):
         if m["n_layers"] <= 2:
             stats.append(assert_close(lg[s], ol, f"logits stream {s}"))
             print(f"logits stream {s}: {stats[-1]}")
-            checked, near, bad = topk_ids_match(idn[s], ol, k, margin=2 * (ATOL + RTOL * np.abs(ol).max()))
+            checked, near, bad = topk_ids_match(idn[s], ol, k, margin=2 * (ATOL + RTOL * np.abs(ol)))
             assert bad == 0, (s, checked, near, bad)
         else:
-            stats.append(compare_draft(lg[s], idn[s], ol, k))
+            stats.append(compare_draft(lg[s], idn[s], ol, ref.draft32(s, int(anchors[s])), k))
     return logits, stats
 
 
@@ -115,7 +115,7 @@ def test_small_multistream_sliding_splitk(D):
     ctx = [300, 57, 1]
     S = len(ctx)
     st = dr.new_state(S, 512)
-    ref = O.OracleStreams(m, O.weights_to_f64(w), S)
+    ref = OraclePair(m, O.weights_to_f64(w), S)
     taps = SI.make_taps(m, sum(ctx), 78, device="cuda")
     segs, r0 = [], 0
     for s, c in enumerate(ctx):
@@ -139,7 +139,7 @@ def test_truncate_and_reappend(D):
     w = SI.make_weights(m, 91, device="cuda")
     dr = D.Drafter(m, w)
     st = dr.new_state(1, 512)
-    ref = O.OracleStreams(m, O.weights_to_f64(w), 1)
+    ref = OraclePair(m, O.weights_to_f64(w), 1)
     taps = SI.make_taps(m, 300, 92, device="cuda")
     st.fuse_taps(taps, [(0, 0, 300)])
     ref.append(0, [f64(t) for t in taps])
@@ -194,8 +194,8 @@ def test_bad_anchor_sets_status(D):
 def test_query_group_sizes(D, nq, nkv):
     """Every query-group size the d = 128 attention kernel handles (1, 2, 4,
     8 and 5 query heads per kv head), on a one-layer full-attention drafter:
-    each stage within the tolerance on the oracle's input, end to end on the
-    mean and the clearly separated top-k ids."""
+    each stage within the tolerance on the oracle's input, end to end within
+    the oracle's envelope, with the clearly separated top-k ids."""
     m = small_model()
     m.update(hidden=nq * 128, n_q_heads=nq, n_kv_heads=nkv, n_layers=1, layer_kinds=[0], ffn=1536)
     w = SI.make_weights(m, 300 + nq * 10 + nkv, device="cuda")
@@ -203,7 +203,7 @@ def test_query_group_sizes(D, nq, nkv):
     ctx = [333, 16]
     S = len(ctx)
     st = dr.new_state(S, 512)
-    ref = O.OracleStreams(m, O.weights_to_f64(w), S)
+    ref = OraclePair(m, O.weights_to_f64(w), S)
     taps = SI.make_taps(m, sum(ctx), 301, device="cuda")
     segs, r0 = [], 0
     for s, c in enumerate(ctx):
@@ -218,7 +218,7 @@ def test_query_group_sizes(D, nq, nkv):
     idn = ids.cpu().numpy().reshape(S, 15, 4)
     for s in range(S):
         ol, _ = ref.draft(s, int(anchors[s]))
-        compare_draft(lg[s], idn[s], ol, 4)
+        compare_draft(lg[s], idn[s], ol, ref.draft32(s, int(anchors[s])), 4)
     staged_vs_oracle(st, ref, m, anchors, 4)
 
 
@@ -274,7 +274,7 @@ def test_wide_round_throughput_paths(D):
     g = torch.Generator().manual_seed(92)
     ctx = torch.randint(1, 200, (S,), generator=g).tolist()
     st = dr.new_state(S, 256)
-    ref = O.OracleStreams(m, O.weights_to_f64(w), S)
+    ref = OraclePair(m, O.weights_to_f64(w), S)
     taps = SI.make_taps(m, sum(ctx), 93, device="cuda")
     segs, r0 = [], 0
     for s, c in enumerate(ctx):
@@ -285,19 +285,20 @@ def test_wide_round_throughput_paths(D):
     for s in (0, S - 1):
         check_state_vs_oracle(st, ref, m, s, ctx[s])
     anchors = SI.anchor_ids(S, m["vocab"], m["mask_token"], 94)
-    # end to end: the mean (at hidden 2048 a few of the 122880 logits of a
-    # stream land just past the element-wise bound: bf16 flips between the
-    # layers, as for the six-layer drafters; this drafter's logits are too
-    # flat for the end-to-end id margin, the staged check below ranks them)
+    # end to end: every logit within the oracle's envelope (at hidden 2048 a
+    # few of a stream's 122880 logits land just past the stated tolerance,
+    # bf16 flips between the layers as for the six-layer drafters); the ids
+    # wherever they are clearly ranked (these logits are flat, so a stream
+    # may have none; the staged check below ranks them all)
     logits, ids, vals = st.draft(anchors.cuda(), k=8)
     rc, bits = st.status()
     assert rc == 0 and bits == 0, (rc, bits)
     check_topk_consistent(logits, ids, vals)
     lg = logits.cpu().float().numpy().reshape(S, 15, -1)
+    idn = ids.cpu().numpy().reshape(S, 15, 8)
     for s in range(S):
         ol, _ = ref.draft(s, int(anchors[s]))
-        rep = tol_report(lg[s], ol)
-        assert rep["mean_abs"] < E2E_MEAN, (s, rep)
+        compare_draft(lg[s], idn[s], ol, ref.draft32(s, int(anchors[s])), 8, require_checked=False)
     # stage by stage, all 24 streams a launch: every element within the tolerance
     staged_parity_all(st, ref, m, anchors, 8)
 

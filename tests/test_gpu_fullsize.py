@@ -1,9 +1,11 @@
 """Full-size parity on the four large workloads, in the launch shapes the bench
 times. The oracle computes sampled outputs one by one: sampled fused rows and
 K/V rows of a fill, and the full draft of sampled streams (it fuses only
-those streams' contexts). Everything else is checked by properties that hold
-at any size (top-k consistent with the logits, planted acceptance lengths,
-valid sampling outcomes).
+those streams' contexts). The end-to-end drafts are compared element by
+element within the envelope the oracle's own float32 run gives (parity_util);
+every stage within the stated tolerance. Everything else is checked by
+properties that hold at any size (top-k consistent with the logits, planted
+acceptance lengths, valid sampling outcomes).
 """
 import numpy as np
 import pytest
@@ -23,10 +25,16 @@ def D():
     return D
 
 
-def sampled_rows(n, k, seed):
+def sampled_rows(n, k, seed, tile=256):
+    """k seeded rows of an n-row fill, plus the first and last rows and the
+    rows on both sides of the first, middle and last row-tile boundaries of
+    the wide fc GEMM (256 rows a tile)."""
     rng = np.random.default_rng(seed)
     idx = set(rng.choice(n, size=min(k, n), replace=False).tolist())
     idx |= {0, n - 1}
+    for b in {tile, (n // 2 // tile) * tile, ((n - 1) // tile) * tile}:
+        if 0 < b < n:
+            idx |= {b - 1, b}
     return np.array(sorted(idx))
 
 
@@ -60,12 +68,13 @@ def nine_b(D):
     m = P["model"]
     w = SI.make_weights(m, P["seed"], device="cuda")
     dr = D.Drafter(m, w)
-    yield P, m, w, dr, O.weights_to_f64(w)
+    w64 = O.weights_to_f64(w)
+    yield P, m, w, dr, (w64, O.weights_as(w64, np.float32))
     dr.close()
 
 
 def test_9b_batch1_decode_round(D, nine_b):
-    P, m, w, dr, w64 = nine_b
+    P, m, w, dr, (w64, w32) = nine_b
     C0 = P["context"][0]
     st = dr.new_state(1, P["ring"])
     ctx = SI.make_taps(m, C0 + 16, P["seed"] + 1, device="cuda")
@@ -77,9 +86,10 @@ def test_9b_batch1_decode_round(D, nine_b):
     anchor = SI.anchor_ids(1, m["vocab"], m["mask_token"], P["seed"] + 2, device="cuda")
     logits, ids, vals = st.draft(anchor, k=P["topk"])
     check_topk_consistent(logits, ids, vals)
-    ref = oracle_stream(m, w64, host)
+    ref = oracle_stream(m, w64, host, w32)
+    o32 = ref.draft32(0, int(anchor[0]))
     ol = staged_parity(st, ref, 0, m, 0, int(anchor[0]), P["topk"])
-    compare_draft(logits.cpu().float().numpy(), ids.cpu().numpy(), ol, P["topk"])
+    compare_draft(logits.cpu().float().numpy(), ids.cpu().numpy(), ol, o32, P["topk"])
     # verification on the drafted top-1 ids: planted acceptance is recovered
     tl = SI.make_logits((1, 16, m["vocab"]), P["target_logit_std"], P["seed"] + 3)
     L = 9
@@ -93,7 +103,7 @@ def test_9b_batch1_decode_round(D, nine_b):
 
 
 def test_long32k_append_and_windowed_draft(D, nine_b):
-    P0, m, w, dr, w64 = nine_b
+    P0, m, w, dr, (w64, w32) = nine_b
     P = SI.preset("long32k")
     C0 = P["context"][0]
     st = dr.new_state(1, P["ring"])
@@ -106,15 +116,16 @@ def test_long32k_append_and_windowed_draft(D, nine_b):
     anchor = SI.anchor_ids(1, m["vocab"], m["mask_token"], P["seed"] + 2, device="cuda")
     logits, ids, vals = st.draft(anchor, k=P["topk"])
     check_topk_consistent(logits, ids, vals)
-    ref = oracle_stream(m, w64, host)
+    ref = oracle_stream(m, w64, host, w32)
+    o32 = ref.draft32(0, int(anchor[0]))
     ol = staged_parity(st, ref, 0, m, 0, int(anchor[0]), P["topk"])
-    compare_draft(logits.cpu().float().numpy(), ids.cpu().numpy(), ol, P["topk"])
+    compare_draft(logits.cpu().float().numpy(), ids.cpu().numpy(), ol, o32, P["topk"])
     rc, bits = st.status()
     assert rc == 0 and bits == 0
 
 
 def test_serve32_shared_round(D, nine_b):
-    P0, m, w, dr, w64 = nine_b
+    P0, m, w, dr, (w64, w32) = nine_b
     P = SI.preset("serve32")
     ctx = P["context"]
     S = len(ctx)
@@ -130,17 +141,23 @@ def test_serve32_shared_round(D, nine_b):
     # concurrent == solo. Up to four streams a call (the split-K fixed by
     # the weights) a stream's draft is bit-identical to its solo draft; a
     # 32-stream round runs the throughput GEMM configuration, another fp32
-    # summation order, and meets the end-to-end criterion against the solo
-    # draft (mean error and the clearly ranked top-k ids).
+    # summation order, so there the stream drafted inside the round and the
+    # same stream drafted alone each meet the end-to-end envelope against the
+    # oracle.
     solo, _, _ = st.draft(anchors[5:6].contiguous(), s_begin=5, k=P["topk"])
     four, _, _ = st.draft(anchors[4:8].contiguous(), s_begin=4, k=P["topk"])
     assert torch.equal(solo, four[15:30])
-    compare_draft(lg[5], idn[5], solo.cpu().double().numpy(), P["topk"])
-    for s in sorted({int(np.argmin(ctx)), int(np.argmax(ctx))}):
+    s_min = int(np.argmin(ctx))
+    solo_lg, solo_ids, _ = st.draft(anchors[s_min : s_min + 1].contiguous(), s_begin=s_min, k=P["topk"])
+    solo_lg, solo_ids = solo_lg.cpu().float().numpy(), solo_ids.cpu().numpy()
+    for s in sorted({s_min, int(np.argmax(ctx))}):
         host = [f64(t[offs[s] : offs[s + 1]]) for t in taps]
-        ref = oracle_stream(m, w64, host)
+        ref = oracle_stream(m, w64, host, w32)
+        o32 = ref.draft32(0, int(anchors[s]))
         ol = staged_parity(st, ref, 0, m, s, int(anchors[s]), P["topk"])
-        compare_draft(lg[s], idn[s], ol, P["topk"])
+        compare_draft(lg[s], idn[s], ol, o32, P["topk"])
+        if s == s_min:
+            compare_draft(solo_lg, solo_ids, ol, o32, P["topk"])
     # greedy verification of every stream against planted target logits
     tl = SI.make_logits((S, 16, m["vocab"]), P["target_logit_std"], P["seed"] + 3)
     lengths = SI.make_accept_lengths(S, P["seed"] + 4)
@@ -186,6 +203,7 @@ def test_dflash2_geometry_sampling_round(D):
     s = S - 1
     host = [f64(t[offs[s] : offs[s + 1]]) for t in taps]
     ref = oracle_stream(m, w64, host)
+    o32 = ref.draft32(0, int(anchors[s]))
     ol = staged_parity(st, ref, 0, m, s, int(anchors[s]), P["topk"])
-    compare_draft(lg[s], idn[s], ol, P["topk"])
+    compare_draft(lg[s], idn[s], ol, o32, P["topk"])
     dr.close()
