@@ -99,6 +99,9 @@ __all__ = [
     "greedy_verify",
     "softmax_t",
     "draft_confidence",
+    "selector_edges",
+    "path_score",
+    "select_path",
     "draft_stop",
     "inverse_cdf",
     "sample_rows",
@@ -487,6 +490,111 @@ def draft_stop(conf, min_p):
             n += 1
         out.append(n)
     return np.asarray(out, dtype=np.int64)
+
+
+# ----------------------------------------------------------------------------
+# DFlash2 candidate-path selector
+
+
+def selector_edges(cand_ids, U, W):
+    """Edge scores of adjacent candidate pairs.
+
+    The explainer's section 五 ("Candidate path selector"): DFlash 2 keeps
+    the top-k candidates at every position and a light selector scores
+    adjacent candidate pairs; the public DFlash2 config gives
+    selector_top_k 16 and selector_rank 256. TensorFold #1851 item 1: with no
+    codebooks (rank 0) the selector's edge term is zero. Reading: the pair
+    score is a rank-r bilinear form of per-token codebooks U, W [V, r]:
+    edge(i, a, b) = sum_j U[c(i, a), j] * W[c(i+1, b), j], where c(i, a) is
+    candidate a of position i. An id outside [0, V) is not a candidate: its
+    codebook rows count as zero.
+
+    cand_ids: [P, k] ints; U, W: [V, r]. Returns float64 [P-1, k, k].
+    """
+    ids = np.asarray(cand_ids, dtype=np.int64)
+    U = np.asarray(U, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    V = U.shape[0]
+    valid = (ids >= 0) & (ids < V)
+    safe = np.where(valid, ids, 0)
+    Uc = U[safe] * valid[..., None]
+    Wc = W[safe] * valid[..., None]
+    return np.einsum("iar,ibr->iab", Uc[:-1], Wc[1:])
+
+
+def path_score(ranks, cand_ids, cand_vals, U, W):
+    """Score of one path (candidate index a_i at every position i): the node
+    scores of its candidates plus the edge scores of its adjacent pairs."""
+    vals = np.asarray(cand_vals, dtype=np.float64)
+    ids = np.asarray(cand_ids, dtype=np.int64)
+    V = np.asarray(U).shape[0]
+    if any(not (0 <= ids[i, a] < V) for i, a in enumerate(ranks)):
+        return -np.inf
+    e = selector_edges(cand_ids, U, W)
+    return float(sum(vals[i, a] for i, a in enumerate(ranks)) + sum(e[i, ranks[i], ranks[i + 1]] for i in range(len(ranks) - 1)))
+
+
+def select_path(cand_ids, cand_vals, U, W):
+    """The selector's choice: the one consistent path of highest score.
+
+    The explainer's section 五: score adjacent candidate pairs, then choose a
+    consistent path; "Port the DFlash2 protocol" ("What is portable"): top
+    candidates at each position, then coherent candidate-path selection,
+    then target verification. Reading: a path's score is the sum of its
+    candidates' node scores (the drafter's logits; a position's
+    log-probabilities differ from its logits by one constant, which moves
+    every path's score alike) and of the edge scores of its adjacent pairs
+    (selector_edges); the best path is found by the max-sum recursion over
+    positions (Viterbi), ties going to the lower candidate index at every
+    step. With rank 0 every edge is zero and the path is each position's
+    highest candidate.
+
+    cand_ids: [P, k] ints (candidate a of position i); cand_vals: [P, k]
+    node scores; U, W: [V, r]. Returns (ranks [P], ids [P], score, margin):
+    margin = score minus the best score of any path that differs from the
+    chosen one (how far the choice is from flipping); ranks and ids are -1
+    and score -inf when some position has no valid candidate.
+    """
+    ids = np.asarray(cand_ids, dtype=np.int64)
+    vals = np.asarray(cand_vals, dtype=np.float64)
+    P, k = ids.shape
+    V = np.asarray(U).shape[0]
+    node = np.where((ids >= 0) & (ids < V), vals, -np.inf)
+    edge = selector_edges(ids, U, W)
+    # forward: F[i][b] = best score of a path over positions 0..i ending in b
+    F = np.empty((P, k))
+    back = np.zeros((P, k), dtype=np.int64)
+    F[0] = node[0]
+    for i in range(1, P):
+        for b in range(k):
+            best, arg = -np.inf, 0
+            for a in range(k):
+                v = F[i - 1][a] + edge[i - 1][a][b]
+                if v > best:
+                    best, arg = v, a
+            F[i][b] = node[i][b] + best
+            back[i][b] = arg
+    last, score = 0, -np.inf
+    for b in range(k):
+        if F[P - 1][b] > score:
+            last, score = b, F[P - 1][b]
+    if score == -np.inf:
+        return [-1] * P, [-1] * P, -np.inf, 0.0
+    ranks = [0] * P
+    ranks[P - 1] = last
+    for i in range(P - 1, 0, -1):
+        ranks[i - 1] = int(back[i][ranks[i]])
+    # backward: G[i][a] = best score of positions i+1..P-1 after a at i
+    G = np.zeros((P, k))
+    for i in range(P - 2, -1, -1):
+        for a in range(k):
+            G[i][a] = max(edge[i][a][b] + node[i + 1][b] + G[i + 1][b] for b in range(k))
+    runner = -np.inf
+    for i in range(P):
+        for a in range(k):
+            if a != ranks[i]:
+                runner = max(runner, F[i][a] + G[i][a])
+    return ranks, [int(ids[i][ranks[i]]) for i in range(P)], float(score), float(score - runner)
 
 
 def inverse_cdf(wts, u):

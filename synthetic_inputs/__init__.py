@@ -337,6 +337,13 @@ def plant_accepts(target_logits, draft_ids, lengths):
     return target_logits
 
 
+def make_codebooks(vocab, rank, seed, std=0.1, device="cpu"):
+    """A selector's pair codebooks U, W: two [vocab, rank] bf16 draws from
+    N(0, std^2) (synthetic: the pages publish only the rank)."""
+    g = _gen(seed, device)
+    return _normal_bf16((vocab, rank), std, 0.0, g, device), _normal_bf16((vocab, rank), std, 0.0, g, device)
+
+
 def anchor_ids(streams, vocab, mask_token, seed, device="cpu"):
     return make_token_ids((streams,), vocab, seed, device, exclude=mask_token)
 

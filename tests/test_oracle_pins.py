@@ -4,6 +4,7 @@ None of these compares the oracle with itself. Each test uses a closed form,
 a value printed on the pages, a library routine for a special case, brute
 force on tiny inputs, or an invariant that a plausible mistake breaks.
 """
+import itertools
 import json
 import math
 import os
@@ -585,3 +586,62 @@ def test_layer_halves_add_to_the_residual():
     g1 = O.mlp_half(m, w, 0, X) - X
     g3 = O.mlp_half(m, w, 0, 3 * X) - 3 * X
     assert np.allclose(g1, g3, rtol=0, atol=1e-6 + 2 ** -6 * np.abs(g1).max())
+
+
+# ---------------------------------------------------------------- candidate-path selector
+def _codebooks(case):
+    V, r = case["vocab"], case["rank"]
+    U = np.zeros((V, r))
+    W = np.zeros((V, r))
+    for k, v in case["U"].items():
+        U[int(k)] = v
+    for k, v in case["W"].items():
+        W[int(k)] = v
+    return U, W
+
+
+def test_selector_golden_cases():
+    with open(os.path.join(GOLDEN, "selector_cases.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        U, W = _codebooks(c)
+        ranks, ids, score, margin = O.select_path(c["cand_ids"], c["cand_vals"], U, W)
+        want = -np.inf if c["score"] == "-inf" else c["score"]
+        assert ranks == c["ranks"] and ids == c["ids"], c["name"]
+        assert score == want and margin == c["margin"], (c["name"], score, margin)
+
+
+def test_selector_brute_force():
+    """Every path enumerated on small cases: the chosen path has the highest
+    score, and the margin is the gap to the best other path."""
+    rng = np.random.default_rng(5)
+    for P in (1, 2, 3, 4):
+        for k in (1, 2, 3, 4):
+            V, r = 20, 5
+            ids = np.stack([rng.choice(V, size=k, replace=False) for _ in range(P)])
+            vals = rng.standard_normal((P, k))
+            U, W = rng.standard_normal((V, r)), rng.standard_normal((V, r))
+            scores = {}
+            for path in itertools.product(range(k), repeat=P):
+                e = sum(U[ids[i, path[i]]] @ W[ids[i + 1, path[i + 1]]] for i in range(P - 1))
+                scores[path] = sum(vals[i, path[i]] for i in range(P)) + e
+            order = sorted(scores, key=lambda p: -scores[p])
+            ranks, got, score, margin = O.select_path(ids, vals, U, W)
+            assert tuple(ranks) == order[0] and got == [int(ids[i, a]) for i, a in enumerate(ranks)]
+            assert abs(score - scores[order[0]]) < 1e-12
+            assert abs(O.path_score(ranks, ids, vals, U, W) - score) < 1e-12
+            if len(order) > 1:
+                assert abs(margin - (scores[order[0]] - scores[order[1]])) < 1e-12
+
+
+def test_selector_rank0_is_per_position_top1():
+    """TensorFold #1851 item 1: with no codebooks (rank 0) the edge term is
+    zero, so the path is each position's highest candidate (the lowest
+    index among equal ones)."""
+    rng = np.random.default_rng(6)
+    ids = rng.integers(0, 100, size=(15, 16))
+    vals = np.round(rng.standard_normal((15, 16)) * 4) / 4  # many exact ties
+    ranks, got, score, _ = O.select_path(ids, vals, np.zeros((100, 0)), np.zeros((100, 0)))
+    assert ranks == [int(np.argmax(v)) for v in vals]
+    assert score == sum(v.max() for v in vals)
+    assert np.all(O.selector_edges(ids, np.zeros((100, 0)), np.zeros((100, 0))) == 0)
