@@ -102,6 +102,9 @@ __all__ = [
     "selector_edges",
     "path_score",
     "select_path",
+    "tree_nodes",
+    "tree_mask",
+    "tree_greedy_verify",
     "draft_stop",
     "inverse_cdf",
     "sample_rows",
@@ -595,6 +598,84 @@ def select_path(cand_ids, cand_vals, U, W):
             if a != ranks[i]:
                 runner = max(runner, F[i][a] + G[i][a])
     return ranks, [int(ids[i][ranks[i]]) for i in range(P)], float(score), float(score - runner)
+
+
+# ----------------------------------------------------------------------------
+# tree drafting and tree verification
+
+
+def tree_nodes(anchor, topk_ids, widths):
+    """A stream's draft tree from each depth's marginals.
+
+    TensorFold #1851: streams draft per-stream trees in the shared rounds,
+    and with no codebooks (rank 0) the trees come from each depth's
+    marginals (item 1). Reading: the root is the anchor (position C); every
+    node at depth j - 1 has as children the top-b_j candidates of mask row j
+    (the drafter's marginal for position C + j, one forward predicts every
+    depth, so every parent gets the same candidates), in candidate order.
+    Nodes are numbered breadth first, children of earlier nodes first.
+
+    topk_ids: [15, k] the draft's per-row top candidates (row j - 1 is depth
+    j); widths: b_1..b_D with 1 <= b_j <= k. Returns (tokens, parents,
+    depths) lists, node 0 the root (parent -1, depth 0).
+    """
+    tokens, parents, depths = [int(anchor)], [-1], [0]
+    level = [0]
+    for j, b in enumerate(widths, start=1):
+        nxt = []
+        for p in level:
+            for r in range(int(b)):
+                tokens.append(int(topk_ids[j - 1][r]))
+                parents.append(p)
+                depths.append(j)
+                nxt.append(len(tokens) - 1)
+        level = nxt
+    return tokens, parents, depths
+
+
+def tree_mask(parents):
+    """Ancestor-or-self relation of the tree's nodes, the attention mask a
+    target applies when it scores the whole tree in one pass: mask[n][m] is
+    True iff m lies on the path from the root to n."""
+    N = len(parents)
+    mask = np.zeros((N, N), dtype=bool)
+    for n in range(N):
+        m = n
+        while m >= 0:
+            mask[n][m] = True
+            m = parents[m]
+    return mask
+
+
+def tree_greedy_verify(tokens, parents, target_logits):
+    """Greedy verification of a draft tree.
+
+    The explainer's section 四 (greedy: accept the drafted tokens that match
+    the target's argmax, take the target's argmax at the first mismatch),
+    applied along the tree: target_logits[n] is the target's prediction for
+    the position after node n, having read the path from the root to n.
+    From the root, step to the child whose token is the target's argmax at
+    the current node (ties to the lowest id) while one exists; the accepted
+    tokens are the path's, the bonus is the argmax at the last node reached
+    ("Port the DFlash2 protocol": accepted prefix plus bonus).
+
+    Returns (a, tokens16, node): a accepted drafts, the 16 committed-token
+    slots (the a path tokens, the bonus, then -1), and the last node reached.
+    """
+    children = [[] for _ in tokens]
+    for n, p in enumerate(parents):
+        if p >= 0:
+            children[p].append(n)
+    cur, path = 0, []
+    while True:
+        t = argmax_lowest(target_logits[cur])
+        nxt = [c for c in children[cur] if tokens[c] == t]
+        if not nxt:
+            break
+        cur = nxt[0]
+        path.append(tokens[cur])
+    a = len(path)
+    return a, path + [t] + [-1] * (BLOCK - 1 - a), cur
 
 
 def inverse_cdf(wts, u):

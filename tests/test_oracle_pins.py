@@ -645,3 +645,63 @@ def test_selector_rank0_is_per_position_top1():
     assert ranks == [int(np.argmax(v)) for v in vals]
     assert score == sum(v.max() for v in vals)
     assert np.all(O.selector_edges(ids, np.zeros((100, 0)), np.zeros((100, 0))) == 0)
+
+
+# ---------------------------------------------------------------- tree drafting and verification
+def _tree_logits(case, N, V):
+    rows = np.zeros((N, V))
+    for n, t in enumerate(case["argmax"]):
+        rows[n][t] = 1.0
+    for n, t in case.get("tie_with", []):
+        rows[n][t] = 1.0
+    return rows
+
+
+def test_tree_golden_cases():
+    with open(os.path.join(GOLDEN, "tree_verify_cases.json")) as f:
+        g = json.load(f)
+    t = g["tree"]
+    tokens, parents, depths = O.tree_nodes(t["anchor"], t["topk_ids"], t["widths"])
+    assert (tokens, parents, depths) == (t["tokens"], t["parents"], t["depths"])
+    mask = O.tree_mask(parents)
+    assert np.nonzero(mask[len(tokens) - 1])[0].tolist() == t["ancestors_of_last"]
+    for c in g["cases"]:
+        a, out, node = O.tree_greedy_verify(tokens, parents, _tree_logits(c, len(tokens), t["vocab"]))
+        assert (a, out, node) == (c["accept"], c["tokens"], c["node"]), c["name"]
+
+
+def test_tree_structure():
+    """Node count 1 + sum_j prod_{i<=j} b_i; breadth-first order (depths
+    non-decreasing, a parent before its children, a node's children
+    contiguous and in candidate order); the mask row of a node has its
+    depth + 1 entries and contains its parent's."""
+    rng = np.random.default_rng(3)
+    for widths in ([1] * 15, [4, 2, 2, 1, 1], [16], [3, 3, 3, 3], [2] * 7):
+        topk = rng.integers(0, 1000, size=(15, 16))
+        tokens, parents, depths = O.tree_nodes(11, topk, widths)
+        assert len(tokens) == 1 + sum(int(np.prod(widths[: j + 1])) for j in range(len(widths)))
+        assert depths == sorted(depths) and all(parents[n] < n for n in range(1, len(tokens)))
+        mask = O.tree_mask(parents)
+        for n in range(1, len(tokens)):
+            assert mask[n].sum() == depths[n] + 1 and np.all(mask[n] >= mask[parents[n]])
+            kids = [c for c in range(len(tokens)) if parents[c] == parents[n]]
+            assert kids == list(range(kids[0], kids[0] + len(kids)))
+            assert tokens[n] == topk[depths[n] - 1][kids.index(n)]
+
+
+def test_single_branch_tree_is_greedy_verify():
+    """A tree with one candidate at every depth is the drafted chain itself;
+    its verification must equal the chain's greedy verification (node j's
+    target row is the chain's row j)."""
+    rng = np.random.default_rng(4)
+    V = 50
+    for trial in range(200):
+        topk = rng.integers(0, V, size=(15, 4))
+        tl = rng.standard_normal((16, V))
+        L = int(rng.integers(0, 17))
+        for i in range(min(L, 15)):  # plant a prefix of accepts
+            tl[i][topk[i][0]] = tl[i].max() + 1.0
+        tokens, parents, _ = O.tree_nodes(3, topk, [1] * 15)
+        a, out, node = O.tree_greedy_verify(tokens, parents, tl)
+        ga, gout = O.greedy_verify(topk[:, 0], tl)
+        assert (a, out) == (ga, gout) and node == a
