@@ -15,8 +15,12 @@ from .drafter import (  # noqa: F401
     fused_row_bytes,
     kind,
     launch_count,
+    select_path,
     tap_row_bytes,
     topk,
+    tree_build,
+    tree_size,
+    tree_verify,
     verify_greedy,
     verify_sample,
 )

@@ -134,6 +134,13 @@ def _load():
     fn("dflash_draft_head", C.c_int, vp, vp, C.c_int, vp, vp, vp, vp, C.c_int, vp, sz, vp)
     fn("dflash_topk", C.c_int, vp, C.c_int, C.c_int, C.c_int, C.c_float, vp, vp, vp, vp, vp)
     fn("dflash_draft_stop", C.c_int, vp, C.c_int, C.c_int, C.c_float, C.c_float, vp, vp, vp)
+    fn("dflash_select_path_workspace_bytes", C.c_int, C.c_int, C.c_int, C.c_int, P(sz))
+    fn("dflash_tree_size", C.c_int, C.c_int, vp, C.c_int, P(C.c_int))
+    fn("dflash_tree_build", C.c_int, C.c_int, C.c_int, vp, C.c_int, vp, vp, vp, vp, vp, vp, vp)
+    fn("dflash_tree_verify_workspace_bytes", C.c_int, C.c_int, C.c_int, P(sz))
+    fn("dflash_tree_verify", C.c_int, C.c_int, C.c_int, vp, C.c_int, vp, vp, vp, vp, vp, vp, sz, vp)
+    fn("dflash_select_path", C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, vp, vp, vp, vp, vp, vp, vp, vp, sz,
+       vp)
     fn("dflash_verify_workspace_bytes", C.c_int, C.c_int, C.c_int, C.c_int, P(sz))
     fn("dflash_verify", C.c_int, C.c_int, C.c_int, C.c_int, vp, C.c_int, vp, vp, vp, C.c_float, vp, vp, vp, sz, vp)
     fn("dflash_verify_sample_noalloc", C.c_int, C.c_int, C.c_int, vp, C.c_int, vp, vp, vp, C.c_float, vp, vp, vp)
@@ -171,6 +178,12 @@ EXPORTED = [
     "dflash_draft_head",
     "dflash_topk",
     "dflash_draft_stop",
+    "dflash_select_path_workspace_bytes",
+    "dflash_select_path",
+    "dflash_tree_size",
+    "dflash_tree_build",
+    "dflash_tree_verify_workspace_bytes",
+    "dflash_tree_verify",
     "dflash_verify_workspace_bytes",
     "dflash_verify",
     "dflash_verify_sample_noalloc",

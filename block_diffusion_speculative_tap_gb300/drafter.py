@@ -24,6 +24,10 @@ __all__ = [
     "topk",
     "verify_greedy",
     "verify_sample",
+    "select_path",
+    "tree_size",
+    "tree_build",
+    "tree_verify",
     "launch_count",
 ]
 
@@ -402,6 +406,102 @@ def draft_stop(logits, min_p, temperature=1.0, conf=None, lens=None):
         "dflash_draft_stop",
     )
     return conf, lens
+
+
+def select_path(cand_ids, cand_vals, U, W, positions=15, path_ids=None, path_ranks=None, path_score=None, ws=None):
+    """dflash_select_path: the DFlash2 selector's path through per-position
+    candidates. cand_ids int32 / cand_vals fp32: [S * positions, k] (the
+    top-k outputs of a draft) or [S, positions, k]; U, W: bf16 [V, rank]
+    codebooks. Returns (path_ids [S, positions], path_ranks [S, positions],
+    path_score [S])."""
+    _need(cand_ids, torch.int32, "cand_ids")
+    _need(cand_vals, torch.float32, "cand_vals")
+    _need(U, torch.bfloat16, "U")
+    _need(W, torch.bfloat16, "W")
+    if U.shape != W.shape or U.dim() != 2:
+        raise ValueError("U, W: bf16 [V, rank] of one shape")
+    k = cand_ids.shape[-1]
+    if cand_vals.shape != cand_ids.shape or cand_ids.numel() % (positions * k):
+        raise ValueError("cand_ids / cand_vals: [S * positions, k] of one shape")
+    S = cand_ids.numel() // (positions * k)
+    V, rank = U.shape
+    dev = cand_ids.device
+    path_ids = path_ids if path_ids is not None else torch.empty(S, positions, dtype=torch.int32, device=dev)
+    path_ranks = path_ranks if path_ranks is not None else torch.empty(S, positions, dtype=torch.int32, device=dev)
+    path_score = path_score if path_score is not None else torch.empty(S, dtype=torch.float32, device=dev)
+    nb = C.c_size_t()
+    check(lib.dflash_select_path_workspace_bytes(S, positions, k, C.byref(nb)), "select_path_workspace_bytes")
+    if ws is None:
+        ws = torch.empty(max(nb.value, 256), dtype=torch.uint8, device=dev)
+    check(
+        lib.dflash_select_path(
+            S, positions, k, V, rank, _ptr(cand_ids), _ptr(cand_vals), _ptr(U), _ptr(W), _ptr(path_ids),
+            _ptr(path_ranks), _ptr(path_score), _ptr(ws), ws.numel(), _stream(),
+        ),
+        "dflash_select_path",
+    )
+    return path_ids, path_ranks, path_score
+
+
+def _widths(widths):
+    w = (C.c_int32 * len(widths))(*[int(x) for x in widths])
+    return w, len(widths)
+
+
+def tree_size(widths, k=16):
+    """dflash_tree_size: nodes of a draft tree of these per-depth widths."""
+    w, depth = _widths(widths)
+    n = C.c_int()
+    check(lib.dflash_tree_size(depth, w, k, C.byref(n)), "dflash_tree_size")
+    return n.value
+
+
+def tree_build(anchors, topk_ids, widths, want_mask=True):
+    """dflash_tree_build: per-stream draft trees from a draft's top-k ids
+    [S * 15, k]. Returns (tokens, parents, depths, mask) with [S, N] int32
+    tables and mask uint32 [S, N, ceil(N / 32)] (as int32) or None."""
+    _need(anchors, torch.int32, "anchors")
+    _need(topk_ids, torch.int32, "topk_ids")
+    S = anchors.numel()
+    k = topk_ids.shape[-1]
+    if topk_ids.numel() != S * 15 * k:
+        raise ValueError("topk_ids: [S * 15, k]")
+    N = tree_size(widths, k)
+    w, depth = _widths(widths)
+    dev = anchors.device
+    tokens = torch.empty(S, N, dtype=torch.int32, device=dev)
+    parents = torch.empty(S, N, dtype=torch.int32, device=dev)
+    depths = torch.empty(S, N, dtype=torch.int32, device=dev)
+    mask = torch.empty(S, N, (N + 31) // 32, dtype=torch.int32, device=dev) if want_mask else None
+    check(
+        lib.dflash_tree_build(S, depth, w, k, _ptr(anchors), _ptr(topk_ids), _ptr(tokens), _ptr(parents),
+                              _ptr(depths), _ptr(mask), _stream()),
+        "dflash_tree_build",
+    )
+    return tokens, parents, depths, mask
+
+
+def tree_verify(node_tokens, target_logits, widths, accept=None, tokens=None, node=None, ws=None):
+    """dflash_tree_verify: node_tokens [S, N] int32, target_logits [S, N, V]
+    bf16 -> (accept [S], tokens [S, 16], last node [S])."""
+    _need(node_tokens, torch.int32, "node_tokens")
+    _need(target_logits, torch.bfloat16, "target_logits")
+    S, N, V = target_logits.shape
+    w, depth = _widths(widths)
+    dev = target_logits.device
+    accept = accept if accept is not None else torch.empty(S, dtype=torch.int32, device=dev)
+    tokens = tokens if tokens is not None else torch.empty(S, 16, dtype=torch.int32, device=dev)
+    node = node if node is not None else torch.empty(S, dtype=torch.int32, device=dev)
+    nb = C.c_size_t()
+    check(lib.dflash_tree_verify_workspace_bytes(S, N, C.byref(nb)), "tree_verify_workspace_bytes")
+    if ws is None:
+        ws = torch.empty(max(nb.value, 256), dtype=torch.uint8, device=dev)
+    check(
+        lib.dflash_tree_verify(S, depth, w, V, _ptr(node_tokens), _ptr(target_logits), _ptr(accept), _ptr(tokens),
+                               _ptr(node), _ptr(ws), ws.numel(), _stream()),
+        "dflash_tree_verify",
+    )
+    return accept, tokens, node
 
 
 def _draft_ld(draft_ids):

@@ -10,6 +10,9 @@
  *   dflash_topk         vocab-wide top-k / argmax / temperature sampling
  *   dflash_verify       greedy longest-prefix + bonus, or speculative sampling
  *                       with residual correction
+ * and the rows after them: dflash_draft_stop (min-p stop),
+ * dflash_select_path (the DFlash2 candidate-path selector), dflash_tree_build
+ * and dflash_tree_verify (tree drafting and greedy tree verification).
  *
  * Sources, cited by page title and section:
  *   [TF1851]  TensorFold pull request #1851, "qwen27 dflash: read and run the
@@ -18,8 +21,8 @@
  *             drafter in place of the MTP layer", sections "Approach" and
  *             "Validation".
  *   [EXPL]    "DFlash 解碼加速：原理、限制與 oMLX 實作" (a DFlash decoding
- *             explainer), sections 三 (how DFlash works) and 四 (target
- *             verification).
+ *             explainer), sections 三 (how DFlash works), 四 (target
+ *             verification) and 五 (DFlash 2).
  *   [PROT]    "Port the DFlash2 protocol, not its checkpoint", sections
  *             "What is portable" and "Golden replay before training".
  *
@@ -317,6 +320,92 @@ int dflash_topk(const void* logits, int rows, int vocab, int k, float temperatur
  * nothing is enqueued. No workspace; asynchronous on `stream`. */
 int dflash_draft_stop(const void* logits, int streams, int vocab, float temperature, float min_p, float* conf,
                       int32_t* draft_len, dflash_stream_t stream);
+
+/* ---------------------------------------------------------------- candidate-path selector
+ * The DFlash2 selector [EXPL 五 "Candidate path selector": keep the top-k
+ * candidates of every position, score adjacent candidate pairs with a light
+ * selector, choose one consistent path (selector_top_k 16, selector_rank 256
+ * in the public DFlash2 config); TF1851 item 1: with no codebooks (rank 0)
+ * the edge term is zero; PROT "What is portable": top candidates at each
+ * position, then coherent candidate-path selection, then verification].
+ * Reading: a path (candidate a_i at each position i) scores
+ *   sum_i cand_vals[i][a_i] + sum_{i < P-1} <U[id(i, a_i)], W[id(i+1, a_{i+1})]>
+ * (node scores: the drafter's logits, which rank paths as its
+ * log-probabilities do); the chosen path maximises it, found by the max-sum
+ * recursion over positions with ties to the lower candidate index at every
+ * step. Edge dot products are fp32 sums in ascending rank order; path sums
+ * fp32.
+ *   cand_ids:   device int32 [streams, positions, k] (e.g. the top-k ids of
+ *               dflash_draft_block or dflash_topk with positions = 15); an id
+ *               outside [0, vocab) is not a candidate.
+ *   cand_vals:  device fp32 [streams, positions, k] node scores.
+ *   U, W:       device bf16 [vocab, rank] codebooks, 16-byte aligned (not
+ *               read, and may be NULL, when rank == 0 or positions == 1).
+ *   path_ids:   device int32 [streams, positions] out: the chosen ids.
+ *   path_ranks: device int32 [streams, positions] out (may be NULL): their
+ *               candidate indices.
+ *   path_score: device fp32 [streams] out (may be NULL): the path's score.
+ *   A stream with a position that has no valid candidate gets ids and ranks
+ *   -1 and score -inf.
+ * 1 <= positions <= 16, 1 <= k <= DFLASH_MAX_TOPK, 0 <= rank <=
+ * DFLASH_MAX_SELECTOR_RANK with rank a multiple of 8; ws: device, 16-byte
+ * aligned, >= dflash_select_path_workspace_bytes (0 bytes when positions ==
+ * 1). Otherwise DFLASH_E_INVALID_ARG / DFLASH_E_WORKSPACE and nothing is
+ * enqueued. Asynchronous on `stream`. */
+#define DFLASH_MAX_SELECTOR_RANK 512
+int dflash_select_path_workspace_bytes(int streams, int positions, int k, size_t* bytes);
+int dflash_select_path(int streams, int positions, int k, int vocab, int rank, const int32_t* cand_ids,
+                       const float* cand_vals, const void* U, const void* W, int32_t* path_ids, int32_t* path_ranks,
+                       float* path_score, void* ws, size_t ws_bytes, dflash_stream_t stream);
+
+/* ---------------------------------------------------------------- draft trees
+ * Tree drafting and greedy tree verification [TF1851: streams draft
+ * per-stream trees; with no codebooks (rank 0) the trees come from each
+ * depth's marginals (item 1); EXPL 四: the greedy rule; PROT "Golden replay
+ * before training": accepted prefix plus bonus]. Reading: the root (node 0,
+ * depth 0) is the anchor; every node of depth j - 1 has as children the top
+ * b_j candidates of mask row j (the drafter's marginal for position C + j),
+ * in candidate order; nodes are numbered breadth first (children of earlier
+ * nodes first), so a tree of widths b_1..b_D has
+ * 1 + sum_j (b_1 * ... * b_j) nodes.
+ *
+ * dflash_tree_size: that node count. 1 <= depth <= 15, 1 <= b_j <= k <=
+ * DFLASH_MAX_TOPK, at most DFLASH_MAX_TREE_NODES nodes; otherwise
+ * DFLASH_E_INVALID_ARG. widths: host int32 [depth].
+ *
+ * dflash_tree_build: the trees of `streams` streams from their drafts.
+ *   anchors:     device int32 [streams].
+ *   topk_ids:    device int32 [streams * 15, k], the draft's per-row top-k
+ *                ids (row s*15 + j - 1 is depth j of stream s), as
+ *                dflash_draft_block writes them.
+ *   node_tokens: device int32 [streams, N] out.
+ *   node_parent: device int32 [streams, N] out, -1 for the root (may be NULL).
+ *   node_depth:  device int32 [streams, N] out (may be NULL); a node's
+ *                position is the stream's length C plus its depth.
+ *   node_mask:   device uint32 [streams, N, ceil(N / 32)] out (may be NULL):
+ *                bit m of row n is set iff node m is on the path from the
+ *                root to n (the attention mask of a one-pass tree score).
+ *
+ * dflash_tree_verify: greedy verification of the trees. target_logits:
+ * device bf16 [streams, N, vocab] (16-byte aligned, vocab a multiple of 8),
+ * row n = the target's scores for the position after node n, having read the
+ * path from the root to n. From the root, step to the child whose token is
+ * the target's argmax at the current node (ties to the lowest id) while one
+ * exists. accept_len: device int32 [streams] out (0..depth); out_tokens:
+ * device int32 [streams, 16] out: the accepted path's tokens, the bonus (the
+ * argmax at the last node reached), then -1; accept_node: device int32
+ * [streams] out (may be NULL): the last node reached. ws: device, 16-byte
+ * aligned, >= dflash_tree_verify_workspace_bytes. A single-branch tree (all
+ * widths 1) verifies exactly as dflash_verify(GREEDY) on the chain. */
+#define DFLASH_MAX_TREE_NODES 1024
+int dflash_tree_size(int depth, const int32_t* widths, int k, int* nodes);
+int dflash_tree_build(int streams, int depth, const int32_t* widths, int k, const int32_t* anchors,
+                      const int32_t* topk_ids, int32_t* node_tokens, int32_t* node_parent, int32_t* node_depth,
+                      uint32_t* node_mask, dflash_stream_t stream);
+int dflash_tree_verify_workspace_bytes(int streams, int nodes, size_t* bytes);
+int dflash_tree_verify(int streams, int depth, const int32_t* widths, int vocab, const int32_t* node_tokens,
+                       const void* target_logits, int32_t* accept_len, int32_t* out_tokens, int32_t* accept_node,
+                       void* ws, size_t ws_bytes, dflash_stream_t stream);
 
 /* ---------------------------------------------------------------- verify
  * Target verification of S drafted blocks [EXPL 四; PROT "What is portable"].
