@@ -91,6 +91,7 @@ __all__ = [
     "attention_half",
     "mlp_half",
     "draft_layer",
+    "block_conv",
     "draft_head",
     "draft_block",
     "OracleStreams",
@@ -337,6 +338,41 @@ def draft_layer(model, w, l, X, ctx_k, ctx_v, C):
     return mlp_half(model, w, l, attention_half(model, w, l, X, ctx_k, ctx_v, C))
 
 
+def block_conv(model, w, X):
+    """DFlash2's two-tap dynamic convolution over the block's rows.
+
+    The explainer's section 五 ("Dynamic short convolution"): candidates
+    further down the block are less accurate (suffix decay); DFlash 2 adds a
+    two-tap dynamic convolution for the short-range dependencies between
+    adjacent positions of the block; the public DFlash2 config gives kernel
+    size 2. The pages give no more. Reading: a dynamic convolution in the
+    published sense (Wu et al. 2019, "Pay Less Attention with Lightweight
+    and Dynamic Convolutions": per-position kernel weights predicted from
+    the position's own input by a linear map, normalised by a softmax over
+    the kernel's taps, shared by the channels of a group), with kernel size
+    2 and causal inside the block, so row i mixes rows i - 1 and i (row 0,
+    the anchor, has no row before it). It is a residual branch on the
+    normed rows after the last layer, before the final norm, as every
+    other branch of the body:
+        h = bf16(RMSNorm(X) * conv_norm)
+        z_i = h_i . conv_proj^T, [groups, 2] (row 2g + t: tap t of group g)
+        a_i = softmax over t of z_i (per group)
+        X_i += a_i[g, 0] * h_{i-1} + a_i[g, 1] * h_i   (channel c in group
+               c // (H / groups); h_{-1} = 0)
+    X: [16, H]; returns the new residual.
+    """
+    G = model["conv_groups"]
+    H = model["hidden"]
+    h = round_bf16(rms_norm(X, w["conv_norm"], model["rms_eps"]))
+    z = (h @ w["conv_proj"].T).reshape(X.shape[0], G, 2)
+    z = z - z.max(axis=2, keepdims=True)
+    a = np.exp(z)
+    a = a / a.sum(axis=2, keepdims=True)
+    prev = np.concatenate([np.zeros((1, H), dtype=h.dtype), h[:-1]], axis=0)
+    gs = H // G
+    return X + np.repeat(a[:, :, 0], gs, axis=1) * prev + np.repeat(a[:, :, 1], gs, axis=1) * h
+
+
 def draft_head(model, w, X):
     """Final norm of the 15 mask rows and the shared LM head (the explainer's
     section 三: embedding and LM head are the target's). Returns bf16 logits
@@ -358,7 +394,8 @@ def draft_block(model, w, ctx_k, ctx_v, C, anchor, keep_residuals=False):
     of the mask rows, X final residual [16, H]); with keep_residuals, X is the
     list of residuals at every stage boundary: before layer 0, after layer
     0's attention add, after its MLP add, ..., after the last layer's MLP add
-    (2L + 1 entries).
+    (2L + 1 entries), then, for a drafter with the two-tap convolution
+    (conv_groups > 0), after the convolution (2L + 2 entries).
     """
     X = block_embed(model, w, anchor)
     Xs = [X]
@@ -366,6 +403,9 @@ def draft_block(model, w, ctx_k, ctx_v, C, anchor, keep_residuals=False):
         X = attention_half(model, w, l, X, ctx_k[l], ctx_v[l], C)
         Xs.append(X)
         X = mlp_half(model, w, l, X)
+        Xs.append(X)
+    if model.get("conv_groups", 0):
+        X = block_conv(model, w, X)
         Xs.append(X)
     logits = draft_head(model, w, X)
     assert logits.shape == (BLOCK - 1, w["embed"].shape[0]) and X.shape == (BLOCK, model["hidden"])
@@ -809,4 +849,11 @@ def validate_config(model):
     for l in range(model["n_layers"]):
         if model["layer_kinds"][l] == SLIDING and model["sliding_window"] <= 0:
             return "window"
+    G = model.get("conv_groups", 0)
+    if G:
+        # the v1 layout has no conv tensor (TensorFold #1851 item 1)
+        if model["variant"] == 1:
+            return "conv in a v1 drafter"
+        if G < 0 or G > 32 or model["hidden"] % G or (model["hidden"] // G) % 16:
+            return "conv groups"
     return None

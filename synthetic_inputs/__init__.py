@@ -276,6 +276,11 @@ def make_weights(model, seed, device="cpu", std=0.02):
                 "down_proj": proj(H, F),
             }
         )
+    if model.get("conv_groups", 0):
+        # DFlash2's two-tap dynamic convolution: its norm gain and the
+        # projection to two tap logits per channel group
+        w["conv_norm"] = gain(H)
+        w["conv_proj"] = proj(2 * model["conv_groups"], H)
     return w
 
 

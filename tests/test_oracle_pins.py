@@ -705,3 +705,86 @@ def test_single_branch_tree_is_greedy_verify():
         a, out, node = O.tree_greedy_verify(tokens, parents, tl)
         ga, gout = O.greedy_verify(topk[:, 0], tl)
         assert (a, out) == (ga, gout) and node == a
+
+
+# ---------------------------------------------------------------- DFlash2 two-tap dynamic convolution
+def _conv_model(H=256, G=4):
+    return dict(hidden=H, conv_groups=G, rms_eps=1e-6)
+
+
+def test_block_conv_zero_projection_averages_adjacent_rows():
+    """conv_proj = 0: every tap logit is 0, so both taps weigh 1/2. With
+    constant rows X_i = c_i (|c_i| = 2) and a unit gain the normed rows are
+    exactly sign(c_i) (bf16 rounds 1 - 1e-7 to 1), so
+    X'_i = c_i + (sign(c_{i-1}) + sign(c_i)) / 2 with nothing before row 0."""
+    m = _conv_model()
+    c = np.array([2.0, -2.0, -2.0, 2.0] * 4)
+    X = np.repeat(c[:, None], m["hidden"], axis=1)
+    w = {"conv_norm": np.ones(m["hidden"]), "conv_proj": np.zeros((2 * m["conv_groups"], m["hidden"]))}
+    out = O.block_conv(m, w, X)
+    sg = np.sign(c)
+    want = c + 0.5 * (np.concatenate([[0.0], sg[:-1]]) + sg)
+    assert np.array_equal(out, np.repeat(want[:, None], m["hidden"], axis=1))
+
+
+def test_block_conv_tap_order():
+    """Tap 0 reads the previous row, tap 1 the row itself: a projection that
+    makes tap 0 dominate adds the previous row's normed values (row 0 gets
+    nothing), one that makes tap 1 dominate adds the row's own."""
+    m = _conv_model()
+    H, G = m["hidden"], m["conv_groups"]
+    rng = np.random.default_rng(1)
+    X = np.abs(rng.standard_normal((16, H))) + 1.0  # positive rows: positive normed values
+    g = np.ones(H)
+    h = O.round_bf16(O.rms_norm(X, g, 1e-6))
+    for tap in (0, 1):
+        P = np.zeros((2 * G, H))
+        P[tap::2] = 1.0  # logit of `tap` = sum of the row's normed values (> 200), the other 0
+        out = O.block_conv(m, {"conv_norm": g, "conv_proj": P}, X)
+        add = np.concatenate([np.zeros((1, H)), h[:-1]]) if tap == 0 else h
+        assert np.allclose(out, X + add, rtol=0, atol=1e-12)
+
+
+def test_block_conv_locality_and_groups():
+    """Row j reaches only rows j and j + 1; a projection that only feeds
+    group 0's logits leaves every other group at the even average."""
+    m = _conv_model(H=512, G=8)
+    H, G = 512, 8
+    rng = np.random.default_rng(2)
+    X = rng.standard_normal((16, H))
+    w = {"conv_norm": 1 + 0.02 * rng.standard_normal(H), "conv_proj": 0.05 * rng.standard_normal((2 * G, H))}
+    out = O.block_conv(m, w, X)
+    for j in (0, 7, 15):
+        X2 = X.copy()
+        X2[j] += rng.standard_normal(H)
+        out2 = O.block_conv(m, w, X2)
+        moved = [i for i in range(16) if not np.array_equal(out[i], out2[i])]
+        assert moved == [i for i in (j, j + 1) if i < 16]
+    P = np.zeros((2 * G, H))
+    P[0:2] = rng.standard_normal((2, H))  # group 0's two taps only
+    out = O.block_conv(m, {"conv_norm": w["conv_norm"], "conv_proj": P}, X)
+    h = O.round_bf16(O.rms_norm(X, w["conv_norm"], 1e-6))
+    prev = np.concatenate([np.zeros((1, H)), h[:-1]])
+    gs = H // G
+    assert np.allclose(out[:, gs:], X[:, gs:] + 0.5 * (prev[:, gs:] + h[:, gs:]), rtol=0, atol=1e-12)
+    assert not np.allclose(out[:, :gs], X[:, :gs] + 0.5 * (prev[:, :gs] + h[:, :gs]))
+
+
+def test_conv_drafter_block_and_config():
+    """A DFlash2-layout drafter with the convolution runs it after the last
+    layer (one more residual in the stage list, equal to block_conv of the
+    one before); a v1 config with a convolution is refused (the v1 layout
+    has no conv tensor, TensorFold #1851 item 1), and so are group counts
+    that do not split the hidden width into multiples of 16."""
+    m = SI.shrink(SI.presets()["tiny"]["model"], variant=2, conv_groups=4)
+    w = O.weights_to_f64(SI.make_weights(m, 5))
+    ref = O.OracleStreams(m, w, 1)
+    ref.append(0, [O.to_f64(t) for t in SI.make_taps(m, 20, 6)])
+    logits, Xs = ref.draft(0, 3, keep_residuals=True)
+    assert len(Xs) == 2 * m["n_layers"] + 2
+    assert np.array_equal(Xs[-1], O.block_conv(m, w, Xs[-2]))
+    assert np.array_equal(logits, O.draft_head(m, w, Xs[-1]))
+    assert O.validate_config(m) is None
+    assert O.validate_config(dict(m, variant=1)) is not None
+    assert O.validate_config(dict(m, conv_groups=3)) is not None  # 256 / 3
+    assert O.validate_config(dict(m, conv_groups=32)) is not None  # groups of 8 channels
