@@ -62,6 +62,7 @@ class Config(C.Structure):
         ("layer_kind", C.c_int32 * MAX_LAYERS),
         ("rope_theta", C.c_float),
         ("rms_eps", C.c_float),
+        ("conv_groups", C.c_int32),
     ]
 
 
@@ -91,6 +92,8 @@ class Weights(C.Structure):
         ("norm", C.c_void_p),
         ("embed", C.c_void_p),
         ("layers", C.POINTER(LayerWeights)),
+        ("conv_norm", C.c_void_p),
+        ("conv_proj", C.c_void_p),
     ]
 
 
@@ -134,6 +137,7 @@ def _load():
     fn("dflash_draft_head", C.c_int, vp, vp, C.c_int, vp, vp, vp, vp, C.c_int, vp, sz, vp)
     fn("dflash_topk", C.c_int, vp, C.c_int, C.c_int, C.c_int, C.c_float, vp, vp, vp, vp, vp)
     fn("dflash_draft_stop", C.c_int, vp, C.c_int, C.c_int, C.c_float, C.c_float, vp, vp, vp)
+    fn("dflash_draft_conv", C.c_int, vp, vp, C.c_int, vp, vp, sz, vp)
     fn("dflash_select_path_workspace_bytes", C.c_int, C.c_int, C.c_int, C.c_int, P(sz))
     fn("dflash_tree_size", C.c_int, C.c_int, vp, C.c_int, P(C.c_int))
     fn("dflash_tree_build", C.c_int, C.c_int, C.c_int, vp, C.c_int, vp, vp, vp, vp, vp, vp, vp)
@@ -178,6 +182,7 @@ EXPORTED = [
     "dflash_draft_head",
     "dflash_topk",
     "dflash_draft_stop",
+    "dflash_draft_conv",
     "dflash_select_path_workspace_bytes",
     "dflash_select_path",
     "dflash_tree_size",
@@ -230,4 +235,5 @@ def make_config(model: dict) -> Config:
         c.layer_kind[i] = k
     c.rope_theta = model.get("rope_theta", 1.0e6)
     c.rms_eps = model.get("rms_eps", 1.0e-6)
+    c.conv_groups = model.get("conv_groups", 0)
     return c

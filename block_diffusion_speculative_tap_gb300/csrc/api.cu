@@ -88,6 +88,8 @@ struct dflash_handle {
   const __nv_bfloat16* hidden_norm = nullptr;
   const __nv_bfloat16* norm = nullptr;
   const __nv_bfloat16* embed = nullptr;
+  const __nv_bfloat16* conv_norm = nullptr;  // two-tap convolution (conv_groups > 0)
+  const __nv_bfloat16* conv_proj = nullptr;
   std::vector<dflash_layer_weights> layers;
   CUtensorMap fc_map, embed_map;
   std::vector<LayerMaps> maps;
@@ -240,6 +242,13 @@ int dflash_config_validate(const dflash_config* c) {
     if (c->layer_kind[l] != DFLASH_LAYER_FULL && c->layer_kind[l] != DFLASH_LAYER_SLIDING) return DFLASH_E_SHAPE;
     if (c->layer_kind[l] == DFLASH_LAYER_SLIDING && c->sliding_window <= 0) return DFLASH_E_SHAPE;
   }
+  if (c->conv_groups != 0) {
+    // the v1 layout has no conv tensor [TF1851 item 1]
+    if (c->variant == DFLASH_VARIANT_V1) return DFLASH_E_SHAPE;
+    if (c->conv_groups < 0 || c->conv_groups > kMaxConvGroups || c->hidden % c->conv_groups ||
+        (c->hidden / c->conv_groups) % 16)
+      return DFLASH_E_SHAPE;
+  }
   return DFLASH_OK;
 }
 
@@ -269,6 +278,8 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return DFLASH_E_INVALID_ARG;
   if (!w->layers) return DFLASH_E_INVALID_ARG;
+  if (cfg->conv_groups > 0 && (!w->conv_norm || !w->conv_proj || !aligned16(w->conv_norm) || !aligned16(w->conv_proj)))
+    return DFLASH_E_INVALID_ARG;
   for (int l = 0; l < cfg->n_layers; ++l) {
     const dflash_layer_weights& L = w->layers[l];
     const void* lp[] = {L.input_norm, L.q_proj, L.k_proj, L.v_proj, L.o_proj, L.q_norm,
@@ -291,6 +302,10 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
   h->hidden_norm = static_cast<const __nv_bfloat16*>(w->hidden_norm);
   h->norm = static_cast<const __nv_bfloat16*>(w->norm);
   h->embed = static_cast<const __nv_bfloat16*>(w->embed);
+  if (cfg->conv_groups > 0) {
+    h->conv_norm = static_cast<const __nv_bfloat16*>(w->conv_norm);
+    h->conv_proj = static_cast<const __nv_bfloat16*>(w->conv_proj);
+  }
   h->layers.assign(w->layers, w->layers + cfg->n_layers);
   const int64_t H = cfg->hidden, N = cfg->n_taps, d = cfg->head_dim, F = cfg->ffn, V = cfg->vocab;
   const int64_t qd = cfg->n_q_heads * d, kvd = cfg->n_kv_heads * d;
@@ -795,6 +810,7 @@ struct DraftWs {
   __nv_bfloat16* logits;
   float* cand_v;  // LM-head per-tile top-k candidates, [rows][V/128][8]
   int* cand_i;
+  float* conv_z;  // two-tap convolution logits [T][2 * groups]
 };
 
 int max_nchunk(const dflash_state* st) {
@@ -917,6 +933,7 @@ size_t draft_ws_layout(const dflash_handle* h, const dflash_state* st, int S, bo
   const size_t ncand = static_cast<size_t>(S) * (DFLASH_BLOCK - 1) * (c.vocab / kTileM) * 8;
   w.cand_v = cv.take<float>(ncand);
   w.cand_i = cv.take<int>(ncand);
+  w.conv_z = cv.take<float>(static_cast<size_t>(T) * 2 * std::max(c.conv_groups, 1));
   if (out) *out = w;
   return cv.off;
 }
@@ -1049,6 +1066,17 @@ int run_stages(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int
   return DFLASH_OK;
 }
 
+// DFlash2's two-tap dynamic convolution on the residual X (sums of squares
+// in w.ss), leaving the new rows' sums of squares in w.ss for the final norm.
+int run_conv(dflash_handle* h, int s_count, float* X, const DraftWs& w, cudaStream_t s) {
+  const dflash_config& c = h->cfg;
+  const int T = s_count * DFLASH_BLOCK;
+  int rc = launch_rmsnorm_rows(w.hbuf, X, h->conv_norm, w.ss, T, T, c.hidden, c.rms_eps, 0, s);
+  if (!rc) rc = launch_block_conv(X, w.hbuf, w.conv_z, h->conv_proj, s_count, c.hidden, c.conv_groups, s);
+  if (!rc) rc = launch_row_sumsq(w.ss, X, T, c.hidden, s);
+  return rc;
+}
+
 // Final norm on the 15 mask rows of every stream (sums of squares of X in
 // w.ss), shared LM head, top-k.
 int run_head(dflash_handle* h, int* status, int s_count, const float* X, const DraftWs& w, __nv_bfloat16* logits,
@@ -1112,7 +1140,24 @@ int dflash_draft_block(dflash_handle* h, dflash_state* st, int s_begin, int s_co
   int* counters = w.counters;
   rc = run_stages(h, st, s_begin, s_count, 0, 2 * c.n_layers, w.X, w, counters, s);
   if (rc) return rc;
+  if (c.conv_groups > 0) {
+    rc = run_conv(h, s_count, w.X, w, s);
+    if (rc) return rc;
+  }
   return run_head(h, st->status, s_count, w.X, w, logits, topk_ids, topk_vals, k, counters, s);
+}
+
+int dflash_draft_conv(dflash_handle* h, dflash_state* st, int s_count, float* X, void* ws, size_t ws_bytes,
+                      dflash_stream_t stream) {
+  int rc = check_draft_args(h, st, 0, s_count, ws, nullptr, nullptr, 0, nullptr);
+  if (rc) return rc;
+  if (!X || !aligned16(X) || h->cfg.conv_groups <= 0) return DFLASH_E_INVALID_ARG;
+  DraftWs w{};
+  if (draft_ws_layout(h, st, s_count, false, ws, &w) > ws_bytes) return DFLASH_E_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  rc = launch_row_sumsq(w.ss, X, s_count * DFLASH_BLOCK, h->cfg.hidden, s);
+  if (rc) return rc;
+  return run_conv(h, s_count, X, w, s);
 }
 
 int dflash_draft_stages(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int stage0, int stage1,

@@ -146,6 +146,14 @@ struct KvSegs {
 // k_norm + RoPE + cache scatter of raw K/V projections y [rows][ld] fp32.
 int launch_kv_rows(const float* y, int64_t ld, const KvSegs& segs, const int* row_stream, const int* row_pos,
                    const int* row_end, const float2* rope, int d, float eps, int rows, cudaStream_t st);
+// DFlash2's two-tap dynamic convolution on the residual X [16 * S, H] from
+// the normed rows h (bf16, [16 * S, H]): z[t] = h[t] . proj^T (2 * groups
+// logits, fp32), then X[t] += a0 * h[t - 1] + a1 * h[t] with (a0, a1) the
+// softmax of the row's two logits of the channel's group (no row before a
+// stream's first).
+constexpr int kMaxConvGroups = 32;
+int launch_block_conv(float* X, const __nv_bfloat16* h, float* z, const __nv_bfloat16* proj, int S, int H, int groups,
+                      cudaStream_t st);
 int launch_hidden_norm(__nv_bfloat16* ring, __nv_bfloat16* fused_tmp, const float* y, const float* ss,
                        const __nv_bfloat16* g, const int* row_stream, const int* row_pos, int rows, int H, int R,
                        float eps, cudaStream_t st);

@@ -292,6 +292,99 @@ int launch_wait_probe(int* err, long long cycles, cudaStream_t st) {
   return cuda_status(cudaGetLastError());
 }
 
+namespace {
+
+// ---------------------------------------------------------------- two-tap dynamic convolution
+// DFlash2's dynamic short convolution over the block's rows: from the normed
+// rows h = bf16(RMSNorm(X) * conv_norm), the tap logits z[t] = h[t] . proj^T
+// (2 * groups of them a row), then X[t] += a0 * h[t - 1] + a1 * h[t] with
+// (a0, a1) = softmax(z[t][2g], z[t][2g + 1]) for the channel's group g.
+constexpr int kConvThreads = 256;
+
+// A warp a logit: lanes take 8-feature pieces in order, then a fixed xor tree.
+__global__ void __launch_bounds__(kConvThreads) conv_logits_kernel(const __nv_bfloat16* __restrict__ h,
+                                                                   const __nv_bfloat16* __restrict__ proj, int H,
+                                                                   int nz, float* __restrict__ z) {
+  pdl_trigger();
+  pdl_wait();
+  const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint4* hr = reinterpret_cast<const uint4*>(h + static_cast<int64_t>(t) * H);
+  for (int q = warp; q < nz; q += kConvThreads / 32) {
+    const uint4* pr = reinterpret_cast<const uint4*>(proj + static_cast<int64_t>(q) * H);
+    float acc = 0.f;
+    for (int i = lane; i < H / 8; i += 32) {
+      const uint4 a = hr[i], b = __ldg(pr + i);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 fa = __bfloat1622float2(a2[k]), fb = __bfloat1622float2(b2[k]);
+        acc = fmaf(fa.x, fb.x, acc);
+        acc = fmaf(fa.y, fb.y, acc);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) z[static_cast<int64_t>(t) * nz + q] = acc;
+  }
+}
+
+// Elementwise mix: a CTA covers 1024 features of one row, 8 a thread (one
+// group: a group holds a multiple of 16 features); a stream's first row (the
+// anchor's) has no row before it.
+__global__ void __launch_bounds__(128) conv_mix_kernel(float* __restrict__ X, const __nv_bfloat16* __restrict__ h,
+                                                       const float* __restrict__ z, int H, int groups) {
+  pdl_trigger();
+  pdl_wait();
+  const int t = blockIdx.y;
+  const int i = (blockIdx.x * 128 + threadIdx.x) * 8;
+  if (i >= H) return;
+  const int g = i / (H / groups);
+  const float z0 = z[static_cast<int64_t>(t) * 2 * groups + 2 * g];
+  const float z1 = z[static_cast<int64_t>(t) * 2 * groups + 2 * g + 1];
+  const float m = fmaxf(z0, z1);
+  const float e0 = expf(z0 - m), e1 = expf(z1 - m);
+  const float inv = 1.f / (e0 + e1);
+  const float a0 = e0 * inv, a1 = e1 * inv;
+  const uint4 hc = *reinterpret_cast<const uint4*>(h + static_cast<int64_t>(t) * H + i);
+  const uint4 hp = (t & 15) ? *reinterpret_cast<const uint4*>(h + static_cast<int64_t>(t - 1) * H + i)
+                            : make_uint4(0u, 0u, 0u, 0u);
+  const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&hc);
+  const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&hp);
+  float4* xr = reinterpret_cast<float4*>(X + static_cast<int64_t>(t) * H + i);
+  float4 x0 = xr[0], x1 = xr[1];
+  float* xs[8] = {&x0.x, &x0.y, &x0.z, &x0.w, &x1.x, &x1.y, &x1.z, &x1.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 fc = __bfloat1622float2(c2[k]), fp = __bfloat1622float2(p2[k]);
+    *xs[2 * k] += a0 * fp.x + a1 * fc.x;
+    *xs[2 * k + 1] += a0 * fp.y + a1 * fc.y;
+  }
+  xr[0] = x0;
+  xr[1] = x1;
+}
+
+}  // namespace
+
+int launch_block_conv(float* X, const __nv_bfloat16* h, float* z, const __nv_bfloat16* proj, int S, int H, int groups,
+                      cudaStream_t st) {
+  if (S <= 0) return DFLASH_OK;
+  if (groups < 1 || groups > kMaxConvGroups || H % groups || (H / groups) % 16) return DFLASH_E_SHAPE;
+  const int T = S * DFLASH_BLOCK, nz = 2 * groups;
+  {
+    TraceScope ts(st, "conv.taps", static_cast<double>(T) * H * 2 + static_cast<double>(nz) * H * 2 + T * nz * 4.0,
+                  2.0 * T * nz * H);
+    const cudaError_t e = launch_pdl(conv_logits_kernel, dim3(T), dim3(kConvThreads), 0, st, h, proj, H, nz, z);
+    count_launch();
+    if (e != cudaSuccess) return DFLASH_E_CUDA;
+  }
+  TraceScope ts(st, "conv.mix", static_cast<double>(T) * H * 10 + T * nz * 4.0, 0.0);
+  const cudaError_t e =
+      launch_pdl(conv_mix_kernel, dim3((H + 1023) / 1024, T), dim3(128), 0, st, X, h, static_cast<const float*>(z), H, groups);
+  count_launch();
+  return cuda_status(e);
+}
+
 int launch_embed(float* X, float* ss, const __nv_bfloat16* embed, const int* anchors, int S, int H, int V, int mask,
                  int* err, cudaStream_t st) {
   TraceScope ts(st, "embed", static_cast<double>(S) * 16 * H * 6 + static_cast<double>(S) * 16 * (H / 128) * 4, 0.0);

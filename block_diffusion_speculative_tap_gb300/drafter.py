@@ -119,12 +119,19 @@ class Drafter:
             for field, key in keys.items():
                 _need(lw[key], torch.bfloat16, f"layers[{l}].{key}")
                 setattr(self._layers[l], field, lw[key].data_ptr())
+        conv = (None, None)
+        if model.get("conv_groups", 0):
+            for name in ("conv_norm", "conv_proj"):
+                _need(weights[name], torch.bfloat16, name)
+            conv = (weights["conv_norm"].data_ptr(), weights["conv_proj"].data_ptr())
         self._w = A.Weights(
             weights["fc"].data_ptr(),
             weights["hidden_norm"].data_ptr(),
             weights["norm"].data_ptr(),
             weights["embed"].data_ptr(),
             C.cast(self._layers, C.POINTER(A.LayerWeights)),
+            conv[0],
+            conv[1],
         )
         h = C.c_void_p()
         with torch.cuda.device(dev):
@@ -334,6 +341,18 @@ class State:
                 self.drafter.handle, self.st, s_begin, S, g0, g1, _ptr(X), _ptr(ws), ws.numel(), _stream()
             ),
             "dflash_draft_stages",
+        )
+        return X
+
+    def draft_conv(self, X):
+        """DFlash2's two-tap dynamic convolution on the fp32 residual X
+        [S*16, H] in place (a drafter with conv_groups > 0)."""
+        _need(X, torch.float32, "X")
+        S = X.shape[0] // 16
+        ws = self.ws_draft.get(self.draft_workspace_bytes(S, False))
+        check(
+            lib.dflash_draft_conv(self.drafter.handle, self.st, S, _ptr(X), _ptr(ws), ws.numel(), _stream()),
+            "dflash_draft_conv",
         )
         return X
 

@@ -112,6 +112,9 @@ typedef struct dflash_config {
   int32_t layer_kind[DFLASH_MAX_LAYERS]; /* DFLASH_LAYER_FULL or _SLIDING per layer */
   float rope_theta;       /* rotate-half RoPE base */
   float rms_eps;          /* RMSNorm epsilon */
+  int32_t conv_groups;    /* 0, or the weight groups of DFlash2's two-tap dynamic
+                             convolution over the block (variant 2 only; see
+                             dflash_draft_conv) */
 } dflash_config;
 
 /* Check a config. Returns DFLASH_OK or the refusal: E_TAPS_RANGE (n_taps
@@ -120,7 +123,9 @@ typedef struct dflash_config {
  * hidden != n_q_heads * head_dim; head_dim not 32/64/128; hidden, ffn or
  * n_kv_heads*head_dim not a multiple of 128; vocab not a multiple of 128;
  * mask token outside the vocabulary; a sliding layer with window <= 0;
- * variant not 1 or 2), E_INVALID_ARG (NULL). [TF1851 item 1] */
+ * variant not 1 or 2; conv_groups != 0 in a v1 drafter, whose layout has no
+ * conv tensor; conv_groups outside 0..32 or hidden / conv_groups not a
+ * multiple of 16), E_INVALID_ARG (NULL). [TF1851 item 1] */
 int dflash_config_validate(const dflash_config* cfg);
 
 /* "DFlash" for a v1 drafter, "DFlash2" otherwise, NULL for NULL. [TF1851
@@ -164,6 +169,8 @@ typedef struct dflash_weights {
   const void* norm;        /* [H] final norm */
   const void* embed;       /* [V, H] embedding, also the LM head */
   const dflash_layer_weights* layers; /* host array of n_layers entries (copied) */
+  const void* conv_norm;   /* [H] two-tap convolution's RMSNorm gain (conv_groups > 0; else unused) */
+  const void* conv_proj;   /* [2 * conv_groups, H]: row 2g + t = tap t of group g */
 } dflash_weights;
 
 typedef struct dflash_handle dflash_handle;
@@ -293,6 +300,24 @@ int dflash_draft_stages(dflash_handle* h, dflash_state* st, int s_begin, int s_c
                         float* X, void* ws, size_t ws_bytes, dflash_stream_t stream);
 int dflash_draft_head(dflash_handle* h, dflash_state* st, int s_count, const float* X, void* logits_out,
                       int32_t* topk_ids, float* topk_vals, int k, void* ws, size_t ws_bytes, dflash_stream_t stream);
+
+/* ---------------------------------------------------------------- two-tap convolution
+ * DFlash2's dynamic short convolution [EXPL 五 "Dynamic short convolution":
+ * a two-tap dynamic convolution over adjacent positions of the block against
+ * suffix decay; kernel size 2]. Reading: a dynamic convolution (Wu et al.
+ * 2019: per-position kernel weights from the position's own input,
+ * softmax-normalised over the taps, shared within a channel group) of kernel
+ * size 2, causal inside the block, as a residual branch after the last layer:
+ *   h = bf16(RMSNorm(X) * conv_norm); z_i = h_i . conv_proj^T  [groups, 2]
+ *   a_i = softmax over the two taps of z_i (per group)
+ *   X_i += a_i[g, 0] * h_{i-1} + a_i[g, 1] * h_i   (h_{-1} = 0; channel c in
+ *          group c / (H / groups))
+ * dflash_draft_block runs it before the final norm whenever conv_groups > 0.
+ * dflash_draft_conv runs it alone on a caller residual X (device fp32
+ * [16 * s_count, H], in place), for stage-by-stage checks; ws as for
+ * dflash_draft_block. E_INVALID_ARG when the handle has no convolution. */
+int dflash_draft_conv(dflash_handle* h, dflash_state* st, int s_count, float* X, void* ws, size_t ws_bytes,
+                      dflash_stream_t stream);
 
 /* ---------------------------------------------------------------- top-k
  * Per row of a bf16 logit matrix [rows, vocab] (device, rows contiguous):

@@ -233,6 +233,11 @@ def staged_parity(st, ref, rs, m, s, anchor, k):
         part = "attention" if g % 2 == 0 else "mlp"
         rep = assert_close(X.cpu().numpy(), Xs[g + 1], f"layer {g // 2} {part} residual")
         print(f"stage layer {g // 2} {part}: {rep}")
+    if m.get("conv_groups", 0):
+        X = torch.from_numpy(Xs[-2].astype(np.float32)).cuda()
+        st.draft_conv(X)
+        rep = assert_close(X.cpu().numpy(), Xs[-1], "two-tap convolution residual")
+        print(f"stage conv: {rep}")
     X = torch.from_numpy(Xs[-1].astype(np.float32)).cuda()
     logits, ids, vals = st.draft_head(X, k=k)
     rep = assert_close(logits.cpu().float().numpy(), ol, "head logits")
@@ -274,6 +279,11 @@ def staged_parity_all(st, ref, m, anchors, k):
         part = "attention" if g % 2 == 0 else "mlp"
         rep = assert_close(X.cpu().numpy(), np.concatenate([Xs[g + 1] for Xs in Xss]), f"layer {g // 2} {part} residual")
         print(f"stage layer {g // 2} {part} ({S} streams): {rep}")
+    if m.get("conv_groups", 0):
+        X = torch.from_numpy(np.concatenate([Xs[-2] for Xs in Xss]).astype(np.float32)).cuda()
+        st.draft_conv(X)
+        rep = assert_close(X.cpu().numpy(), np.concatenate([Xs[-1] for Xs in Xss]), "two-tap convolution residual")
+        print(f"stage conv ({S} streams): {rep}")
     X = torch.from_numpy(np.concatenate([Xs[-1] for Xs in Xss]).astype(np.float32)).cuda()
     logits, ids, vals = st.draft_head(X, k=k)
     ol = np.concatenate(ols)

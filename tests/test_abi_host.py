@@ -55,6 +55,10 @@ def test_refusals_match_the_oracle(D):
         (dict(m, n_kv_heads=5), -5),
         (dict(m, layer_kinds=[1] * 6, sliding_window=0), -5),
         (dict(m, hidden=4224), -5),  # hidden != q heads x head dim
+        (dict(m, conv_groups=16), -5),  # a v1 drafter has no convolution
+        (dict(m, variant=2, conv_groups=16), 0),
+        (dict(m, variant=2, conv_groups=3), -5),  # 4096 / 3
+        (dict(m, variant=2, conv_groups=64), -5),  # more than 32 groups
     ]
     for cfg, code in cases:
         assert D.config_validate(cfg) == code, cfg

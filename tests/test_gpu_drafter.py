@@ -349,3 +349,65 @@ def test_bounded_wait_expires_and_context_survives(D):
     ref.append(0, [f64(t) for t in taps])
     anchors = SI.anchor_ids(1, m["vocab"], m["mask_token"], 53)
     draft_vs_oracle(D, st, ref, m, anchors, P["topk"])
+
+
+def test_conv_drafter_tiny_end_to_end(D):
+    """A DFlash2-layout tiny drafter with the two-tap dynamic convolution
+    (4 groups of 64 channels): fill, draft against the oracle element by
+    element (two layers: the stated tolerance), then the convolution stage
+    alone on the oracle's residual, and the head."""
+    P = SI.preset("tiny")
+    m = SI.shrink(P["model"], variant=2, conv_groups=4)
+    w = SI.make_weights(m, 811, device="cuda")
+    dr = D.Drafter(m, w)
+    ctx = [96, 17]
+    st = dr.new_state(2, 256)
+    ref = O.OracleStreams(m, O.weights_to_f64(w), 2)
+    taps = SI.make_taps(m, sum(ctx), 812, device="cuda")
+    st.fuse_taps(taps, [(0, 0, ctx[0]), (1, 0, ctx[1])])
+    ref.append(0, [f64(t[: ctx[0]]) for t in taps])
+    ref.append(1, [f64(t[ctx[0] :]) for t in taps])
+    anchors = SI.anchor_ids(2, m["vocab"], m["mask_token"], 813)
+    draft_vs_oracle(D, st, ref, m, anchors, P["topk"])
+    staged_vs_oracle(st, ref, m, anchors, P["topk"])
+
+
+def test_conv_drafter_scaled(D):
+    """A three-layer drafter (sliding and full layers, split-K GEMMs) with
+    the convolution over 16 groups: end to end within the oracle's envelope,
+    stage by stage (the convolution included) within the tolerance."""
+    m = small_model()
+    m.update(variant=2, conv_groups=16)
+    w = SI.make_weights(m, 821, device="cuda")
+    dr = D.Drafter(m, w)
+    ctx = [250, 33]
+    st = dr.new_state(2, 512)
+    ref = OraclePair(m, O.weights_to_f64(w), 2)
+    taps = SI.make_taps(m, sum(ctx), 822, device="cuda")
+    st.fuse_taps(taps, [(0, 0, ctx[0]), (1, 0, ctx[1])])
+    ref.append(0, [f64(t[: ctx[0]]) for t in taps])
+    ref.append(1, [f64(t[ctx[0] :]) for t in taps])
+    anchors = SI.anchor_ids(2, m["vocab"], m["mask_token"], 823)
+    draft_vs_oracle(D, st, ref, m, anchors, 8)
+    staged_vs_oracle(st, ref, m, anchors, 8)
+
+
+def test_conv_stage_dflash2_geometry(D):
+    """The convolution stage at the DFlash2 geometry (hidden 5120, 16
+    groups of 320 channels) for 8 streams, on seeded residual rows, every
+    element against the oracle."""
+    base = SI.preset("dflash2geom")["model"]
+    m = SI.shrink(base, n_layers=1, layer_kinds=[SI.FULL], vocab=1024, variant=2, conv_groups=16)
+    w = SI.make_weights(m, 831, device="cuda")
+    dr = D.Drafter(m, w)
+    S = 8
+    st = dr.new_state(S, 64)
+    X = torch.randn(S * 16, m["hidden"], generator=torch.Generator().manual_seed(832)).mul_(3.0)
+    w64 = O.weights_to_f64(w)
+    want = np.concatenate([O.block_conv(m, w64, O.to_f64(X[16 * s : 16 * s + 16])) for s in range(S)])
+    Xg = X.cuda()
+    st.draft_conv(Xg)
+    rep = assert_close(Xg.cpu().numpy(), want, "two-tap convolution at the DFlash2 geometry")
+    print(f"conv stage, 8 x 16 rows x 5120: {rep}")
+    rc, bits = st.status()
+    assert rc == 0 and bits == 0
