@@ -333,6 +333,94 @@ def measure_config(name, dev, pk, steps, dr=None):
     return out
 
 
+# ---------------------------------------------------------------- the rows after the draft
+def measure_next_rows(dev, pk, steps):
+    """The DFlash2 candidate-path selector (32 streams x 15 positions x top-16
+    over a 151936-token vocabulary, rank-256 codebooks), tree verification
+    (32 streams, 93-node trees of widths 4, 2, 2, 1, 1, 1, 1: the arg-max scan
+    of every node's target row and the walk) and the two-tap convolution
+    stage (8 streams of the DFlash2 geometry, hidden 5120, 16 groups): each
+    timed with CUDA events over `steps` back-to-back calls, with its
+    algorithmic bytes (each input and output touched once) against the HBM
+    peak."""
+    import torch
+
+    import block_diffusion_speculative_tap_gb300 as D
+    import synthetic_inputs as SI
+
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    out = {}
+    S, P, k, V, r = 32, 15, 16, 151936, 256
+    logits = SI.make_logits((S * P, V), 2.0, 4242, device=dev)
+    ids, vals, _ = D.topk(logits, k)
+    del logits
+    U, W = SI.make_codebooks(V, r, 4243, device=dev)
+    pid = torch.empty(S, P, dtype=torch.int32, device=dev)
+    prk = torch.empty(S, P, dtype=torch.int32, device=dev)
+    psc = torch.empty(S, dtype=torch.float32, device=dev)
+    ws = torch.empty(S * (P - 1) * k * k * 4, dtype=torch.uint8, device=dev)
+    ms = timed(lambda: D.select_path(ids, vals, U, W, positions=P, path_ids=pid, path_ranks=prk, path_score=psc, ws=ws))
+    b = S * (P - 1) * 2 * k * r * 2 + S * P * k * 8 + 2 * S * (P - 1) * k * k * 4 + S * P * 8 + S * 4
+    out["selector"] = {
+        "workload": "32 streams x 15 positions x top-16, vocabulary 151936, rank-256 codebooks",
+        "ms": ms, "streams_per_s": S * 1e3 / ms, "algorithmic_bytes": b,
+        "achieved_gbs": b / (ms * 1e-3) / 1e9, "frac_of_hbm_peak": b / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+        "bound": "latency (14 pair tables and a 15-step recursion a stream)",
+    }
+    del U, W, ws
+    widths = [4, 2, 2, 1, 1, 1, 1]
+    topk_ids, _, _ = D.topk(SI.make_logits((S * 15, V), 2.0, 800, device=dev), 8)
+    anchors = SI.anchor_ids(S, V, V - 1, 801, device=dev)
+    N = D.tree_size(widths, 8)
+    tokens, parents, depths, mask = D.tree_build(anchors, topk_ids, widths)
+    tl = SI.make_logits((S, N, V), 2.0, 802, device=dev)
+    acc = torch.empty(S, dtype=torch.int32, device=dev)
+    toks = torch.empty(S, 16, dtype=torch.int32, device=dev)
+    node = torch.empty(S, dtype=torch.int32, device=dev)
+    tws = torch.empty(S * N * 8, dtype=torch.uint8, device=dev)
+    ms_b = timed(lambda: D.tree_build(anchors, topk_ids, widths))
+    ms_v = timed(lambda: D.tree_verify(tokens, tl, widths, accept=acc, tokens=toks, node=node, ws=tws))
+    bv = S * N * V * 2 + S * N * 4 + S * 17 * 4
+    out["tree"] = {
+        "workload": f"32 streams, {N}-node trees (widths {widths}), vocabulary 151936",
+        "build_ms": ms_b, "verify_ms": ms_v, "verify_rows_per_s": S * N * 1e3 / ms_v,
+        "verify_algorithmic_bytes": bv, "verify_achieved_gbs": bv / (ms_v * 1e-3) / 1e9,
+        "verify_frac_of_hbm_peak": bv / (ms_v * 1e-3) / 1e9 / pk["hbm_gbs"], "bound": "hbm (target rows scanned once)",
+    }
+    del tl, tws
+    base = SI.preset("dflash2geom")["model"]
+    m = SI.shrink(base, n_layers=1, layer_kinds=[SI.FULL], vocab=1024, variant=2, conv_groups=16)
+    dr = D.Drafter(m, SI.make_weights(m, 831, device=dev))
+    Sc = 8
+    st = dr.new_state(Sc, 64)
+    X = torch.randn(Sc * 16, m["hidden"], device=dev)
+    ms_c = timed(lambda: st.draft_conv(X))
+    T, H, G = Sc * 16, m["hidden"], 16
+    bc = T * H * (4 + 4) + 2 * G * H * 2 + H * 2  # the residual read and written once, the weights once
+    out["conv"] = {
+        "workload": "8 streams x 16 rows, hidden 5120, 16 groups (the whole stage: norm, tap logits, mix, "
+        "sums of squares for the final norm)",
+        "ms": ms_c, "algorithmic_bytes": bc, "achieved_gbs": bc / (ms_c * 1e-3) / 1e9,
+        "frac_of_hbm_peak": bc / (ms_c * 1e-3) / 1e9 / pk["hbm_gbs"], "bound": "latency (5 MB a call)",
+    }
+    del st, dr
+    torch.cuda.empty_cache()
+    return out
+
+
 # ---------------------------------------------------------------- our arm
 def max_over_ranks(value, world, device):
     """The largest of every rank's value (the slowest replica's time), as
@@ -651,6 +739,7 @@ def run_ours(args, rank, world):
         del st
         torch.cuda.empty_cache()
         others["dflash2geom"] = measure_config("dflash2geom", dev, pk, 20)
+        others["next_rows"] = measure_next_rows(dev, pk, 20)
         out["other_configs"] = {
             "note": "supplementary: the parity workloads measured at their own streams and contexts "
             "(draft = block forward + LM head + top-k; verify = the workload's mode); not the headline",
