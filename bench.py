@@ -1116,7 +1116,10 @@ def profile_workload(name):
     two-layer 9B-shaped drafter (both layers sliding) three times, so the
     many-stream attention launch is captured at a few GB of device memory;
     'fill4096' runs a 4096-row prompt fill of the 9B-shaped drafter three
-    times (fc GEMM, hidden_norm, K/V injection)."""
+    times (fc GEMM, hidden_norm, K/V injection); 'attention8d2' drafts 8
+    streams x 8192 context rows through a one-layer drafter of the DFlash2
+    geometry (40 q / 8 kv heads of 128) three times, so the tensor-memory
+    attention launch is captured."""
     import torch
 
     import block_diffusion_speculative_tap_gb300 as D
@@ -1137,10 +1140,14 @@ def profile_workload(name):
         if rc != 0:
             raise RuntimeError(f"device status {rc} bits {bits}")
         return
-    if name != "attention32":
+    if name == "attention8d2":
+        m = SI.shrink(SI.preset("dflash2geom")["model"], n_layers=1, layer_kinds=[SI.FULL], vocab=8192)
+        S, C = 8, 8192
+    elif name == "attention32":
+        m = SI.shrink(SI.preset("9b")["model"], n_layers=2, layer_kinds=[SI.SLIDING] * 2)
+        S, C = 32, 2048
+    else:
         raise SystemExit(f"unknown profile workload {name}")
-    m = SI.shrink(SI.preset("9b")["model"], n_layers=2, layer_kinds=[SI.SLIDING] * 2)
-    S, C = 32, 2048
     dr = D.Drafter(m, SI.make_weights(m, 5, device="cuda"))
     st = dr.new_state(S, C + 1024)
     for s in range(S):
@@ -1167,7 +1174,7 @@ def main():
     ap.add_argument("--workload", default="9b", choices=["9b"] + sorted(SHARDED),
                     help="9b: the batch-1 decode round (default); serve32 / dflash2geom: a multi-stream round, "
                     "streams split over ranks")
-    ap.add_argument("--profile-workload", default=None, help="run a small workload for ncu (attention32, fill4096) and exit")
+    ap.add_argument("--profile-workload", default=None, help="run a small workload for ncu (attention32, attention8d2, fill4096) and exit")
     args = ap.parse_args()
     if args.profile_workload:
         profile_workload(args.profile_workload)

@@ -131,6 +131,7 @@ int head_threads_ok(int d) { return d == 32 || d == 64 || d == 128; }
 //    (global partials, persistent CTAs, at least 8 reduction blocks a chunk);
 //  * above, no split.
 constexpr int kInvariantN = 64;
+constexpr int kInvariantStreams = kInvariantN / DFLASH_BLOCK;  // four streams of a draft call
 
 void set_split(const dflash_handle* h, GemmPlan& p, int invariant_n = kInvariantN) {
   p.no_cluster = false;
@@ -1052,8 +1053,18 @@ int run_stages(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int
       a.trace_bytes = keys * kvd * 2.0 * 2.0 + 2.0 * T * qd * 2.0;
     }
     a.err = st->status;
-    rc = attention_cluster_supported(a) ? launch_attention_cluster(a, st->kmap[l], st->vmap[l], s_count, s)
-                                        : launch_attention(a, s_count, s);
+    // more than four streams whose (stream, kv head) pairs fit one wave of
+    // SMs: the tensor-memory kernel, one 128-row MMA per kv head's query
+    // group (the DFlash2 geometry, 8 streams x 8 kv heads: 0.74 -> 0.39 ms a
+    // round). Up to four streams the batch-invariant 8-way split of the
+    // cluster kernel stays; with more pairs than SMs the cluster kernel's
+    // finer key split balances uneven contexts better (32 streams of the 9B
+    // shape: 0.77 ms against 0.79-0.85 ms a round).
+    if (s_count > kInvariantStreams && s_count * a.nkv <= h->num_sms && attention_tc_supported(a))
+      rc = launch_attention_tc(a, st->kmap[l], st->vmap[l], s_count, h->num_sms, s);
+    else
+      rc = attention_cluster_supported(a) ? launch_attention_cluster(a, st->kmap[l], st->vmap[l], s_count, s)
+                                          : launch_attention(a, s_count, s);
     if (rc) return rc;
     // O projection added to the residual
     o.b_ptr[0] = w.attn;

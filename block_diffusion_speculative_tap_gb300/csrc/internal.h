@@ -186,6 +186,13 @@ int attention_cluster_maps(CUtensorMap* kmap, CUtensorMap* vmap, const void* kc,
 int launch_attention_cluster(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap, int s_count,
                              cudaStream_t st);
 size_t attn_partial_floats(int s_count, int nq, int nchunk, int d);
+// Tensor-memory variant for head dimension 128 and more than four streams a
+// call (attention_tc.cu): one CTA per (stream, kv head, key slice) takes the
+// kv head's whole query group as one 128-row MMA (tcgen05, S and P*V in
+// tensor memory), slices reduced through distributed shared memory.
+bool attention_tc_supported(const AttnArgs& a);
+int launch_attention_tc(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap, int s_count,
+                        int num_sms, cudaStream_t st);
 
 // ---------------------------------------------------------------- selection (select.cu)
 // Row-wise top-k (k <= 8) from per-tile candidate lists written by a GEMM

@@ -411,3 +411,41 @@ def test_conv_stage_dflash2_geometry(D):
     print(f"conv stage, 8 x 16 rows x 5120: {rep}")
     rc, bits = st.status()
     assert rc == 0 and bits == 0
+
+
+@pytest.mark.parametrize("nq,nkv", [(8, 8), (8, 4), (8, 2), (10, 2), (8, 1)])
+def test_many_stream_attention_group_sizes(D, nq, nkv):
+    """More than four streams a draft call: the tensor-memory attention (one
+    128-row MMA per kv head's query group), for every group size 1, 2, 4,
+    5 and 8, on six streams whose contexts are empty, one row, a ragged
+    tile, exactly one tile, and long enough to wrap the tile ring, over a
+    sliding and a full layer: each stage within the tolerance on the
+    oracle's input, end to end within the oracle's envelope."""
+    m = small_model()
+    m.update(hidden=nq * 128, n_q_heads=nq, n_kv_heads=nkv, n_layers=2, layer_kinds=[1, 0], ffn=1536,
+             sliding_window=256)
+    w = SI.make_weights(m, 900 + nq * 10 + nkv, device="cuda")
+    dr = D.Drafter(m, w)
+    ctx = [0, 1, 63, 64, 300, 700]
+    S = len(ctx)
+    st = dr.new_state(S, 1024)
+    ref = OraclePair(m, O.weights_to_f64(w), S)
+    taps = SI.make_taps(m, sum(ctx), 901, device="cuda")
+    segs, r0 = [], 0
+    for s, c in enumerate(ctx):
+        if c:
+            segs.append((s, 0, c))
+            ref.append(s, [f64(t[r0 : r0 + c]) for t in taps])
+        r0 += c
+    st.fuse_taps(taps, segs)
+    anchors = SI.anchor_ids(S, m["vocab"], m["mask_token"], 902)
+    logits, ids, vals = st.draft(anchors.cuda(), k=8)
+    rc, bits = st.status()
+    assert rc == 0 and bits == 0, (rc, bits)
+    check_topk_consistent(logits, ids, vals)
+    lg = logits.cpu().float().numpy().reshape(S, 15, -1)
+    idn = ids.cpu().numpy().reshape(S, 15, 8)
+    for s in range(S):
+        ol, _ = ref.draft(s, int(anchors[s]))
+        compare_draft(lg[s], idn[s], ol, ref.draft32(s, int(anchors[s])), 8, require_checked=False)
+    staged_parity_all(st, ref, m, anchors, 8)
