@@ -1119,7 +1119,9 @@ def profile_workload(name):
     times (fc GEMM, hidden_norm, K/V injection); 'attention8d2' drafts 8
     streams x 8192 context rows through a one-layer drafter of the DFlash2
     geometry (40 q / 8 kv heads of 128) three times, so the tensor-memory
-    attention launch is captured."""
+    attention launch is captured; 'treeverify' verifies 32 streams of
+    93-node draft trees over a 151936-token vocabulary three times (the
+    arg-max scan of 2976 target rows, 904 MB)."""
     import torch
 
     import block_diffusion_speculative_tap_gb300 as D
@@ -1139,6 +1141,16 @@ def profile_workload(name):
         rc, bits = st.status()
         if rc != 0:
             raise RuntimeError(f"device status {rc} bits {bits}")
+        return
+    if name == "treeverify":
+        S, V, widths = 32, 151936, [4, 2, 2, 1, 1, 1, 1]
+        topk_ids, _, _ = D.topk(SI.make_logits((S * 15, V), 2.0, 800, device="cuda"), 8)
+        anchors = SI.anchor_ids(S, V, V - 1, 801, device="cuda")
+        tokens, _, _, _ = D.tree_build(anchors, topk_ids, widths, want_mask=False)
+        tl = SI.make_logits((S, D.tree_size(widths, 8), V), 2.0, 802, device="cuda")
+        for _ in range(3):
+            D.tree_verify(tokens, tl, widths)
+        torch.cuda.synchronize()
         return
     if name == "attention8d2":
         m = SI.shrink(SI.preset("dflash2geom")["model"], n_layers=1, layer_kinds=[SI.FULL], vocab=8192)
@@ -1174,7 +1186,7 @@ def main():
     ap.add_argument("--workload", default="9b", choices=["9b"] + sorted(SHARDED),
                     help="9b: the batch-1 decode round (default); serve32 / dflash2geom: a multi-stream round, "
                     "streams split over ranks")
-    ap.add_argument("--profile-workload", default=None, help="run a small workload for ncu (attention32, attention8d2, fill4096) and exit")
+    ap.add_argument("--profile-workload", default=None, help="run a small workload for ncu (attention32, attention8d2, fill4096, treeverify) and exit")
     args = ap.parse_args()
     if args.profile_workload:
         profile_workload(args.profile_workload)

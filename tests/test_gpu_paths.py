@@ -309,3 +309,60 @@ def test_tree_refusals(D):
     assert A.lib.dflash_tree_size(4, big, 16, C.byref(n)) == -1  # more than 1024 nodes
     assert A.lib.dflash_tree_size(0, w, 8, C.byref(n)) == -1
     assert A.lib.dflash_tree_size(16, (C.c_int32 * 16)(*([1] * 16)), 8, C.byref(n)) == -1
+
+
+def test_dflash2_style_round(D):
+    """The rows chained as a DFlash2-style round on six streams of a
+    three-layer drafter with the two-tap convolution: fill, a top-16 draft
+    (end to end within the oracle's envelope), the selector's path through
+    the GPU's own candidates, greedy verification of that path against
+    planted target logits, and a tree from the same draft verified against
+    its own target rows; every integer output against the oracle on the
+    same inputs."""
+    from parity_util import OraclePair, compare_draft
+
+    m = SI.shrink(SI.presets()["tiny"]["model"], variant=2, conv_groups=4, n_layers=3, layer_kinds=[1, 1, 0],
+                  sliding_window=64)
+    w = SI.make_weights(m, 951, device="cuda")
+    dr = D.Drafter(m, w)
+    ctx = [40, 100, 7, 200, 64, 1]
+    S, V, k = len(ctx), m["vocab"], 16
+    st = dr.new_state(S, 512)
+    ref = OraclePair(m, O.weights_to_f64(w), S)
+    taps = SI.make_taps(m, sum(ctx), 952, device="cuda")
+    segs, r0 = [], 0
+    for s, c in enumerate(ctx):
+        segs.append((s, 0, c))
+        ref.append(s, [O.to_f64(t[r0 : r0 + c]) for t in taps])
+        r0 += c
+    st.fuse_taps(taps, segs)
+    anchors = SI.anchor_ids(S, V, m["mask_token"], 953, device="cuda")
+    logits, ids, vals = st.draft(anchors, k=k)
+    rc, bits = st.status()
+    assert rc == 0 and bits == 0
+    lg = logits.cpu().float().numpy().reshape(S, 15, V)
+    idn = ids.cpu().numpy().reshape(S, 15, k)
+    for s in range(S):
+        ol, _ = ref.draft(s, int(anchors[s]))
+        compare_draft(lg[s], idn[s], ol, ref.draft32(s, int(anchors[s])), k, require_checked=False)
+    # the selector on the draft's own top-16
+    U, W = SI.make_codebooks(V, 64, 954)
+    exact, exempt = check_paths(D, idn, vals.cpu().numpy().reshape(S, 15, k), U, W, 15)
+    assert exact >= S - 1
+    pid, _, _ = D.select_path(ids.view(S, 15, k).contiguous(), vals.view(S, 15, k).contiguous(), U.cuda(), W.cuda())
+    # greedy verification of the chosen path
+    tl = SI.make_logits((S, 16, V), 1.0, 955)
+    SI.plant_accepts(tl, pid.cpu(), SI.make_accept_lengths(S, 956))
+    a, toks = D.verify_greedy(pid.contiguous(), tl.cuda())
+    for s in range(S):
+        oa, ot = O.greedy_verify(pid[s].cpu().tolist(), O.to_f64(tl[s]))
+        assert int(a[s]) == oa and toks[s].cpu().tolist() == ot
+    # a tree from the same draft
+    widths = [4, 2, 1, 1]
+    N = D.tree_size(widths, k)
+    tt = SI.make_logits((S, N, V), 1.0, 957)
+    rng = np.random.default_rng(958)
+    for s in range(S):
+        t, p, _ = O.tree_nodes(int(anchors[s]), idn[s], widths)
+        _plant_tree_path(tt[s], t, p, rng)
+    check_trees(D, anchors, ids, widths, tt.cuda())
