@@ -43,6 +43,25 @@ __device__ __forceinline__ void load8(const __nv_bfloat16* row, int g, float (&x
   }
 }
 
+// The 8 bf16 values of a 16-byte piece as floats.
+__device__ __forceinline__ void unpack8(const uint4& raw, float (&x)[8]) {
+  const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(p[i]);
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
+}
+
+// The largest of the 8 bf16 values of a 16-byte piece, as a float: packed
+// bf16 maxima (exact, no rounding), then one conversion a half.
+__device__ __forceinline__ float max8(const uint4& raw) {
+  const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&raw);
+  const __nv_bfloat162 m = __hmax2(__hmax2(p[0], p[1]), __hmax2(p[2], p[3]));
+  return fmaxf(__low2float(m), __high2float(m));
+}
+
 // (va, ia) ranks before (vb, ib): larger value, then lower id
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
@@ -174,20 +193,21 @@ __device__ float range_topk(const __nv_bfloat16* row, int g_begin, int g_end, in
   float lv = -INFINITY;  // KM == 1: the lane's own running best
   int li = INT_MAX;
   // four 16-byte loads in flight before any is ranked; the trip count is
-  // the warp's (every lane reaches the ballots)
+  // the warp's (every lane reaches the ballots). A piece's largest value
+  // is taken on the packed bf16 values; a piece is converted to floats only
+  // when it can change the result.
   for (int base = wg0; base < wg1; base += 4 * 32) {
     const int g0 = base + lane;
-    float x[4][8];
+    uint4 raw[4];
+    float gm[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int g = g0 + u * 32;
-      if (g < wg1) {
-        load8(row, g, x[u]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[u][e] = -INFINITY;
-      }
+      raw[u] = g < wg1 ? *reinterpret_cast<const uint4*>(row + static_cast<int64_t>(g) * 8)
+                       : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);  // bf16 -inf
     }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) gm[u] = max8(raw[u]);
     if constexpr (KM == 1) {
       // arg-max, one warp reduction at the end: a lane's groups arrive in
       // ascending id order, so a group replaces the lane's best only with a
@@ -195,15 +215,14 @@ __device__ float range_topk(const __nv_bfloat16* row, int g_begin, int g_end, in
       // empty lane (li == INT_MAX) also takes a group that only ties
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        float gm = x[u][0];
-#pragma unroll
-        for (int e = 1; e < 8; ++e) gm = fmaxf(gm, x[u][e]);
-        if (g0 + u * 32 < wg1 && (gm > lv || (gm == lv && li == INT_MAX))) {
+        if (g0 + u * 32 < wg1 && (gm[u] > lv || (gm[u] == lv && li == INT_MAX))) {
+          float x[8];
+          unpack8(raw[u], x);
           int first = 7;
 #pragma unroll
           for (int e = 6; e >= 0; --e)
-            if (x[u][e] == gm) first = e;
-          lv = gm;
+            if (x[e] == gm[u]) first = e;
+          lv = gm[u];
           li = (g0 + u * 32) * 8 + first;
         }
       }
@@ -212,18 +231,17 @@ __device__ float range_topk(const __nv_bfloat16* row, int g_begin, int g_end, in
       for (int u = 0; u < 4; ++u) {
         // a group of 8 whose largest value is below the floor holds no
         // candidate (ties at the floor go on to the exact test)
-        float gm = x[u][0];
-#pragma unroll
-        for (int e = 1; e < 8; ++e) gm = fmaxf(gm, x[u][e]);
-        if (__ballot_sync(0xffffffffu, g0 + u * 32 < wg1 && !(gm < fv)) == 0u) continue;
+        if (__ballot_sync(0xffffffffu, g0 + u * 32 < wg1 && !(gm[u] < fv)) == 0u) continue;
+        float x[8];
+        unpack8(raw[u], x);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int id = (g0 + u * 32) * 8 + e;
-          unsigned cand = __ballot_sync(0xffffffffu, g0 + u * 32 < wg1 && better(x[u][e], id, fv, fi));
+          unsigned cand = __ballot_sync(0xffffffffu, g0 + u * 32 < wg1 && better(x[e], id, fv, fi));
           while (cand) {
             const int src = __ffs(cand) - 1;
             cand &= cand - 1;
-            const float cv = __shfl_sync(0xffffffffu, x[u][e], src);
+            const float cv = __shfl_sync(0xffffffffu, x[e], src);
             const int ci = __shfl_sync(0xffffffffu, id, src);
             if (better(cv, ci, fv, fi)) {  // the floor may have risen since the ballot
               wt.insert(cv, ci, lane);
@@ -878,8 +896,11 @@ int launch_topk(const __nv_bfloat16* logits, int rows, int V, int k, float T, co
   TraceScope ts(st, "topk", static_cast<double>(rows) * V * 2, 0.0);
   cudaError_t e;
   if (uniforms == nullptr && k >= 1) {
-    e = k <= 8 ? launch_topk_scan<8>(logits, rows, V, k, ids, vals, st)
-               : launch_topk_scan<kKMax>(logits, rows, V, k, ids, vals, st);
+    // k = 1 takes the lanes' own running arg-max (one compare-select a
+    // value, one warp reduction at the end) instead of the warp lists
+    e = k == 1   ? launch_topk_scan<1>(logits, rows, V, k, ids, vals, st)
+        : k <= 8 ? launch_topk_scan<8>(logits, rows, V, k, ids, vals, st)
+                 : launch_topk_scan<kKMax>(logits, rows, V, k, ids, vals, st);
   } else if (k <= 8) {
     e = launch_pdl(topk_kernel<8>, dim3(rows), dim3(kSelThreads), 0, st, logits, V, k, 1.0f / T, uniforms, ids, vals,
                    sampled);
