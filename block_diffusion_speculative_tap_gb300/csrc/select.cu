@@ -473,6 +473,14 @@ cudaError_t launch_topk_cluster(const __nv_bfloat16* logits, int rows, int V, in
   return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<KM>, logits, V, k, ids, vals);
 }
 
+// 2^x by the SFU's approximate base-2 exponential (relative error a few
+// units of fp32's last place; -inf gives +0).
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Weight of id j for inverse-CDF draws; `mode` 0: exp((x - mx) / T) of one
 // row; mode 1: max(p - q, 0) of two rows with their (max, sum).
 struct Weights {
@@ -480,19 +488,26 @@ struct Weights {
   const __nv_bfloat16* b;
   float ma, sa, mb, sb, invT;
   int mode;
+  // exp((x - m) / T) as 2^(x k - m k) with k = log2(e) / T: one fused
+  // multiply-add and the SFU's base-2 exponential a value; the row sums
+  // divide through reciprocals
   __device__ __forceinline__ void eval8(int g, float (&w)[8]) const {
+    const float k = invT * 1.4426950408889634f;
     float x[8];
     load8(a, g, x);
     if (mode == 0) {
+      const float c = -ma * k;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) w[e] = expf((x[e] - ma) * invT);
+      for (int e = 0; e < 8; ++e) w[e] = ex2f(fmaf(x[e], k, c));
     } else {
       float y[8];
       load8(b, g, y);
+      const float ca = -ma * k, cb = -mb * k;
+      const float ra = 1.f / sa, rb = 1.f / sb;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float p = expf((x[e] - ma) * invT) / sa;
-        const float q = expf((y[e] - mb) * invT) / sb;
+        const float p = ex2f(fmaf(x[e], k, ca)) * ra;
+        const float q = ex2f(fmaf(y[e], k, cb)) * rb;
         w[e] = fmaxf(p - q, 0.f);
       }
     }
@@ -508,12 +523,20 @@ __device__ __forceinline__ float warp_incl_scan(float v, int lane) {
   return v;
 }
 
-// Sum of the weights in the fixed scan order; every thread gets the total.
-__device__ float weights_total(const Weights& W, int V, float* sw) {
+// Warp w's contiguous piece of the 8-element groups [gb, ge).
+__device__ __forceinline__ Slice range_slice(int gb, int ge, int w) {
+  const int ng = ge - gb;
+  return {gb + static_cast<int>(static_cast<long long>(ng) * w / kSelWarps),
+          gb + static_cast<int>(static_cast<long long>(ng) * (w + 1) / kSelWarps)};
+}
+
+// Sum of the weights of the groups [gb, ge) in the fixed scan order (each
+// warp its piece, lanes interleaved); every thread gets the total.
+__device__ float weights_total(const Weights& W, int gb, int ge, float* sw) {
   __syncthreads();  // sw may still be read by a previous total / draw
   const int w = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const Slice sl = warp_slice(V, w);
+  const Slice sl = range_slice(gb, ge, w);
   float run = 0.f;
   for (int g0 = sl.g0; g0 < sl.g1; g0 += 32) {
     const int g = g0 + lane;
@@ -533,6 +556,7 @@ __device__ float weights_total(const Weights& W, int V, float* sw) {
   for (int j = 0; j < kSelWarps; ++j) tot += sw[j];
   return tot;  // sw[] stays valid for weights_draw
 }
+__device__ float weights_total(const Weights& W, int V, float* sw) { return weights_total(W, 0, V >> 3, sw); }
 
 // Smallest id whose running sum exceeds thr, summed in the order of
 // weights_total (which must have filled sw). Lane ranges inside a step are
@@ -540,7 +564,7 @@ __device__ float weights_total(const Weights& W, int V, float* sw) {
 // every lane, so they tile the step exactly. Rounding can still leave thr at
 // or past the end of a slice or a lane; the draw then falls back to the last
 // id with positive weight there.
-__device__ int weights_draw(const Weights& W, int V, float thr, const float* sw, int* sres) {
+__device__ int weights_draw(const Weights& W, int gb, int ge, float thr, const float* sw, int* sres) {
   const int w = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) sres[0] = -1;
@@ -563,7 +587,7 @@ __device__ int weights_draw(const Weights& W, int V, float thr, const float* sw,
   }
   __syncthreads();
   if (w == ws) {
-    const Slice sl = warp_slice(V, w);
+    const Slice sl = range_slice(gb, ge, w);
     float run = 0.f;
     int last_pos = -1;
     bool done = false;
@@ -615,6 +639,9 @@ __device__ int weights_draw(const Weights& W, int V, float thr, const float* sw,
   const int r = sres[0];
   __syncthreads();
   return r;
+}
+__device__ int weights_draw(const Weights& W, int V, float thr, const float* sw, int* sres) {
+  return weights_draw(W, 0, V >> 3, thr, sw, sres);
 }
 
 // One CTA a row: the top-k (k <= KM) of the row and, with uniforms, one
@@ -672,30 +699,81 @@ __global__ void greedy_prefix_kernel(int S, int V, const int* __restrict__ draft
   accept[s] = a;
 }
 
-// sampling, step 1: (max, sum of exp((x - max) / T)) of the 16 target rows
-// (r < 16) and the 15 draft rows (r >= 16) of every stream.
+// sampling, step 1: (max, sum of exp((x - max) / T)) of every target row
+// (r < 16) and draft row (r >= 16) of a stream in one pass: every thread
+// keeps a running (max, sum) over its 8-element groups (rescaled when the
+// max moves), merged over the warp by a xor tree and over the warps in
+// order.
+__device__ __forceinline__ void ms_merge2(float& m, float& sum, float m2, float s2, float k) {
+  const float mm = fmaxf(m, m2);
+  const float a = m == -INFINITY ? 0.f : sum * ex2f((m - mm) * k);
+  const float b = m2 == -INFINITY ? 0.f : s2 * ex2f((m2 - mm) * k);
+  m = mm;
+  sum = a + b;
+}
+
 __global__ void __launch_bounds__(kSelThreads) softmax_stats_kernel(const __nv_bfloat16* __restrict__ tl,
                                                                     const __nv_bfloat16* __restrict__ dl, int V,
                                                                     float invT, float* __restrict__ stats) {
   pdl_trigger();
   pdl_wait();
-  __shared__ float sw[kSelWarps];
-  __shared__ int sid[1];
-  __shared__ float sval[1];
+  __shared__ float wm[kSelWarps], wsum[kSelWarps];
   const int r = blockIdx.x;
   const int s = blockIdx.y;
   const __nv_bfloat16* row =
       r < 16 ? tl + (static_cast<int64_t>(s) * 16 + r) * V : dl + (static_cast<int64_t>(s) * 15 + (r - 16)) * V;
-  const float mx = row_topk<1>(row, V, 1, sid, sval);
-  Weights W{row, nullptr, mx, 1.f, 0.f, 1.f, invT, 0};
-  const float tot = weights_total(W, V, sw);
+  const float k = invT * 1.4426950408889634f;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Slice sl = warp_slice(V, w);
+  float m = -INFINITY, sum = 0.f;
+  for (int g0 = sl.g0 + lane; g0 < sl.g1; g0 += 4 * 32) {
+    uint4 raw[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int g = g0 + u * 32;
+      raw[u] = g < sl.g1 ? *reinterpret_cast<const uint4*>(row + static_cast<int64_t>(g) * 8)
+                         : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);  // bf16 -inf
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float gm = max8(raw[u]);
+      if (gm == -INFINITY) continue;
+      const float nm = fmaxf(m, gm);
+      if (nm > m) {
+        sum = m == -INFINITY ? 0.f : sum * ex2f((m - nm) * k);
+        m = nm;
+      }
+      float x[8];
+      unpack8(raw[u], x);
+      const float c = -m * k;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sum += ex2f(fmaf(x[e], k, c));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+    const float s2 = __shfl_xor_sync(0xffffffffu, sum, off);
+    ms_merge2(m, sum, m2, s2, k);
+  }
+  if (lane == 0) {
+    wm[w] = m;
+    wsum[w] = sum;
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
-    stats[(s * 31 + r) * 2] = mx;
-    stats[(s * 31 + r) * 2 + 1] = tot;
+    float M = wm[0], Sm = wsum[0];
+    for (int j = 1; j < kSelWarps; ++j) ms_merge2(M, Sm, wm[j], wsum[j], k);
+    stats[(s * 31 + r) * 2] = M;
+    stats[(s * 31 + r) * 2 + 1] = Sm;
   }
 }
 
-// sampling, step 2: the accept chain, then the residual or bonus draw.
+// sampling, step 2: the accept chain (every CTA of the stream's cluster
+// takes it), then the residual or bonus draw with the row split over the
+// kSlices CTAs: each sums the weights of its slice, the slice sums meet
+// through distributed shared memory (added in rank order), and the CTA
+// whose slice holds the threshold draws within it.
 __global__ void __launch_bounds__(kSelThreads) sample_verify_kernel(int V, const int* __restrict__ draft, int dld,
                                                                     const __nv_bfloat16* __restrict__ tl,
                                                                     const __nv_bfloat16* __restrict__ dl,
@@ -706,7 +784,9 @@ __global__ void __launch_bounds__(kSelThreads) sample_verify_kernel(int V, const
   pdl_wait();
   __shared__ float sw[kSelWarps];
   __shared__ int sres[1];
-  const int s = blockIdx.x;
+  __shared__ float slice_tot[2];  // read by the other CTAs of the cluster
+  const uint32_t rank = cluster_rank();
+  const int s = blockIdx.y;
   const float* st = stats + s * 31 * 2;
   int a = 15;
   for (int i = 0; i < 15; ++i) {
@@ -725,34 +805,61 @@ __global__ void __launch_bounds__(kSelThreads) sample_verify_kernel(int V, const
       break;
     }
   }
-  int tok;
+  const int ng = V >> 3;
+  const int gb = static_cast<int>(static_cast<long long>(ng) * rank / kSlices);
+  const int ge = static_cast<int>(static_cast<long long>(ng) * (rank + 1) / kSlices);
   const __nv_bfloat16* trow = tl + (static_cast<int64_t>(s) * 16 + a) * V;
   const float ud = u[(s * 16 + a) * 2 + 1];
-  if (a < 15) {
-    const __nv_bfloat16* drow = dl + (static_cast<int64_t>(s) * 15 + a) * V;
-    Weights R{trow, drow, st[a * 2], st[a * 2 + 1], st[(16 + a) * 2], st[(16 + a) * 2 + 1], invT, 1};
-    const float tot = weights_total(R, V, sw);
-    __syncthreads();
-    if (tot > 0.f) {
-      tok = weights_draw(R, V, ud * tot, sw, sres);
-    } else {
-      Weights P{trow, nullptr, st[a * 2], 1.f, 0.f, 1.f, invT, 0};
-      const float tp = weights_total(P, V, sw);
-      tok = weights_draw(P, V, ud * tp, sw, sres);
+  Weights W{trow, nullptr, st[a * 2], 1.f, 0.f, 1.f, invT, 0};
+  if (a < 15)
+    W = Weights{trow, dl + (static_cast<int64_t>(s) * 15 + a) * V, st[a * 2], st[a * 2 + 1], st[(16 + a) * 2],
+                st[(16 + a) * 2 + 1], invT, 1};
+  // the slice sums of the cluster, in rank order
+  float tots[kSlices];
+  float total = 0.f;
+  for (int pass = 0; pass < 2; ++pass) {
+    const float t = weights_total(W, gb, ge, sw);
+    if (threadIdx.x == 0) slice_tot[pass] = t;
+    cluster_sync_all();
+    total = 0.f;
+#pragma unroll
+    for (int r2 = 0; r2 < kSlices; ++r2) {
+      tots[r2] = dsmem_ld_f32(dsmem_addr(&slice_tot[pass], r2));
+      total += tots[r2];
     }
-  } else {
-    Weights P{trow, nullptr, st[15 * 2], 1.f, 0.f, 1.f, invT, 0};
-    const float tp = weights_total(P, V, sw);
-    tok = weights_draw(P, V, ud * tp, sw, sres);
+    // an all-zero residual: draw from the target's distribution instead
+    if (total > 0.f || W.mode == 0) break;
+    W = Weights{trow, nullptr, st[a * 2], 1.f, 0.f, 1.f, invT, 0};
   }
-  if (threadIdx.x < 16) {
-    const int i = threadIdx.x;
-    int v = -1;
-    if (i < a) v = draft[(s * 15 + i) * dld];
-    if (i == a) v = tok;
-    out[s * 16 + i] = v;
+  const float thr = ud * total;
+  int js = -1;
+  float pre = 0.f, tin = 0.f;
+  for (int r2 = 0; r2 < kSlices; ++r2) {
+    if (thr - pre < tots[r2] && tots[r2] > 0.f) {
+      js = r2;
+      tin = thr - pre;
+      break;
+    }
+    pre += tots[r2];
   }
-  if (threadIdx.x == 0) accept[s] = a;
+  if (js < 0) {  // rounding left the threshold past the end: the last slice with weight
+    for (int r2 = kSlices - 1; r2 >= 0 && js < 0; --r2)
+      if (tots[r2] > 0.f) js = r2;
+    if (js < 0) js = 0;  // no weight anywhere: rank 0's draw returns id 0
+    tin = INFINITY;
+  }
+  if (static_cast<int>(rank) == js) {
+    const int tok = weights_draw(W, gb, ge, tin, sw, sres);
+    if (threadIdx.x == 0) out[s * 16 + a] = tok;
+  }
+  if (rank == 0) {
+    if (threadIdx.x < 16 && threadIdx.x != a) {
+      const int i = threadIdx.x;
+      out[s * 16 + i] = i < a ? draft[(s * 15 + i) * dld] : -1;
+    }
+    if (threadIdx.x == 0) accept[s] = a;
+  }
+  cluster_sync_all();  // the slice sums stay alive until every rank has read them
 }
 
 }  // namespace
@@ -941,8 +1048,21 @@ int launch_verify_sample(int S, int V, const int* draft, int dld, const __nv_bfl
   }
   {
     TraceScope ts(st, "verify.sample", static_cast<double>(S) * 2 * V * 2, 0.0);
-    const cudaError_t e = launch_pdl(sample_verify_kernel, dim3(S), dim3(kSelThreads), 0, st, V, draft, dld, tl, dl, u,
-                                     1.0f / T, stats, accept, out);
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kSlices;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(kSlices, S);
+    cfg.blockDim = dim3(kSelThreads);
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, sample_verify_kernel, V, draft, dld, tl, dl, u, 1.0f / T,
+                                             static_cast<const float*>(stats), accept, out);
     count_launch();
     if (e != cudaSuccess) return DFLASH_E_CUDA;
   }
