@@ -717,11 +717,13 @@ int dflash_fuse_taps(dflash_handle* h, dflash_state* st, const void* const* plan
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool inject = (flags & DFLASH_FUSE_INJECT_KV) != 0;
 
-  int rc = launch_prep_rows(w.row_stream, w.row_pos, w.row_end, nullptr, nseg, rows, packed.data(), s);
-  if (rc) return rc;
-  // zero every split-K counter of this call at once
+  // one launch: the row tables, every split-K counter of this call cleared,
+  // and (with K/V injection) the new stream lengths, which no kernel of this
+  // call reads (the K/V epilogue places rows by their table positions)
   const size_t counters_bytes = reinterpret_cast<char*>(w.row_stream) - reinterpret_cast<char*>(w.counters);
-  if (cudaMemsetAsync(w.counters, 0, counters_bytes, s) != cudaSuccess) return DFLASH_E_CUDA;
+  int rc = launch_prep_rows(w.row_stream, w.row_pos, w.row_end, inject ? st->lens : nullptr, nseg, rows,
+                            packed.data(), w.counters, static_cast<int>(counters_bytes / sizeof(int)), s);
+  if (rc) return rc;
   int* counters = w.counters;
   for (int r0 = 0; r0 < rows; r0 += kFusePass) {
     const int n = std::min(kFusePass, rows - r0);
@@ -743,11 +745,8 @@ int dflash_fuse_taps(dflash_handle* h, dflash_state* st, const void* const* plan
       if (rc) return rc;
     }
   }
-  if (inject) {
-    rc = launch_prep_rows(nullptr, nullptr, nullptr, st->lens, nseg, 0, packed.data(), s);
-    if (rc) return rc;
+  if (inject)
     for (int i = 0; i < nseg; ++i) st->host_len[seg_stream[i]] = seg_start[i] + seg_rows[i];
-  }
   return DFLASH_OK;
 }
 
@@ -772,9 +771,9 @@ int dflash_state_truncate(dflash_handle* h, dflash_state* st, int s_id, int64_t 
     FuseWs w{};
     if (fuse_ws_layout(h, n, ws, &w) > ws_bytes) return DFLASH_E_WORKSPACE;
     const size_t counters_bytes = reinterpret_cast<char*>(w.row_stream) - reinterpret_cast<char*>(w.counters);
-    if (cudaMemsetAsync(w.counters, 0, counters_bytes, s) != cudaSuccess) return DFLASH_E_CUDA;
     int seg[3] = {s_id, static_cast<int>(lo), n};
-    int rc = launch_prep_rows(w.row_stream, w.row_pos, w.row_end, nullptr, 1, n, seg, s);
+    int rc = launch_prep_rows(w.row_stream, w.row_pos, w.row_end, nullptr, 1, n, seg, w.counters,
+                              static_cast<int>(counters_bytes / sizeof(int)), s);
     if (rc) return rc;
     int* counters = w.counters;
     for (int r0 = 0; r0 < n; r0 += kFusePass) {
@@ -785,7 +784,7 @@ int dflash_state_truncate(dflash_handle* h, dflash_state* st, int s_id, int64_t 
       if (rc) return rc;
     }
   }
-  const int rc = launch_prep_rows(nullptr, nullptr, nullptr, st->lens, 1, 0, packed, s);
+  const int rc = launch_prep_rows(nullptr, nullptr, nullptr, st->lens, 1, 0, packed, nullptr, 0, s);
   if (rc) return rc;
   st->host_len[s_id] = new_len;
   return DFLASH_OK;
@@ -979,9 +978,11 @@ void resid_add(EpiArgs& e, float* X, const dflash_config& c, const DraftWs& w, i
 // whose per-part sums of squares are in w.ss: stage 2l is layer l's
 // attention half (input norm, QKV, attention, O-proj added to X), stage 2l+1
 // its MLP half (post norm, SwiGLU, down added to X). Each residual add
-// leaves the sums of squares of the new rows for the next stage's norm.
+// leaves the sums of squares of the new rows for the next stage's norm;
+// first_ready: stage g0's normalised rows are in w.hbuf already.
 int run_stages(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int g0, int g1, float* X,
-               const DraftWs& w, int*& counters, cudaStream_t s) {
+               const DraftWs& w, int*& counters, cudaStream_t s, bool first_ready = false) {
+  bool ready = first_ready;
   const dflash_config& c = h->cfg;
   const int T = s_count * DFLASH_BLOCK;
   const int qd = c.n_q_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim;
@@ -994,8 +995,14 @@ int run_stages(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int
     layer_plans(h, l, T, qkv, o, gu, dn);
     if (g & 1) {
       // post-attention RMSNorm -> SwiGLU -> down projection added to the residual
-      rc = stage_norm(h, g, gu, X, w, T, s);
-      if (rc) return rc;
+      if (ready) {
+        gu.n_b = 1;
+        gu.ldb = c.hidden;
+        gu.b_ptr[0] = w.hbuf;
+      } else {
+        rc = stage_norm(h, g, gu, X, w, T, s);
+        if (rc) return rc;
+      }
       gu.epi_args.out = w.mid;
       gu.epi_args.ldo = c.ffn;
       rc = gemm_launch(gu, w.partial, counters, st->status, h->num_sms, s);
@@ -1004,14 +1011,21 @@ int run_stages(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int
       dn.b_ptr[0] = w.mid;
       dn.ldb = c.ffn;
       resid_add(dn.epi_args, X, c, w, T);
+      ready = false;
       rc = gemm_launch(dn, w.partial, counters, st->status, h->num_sms, s);
       if (rc) return rc;
       counters += gemm_counter_count(dn);
       continue;
     }
     // input RMSNorm -> QKV with q_norm / k_norm + RoPE at positions C..C+15
-    rc = stage_norm(h, g, qkv, X, w, T, s);
-    if (rc) return rc;
+    if (ready) {
+      qkv.n_b = 1;
+      qkv.ldb = c.hidden;
+      qkv.b_ptr[0] = w.hbuf;
+    } else {
+      rc = stage_norm(h, g, qkv, X, w, T, s);
+      if (rc) return rc;
+    }
     EpiArgs& e = qkv.epi_args;
     e.head_dim = c.head_dim;
     e.eps = c.rms_eps;
@@ -1070,6 +1084,7 @@ int run_stages(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int
     o.b_ptr[0] = w.attn;
     o.ldb = qd;
     resid_add(o.epi_args, X, c, w, T);
+    ready = false;
     rc = gemm_launch(o, w.partial, counters, st->status, h->num_sms, s);
     if (rc) return rc;
     counters += gemm_counter_count(o);
@@ -1145,11 +1160,12 @@ int dflash_draft_block(dflash_handle* h, dflash_state* st, int s_begin, int s_co
   if (draft_ws_layout(h, st, s_count, logits_out == nullptr, ws, &w) > ws_bytes) return DFLASH_E_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   __nv_bfloat16* logits = logits_out ? static_cast<__nv_bfloat16*>(logits_out) : w.logits;
-  if (cudaMemsetAsync(w.counters, 0, w.n_counters * sizeof(int), s) != cudaSuccess) return DFLASH_E_CUDA;
-  rc = launch_embed(w.X, w.ss, h->embed, anchor_ids, s_count, c.hidden, c.vocab, c.mask_token, st->status, s);
+  // the embedding launch also writes the first layer's input norm
+  rc = launch_embed(w.X, w.ss, h->embed, anchor_ids, s_count, c.hidden, c.vocab, c.mask_token, st->status, w.counters,
+                    static_cast<int>(w.n_counters), w.hbuf, stage_gain(h, 0), c.rms_eps, s);
   if (rc) return rc;
   int* counters = w.counters;
-  rc = run_stages(h, st, s_begin, s_count, 0, 2 * c.n_layers, w.X, w, counters, s);
+  rc = run_stages(h, st, s_begin, s_count, 0, 2 * c.n_layers, w.X, w, counters, s, true);
   if (rc) return rc;
   if (c.conv_groups > 0) {
     rc = run_conv(h, s_count, w.X, w, s);

@@ -262,9 +262,10 @@ __global__ void __launch_bounds__(32 * (2 * G + 1), G <= 2 ? 2 : 1) attn_cluster
   __syncthreads();
   pdl_trigger();
   // The context K/V tiles and the stream lengths come from earlier fills,
-  // which every draft call's stream-ordered workspace reset completes before
-  // its first kernel: the producer loads the first stages before the PDL
-  // wait. Q and the block's own K/V come from the Q/K/V GEMM, after it.
+  // complete before a draft call's first kernel starts (that kernel is
+  // launched without programmatic dependence, or after a memset): the
+  // producer loads the first stages before the PDL wait. Q and the block's
+  // own K/V come from the Q/K/V GEMM, after it.
   const bool producer = warp == 2 * G && lane == 0;
   if (!producer) pdl_wait();
 

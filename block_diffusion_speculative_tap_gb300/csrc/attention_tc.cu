@@ -245,9 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const uint32_t tmem = *tmem_slot;
   pdl_trigger();
   // The context K/V tiles and the stream lengths come from earlier fills,
-  // which every draft call's stream-ordered workspace reset completes before
-  // its first kernel: the producer loads the first stages before the PDL
-  // wait. Q and the block's own K/V come from the Q/K/V GEMM, after it.
+  // complete before a draft call's first kernel starts (that kernel is
+  // launched without programmatic dependence, or after a memset): the
+  // producer loads the first stages before the PDL wait. Q and the block's
+  // own K/V come from the Q/K/V GEMM, after it.
   const bool producer = warp == 0 && lane == 0;
   if (!producer) pdl_wait();
 

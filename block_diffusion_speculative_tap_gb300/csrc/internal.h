@@ -113,9 +113,12 @@ int gemm_launch(const GemmPlan& p, float* partial, int* counters, int* err, int 
 
 // ---------------------------------------------------------------- small kernels (rows.cu)
 // X = embedding rows of [anchor + 15 mask] per stream, with the per-128-
-// feature sums of squares of every row, ss[p][T], for a fused input norm.
+// feature sums of squares of every row, ss[p][T], and (xn != null) the
+// rows' RMSNorm with gain g into xn; zero[0, nzero) is cleared (the call's
+// split-K counters). A plain launch.
 int launch_embed(float* X, float* ss, const __nv_bfloat16* embed, const int* anchors, int S, int H, int V, int mask,
-                 int* err, cudaStream_t st);
+                 int* err, int* zero, int nzero, __nv_bfloat16* xn, const __nv_bfloat16* g, float eps,
+                 cudaStream_t st);
 // The same sums of squares for rows of a caller-given X [rows, H].
 int launch_row_sumsq(float* ss, const float* X, int rows, int H, cudaStream_t st);
 int launch_wait_probe(int* err, long long cycles, cudaStream_t st);
@@ -125,11 +128,12 @@ int launch_wait_probe(int* err, long long cycles, cudaStream_t st);
 // mask_rows_only. Elementwise: 8 features a thread.
 int launch_rmsnorm_rows(__nv_bfloat16* out, const float* x, const __nv_bfloat16* g, const float* ss, int ss_ld,
                         int rows, int H, float eps, int mask_rows_only, cudaStream_t st);
-// Row tables (stream, position) of appended segments, and/or the new stream
-// lengths (start + rows of each segment). seg_info_host_packed holds
+// Row tables (stream, position) of appended segments (rows > 0), the new
+// stream lengths (start + rows of each segment; lens != null) and a cleared
+// counter range zero[0, nzero), in one launch. seg_info_host_packed holds
 // (stream, start, rows) per segment, on the host.
 int launch_prep_rows(int* row_stream, int* row_pos, int* row_end, int* lens, int nseg, int rows,
-                     const int* seg_info_host_packed, cudaStream_t st);
+                     const int* seg_info_host_packed, int* zero, int nzero, cudaStream_t st);
 // Segments of a wide K/V-injection pass for kv_rows: segment s covers heads
 // [head0[s], head0[s+1]) of the pass and columns [col0[s], ...) of the raw
 // projection rows; gain null for V.
