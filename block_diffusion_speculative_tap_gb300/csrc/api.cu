@@ -149,12 +149,18 @@ void set_split(const dflash_handle* h, GemmPlan& p, int invariant_n = kInvariant
   if (m_tiles * ((p.N + 255) / 256) < 2 * h->num_sms) p.bn = 128;
   const int BN = plan_bn(p);
   const int tiles = m_tiles * ((p.N + BN - 1) / BN);
+  // fewer tiles than half the SMs: the largest split (<= 4, at least eight
+  // reduction blocks a chunk) whose CTAs still fit one wave at one CTA an SM.
+  // The chunks of a tile form a cluster, so its epilogue (up to 128 columns
+  // of heads, residual or SwiGLU work) is shared by the ranks instead of
+  // falling to the last chunk to finish (measured on the DFlash2 geometry,
+  // 128 tokens: Q/K/V 56 us -> see the design notes).
   int ks = 1;
   if (2 * tiles < h->num_sms) {
-    while (ks < 4 && tiles * ks * 4 < 3 * h->num_sms && kb / (ks + 1) >= 8) ++ks;
+    while (ks < 4 && tiles * (ks + 1) <= h->num_sms && kb / (ks + 1) >= 8) ++ks;
   }
   p.ksplit = ks;
-  p.no_cluster = true;
+  p.no_cluster = false;
 }
 
 int attn_chunk(int cap) { return cap <= 8192 ? 256 : 512; }
