@@ -506,8 +506,10 @@ struct Weights {
       const float ra = 1.f / sa, rb = 1.f / sb;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float p = ex2f(fmaf(x[e], k, ca)) * ra;
-        const float q = ex2f(fmaf(y[e], k, cb)) * rb;
+        // p and q rounded on their own (__fmul_rn is never fused into the
+        // subtraction): equal rows give a residual of exactly zero
+        const float p = __fmul_rn(ex2f(fmaf(x[e], k, ca)), ra);
+        const float q = __fmul_rn(ex2f(fmaf(y[e], k, cb)), rb);
         w[e] = fmaxf(p - q, 0.f);
       }
     }

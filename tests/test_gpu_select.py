@@ -6,10 +6,12 @@ oracle's float64 margin to the other outcome is below 1e-5 of the total, and
 such cases are counted and checked for validity instead.
 
 The 1e-5 bound is the kernel's fp32 error budget: each weight exp((x-m)/T)
-carries <= 2 ulp from expf plus |x-m|/T * 2^-24 from rounding its argument
-(<= 2e-6 for |x-m|/T <= 30), and the running sums add <= 8 + 5 + 37 + 16
-fp32 roundings along any path (lane, warp scan, warp-slice steps, warps),
-about 4e-6 of the total; probabilities divide two such sums.
+is the SFU's base-2 exponential of one fused multiply-add, x*log2(e)/T -
+m*log2(e)/T, with relative error <= 2^-22 plus |x-m|/T * 2^-23 from rounding
+the argument (<= 4e-6 for |x-m|/T <= 30), and the running sums add
+<= 8 + 5 + 37 + 16 + 8 fp32 roundings along any path (lane, warp scan,
+warp-slice steps, warps, the eight slices of a verification row's cluster),
+about 5e-6 of the total; probabilities divide two such sums.
 """
 import json
 import os
@@ -140,7 +142,15 @@ def _sampling_inputs(S, V, seed, noise, std):
 
 
 @pytest.mark.parametrize(
-    "S,V,noise,T,std", [(8, 151936, 0.3, 1.0, 3.0), (16, 4096, 1.0, 1.0, 2.0), (16, 4096, 0.5, 0.6, 2.0)]
+    "S,V,noise,T,std",
+    [
+        (8, 151936, 0.3, 1.0, 3.0),
+        (16, 4096, 1.0, 1.0, 2.0),
+        (16, 4096, 0.5, 0.6, 2.0),
+        # 17 and 3 groups of 8 values over a row's 8 cluster slices: uneven and empty slices
+        (16, 136, 1.0, 1.0, 2.0),
+        (16, 24, 1.0, 0.8, 1.0),
+    ],
 )
 def test_sampling_verify_matches_oracle(D, S, V, noise, T, std):
     tl, dl, draft, u = _sampling_inputs(S, V, 31 + S, noise, std)
@@ -160,6 +170,39 @@ def test_sampling_verify_matches_oracle(D, S, V, noise, T, std):
         assert a[s] == oa, s
         assert toks[s] == ot, s
     assert checked >= max(2, S // 4), checked
+
+
+@pytest.mark.parametrize("V", [8, 136, 4096, 151936])
+def test_sampling_verify_zero_residual_draws_target(D, V):
+    """A rejection whose draft distribution equals the target's leaves an
+    all-zero residual max(p - q, 0): the token is then drawn from the
+    target's distribution (the oracle's fallback). Identical target and draft
+    rows accept every in-vocabulary draft (u * q < p with q = p); an id
+    outside the vocabulary is rejected, at positions 0, 7 and 14."""
+    S = 3
+    tl = SI.make_logits((S, 16, V), 2.0, seed=900 + V)
+    dl = tl[:, :15].clone()
+    draft = SI.make_token_ids((S, 15), V, seed=901 + V)
+    rej = [0, 7, 14]
+    for s in range(S):
+        draft[s, rej[s]] = V + 3
+    u = SI.make_uniforms((S, 16, 2), seed=902 + V)
+    a, toks = D.verify_sample(draft.cuda(), tl.cuda(), dl.cuda(), u.cuda(), 1.0)
+    a, toks = a.cpu().tolist(), toks.cpu().tolist()
+    for s in range(S):
+        i = rej[s]
+        assert a[s] == i, (s, a[s])
+        assert toks[s][:i] == draft[s].tolist()[:i]
+        assert all(t == -1 for t in toks[s][i + 1 :])
+        p = O.softmax_t(f64(tl[s, i]), 1.0)
+        j, m = O.inverse_cdf(p, float(u[s, i, 1]))
+        if m > MARGIN:
+            assert toks[s][i] == j, (s, toks[s][i], j)
+        else:
+            c = np.cumsum(p)
+            t = toks[s][i]
+            lo = c[t - 1] if t > 0 else 0.0
+            assert p[t] > 0 and lo - 2 * MARGIN <= float(u[s, i, 1]) <= c[t] + 2 * MARGIN
 
 
 def test_sampling_verify_distribution_is_target(D):
