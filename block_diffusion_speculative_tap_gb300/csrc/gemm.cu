@@ -294,44 +294,59 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int m_tile, int n0,
       if (j < nvalid && t < a.N && m < a.M) static_cast<__nv_bfloat16*>(a.epi.out)[static_cast<int64_t>(t) * a.epi.ldo + m] = b;
     }
     if (a.epi.cand_k > 0) {
-      // per column: the tile's top cand_k rows, one column at a time per warp
-      // (warp q takes columns q, q + 4, ...), lane l holding rows l + 32i
+      // per column: the tile's top cand_k rows (warp q takes columns q, q + 4,
+      // q + 8, q + 12), lane l holding rows l + 32i
 #pragma unroll
       for (int j = 0; j < 16; ++j) xch[j * (kTileM + 1) + row] = m < a.M ? y[j] : -INFINITY;
       named_bar_sync(1, 128);
-      for (int j = q; j < 16; j += 4) {
-        const int t = n0 + j;
-        if (j >= nvalid || t >= a.N) continue;
-        float lv[4];
+      // the warp's four columns go through the k rounds together, so their
+      // shuffle chains overlap (each column's selection is unchanged)
+      float lv[4][4];
+      uint32_t used[4];
+      bool live[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) lv[i] = xch[j * (kTileM + 1) + lane + 32 * i];
-        uint32_t used = 0;
-        float* cv = a.epi.cand_v + (static_cast<int64_t>(t) * a.m_tiles + m_tile) * a.epi.cand_k;
-        int* ci = a.epi.cand_i + (static_cast<int64_t>(t) * a.m_tiles + m_tile) * a.epi.cand_k;
-        for (int r = 0; r < a.epi.cand_k; ++r) {
+      for (int jj = 0; jj < 4; ++jj) {
+        const int j = q + 4 * jj;
+        live[jj] = j < nvalid && n0 + j < a.N;
+        used[jj] = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) lv[jj][i] = xch[j * (kTileM + 1) + lane + 32 * i];
+      }
+      for (int r = 0; r < a.epi.cand_k; ++r) {
+        float bv[4];
+        int bi[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
           // lane-local best unused (rows ascend with i, so strict > keeps the lower row)
-          float bv = -INFINITY;
-          int bi = 0x7fffffff;
+          bv[jj] = -INFINITY;
+          bi[jj] = 0x7fffffff;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            if (!(used >> i & 1u) && (lv[i] > bv || bi == 0x7fffffff)) {
-              bv = lv[i];
-              bi = lane + 32 * i;
+            if (!(used[jj] >> i & 1u) && (lv[jj][i] > bv[jj] || bi[jj] == 0x7fffffff)) {
+              bv[jj] = lv[jj][i];
+              bi[jj] = lane + 32 * i;
             }
           }
+        }
 #pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            if (ov > bv || (ov == bv && oi < bi)) {
-              bv = ov;
-              bi = oi;
+        for (int off = 16; off >= 1; off >>= 1) {
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv[jj], off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi[jj], off);
+            if (ov > bv[jj] || (ov == bv[jj] && oi < bi[jj])) {
+              bv[jj] = ov;
+              bi[jj] = oi;
             }
           }
-          if (bi != 0x7fffffff && (bi & 31) == lane) used |= 1u << (bi >> 5);
-          if (lane == 0) {
-            cv[r] = bv;
-            ci[r] = bi == 0x7fffffff ? 0x7fffffff : m_tile * kTileM + bi;
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          if (bi[jj] != 0x7fffffff && (bi[jj] & 31) == lane) used[jj] |= 1u << (bi[jj] >> 5);
+          if (lane == 0 && live[jj]) {
+            const int64_t base = (static_cast<int64_t>(n0 + q + 4 * jj) * a.m_tiles + m_tile) * a.epi.cand_k;
+            a.epi.cand_v[base + r] = bv[jj];
+            a.epi.cand_i[base + r] = bi[jj] == 0x7fffffff ? 0x7fffffff : m_tile * kTileM + bi[jj];
           }
         }
       }
