@@ -4,9 +4,9 @@
 // appended rows.
 //
 // A row's sum of squares arrives as per-128-feature parts (published by the
-// kernel that wrote the row, or by row_sumsq) and is summed in part order, so
-// the norms are elementwise and a row's result does not depend on which other
-// rows share the launch.
+// kernel that wrote the row, or by row_sumsq) and is summed in one fixed
+// order, so the norms are elementwise and a row's result does not depend on
+// which other rows share the launch.
 #include <algorithm>
 
 #include "internal.h"
@@ -32,6 +32,22 @@ __device__ __forceinline__ void row_sumsq(float* __restrict__ ss, int ss_ld, int
     for (int off = 16; off >= 1; off >>= 1) q += __shfl_xor_sync(0xffffffffu, q, off);
     if (lane == 0) ss[static_cast<int64_t>(p) * ss_ld + t] = q;
   }
+}
+
+// rstd of row r from its per-128-feature sums of squares ss[p][r]: lane l
+// adds parts l, l + 32, ... in order, then a fixed xor butterfly over the
+// lanes (five steps instead of a 32-step chain; floating-point addition is
+// commutative, so every lane ends with the same value, and the order is the
+// same for every row and launch).
+__device__ __forceinline__ float parts_rstd(const float* __restrict__ ss, int ss_ld, int r, int H, float inv_h,
+                                            float eps) {
+  const int lane = threadIdx.x & 31;
+  const int parts = H / 128;
+  float sum = 0.f;
+  for (int p = lane; p < parts; p += 32) sum += __ldcg(&ss[static_cast<int64_t>(p) * ss_ld + r]);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  return rsqrtf(__fmaf_rn(sum, inv_h, eps));
 }
 
 // X[t] = embed[token_t] as fp32; token 16s is the anchor of stream s, the
@@ -69,15 +85,8 @@ __global__ void __launch_bounds__(kStatThreads) embed_kernel(float* __restrict__
     return v;
   });
   if (xn == nullptr) return;
-  __shared__ float rstd_s;
   __syncthreads();  // the row's part sums and values are written
-  if (threadIdx.x == 0) {
-    float sum = 0.f;
-    for (int p = 0; p < H / 128; ++p) sum += ss[static_cast<int64_t>(p) * ss_ld + t];
-    rstd_s = rsqrtf(__fmaf_rn(sum, inv_h, eps));
-  }
-  __syncthreads();
-  const float rstd = rstd_s;
+  const float rstd = parts_rstd(ss, ss_ld, t, H, inv_h, eps);
   for (int i = threadIdx.x; i < H / 8; i += blockDim.x) {
     const float4 a = x[2 * i], b = x[2 * i + 1];
     const uint4 gr = *reinterpret_cast<const uint4*>(g + 8 * i);
@@ -105,25 +114,9 @@ __global__ void __launch_bounds__(kStatThreads) row_sumsq_kernel(float* __restri
   row_sumsq(ss, ss_ld, t, H, [&](int i) { return x[i]; });
 }
 
-// rstd of row r from its per-128-feature sums of squares ss[p][r]: lane p
-// loads parts p, p + 32, ...; they are added in part order through shuffles.
-__device__ __forceinline__ float parts_rstd(const float* __restrict__ ss, int ss_ld, int r, int H, float inv_h,
-                                            float eps) {
-  const int lane = threadIdx.x & 31;
-  const int parts = H / 128;
-  float sum = 0.f;
-  for (int p0 = 0; p0 < parts; p0 += 32) {
-    const int p = p0 + lane;
-    const float v = p < parts ? __ldcg(&ss[static_cast<int64_t>(p) * ss_ld + r]) : 0.f;
-    const int n = parts - p0 < 32 ? parts - p0 : 32;
-    for (int q = 0; q < n; ++q) sum += __shfl_sync(0xffffffffu, v, q);
-  }
-  return rsqrtf(__fmaf_rn(sum, inv_h, eps));
-}
-
 // out[r] = bf16(x[src] * rstd * g), rstd = 1 / sqrt(sum_p ss[p][src] / H +
 // eps): the row's sum of squares comes as per-128-feature parts published by
-// the kernel that wrote the row (summed here in part order), so the norm is
+// the kernel that wrote the row (summed here in one fixed order), so the norm is
 // elementwise. A CTA covers 1024 features of one row, 8 a thread.
 constexpr int kNormThreads = 128;
 
