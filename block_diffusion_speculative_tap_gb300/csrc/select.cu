@@ -227,26 +227,67 @@ __device__ float range_topk(const __nv_bfloat16* row, int g_begin, int g_end, in
         }
       }
     } else {
+      if (base == wg0) {
+        // The first chunk seeds the floor: t = the KM-th largest of the 32
+        // lanes' chunk maxima. At least KM values of this warp's range are
+        // >= t, so no value below t can be in its top KM, and the floor
+        // (t, worst id) admits exactly the values >= t. Without it every
+        // value of the first chunk would take the serial insert path.
+        float m = fmaxf(fmaxf(gm[0], gm[1]), fmaxf(gm[2], gm[3]));
+        int rank = 0;  // lanes with a larger maximum, ties to the lower lane: a permutation
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float mj = __shfl_sync(0xffffffffu, m, j);
+          rank += (mj > m || (mj == m && j < lane)) ? 1 : 0;
+        }
+        const unsigned who = __ballot_sync(0xffffffffu, rank == KM - 1);
+        const float t = __shfl_sync(0xffffffffu, m, __ffs(who) - 1);
+        fv = t;
+        fi = INT_MAX;
+      }
+      // a group of 8 whose largest value is below the floor holds no
+      // candidate (ties at the floor go on to the exact test); one vote for
+      // the whole chunk, since past the first chunks almost none has one
+      bool hit = false;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) hit |= g0 + u * 32 < wg1 && !(gm[u] < fv);
+      if (!__any_sync(0xffffffffu, hit)) continue;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        // a group of 8 whose largest value is below the floor holds no
-        // candidate (ties at the floor go on to the exact test)
         if (__ballot_sync(0xffffffffu, g0 + u * 32 < wg1 && !(gm[u] < fv)) == 0u) continue;
         float x[8];
         unpack8(raw[u], x);
+        // each lane's candidates of this group as an 8-bit mask; one ballot
+        // finds the lanes that have any, and only real candidates travel
+        const int gid = (g0 + u * 32) * 8;
+        uint32_t lm = 0;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int id = (g0 + u * 32) * 8 + e;
-          unsigned cand = __ballot_sync(0xffffffffu, g0 + u * 32 < wg1 && better(x[e], id, fv, fi));
-          while (cand) {
-            const int src = __ffs(cand) - 1;
-            cand &= cand - 1;
-            const float cv = __shfl_sync(0xffffffffu, x[e], src);
-            const int ci = __shfl_sync(0xffffffffu, id, src);
-            if (better(cv, ci, fv, fi)) {  // the floor may have risen since the ballot
+        for (int e = 0; e < 8; ++e)
+          if (g0 + u * 32 < wg1 && better(x[e], gid + e, fv, fi)) lm |= 1u << e;
+        unsigned lanes = __ballot_sync(0xffffffffu, lm != 0u);
+        while (lanes) {
+          const int src = __ffs(lanes) - 1;
+          lanes &= lanes - 1;
+          uint32_t sm = __shfl_sync(0xffffffffu, lm, src);
+          const int sg = __shfl_sync(0xffffffffu, gid, src);
+          while (sm) {
+            const int e = __ffs(sm) - 1;
+            sm &= sm - 1;
+            float mine = x[0];
+#pragma unroll
+            for (int q = 1; q < 8; ++q)
+              if (e == q) mine = x[q];
+            const float cv = __shfl_sync(0xffffffffu, mine, src);
+            const int ci = sg + e;
+            if (better(cv, ci, fv, fi)) {  // the floor may have risen since the masks
               wt.insert(cv, ci, lane);
-              fv = __shfl_sync(0xffffffffu, wt.v, KM - 1);
-              fi = __shfl_sync(0xffffffffu, wt.i, KM - 1);
+              // the floor only rises: the list's KM-th entry once it beats the seed
+              const float nv = __shfl_sync(0xffffffffu, wt.v, KM - 1);
+              const int ni = __shfl_sync(0xffffffffu, wt.i, KM - 1);
+              if (better(nv, ni, fv, fi)) {
+                fv = nv;
+                fi = ni;
+              }
             }
           }
         }
