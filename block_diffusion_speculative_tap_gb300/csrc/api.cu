@@ -1273,6 +1273,7 @@ int dflash_verify(int mode, int streams, int vocab, const int32_t* draft_ids, in
   }
   if (mode != DFLASH_VERIFY_SAMPLE) return DFLASH_E_INVALID_ARG;
   if (!draft_logits || !uniforms || !(temperature > 0.f) || !aligned16(draft_logits)) return DFLASH_E_INVALID_ARG;
+  if (streams > DFLASH_MAX_SAMPLE_STREAMS) return DFLASH_E_INVALID_ARG;
   size_t need = 0;
   dflash_verify_workspace_bytes(mode, streams, vocab, &need);
   if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 15u)) return DFLASH_E_WORKSPACE;

@@ -87,6 +87,7 @@ enum {
 enum { DFLASH_LAYER_FULL = 0, DFLASH_LAYER_SLIDING = 1 };
 enum { DFLASH_VARIANT_V1 = 1, DFLASH_VARIANT_2 = 2 };
 enum { DFLASH_VERIFY_GREEDY = 0, DFLASH_VERIFY_SAMPLE = 1 };
+#define DFLASH_MAX_SAMPLE_STREAMS 65535
 enum { DFLASH_FUSE_INJECT_KV = 1 }; /* dflash_fuse_taps flags */
 
 /* ---------------------------------------------------------------- config
@@ -446,7 +447,8 @@ int dflash_tree_verify(int streams, int depth, const int32_t* widths, int vocab,
  *   u[s][i][0] * q(d) < p_i(d); at the first rejection draw from
  *   max(p_i - q_{i+1}, 0) (p_i if that is all zero); if none is rejected draw
  *   the bonus from p_15; draws use u[s][i][1] by inverse CDF. uniforms: device
- *   fp32 [S, 16, 2].
+ *   fp32 [S, 16, 2]. At most DFLASH_MAX_SAMPLE_STREAMS streams a call
+ *   (E_INVALID_ARG above: a stream is one row of the kernels' grids).
  * Outputs: accept_len device int32 [S] (a in 0..15); out_tokens device int32
  * [S, 16]: the a+1 committed tokens then -1. A draft id outside [0, V) is
  * never accepted (and sets nothing else). ws: >= dflash_verify_workspace_bytes. */

@@ -100,6 +100,18 @@ def test_null_arguments_are_refused(A):
     assert A.lib.dflash_verify_workspace_bytes(7, 4, 4096, C.byref(nb)) == -1
 
 
+def test_sampling_stream_limit_is_refused(A):
+    """Sampling verification takes at most DFLASH_MAX_SAMPLE_STREAMS (65535)
+    streams a call; more are refused before any device work (the pointers
+    here are never dereferenced)."""
+    import ctypes as C
+
+    p = C.c_void_p(0x10000)
+    args = lambda S: (1, S, 4096, p, 1, p, p, p, C.c_float(1.0), p, p, p, C.c_size_t(1 << 30), None)
+    assert A.lib.dflash_verify(*args(65536)) == -1
+    assert A.lib.dflash_verify(*args(1 << 20)) == -1
+
+
 def test_kernel_shape_limits_are_refused(D):
     """Shapes the method allows but the kernels do not serve are refused
     up front (DFLASH_E_SHAPE), never run: query groups over 8 heads a kv head,
