@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(kSelEdgeThreads)
   extern __shared__ uint32_t rows[];  // [2k][r/2 + 1] bf16 pairs: U rows of position i, then W rows of i+1
   pdl_trigger();
   pdl_wait();
-  const int i = blockIdx.x, s = blockIdx.y;
+  const int s = blockIdx.x, i = blockIdx.y;  // streams on x: no 65535 limit
   const int words = r / 2, stride = words + 1;
   const int* ids_i = cand_ids + (static_cast<int64_t>(s) * P + i) * k;
   // stage: row q < k is U[c(i, q)], row k + q is W[c(i+1, q)]; an id outside
@@ -274,7 +274,7 @@ int launch_select_path(int S, int P, int k, int V, int r, const int* cand_ids, c
     const size_t smem = static_cast<size_t>(2 * k) * (r / 2 + 1) * sizeof(uint32_t);
     const double bytes = static_cast<double>(S) * (P - 1) * (2.0 * k * r * 2 + k * 4 * 2 + k * k * 4.0);
     TraceScope ts(st, "selector.edges", bytes, 2.0 * S * (P - 1) * k * k * r);
-    const cudaError_t e = launch_pdl(selector_edges_kernel, dim3(P - 1, S), dim3(kSelEdgeThreads), smem, st,
+    const cudaError_t e = launch_pdl(selector_edges_kernel, dim3(S, P - 1), dim3(kSelEdgeThreads), smem, st,
                                      cand_ids, P, k, V, r, U, W, E);
     count_launch();
     if (e != cudaSuccess) return DFLASH_E_CUDA;
