@@ -727,16 +727,21 @@ __global__ void greedy_prefix_kernel(int S, int V, const int* __restrict__ draft
   pdl_wait();
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= S) return;
-  int t[16];
+  // every load issued before the first comparison (no chain of dependent loads)
+  int t[16], d[15];
 #pragma unroll
   for (int i = 0; i < 16; ++i) t[i] = out[s * 16 + i];
-  int a = 0;
-  while (a < 15 && draft[(s * 15 + a) * dld] == t[a]) ++a;
+#pragma unroll
+  for (int i = 0; i < 15; ++i) d[i] = draft[(s * 15 + i) * dld];
+  int a = 15;
+#pragma unroll
+  for (int i = 14; i >= 0; --i)
+    if (d[i] != t[i]) a = i;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     int v = -1;
-    if (i < a) v = draft[(s * 15 + i) * dld];
-    if (i == a) v = t[a];
+    if (i < a) v = d[i];
+    if (i == a) v = t[i];
     out[s * 16 + i] = v;
   }
   accept[s] = a;
@@ -828,11 +833,14 @@ __global__ void __launch_bounds__(kSelThreads) sample_verify_kernel(int V, const
   __shared__ float sw[kSelWarps];
   __shared__ int sres[1];
   __shared__ float slice_tot[2];  // read by the other CTAs of the cluster
+  __shared__ int rejected[16];
   const uint32_t rank = cluster_rank();
   const int s = blockIdx.y;
   const float* st = stats + s * 31 * 2;
-  int a = 15;
-  for (int i = 0; i < 15; ++i) {
+  // the 15 acceptance tests at once, thread i taking position i (their
+  // loads in parallel, not a chain); a = the first rejected position
+  if (threadIdx.x < 15) {
+    const int i = threadIdx.x;
     const int x = draft[(s * 15 + i) * dld];
     bool acc = false;
     if (x >= 0 && x < V) {
@@ -843,11 +851,12 @@ __global__ void __launch_bounds__(kSelThreads) sample_verify_kernel(int V, const
           st[(16 + i) * 2 + 1];
       acc = u[(s * 16 + i) * 2] * q < p;
     }
-    if (!acc) {
-      a = i;
-      break;
-    }
+    rejected[i] = acc ? 0 : 1;
   }
+  __syncthreads();
+  int a = 15;
+  for (int i = 14; i >= 0; --i)
+    if (rejected[i]) a = i;
   const int ng = V >> 3;
   const int gb = static_cast<int>(static_cast<long long>(ng) * rank / kSlices);
   const int ge = static_cast<int>(static_cast<long long>(ng) * (rank + 1) / kSlices);
