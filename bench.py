@@ -1121,7 +1121,11 @@ def profile_workload(name):
     geometry (40 q / 8 kv heads of 128) three times, so the tensor-memory
     attention launch is captured; 'treeverify' verifies 32 streams of
     93-node draft trees over a 151936-token vocabulary three times (the
-    arg-max scan of 2976 target rows, 904 MB)."""
+    arg-max scan of 2976 target rows, 904 MB); 'topk480' takes the top 8 of
+    480 rows of 151936 logits three times (the vocabulary scan of a
+    32-stream draft, 146 MB); 'sampleverify' runs sampling verification of
+    8 streams over a 151936-token vocabulary three times (the DFlash2
+    geometry's round: 31 rows of statistics and the cluster draw a stream)."""
     import torch
 
     import block_diffusion_speculative_tap_gb300 as D
@@ -1150,6 +1154,22 @@ def profile_workload(name):
         tl = SI.make_logits((S, D.tree_size(widths, 8), V), 2.0, 802, device="cuda")
         for _ in range(3):
             D.tree_verify(tokens, tl, widths)
+        torch.cuda.synchronize()
+        return
+    if name == "topk480":
+        lg = SI.make_logits((480, 151936), 2.0, 810, device="cuda")
+        for _ in range(3):
+            D.topk(lg, 8)
+        torch.cuda.synchronize()
+        return
+    if name == "sampleverify":
+        S, V = 8, 151936
+        tl = SI.make_logits((S, 16, V), 1.0, 820, device="cuda")
+        dl = (tl[:, :15].float() + 0.5 * SI.make_logits((S, 15, V), 1.0, 821, device="cuda").float()).to(torch.bfloat16)
+        draft = SI.make_token_ids((S, 15), V, 822, device="cuda")
+        u = SI.make_uniforms((S, 16, 2), 823, device="cuda")
+        for _ in range(3):
+            D.verify_sample(draft, tl, dl, u, 1.0)
         torch.cuda.synchronize()
         return
     if name == "attention8d2":
@@ -1186,7 +1206,7 @@ def main():
     ap.add_argument("--workload", default="9b", choices=["9b"] + sorted(SHARDED),
                     help="9b: the batch-1 decode round (default); serve32 / dflash2geom: a multi-stream round, "
                     "streams split over ranks")
-    ap.add_argument("--profile-workload", default=None, help="run a small workload for ncu (attention32, attention8d2, fill4096, treeverify) and exit")
+    ap.add_argument("--profile-workload", default=None, help="run a small workload for ncu (attention32, attention8d2, fill4096, treeverify, topk480, sampleverify) and exit")
     args = ap.parse_args()
     if args.profile_workload:
         profile_workload(args.profile_workload)
