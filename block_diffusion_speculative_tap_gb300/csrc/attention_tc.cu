@@ -8,24 +8,32 @@
 // the whole group. The visible context keys are split evenly over the CS CTAs
 // of a thread-block cluster; the last CTA also takes the block's own 16 keys.
 //
-// Roles (320 threads):
-//   warp 0     TMA producer: the group's Q rows once, then 64-key tiles of K
-//              and V (head-major cache, 3-D tensor maps, 128-byte swizzle)
-//              through a ring of kStages stages, and the block's K/V.
-//   warp 1     tensor-memory owner and MMA issuer: S = Q K^T into one of two
-//              64-column score buffers, then O_t = P V (V read MN-major) into
-//              a 128-column output buffer.
-//   warps 2-9  softmax: two warps a tensor-memory lane quadrant, each taking
-//              half of a tile's keys for the quadrant's 32 rows (thread r of
-//              a warp owns row r of its half). The pair shares its tile
-//              maximum through shared memory and a named barrier; each keeps
-//              its half's sum and the maximum the probabilities are taken
-//              against (log2 domain), and writes its half of P as bf16 into a
-//              128-byte-swizzled tile for the next MMA. The output accumulates over the tiles
-//              in tensor memory; the maximum in use moves (and the row's
-//              output and sum are rescaled in place) only when a tile's
-//              maximum exceeds it by more than kRescaleLog2, so a
-//              probability never exceeds 2^kRescaleLog2. Warps whose rows
+// A 128-row MMA costs about the same time whether it is 64 or 128 columns
+// wide, so the scores of two 64-key tiles are taken in one 128-column MMA: a
+// step is 128 keys. K and V stream through four rings of 64-key slots (K
+// dims 0-63, K dims 64-127, V dims 0-63, V dims 64-127) so that a step's two
+// tiles sit in adjacent slots and read as one 128-row operand. Both A operands
+// live in tensor memory (row i of A in lane i, two bf16 of consecutive k in
+// each 32-bit column): the softmax warps copy Q there once and write P there.
+//
+// Roles (576 threads):
+//   warp 0     TMA producer: 64-key tiles of K and V (head-major cache, 3-D
+//              tensor maps, 128-byte swizzle) into the rings, and the block's
+//              K/V.
+//   warp 1     tensor-memory owner and MMA issuer: S = Q K^T of step u+1 as
+//              soon as the softmax warps have read step u's scores, then
+//              O += P_u V_u (V read MN-major) once they have written P_u.
+//   warps 2-17 softmax: four warps a tensor-memory lane quadrant, each taking
+//              32 of a step's keys for the quadrant's 32 rows (thread r of a
+//              warp owns row r). The four share their step maximum through
+//              shared memory and a named barrier; each keeps its keys' sum and
+//              the maximum the probabilities are taken against (log2 domain),
+//              and writes its keys of P as bf16 into one of two P buffers in
+//              tensor memory. The output accumulates over the steps in tensor
+//              memory; the maximum in use moves (and the row's output and sum
+//              are rescaled in place, each warp its 32 output columns) only
+//              when a step's maximum exceeds it by more than kRescaleLog2, so
+//              a probability never exceeds 2^kRescaleLog2. Warps whose rows
 //              are all padding take no part.
 // The CTAs of a cluster then reduce-scatter their (max, sum, output) rows
 // through distributed shared memory in rank order and write bf16 rows.
@@ -42,34 +50,45 @@ namespace dfl {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kTK = 64;         // keys a context tile
-constexpr int kBK = 16;         // the block's own keys
-constexpr int kStages = 4;
-constexpr int kRows = 128;      // MMA rows: 16 query rows x G, zero-padded
-constexpr int kQSub = kRows * 128;       // 128 rows x 64 dims bf16 (16 KiB)
-constexpr int kKVSub = kTK * 128;        // 64 keys x 64 dims (8 KiB)
-constexpr int kStageBytes = 4 * kKVSub;  // K lo, K hi, V lo, V hi (32 KiB)
+constexpr int kTK = 64;                  // keys a context tile (one TMA box, one ring slot)
+constexpr int kSK = 2 * kTK;             // keys a step: two tiles, one 128-column score MMA
+constexpr int kBK = 16;                  // the block's own keys
+constexpr int kStages = 6;               // ring slots (even: a step's tiles take adjacent slots)
+constexpr int kRows = 128;               // MMA rows: 16 query rows x G, zero-padded
+constexpr int kSlot = kTK * 128;         // 64 keys x 64 dims bf16 (8 KiB)
+constexpr int kRing = kStages * kSlot;   // one ring (48 KiB)
+constexpr int kTileBytes = 4 * kSlot;    // a tile's K and V (32 KiB)
 constexpr int kBSub = kBK * 128;         // 16 keys x 64 dims (2 KiB)
-constexpr int kPBytes = kRows * 128;     // 128 rows x 64 keys bf16 (16 KiB)
 constexpr int kPartLd = kD + 4;          // fp32 partial row stride
-constexpr int kThreads = 320;
-constexpr int kTmemCols = 256;           // two 64-column score buffers + a 128-column output
+constexpr int kParts = 4;                // softmax warps a lane quadrant
+constexpr int kThreads = 64 + 128 * kParts;
+// tensor-memory columns: the step's scores (0..127), the output (128..255),
+// Q as the score MMAs' A operand (64 columns: 128 dims as bf16 pairs) and two
+// P buffers (64 columns each: 128 keys as bf16 pairs)
+constexpr int kColS = 0;
+constexpr int kColO = 128;
+constexpr int kColQ = 256;
+constexpr int kColP = 320;
+constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;      // a row's maximum in use moves only past this margin
 
 struct TcSmem {
-  static constexpr int kQ = 0;
-  static constexpr int kStage = kQ + 2 * kQSub;
-  static constexpr int kBlock = kStage + kStages * kStageBytes;
-  static constexpr int kP = kBlock + 4 * kBSub;
-  static constexpr int kBar = kP + 2 * kPBytes;
-  static constexpr int kXchg = kBar + 256;                    // [4 quadrants][2 halves][2][32] tile maxima
-  static constexpr int kLPart = kXchg + 4 * 2 * 2 * 32 * 4;  // [2 halves][128] row sums
-  static constexpr int kBytes = kLPart + 2 * kRows * 4;
+  static constexpr int kKlo = 0;
+  static constexpr int kKhi = kKlo + kRing;
+  static constexpr int kVlo = kKhi + kRing;
+  static constexpr int kVhi = kVlo + kRing;
+  static constexpr int kBlock = kVhi + kRing;  // the block's K lo, K hi, V lo, V hi
+  static constexpr int kBar = kBlock + 4 * kBSub;
+  static constexpr int kXchg = kBar + 256;                        // [4 quadrants][kParts][2][32] step maxima
+  static constexpr int kLPart = kXchg + 4 * kParts * 2 * 32 * 4;  // [kParts][128] row sums
+  static constexpr int kBytes = kLPart + kParts * kRows * 4;
 };
-static_assert(TcSmem::kStage % 1024 == 0 && TcSmem::kBlock % 1024 == 0 && TcSmem::kP % 1024 == 0,
+static_assert(kStages % 2 == 0, "a step's two tiles must sit in adjacent ring slots");
+static_assert(TcSmem::kKhi % 1024 == 0 && TcSmem::kBlock % 1024 == 0,
               "swizzled tiles must start on 1024-byte boundaries");
-static_assert(sizeof(float) * (kRows * kPartLd + kRows * 2) <= kStages * kStageBytes,
-              "the partials must fit the stage memory");
+static_assert(sizeof(float) * (kRows * kPartLd + kRows * 2) <= 4 * kRing,
+              "the partials must fit the ring memory");
+static_assert(8 * (2 * kStages + 10) <= 256, "the barriers must fit their region");
 constexpr int kSmemLaunch = TcSmem::kBytes + 1024;
 
 // MN-major operand stored with the 128-byte swizzle, as TMA writes a tile of
@@ -131,7 +150,6 @@ __device__ __forceinline__ float4 cld4(uint32_t a) {
                : "memory");
   return v;
 }
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Load 32 consecutive 32-bit tensor-memory columns of this warp's 32 lanes
 // (one lane per thread); the caller waits with tmem_wait_ld before use.
@@ -171,12 +189,35 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Store 16 consecutive 32-bit tensor-memory columns of this warp's 32 lanes
+// (one lane per thread); the caller waits with tmem_wait_st.
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] * B[smem], issued by one thread: A's row i is lane i
+// of the columns from a_tmem on, two bf16 of consecutive k a column.
+__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 struct TcArgs {
   CUtensorMap kmap;   // cache K: 3-D [S*nkv][cap][128], box {64, 64, 1}
   CUtensorMap vmap;
   CUtensorMap kbmap;  // block K: 2-D [T][nkv*128], box {64, 16}
   CUtensorMap vbmap;
-  CUtensorMap qmap;   // Q: 2-D [T][nq*128], box {64, 16}
   AttnArgs a;
 };
 
@@ -186,16 +227,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const AttnArgs& a = P.a;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + TcSmem::kBar);
-  uint64_t* full = bars;            // [kStages] a context tile landed
-  uint64_t* empty = bars + 4;       // [kStages] its MMAs are done
-  uint64_t* s_full = bars + 8;      // [2] scores ready in tensor memory
-  uint64_t* s_empty = bars + 10;    // [2] scores read by the softmax warps
-  uint64_t* p_full = bars + 12;     // [2] P written to shared memory (and the output rescaled)
-  uint64_t* o_full = bars + 14;     // [2] P*V of a tile using P buffer b has landed in the output
-  uint64_t* blk_full = bars + 16;   // the block's K/V landed
-  uint64_t* q_full = bars + 17;     // the Q rows landed
-  uint64_t* drain = bars + 18;      // every MMA of the CTA is done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
+  uint64_t* full = bars;                  // [kStages] a context tile landed in its ring slot
+  uint64_t* empty = bars + kStages;       // [kStages] the MMAs reading the slot are done
+  uint64_t* s_full = bars + 2 * kStages;  // the step's scores are in tensor memory
+  uint64_t* s_empty = s_full + 1;         // the softmax warps have read them
+  uint64_t* p_full = s_full + 2;          // [2] P written to tensor memory (and the output rescaled)
+  uint64_t* o_full = s_full + 4;          // [2] P*V of a step using P buffer b has landed in the output
+  uint64_t* blk_full = s_full + 6;        // the block's K/V landed
+  uint64_t* q_tm = s_full + 7;            // the Q rows are in tensor memory
+  uint64_t* drain = s_full + 8;           // every MMA of the CTA is done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 9);
   int* abort_word = reinterpret_cast<int*>(tmem_slot + 1);
   const uint32_t sbase = smem_u32(smem);
 
@@ -204,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const int kvh = blockIdx.y, si = blockIdx.z;
   const int G = a.nq / a.nkv;
   const int rows = 16 * G;
-  const int nact = (rows + 31) / 32;  // lane quadrants with real rows: 0 .. nact-1 (two softmax warps each)
+  const int nact = (rows + 31) / 32;  // lane quadrants with real rows: 0 .. nact-1 (kParts softmax warps each)
   int* err = a.err;
 
   if (threadIdx.x == 0) {
@@ -212,28 +253,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
+    mbar_init(s_full, 1);
+    mbar_init(s_empty, 128 * nact);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&s_empty[b], 64 * nact);
-      mbar_init(&p_full[b], 64 * nact);
+      mbar_init(&p_full[b], 128 * nact);
       mbar_init(&o_full[b], 1);
     }
     mbar_init(blk_full, 1);
-    mbar_init(q_full, 1);
+    mbar_init(q_tm, 128 * nact);
     mbar_init(drain, 1);
     *abort_word = 0;
     fence_barrier_init();
-  }
-  // the Q tile's rows past 16*G are never loaded: zero them (row r of a
-  // swizzled sub-tile is the 128 bytes at r * 128, its chunks permuted)
-  {
-    const int pad = kRows - rows;
-    for (int i = threadIdx.x; i < 2 * pad * 8; i += blockDim.x) {
-      const int sub = i / (pad * 8), rem = i - sub * pad * 8;
-      *reinterpret_cast<uint4*>(smem + TcSmem::kQ + sub * kQSub + (rows + rem / 8) * 128 + (rem & 7) * 16) =
-          make_uint4(0u, 0u, 0u, 0u);
-    }
-    fence_proxy_async();
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -246,9 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   pdl_trigger();
   // The context K/V tiles and the stream lengths come from earlier fills,
   // complete before a draft call's first kernel starts (that kernel is
-  // launched without programmatic dependence, or after a memset): the
-  // producer loads the first stages before the PDL wait. Q and the block's
-  // own K/V come from the Q/K/V GEMM, after it.
+  // launched without programmatic dependence): the producer loads the first
+  // slots before the PDL wait. Q and the block's own K/V come from the
+  // Q/K/V GEMM, after it.
   const bool producer = warp == 0 && lane == 0;
   if (!producer) pdl_wait();
 
@@ -257,32 +287,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const int nvis = a.window > 0 ? min(C, a.window) : C;
   const int k0 = static_cast<int>(static_cast<long long>(nvis) * rank / CS);
   const int k1 = static_cast<int>(static_cast<long long>(nvis) * (rank + 1) / CS);
-  const int nctx = (k1 - k0 + kTK - 1) / kTK;
+  const int nkeys = k1 - k0;
+  const int nctx = (nkeys + kTK - 1) / kTK;  // context tiles
+  const int nsc = (nctx + 1) / 2;            // context steps: tiles 2j and 2j+1
   const bool has_block = rank == CS - 1;
-  const int nT = nctx + (has_block ? 1 : 0);  // tile nctx is the block's own keys
+  const int nS = nsc + (has_block ? 1 : 0);  // step nsc is the block's own keys
   const int slab = s * a.nkv + kvh;
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer
-      const int npre = nctx < kStages ? nctx : kStages;
-      for (int t = 0; t < npre; ++t) {
-        mbar_arrive_expect_tx(&full[t], kStageBytes);
-        const uint32_t d = sbase + TcSmem::kStage + t * kStageBytes;
+      auto load_tile = [&](int t) {
+        const int sl = t % kStages;
         const int row = k0 + t * kTK;
-        tma3d(d, &P.kmap, &full[t], 0, row, slab);
-        tma3d(d + kKVSub, &P.kmap, &full[t], 64, row, slab);
-        tma3d(d + 2 * kKVSub, &P.vmap, &full[t], 0, row, slab);
-        tma3d(d + 3 * kKVSub, &P.vmap, &full[t], 64, row, slab);
-      }
+        mbar_arrive_expect_tx(&full[sl], kTileBytes);
+        tma3d(sbase + TcSmem::kKlo + sl * kSlot, &P.kmap, &full[sl], 0, row, slab);
+        tma3d(sbase + TcSmem::kKhi + sl * kSlot, &P.kmap, &full[sl], 64, row, slab);
+        tma3d(sbase + TcSmem::kVlo + sl * kSlot, &P.vmap, &full[sl], 0, row, slab);
+        tma3d(sbase + TcSmem::kVhi + sl * kSlot, &P.vmap, &full[sl], 64, row, slab);
+      };
+      const int npre = nctx < kStages ? nctx : kStages;
+      for (int t = 0; t < npre; ++t) load_tile(t);
       pdl_wait();
-      mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(rows) * kD * 2);
-      for (int j = 0; j < G; ++j) {
-        const uint32_t d = sbase + TcSmem::kQ + j * 16 * 128;
-        const int col = (kvh * G + j) * kD;
-        tma2d(d, &P.qmap, q_full, col, 16 * si);
-        tma2d(d + kQSub, &P.qmap, q_full, col + 64, 16 * si);
-      }
       if (has_block) {
         mbar_arrive_expect_tx(blk_full, 4 * kBSub);
         const uint32_t b = sbase + TcSmem::kBlock;
@@ -292,69 +318,83 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         tma2d(b + 3 * kBSub, &P.vbmap, blk_full, kvh * kD + 64, 16 * si);
       }
       for (int t = npre; t < nctx; ++t) {
-        const int st = t % kStages;
-        if (!mbar_wait(&empty[st], ((t / kStages) & 1) ^ 1u, err, DFLASH_STATUS_TIMEOUT, abort_word)) break;
-        mbar_arrive_expect_tx(&full[st], kStageBytes);
-        const uint32_t d = sbase + TcSmem::kStage + st * kStageBytes;
-        const int row = k0 + t * kTK;
-        tma3d(d, &P.kmap, &full[st], 0, row, slab);
-        tma3d(d + kKVSub, &P.kmap, &full[st], 64, row, slab);
-        tma3d(d + 2 * kKVSub, &P.vmap, &full[st], 0, row, slab);
-        tma3d(d + 3 * kKVSub, &P.vmap, &full[st], 64, row, slab);
+        const int sl = t % kStages;
+        if (!mbar_wait(&empty[sl], ((t / kStages) & 1) ^ 1u, err, DFLASH_STATUS_TIMEOUT, abort_word)) break;
+        load_tile(t);
       }
-      // no copy may still be landing when the stage memory is reused below
-      for (int st = 0; st < kStages && st < nctx; ++st) {
-        const int last = st + ((nctx - 1 - st) / kStages) * kStages;
-        mbar_wait(&full[st], (last / kStages) & 1, err, DFLASH_STATUS_TIMEOUT, nullptr);
+      // no copy may still be landing when the ring memory is reused below
+      for (int sl = 0; sl < kStages && sl < nctx; ++sl) {
+        const int last = sl + ((nctx - 1 - sl) / kStages) * kStages;
+        mbar_wait(&full[sl], (last / kStages) & 1, err, DFLASH_STATUS_TIMEOUT, nullptr);
       }
-      mbar_wait(q_full, 0, err, DFLASH_STATUS_TIMEOUT, nullptr);
       if (has_block) mbar_wait(blk_full, 0, err, DFLASH_STATUS_TIMEOUT, nullptr);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
-      constexpr uint32_t kIdS = idesc_bf16_f32(kRows, kTK);
+      constexpr uint32_t kIdS2 = idesc_bf16_f32(kRows, kSK);
+      constexpr uint32_t kIdS1 = idesc_bf16_f32(kRows, kTK);
       constexpr uint32_t kIdSB = idesc_bf16_f32(kRows, kBK);
       constexpr uint32_t kIdO = idesc_bf16_f32(kRows, kD) | kIdescBTransposed;
-      bool ok = mbar_wait(q_full, 0, err, DFLASH_STATUS_TIMEOUT, abort_word);
+      bool ok = mbar_wait(q_tm, 0, err, DFLASH_STATUS_TIMEOUT, abort_word);
       bool any = false;
-      // O += P_u V_u once the softmax warps wrote P_u (and rescaled O)
-      auto issue_pv = [&](int u) -> bool {
-        const bool blk = u == nctx;
-        if (!mbar_wait(&p_full[u & 1], (u >> 1) & 1, err, DFLASH_STATUS_TIMEOUT, abort_word)) return false;
+      // S_j = Q K_j^T once step j's keys have landed: one MMA per 16 dims,
+      // 128 (or, for a last odd tile, 64) columns wide
+      auto s_issue = [&](int j) -> bool {
+        const bool blk = j == nsc;
+        const int t0 = 2 * j;
+        bool r;
+        if (blk) {
+          r = mbar_wait(blk_full, 0, err, DFLASH_STATUS_TIMEOUT, abort_word);
+        } else {
+          r = mbar_wait(&full[t0 % kStages], (t0 / kStages) & 1, err, DFLASH_STATUS_TIMEOUT, abort_word);
+          if (r && t0 + 1 < nctx)
+            r = mbar_wait(&full[(t0 + 1) % kStages], ((t0 + 1) / kStages) & 1, err, DFLASH_STATUS_TIMEOUT,
+                          abort_word);
+        }
+        if (!r) return false;
         tc_fence_after();
-        const uint32_t pa = sbase + TcSmem::kP + (u & 1) * kPBytes;
-        const uint32_t vb = blk ? sbase + TcSmem::kBlock + 2 * kBSub
-                                : sbase + TcSmem::kStage + (u % kStages) * kStageBytes + 2 * kKVSub;
-        const uint32_t lbo = blk ? kBSub : kKVSub;  // V lo -> V hi
-        const int nks = blk ? kBK / 16 : kTK / 16;
-        for (int kk = 0; kk < nks; ++kk)
-          umma_bf16(tmem + 128, sdesc_sw128(pa + kk * 32), sdesc_sw128_mn(vb + kk * 16 * 128, lbo), kIdO,
-                    (u > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&o_full[u & 1]);
-        if (!blk) umma_commit(&empty[u % kStages]);
-        return true;
-      };
-      for (int t = 0; t < nT && ok; ++t) {
-        const bool blk = t == nctx;
-        const int st = t % kStages;
-        ok = blk ? mbar_wait(blk_full, 0, err, DFLASH_STATUS_TIMEOUT, abort_word)
-                 : mbar_wait(&full[st], (t / kStages) & 1, err, DFLASH_STATUS_TIMEOUT, abort_word);
-        if (ok) ok = mbar_wait(&s_empty[t & 1], ((t >> 1) & 1) ^ 1u, err, DFLASH_STATUS_TIMEOUT, abort_word);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t kb = blk ? sbase + TcSmem::kBlock : sbase + TcSmem::kStage + st * kStageBytes;
-        const uint32_t ksub = blk ? kBSub : kKVSub;  // K lo -> K hi
+        const uint32_t id = blk ? kIdSB : (t0 + 1 < nctx ? kIdS2 : kIdS1);
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk & 3) * 32;
-          umma_bf16(tmem + (t & 1) * kTK, sdesc_sw128(sbase + TcSmem::kQ + (kk >> 2) * kQSub + off),
-                    sdesc_sw128(kb + (kk >> 2) * ksub + off), blk ? kIdSB : kIdS, kk > 0 ? 1u : 0u);
+          const uint32_t kb = blk ? sbase + TcSmem::kBlock + (kk >> 2) * kBSub
+                                  : sbase + (kk >= 4 ? TcSmem::kKhi : TcSmem::kKlo) + (t0 % kStages) * kSlot;
+          umma_bf16_ta(tmem + kColS, tmem + kColQ + kk * 8, sdesc_sw128(kb + off), id, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&s_full[t & 1]);
-        any = true;
-        if (t >= 1) ok = issue_pv(t - 1);
+        umma_commit(s_full);
+        return true;
+      };
+      if (ok && nS >= 1) {
+        ok = s_issue(0);
+        any = ok;
       }
-      if (ok && nT >= 1) issue_pv(nT - 1);
+      for (int u = 0; u < nS && ok; ++u) {
+        // the next step's scores as soon as softmax u has read this step's
+        if (u + 1 < nS) {
+          ok = mbar_wait(s_empty, u & 1, err, DFLASH_STATUS_TIMEOUT, abort_word);
+          if (ok) ok = s_issue(u + 1);
+          if (!ok) break;
+        }
+        // O += P_u V_u once the softmax warps wrote P_u (and rescaled O)
+        ok = mbar_wait(&p_full[u & 1], (u >> 1) & 1, err, DFLASH_STATUS_TIMEOUT, abort_word);
+        if (!ok) break;
+        tc_fence_after();
+        const bool blk = u == nsc;
+        const int t0 = 2 * u;
+        const int nks = blk ? kBK / 16 : (t0 + 1 < nctx ? kSK : kTK) / 16;
+        const uint32_t pa = tmem + static_cast<uint32_t>(kColP + (u & 1) * 64);
+        for (int kk = 0; kk < nks; ++kk) {
+          const uint32_t vb = blk ? sbase + TcSmem::kBlock + 2 * kBSub + kk * 16 * 128
+                                  : sbase + TcSmem::kVlo + ((t0 + (kk >> 2)) % kStages) * kSlot + (kk & 3) * 16 * 128;
+          const uint32_t lbo = blk ? kBSub : kRing;  // V dims 0-63 -> 64-127
+          umma_bf16_ta(tmem + kColO, pa + kk * 8, sdesc_sw128_mn(vb, lbo), kIdO, (u > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&o_full[u & 1]);
+        if (!blk) {
+          umma_commit(&empty[t0 % kStages]);
+          if (t0 + 1 < nctx) umma_commit(&empty[(t0 + 1) % kStages]);
+        }
+      }
       // every MMA of this CTA completes before tensor memory is released
       if (any) {
         umma_commit(drain);
@@ -363,97 +403,123 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
   }
 
-  // ---------------------------------------------------- softmax (warps 2-9)
-  const int q4 = warp & 3;                         // the lane quadrant this warp may read
-  const int half = warp >= 6 ? 1 : 0;              // which 32 keys of a tile (and 64 output columns)
+  // ---------------------------------------------------- softmax (warps 2-17)
+  const int q4 = warp & 3;                     // the lane quadrant this warp may access
+  const int part = warp >= 2 ? (warp - 2) >> 2 : 0;  // which 32 keys of a step (and 32 output columns)
   const int r = q4 * 32 + lane;
   const uint32_t tl = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
   float* xchg = reinterpret_cast<float*>(smem + TcSmem::kXchg);
   float* lpart = reinterpret_cast<float*>(smem + TcSmem::kLPart);
-  float m = -INFINITY, l = 0.f;  // the maximum the probabilities use, and this half's sum
-  bool done_all = false;         // the last tile's P*V has landed
+  float m = -INFINITY, l = 0.f;  // the maximum the probabilities use, and this warp's keys' sum
+  bool done_all = false;         // the last step's P*V has landed
   if (warp >= 2 && q4 < nact) {
     const float sc = rsqrtf(static_cast<float>(kD)) * 1.4426950408889634f;
-    const int key0 = half * 32;
-    // Both warps of a pair run every step and meet once a step at a named
-    // barrier that also ORs their failure flags, so a wait that gives up in
-    // one warp stops both (never one warp alone at the barrier); after a
-    // failure the steps only keep the barrier count.
+    const int key0 = part * 32;
+    {
+      // this warp's rows of Q, dims 32*part .. 32*part+31, into tensor memory
+      uint32_t qv[16];
+      if (r < rows) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            a.Q + (static_cast<int64_t>(si) * 16 + (r & 15)) * (a.nq * kD) + (kvh * G + (r >> 4)) * kD + key0);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 w = src[c];
+          qv[4 * c] = w.x;
+          qv[4 * c + 1] = w.y;
+          qv[4 * c + 2] = w.z;
+          qv[4 * c + 3] = w.w;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) qv[c] = 0u;
+      }
+      tmem_st16u(tl + kColQ + part * 16, qv);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(q_tm);
+    }
+    // The four warps of a quadrant run every step and meet once a step at a
+    // named barrier that also ORs their failure flags, so a wait that gives
+    // up in one warp stops all four (never a warp alone at the barrier);
+    // after a failure the steps only keep the barrier count.
     bool ok = true;
-    for (int t = 0; t < nT; ++t) {
-      const bool blk = t == nctx;
-      const int nvalid = blk ? kBK : min(kTK, k1 - k0 - t * kTK);
-      const int nmine = max(0, min(32, nvalid - key0));  // valid keys of this half
+    for (int j = 0; j < nS; ++j) {
+      const bool blk = j == nsc;
+      const int nvalid = blk ? kBK : min(kSK, nkeys - j * kSK);
+      const int nmine = max(0, min(32, nvalid - key0));  // valid keys of this warp
       // every wait's outcome is made warp-uniform: the tensor-memory loads
       // and stores after it are warp-collective
-      if (ok) ok = mbar_wait(&s_full[t & 1], (t >> 1) & 1, err, DFLASH_STATUS_TIMEOUT, abort_word);
+      if (ok) ok = mbar_wait(s_full, j & 1, err, DFLASH_STATUS_TIMEOUT, abort_word);
       ok = __all_sync(0xffffffffu, ok);
       float sv[32];
       if (ok) {
         tc_fence_after();
         uint32_t u[32];
-        tmem_ld32_async(tl + (t & 1) * kTK + key0, u);
+        tmem_ld32_async(tl + kColS + key0, u);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(u[j]);
+        for (int i = 0; i < 32; ++i) sv[i] = __uint_as_float(u[i]);
         tc_fence_before();
-        mbar_arrive(&s_empty[t & 1]);
+        mbar_arrive(s_empty);
       } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) sv[j] = -INFINITY;
+        for (int i = 0; i < 32; ++i) sv[i] = -INFINITY;
       }
       if (nmine < 32) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j >= nmine) sv[j] = -INFINITY;
+        for (int i = 0; i < 32; ++i)
+          if (i >= nmine) sv[i] = -INFINITY;
       }
       float t0 = sv[0], t1 = sv[1], t2 = sv[2], t3 = sv[3];
 #pragma unroll
-      for (int j = 4; j < 32; j += 4) {
-        t0 = fmaxf(t0, sv[j]);
-        t1 = fmaxf(t1, sv[j + 1]);
-        t2 = fmaxf(t2, sv[j + 2]);
-        t3 = fmaxf(t3, sv[j + 3]);
+      for (int i = 4; i < 32; i += 4) {
+        t0 = fmaxf(t0, sv[i]);
+        t1 = fmaxf(t1, sv[i + 1]);
+        t2 = fmaxf(t2, sv[i + 2]);
+        t3 = fmaxf(t3, sv[i + 3]);
       }
-      // the tile's maximum over both halves (raw scores; the scale is positive)
+      // the step's maximum over the quadrant's four warps (raw scores; the
+      // scale is positive)
       {
-        float* slot = xchg + ((q4 * 2 + half) * 2 + (t & 1)) * 32;
+        float* slot = xchg + ((q4 * kParts + part) * 2 + (j & 1)) * 32;
         slot[lane] = fmaxf(fmaxf(t0, t1), fmaxf(t2, t3));
-        if (named_bar_or(1 + q4, 64, ok ? 0 : 1)) ok = false;
-        const float other = xchg[((q4 * 2 + (half ^ 1)) * 2 + (t & 1)) * 32 + lane];
-        t0 = fmaxf(slot[lane], other);
+        if (named_bar_or(1 + q4, 128, ok ? 0 : 1)) ok = false;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int p2 = 0; p2 < kParts; ++p2) mx = fmaxf(mx, xchg[((q4 * kParts + p2) * 2 + (j & 1)) * 32 + lane]);
+        t0 = mx;
       }
       if (!ok) continue;
       const float tmax = t0 * sc;
-      // P*V of tile t-2, the last reader of this step's P buffer, must have
-      // landed (o_full[b] completes once for each tile using P buffer b;
+      // P*V of step j-2, the last reader of this step's P buffer, must have
+      // landed (o_full[b] completes once for each step using P buffer b;
       // the next of them needs this step's P, so the wait cannot fall two
-      // phases behind). A rescale of the output also waits for P*V of t-1.
-      if (t >= 2) ok = mbar_wait(&o_full[t & 1], ((t - 2) >> 1) & 1, err, DFLASH_STATUS_TIMEOUT, abort_word);
+      // phases behind). A rescale of the output also waits for P*V of j-1.
+      if (j >= 2) ok = mbar_wait(&o_full[j & 1], ((j - 2) >> 1) & 1, err, DFLASH_STATUS_TIMEOUT, abort_word);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) continue;
-      // a row needs a rescale when its tile maximum passes the one in use by
+      // a row needs a rescale when its step maximum passes the one in use by
       // more than the margin; the tensor-memory loads and stores are
       // warp-collective, so the warp rescales when any of its rows needs it
-      // (alpha = 1 for the others). Both warps of a pair decide alike: they
-      // hold the same rows and the same tile maxima.
+      // (alpha = 1 for the others). The four warps of a quadrant decide
+      // alike: they hold the same rows and the same step maxima.
       const bool need = tmax > m + kRescaleLog2;
       const bool rescale = __any_sync(0xffffffffu, need);
       if (rescale) {
-        if (t >= 1) ok = mbar_wait(&o_full[(t - 1) & 1], ((t - 1) >> 1) & 1, err, DFLASH_STATUS_TIMEOUT, abort_word);
+        if (j >= 1) ok = mbar_wait(&o_full[(j - 1) & 1], ((j - 1) >> 1) & 1, err, DFLASH_STATUS_TIMEOUT, abort_word);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) continue;
         tc_fence_after();
         const float alpha = !need ? 1.f : (m == -INFINITY ? 0.f : ex2(m - tmax));
         l *= alpha;
-        if (t >= 1) {
+        if (j >= 1) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             float v[16];
-            tmem_ld16(tl + 128 + half * 64 + c * 16, v);
+            tmem_ld16(tl + kColO + part * 32 + c * 16, v);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] *= alpha;
-            tmem_st16(tl + 128 + half * 64 + c * 16, v);
+            for (int i = 0; i < 16; ++i) v[i] *= alpha;
+            tmem_st16(tl + kColO + part * 32 + c * 16, v);
           }
         }
         if (need) m = tmax;
@@ -461,68 +527,65 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       const float negm = -m;
       float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
 #pragma unroll
-      for (int j = 0; j < 32; j += 4) {
-        sv[j] = ex2(fmaf(sv[j], sc, negm));
-        sv[j + 1] = ex2(fmaf(sv[j + 1], sc, negm));
-        sv[j + 2] = ex2(fmaf(sv[j + 2], sc, negm));
-        sv[j + 3] = ex2(fmaf(sv[j + 3], sc, negm));
-        ps0 += sv[j];
-        ps1 += sv[j + 1];
-        ps2 += sv[j + 2];
-        ps3 += sv[j + 3];
+      for (int i = 0; i < 32; i += 4) {
+        sv[i] = ex2(fmaf(sv[i], sc, negm));
+        sv[i + 1] = ex2(fmaf(sv[i + 1], sc, negm));
+        sv[i + 2] = ex2(fmaf(sv[i + 2], sc, negm));
+        sv[i + 3] = ex2(fmaf(sv[i + 3], sc, negm));
+        ps0 += sv[i];
+        ps1 += sv[i + 1];
+        ps2 += sv[i + 2];
+        ps3 += sv[i + 3];
       }
       l += (ps0 + ps1) + (ps2 + ps3);
-      // this half's keys of P as bf16: 16-byte chunks 4*half .. 4*half+3 of the row
-      uint8_t* prow = smem + TcSmem::kP + (t & 1) * kPBytes + r * 128;
-      const int nchunk = blk ? (half == 0 ? kBK / 8 : 0) : 4;
+      // this warp's keys of P as bf16 pairs into the step's P buffer
+      {
+        uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (c < nchunk) {
-          uint4 w;
-          uint32_t* w2 = reinterpret_cast<uint32_t*>(&w);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __nv_bfloat162 h = __floats2bfloat162_rn(sv[c * 8 + 2 * e], sv[c * 8 + 2 * e + 1]);
-            w2[e] = *reinterpret_cast<const uint32_t*>(&h);
-          }
-          *reinterpret_cast<uint4*>(prow + (((4 * half + c) ^ (r & 7)) << 4)) = w;
+        for (int e = 0; e < 16; ++e) {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(sv[2 * e], sv[2 * e + 1]);
+          pk[e] = *reinterpret_cast<const uint32_t*>(&h);
         }
+        tmem_st16u(tl + kColP + (j & 1) * 64 + part * 16, pk);
+        tmem_wait_st();
       }
-      fence_proxy_async();
       tc_fence_before();
-      mbar_arrive(&p_full[t & 1]);
+      mbar_arrive(&p_full[j & 1]);
     }
     // the last P*V (its completion implies every earlier one)
-    if (ok && nT >= 1)
-      done_all = mbar_wait(&o_full[(nT - 1) & 1], ((nT - 1) >> 1) & 1, err, DFLASH_STATUS_TIMEOUT, abort_word);
+    if (ok && nS >= 1)
+      done_all = mbar_wait(&o_full[(nS - 1) & 1], ((nS - 1) >> 1) & 1, err, DFLASH_STATUS_TIMEOUT, abort_word);
     done_all = __all_sync(0xffffffffu, done_all);
-    lpart[half * kRows + r] = l;
+    lpart[part * kRows + r] = l;
   }
-  __syncthreads();  // every tile consumed: the stage memory is free
+  __syncthreads();  // every step consumed: the ring memory is free
 
   // this CTA's partial rows: part[r][kPartLd] (fp32) and ml[r][2]
-  float* part = reinterpret_cast<float*>(smem + TcSmem::kStage);
-  float* ml = part + kRows * kPartLd;
+  float* partial = reinterpret_cast<float*>(smem + TcSmem::kKlo);
+  float* ml = partial + kRows * kPartLd;
   if (warp >= 2 && q4 < nact) {
     if (done_all) tc_fence_after();
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 2; ++c) {
       float v[16];
       if (done_all) {
-        tmem_ld16(tl + 128 + half * 64 + c * 16, v);
+        tmem_ld16(tl + kColO + part * 32 + c * 16, v);
       } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = 0.f;
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
       }
       if (r < rows) {
-        float4* pr = reinterpret_cast<float4*>(part + r * kPartLd + half * 64 + c * 16);
+        float4* pr = reinterpret_cast<float4*>(partial + r * kPartLd + part * 32 + c * 16);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) pr[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        for (int i = 0; i < 4; ++i) pr[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
       }
     }
-    if (r < rows && half == 0) {
+    if (r < rows && part == 0) {
+      float lsum = 0.f;
+#pragma unroll
+      for (int p2 = 0; p2 < kParts; ++p2) lsum += lpart[p2 * kRows + r];
       ml[r * 2] = done_all ? m : -INFINITY;
-      ml[r * 2 + 1] = done_all ? lpart[r] + lpart[kRows + r] : 0.f;
+      ml[r * 2 + 1] = done_all ? lsum : 0.f;
     }
   }
   csync();  // every CTA's partial is ready
@@ -531,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   {
     const int v0 = static_cast<int>(rank) * rows / CS;
     const int v1 = (static_cast<int>(rank) + 1) * rows / CS;
-    const uint32_t pbase = smem_u32(part), mlbase = smem_u32(ml);
+    const uint32_t pbase = smem_u32(partial), mlbase = smem_u32(ml);
     for (int idx = threadIdx.x; idx < (v1 - v0) * 32; idx += blockDim.x) {
       const int vec = v0 + idx / 32;
       const int d4 = (idx & 31) * 4;
@@ -627,13 +690,6 @@ int launch_attention_tc(const AttnArgs& a, const CUtensorMap& kmap, const CUtens
     const cuuint32_t box[2] = {64, 16};
     int rc = encode_map(&P.kbmap, a.Kb, 2, dims, strides, box);
     if (!rc) rc = encode_map(&P.vbmap, a.Vb, 2, dims, strides, box);
-    if (rc) return rc;
-  }
-  {
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.nq) * kD, static_cast<cuuint64_t>(T)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.nq) * kD * 2};
-    const cuuint32_t box[2] = {64, 16};
-    const int rc = encode_map(&P.qmap, a.Q, 2, dims, strides, box);
     if (rc) return rc;
   }
   // keys a CTA: each (stream, kv head) splits over the most CTAs (a power
