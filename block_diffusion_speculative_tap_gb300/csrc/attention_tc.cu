@@ -8,22 +8,25 @@
 // the whole group. The visible context keys are split evenly over the CS CTAs
 // of a thread-block cluster; the last CTA also takes the block's own 16 keys.
 //
-// A 128-row MMA costs about the same time whether it is 64 or 128 columns
-// wide, so the scores of two 64-key tiles are taken in one 128-column MMA: a
-// step is 128 keys. K and V stream through four rings of 64-key slots (K
+// A 128-row MMA of 16 k-steps takes about 120 cycles on GB300 whether it is
+// 16, 64 or 128 columns wide (measured), so the scores of two 64-key tiles
+// are taken in one 128-column MMA: a step is 128 keys. K and V stream through four rings of 64-key slots (K
 // dims 0-63, K dims 64-127, V dims 0-63, V dims 64-127) so that a step's two
 // tiles sit in adjacent slots and read as one 128-row operand. Both A operands
 // live in tensor memory (row i of A in lane i, two bf16 of consecutive k in
 // each 32-bit column): the softmax warps copy Q there once and write P there.
 //
-// Roles (576 threads):
+// Roles (608 threads):
 //   warp 0     TMA producer: 64-key tiles of K and V (head-major cache, 3-D
 //              tensor maps, 128-byte swizzle) into the rings, and the block's
 //              K/V.
-//   warp 1     tensor-memory owner and MMA issuer: S = Q K^T of step u+1 as
-//              soon as the softmax warps have read step u's scores, then
-//              O += P_u V_u (V read MN-major) once they have written P_u.
-//   warps 2-17 softmax: four warps a tensor-memory lane quadrant, each taking
+//   warp 1     tensor-memory owner and score MMA issuer: S = Q K^T of step
+//              u+1 as soon as the softmax warps have read step u's scores.
+//   warp 2     output MMA issuer: O += P_u V_u (V read MN-major) once the
+//              softmax warps have written P_u. Issuing blocks while the
+//              tensor pipe is busy, so the two kinds of MMA have a thread
+//              each: the next scores never queue behind the previous P*V.
+//   warps 3-18 softmax: four warps a tensor-memory lane quadrant, each taking
 //              32 of a step's keys for the quadrant's 32 rows (thread r of a
 //              warp owns row r). The four share their step maximum through
 //              shared memory and a named barrier; each keeps its keys' sum and
@@ -61,7 +64,7 @@ constexpr int kTileBytes = 4 * kSlot;    // a tile's K and V (32 KiB)
 constexpr int kBSub = kBK * 128;         // 16 keys x 64 dims (2 KiB)
 constexpr int kPartLd = kD + 4;          // fp32 partial row stride
 constexpr int kParts = 4;                // softmax warps a lane quadrant
-constexpr int kThreads = 64 + 128 * kParts;
+constexpr int kThreads = 96 + 128 * kParts;
 // tensor-memory columns: the step's scores (0..127), the output (128..255),
 // Q as the score MMAs' A operand (64 columns: 128 dims as bf16 pairs) and two
 // P buffers (64 columns each: 128 keys as bf16 pairs)
@@ -88,7 +91,7 @@ static_assert(TcSmem::kKhi % 1024 == 0 && TcSmem::kBlock % 1024 == 0,
               "swizzled tiles must start on 1024-byte boundaries");
 static_assert(sizeof(float) * (kRows * kPartLd + kRows * 2) <= 4 * kRing,
               "the partials must fit the ring memory");
-static_assert(8 * (2 * kStages + 10) <= 256, "the barriers must fit their region");
+static_assert(8 * (2 * kStages + 11) <= 256, "the barriers must fit their region");
 constexpr int kSmemLaunch = TcSmem::kBytes + 1024;
 
 // MN-major operand stored with the 128-byte swizzle, as TMA writes a tile of
@@ -235,8 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   uint64_t* o_full = s_full + 4;          // [2] P*V of a step using P buffer b has landed in the output
   uint64_t* blk_full = s_full + 6;        // the block's K/V landed
   uint64_t* q_tm = s_full + 7;            // the Q rows are in tensor memory
-  uint64_t* drain = s_full + 8;           // every MMA of the CTA is done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 9);
+  uint64_t* drain = s_full + 8;           // [2] every MMA of either issuer is done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 10);
   int* abort_word = reinterpret_cast<int*>(tmem_slot + 1);
   const uint32_t sbase = smem_u32(smem);
 
@@ -261,7 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
     mbar_init(blk_full, 1);
     mbar_init(q_tm, 128 * nact);
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     *abort_word = 0;
     fence_barrier_init();
   }
@@ -331,11 +335,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ------------------------------------------------ MMA issuer
+      // ------------------------------------------------ score MMA issuer
       constexpr uint32_t kIdS2 = idesc_bf16_f32(kRows, kSK);
       constexpr uint32_t kIdS1 = idesc_bf16_f32(kRows, kTK);
       constexpr uint32_t kIdSB = idesc_bf16_f32(kRows, kBK);
-      constexpr uint32_t kIdO = idesc_bf16_f32(kRows, kD) | kIdescBTransposed;
       bool ok = mbar_wait(q_tm, 0, err, DFLASH_STATUS_TIMEOUT, abort_word);
       bool any = false;
       // S_j = Q K_j^T once step j's keys have landed: one MMA per 16 dims,
@@ -368,14 +371,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         ok = s_issue(0);
         any = ok;
       }
+      // the next step's scores as soon as softmax u has read this step's
+      for (int u = 0; u + 1 < nS && ok; ++u) {
+        ok = mbar_wait(s_empty, u & 1, err, DFLASH_STATUS_TIMEOUT, abort_word);
+        if (ok) ok = s_issue(u + 1);
+      }
+      // every score MMA completes before tensor memory is released
+      if (any) {
+        umma_commit(&drain[0]);
+        mbar_wait(&drain[0], 0, err, DFLASH_STATUS_TIMEOUT, nullptr);
+      }
+    }
+  } else if (warp == 2) {
+    if (lane == 0) {
+      // ------------------------------------------------ output MMA issuer
+      constexpr uint32_t kIdO = idesc_bf16_f32(kRows, kD) | kIdescBTransposed;
+      bool ok = true;
+      bool any = false;
+      // O += P_u V_u once the softmax warps wrote P_u (and rescaled O)
       for (int u = 0; u < nS && ok; ++u) {
-        // the next step's scores as soon as softmax u has read this step's
-        if (u + 1 < nS) {
-          ok = mbar_wait(s_empty, u & 1, err, DFLASH_STATUS_TIMEOUT, abort_word);
-          if (ok) ok = s_issue(u + 1);
-          if (!ok) break;
-        }
-        // O += P_u V_u once the softmax warps wrote P_u (and rescaled O)
         ok = mbar_wait(&p_full[u & 1], (u >> 1) & 1, err, DFLASH_STATUS_TIMEOUT, abort_word);
         if (!ok) break;
         tc_fence_after();
@@ -389,30 +403,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           const uint32_t lbo = blk ? kBSub : kRing;  // V dims 0-63 -> 64-127
           umma_bf16_ta(tmem + kColO, pa + kk * 8, sdesc_sw128_mn(vb, lbo), kIdO, (u > 0 || kk > 0) ? 1u : 0u);
         }
+        any = true;
         umma_commit(&o_full[u & 1]);
         if (!blk) {
           umma_commit(&empty[t0 % kStages]);
           if (t0 + 1 < nctx) umma_commit(&empty[(t0 + 1) % kStages]);
         }
       }
-      // every MMA of this CTA completes before tensor memory is released
+      // every output MMA completes before tensor memory is released
       if (any) {
-        umma_commit(drain);
-        mbar_wait(drain, 0, err, DFLASH_STATUS_TIMEOUT, nullptr);
+        umma_commit(&drain[1]);
+        mbar_wait(&drain[1], 0, err, DFLASH_STATUS_TIMEOUT, nullptr);
       }
     }
   }
 
-  // ---------------------------------------------------- softmax (warps 2-17)
+  // ---------------------------------------------------- softmax (warps 3-18)
   const int q4 = warp & 3;                     // the lane quadrant this warp may access
-  const int part = warp >= 2 ? (warp - 2) >> 2 : 0;  // which 32 keys of a step (and 32 output columns)
+  const int part = warp >= 3 ? (warp - 3) >> 2 : 0;  // which 32 keys of a step (and 32 output columns)
   const int r = q4 * 32 + lane;
   const uint32_t tl = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
   float* xchg = reinterpret_cast<float*>(smem + TcSmem::kXchg);
   float* lpart = reinterpret_cast<float*>(smem + TcSmem::kLPart);
   float m = -INFINITY, l = 0.f;  // the maximum the probabilities use, and this warp's keys' sum
   bool done_all = false;         // the last step's P*V has landed
-  if (warp >= 2 && q4 < nact) {
+  if (warp >= 3 && q4 < nact) {
     const float sc = rsqrtf(static_cast<float>(kD)) * 1.4426950408889634f;
     const int key0 = part * 32;
     {
@@ -563,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   // this CTA's partial rows: part[r][kPartLd] (fp32) and ml[r][2]
   float* partial = reinterpret_cast<float*>(smem + TcSmem::kKlo);
   float* ml = partial + kRows * kPartLd;
-  if (warp >= 2 && q4 < nact) {
+  if (warp >= 3 && q4 < nact) {
     if (done_all) tc_fence_after();
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
