@@ -1075,11 +1075,12 @@ int run_stages(dflash_handle* h, dflash_state* st, int s_begin, int s_count, int
     a.err = st->status;
     // more than four streams whose (stream, kv head) pairs fit one wave of
     // SMs: the tensor-memory kernel, one 128-row MMA per kv head's query
-    // group (the DFlash2 geometry, 8 streams x 8 kv heads: 0.74 -> 0.39 ms a
-    // round). Up to four streams the batch-invariant 8-way split of the
-    // cluster kernel stays; with more pairs than SMs the cluster kernel's
-    // finer key split balances uneven contexts better (32 streams of the 9B
-    // shape: 0.77 ms against 0.79-0.85 ms a round).
+    // group (the DFlash2 geometry, 8 streams x 8 kv heads: 0.74 ms a draft
+    // with the cluster kernel, 0.29 ms). Up to four streams the
+    // batch-invariant 8-way split of the cluster kernel stays; with more
+    // pairs than SMs the cluster kernel's finer key split balanced uneven
+    // contexts better when the tensor-memory kernel still took 64-key tiles
+    // (32 streams of the 9B shape: 0.77 ms against 0.79-0.85 ms a round).
     if (s_count > kInvariantStreams && s_count * a.nkv <= h->num_sms && attention_tc_supported(a))
       rc = launch_attention_tc(a, st->kmap[l], st->vmap[l], s_count, h->num_sms, s);
     else
