@@ -72,6 +72,9 @@ constexpr int kColS = 0;
 constexpr int kColO = 128;
 constexpr int kColQ = 256;
 constexpr int kColP = 320;
+// All of an SM's tensor memory: the CTA's 207 KB of shared memory leave no
+// room on its SM for a CTA of the other tensor-memory user (every GEMM CTA
+// takes at least 93 KB), so the allocation never waits on another kernel.
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;      // a row's maximum in use moves only past this margin
 
