@@ -127,3 +127,118 @@ def test_kernel_shape_limits_are_refused(D):
         dict(m, mask_token=151936),
     ):
         assert D.config_validate(cfg) == -5, cfg
+
+
+def test_tree_sizes_match_the_oracle_and_limits_are_refused(A):
+    """dflash_tree_size counts the nodes of a tree of widths b_1..b_D as the
+    oracle builds it (root plus b_1 * ... * b_j nodes at depth j, breadth
+    first); depths outside 1..15, widths outside 1..k, k over
+    DFLASH_MAX_TOPK and trees over DFLASH_MAX_TREE_NODES nodes are refused
+    (DFLASH_E_INVALID_ARG)."""
+    import ctypes as C
+
+    import numpy as np
+
+    def size(widths, k):
+        n = C.c_int(-7)
+        arr = (C.c_int32 * max(1, len(widths)))(*widths)
+        rc = A.lib.dflash_tree_size(len(widths), arr, k, C.byref(n))
+        return rc, n.value
+
+    topk = np.arange(15 * 16, dtype=np.int64).reshape(15, 16)
+    for widths in ([4, 2, 2, 1, 1, 1, 1], [1] * 15, [16, 8], [3, 3, 3, 3, 3], [2] * 9):
+        tokens, parents, depths = O.tree_nodes(7, topk, widths)
+        assert size(widths, 16) == (0, len(tokens)), widths
+    assert size([4, 2, 2, 1, 1, 1, 1], 16) == (0, 93)  # the bench's tree
+    for widths, k in (([], 16), ([1] * 16, 16), ([0, 2], 16), ([5], 4), ([2], 17), ([2], 0),
+                      ([16, 16, 16], 16), ([2] * 10, 16)):
+        rc, n = size(widths, k)
+        assert rc == -1 and n == -7, (widths, k)
+    assert A.lib.dflash_tree_size(2, None, 16, C.byref(C.c_int())) == -1
+    assert A.lib.dflash_tree_size(2, (C.c_int32 * 2)(1, 1), 16, None) == -1
+
+
+def test_path_and_tree_workspace_prices(A):
+    """Workspace prices of the selector and of tree verification: the
+    selector's pair-score table takes streams * (positions - 1) * k^2 fp32
+    (nothing for one position), tree verification an arg-max id and value a
+    node; shapes outside the documented ranges are refused."""
+    import ctypes as C
+
+    nb = C.c_size_t(123)
+    assert A.lib.dflash_select_path_workspace_bytes(32, 15, 16, C.byref(nb)) == 0
+    assert nb.value == 32 * 14 * 16 * 16 * 4
+    assert A.lib.dflash_select_path_workspace_bytes(32, 1, 16, C.byref(nb)) == 0 and nb.value == 0
+    for S, P, k in ((-1, 15, 16), (4, 0, 16), (4, 17, 16), (4, 15, 0), (4, 15, 17)):
+        assert A.lib.dflash_select_path_workspace_bytes(S, P, k, C.byref(nb)) == -1, (S, P, k)
+    assert A.lib.dflash_select_path_workspace_bytes(4, 15, 16, None) == -1
+    assert A.lib.dflash_tree_verify_workspace_bytes(32, 93, C.byref(nb)) == 0 and nb.value == 32 * 93 * 8
+    for S, N in ((-1, 93), (4, 0), (4, 1025)):
+        assert A.lib.dflash_tree_verify_workspace_bytes(S, N, C.byref(nb)) == -1, (S, N)
+
+
+def test_selector_tree_stop_and_topk_refusals(A):
+    """Every refusal the header documents for the candidate-path selector,
+    the draft trees, the min-p stop and the top-k scan happens on the host,
+    before anything is enqueued (the device pointers below are never
+    dereferenced: each call is refused, or has no rows, before any launch)."""
+    import ctypes as C
+
+    p = C.c_void_p(0x10000)        # a 16-byte-aligned stand-in, never read
+    odd = C.c_void_p(0x10008)      # misaligned
+    big = C.c_size_t(1 << 30)
+    f = C.c_float
+    w3 = (C.c_int32 * 3)(2, 2, 1)
+    bad_w = (C.c_int32 * 3)(2, 0, 1)
+
+    # selector: positions, k, vocab, rank (0..512, a multiple of 8), codebooks, workspace
+    sel = lambda S, P, k, V, r, U=p, W=p, ws=p, wsb=big: A.lib.dflash_select_path(
+        S, P, k, V, r, p, p, U, W, p, None, None, ws, wsb, None)
+    assert sel(0, 15, 16, 4096, 256) == 0          # no streams: nothing to do
+    for args in ((-1, 15, 16, 4096, 256), (4, 0, 16, 4096, 256), (4, 17, 16, 4096, 256), (4, 15, 0, 4096, 256),
+                 (4, 15, 17, 4096, 256), (4, 15, 16, 0, 256), (4, 15, 16, 4096, -8), (4, 15, 16, 4096, 12),
+                 (4, 15, 16, 4096, 520)):
+        assert sel(*args) == -1, args
+    assert sel(4, 15, 16, 4096, 256, U=None) == -1
+    assert sel(4, 15, 16, 4096, 256, W=odd) == -1
+    assert sel(4, 15, 16, 4096, 256, ws=None) == -7
+    assert sel(4, 15, 16, 4096, 256, wsb=C.c_size_t(4 * 14 * 16 * 16 * 4 - 1)) == -7
+    assert sel(4, 15, 16, 4096, 256, ws=odd) == -7
+    assert A.lib.dflash_select_path(4, 15, 16, 4096, 256, None, p, p, p, p, None, None, p, big, None) == -1
+
+    # trees: shape refusals before the stream count, null outputs, workspace
+    assert A.lib.dflash_tree_build(-1, 3, w3, 16, p, p, p, None, None, None, None) == -1
+    assert A.lib.dflash_tree_build(4, 3, bad_w, 16, p, p, p, None, None, None, None) == -1
+    assert A.lib.dflash_tree_build(4, 0, w3, 16, p, p, p, None, None, None, None) == -1
+    assert A.lib.dflash_tree_build(0, 3, w3, 16, p, p, p, None, None, None, None) == 0
+    assert A.lib.dflash_tree_build(4, 3, w3, 16, None, p, p, None, None, None, None) == -1
+    assert A.lib.dflash_tree_build(4, 3, w3, 16, p, p, None, None, None, None, None) == -1
+    tv = lambda S, V, w=w3, logits=p, ws=p, wsb=big: A.lib.dflash_tree_verify(
+        S, 3, w, V, p, logits, p, p, None, ws, wsb, None)
+    assert tv(0, 4096) == 0
+    assert tv(4, 4092) == -1 and tv(4, 4) == -1 and tv(-1, 4096) == -1
+    assert tv(4, 4096, w=bad_w) == -1
+    assert tv(4, 4096, logits=odd) == -1
+    assert tv(4, 4096, ws=None) == -7
+    assert tv(4, 4096, wsb=C.c_size_t(4 * 11 * 8 - 1)) == -7   # 11 nodes a stream (1 + 2 + 4 + 4)
+
+    # min-p stop: temperature > 0, 0 <= min_p <= 1, vocab a multiple of 8
+    stop = lambda S, V, T, mp, logits=p: A.lib.dflash_draft_stop(logits, S, V, f(T), f(mp), p, p, None)
+    assert stop(0, 4096, 1.0, 0.5) == 0
+    for args in ((4, 4096, 0.0, 0.5), (4, 4096, -1.0, 0.5), (4, 4096, float("nan"), 0.5), (4, 4096, 1.0, -0.01),
+                 (4, 4096, 1.0, 1.01), (4, 4096, 1.0, float("nan")), (4, 4092, 1.0, 0.5), (-1, 4096, 1.0, 0.5)):
+        assert stop(*args) == -1, args
+    assert stop(4, 4096, 1.0, 0.5, logits=odd) == -1
+
+    # top-k: k in 0..16, vocab a multiple of 8, uniforms and sampled together, T > 0 to sample
+    tk = lambda rows, V, k, T=1.0, u=None, smp=None, ids=p, vals=p, logits=p: A.lib.dflash_topk(
+        logits, rows, V, k, f(T), u, ids, vals, smp, None)
+    assert tk(0, 4096, 8) == 0
+    for args in ((4, 4092, 8), (4, 4096, 17), (4, 4096, -1), (-1, 4096, 8)):
+        assert tk(*args) == -1, args
+    assert tk(4, 4096, 8, ids=None) == -1
+    assert tk(4, 4096, 8, u=p) == -1               # uniforms without an output for the draws
+    assert tk(4, 4096, 8, smp=p) == -1             # an output for draws without uniforms
+    assert tk(4, 4096, 8, T=0.0, u=p, smp=p) == -1
+    assert tk(4, 4096, 8, logits=odd) == -1
+    assert tk(4, 4096, 0) == 0                     # nothing asked: nothing enqueued
